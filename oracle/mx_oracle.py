@@ -1,0 +1,302 @@
+"""CPU oracle for MXFP8 block-scaled quantisation and the MXFP8 GEMM.
+
+TEST INFRASTRUCTURE ONLY.  This module is the slow, obviously-correct
+definition that the CUDA path is checked against.  Only the test suite, the
+smoke check of the package entry point and the CPU-baseline leg of the bench
+may import it.  The product path never calls it, and it shares no code with
+the CUDA library: it imports numpy alone.
+
+All arithmetic is float64 (exact for every value that occurs here: bf16 and
+E4M3 values times powers of two), rounding steps are written out as
+definitions, and a library primitive (numpy's matmul) is the only "fast" step.
+
+Sources of the definitions
+--------------------------
+* "HipKittens MXFP8 GEMM Support", ROCm/TransformerEngine PR #566 (PR
+  description and review thread): the GEMM is an MXFP8 TN GEMM with a per-K
+  block scale array (``scale_K``), BIAS and GELU-AUX epilogues, K a multiple
+  of 128 "for MXFP8 scaling", and the MXFP8 1D scaling mode.
+* ROCm/TransformerEngine README, sections "MXFP8 support on ROCm" and
+  "Blockwise FP8 GEMM support on ROCm": MX scales are E8M0 (power of two).
+* leeroopedia "FP8 Training Quickstart", step on autocast recipes: E4M3 is the
+  forward-pass FP8 format.
+* The pages name MXFP8 but never define its numerics.  The block size (32),
+  the scale rule and the element format are those of the OCP Microscaling
+  Formats (MX) v1.0 specification, FP32 -> MX conversion: shared exponent
+  = floor(log2(max |V_i|)) - emax(element), element = V_i / 2^shared_exp
+  rounded to nearest-even in E4M3 and clamped to the largest normal (448).
+  E4M3 itself is the OCP 8-bit floating point "E4M3" encoding (bias 7, no
+  infinities, S.1111.111 is NaN, largest normal 448).
+* GELU-tanh: the tanh approximation of GELU named on the TE "Getting
+  Started" page (``approximate=True``), 0.5 x (1 + tanh(sqrt(2/pi) (x +
+  0.044715 x^3))).
+
+Readings where the sources are silent (each one is listed in the design notes):
+* amax == 0: the scale byte is 0x00 (2^-127, the smallest E8M0 value); every
+  element is +-0.
+* The scale exponent is clamped to [-127, 127] (E8M0's finite range).
+* A negative value that rounds to zero keeps its sign (code 0x80).
+* A block holding a NaN or an infinity: scale byte 0xFF (E8M0 NaN) and every
+  element code 0x7F (E4M3 NaN).
+* GELU is applied to the unrounded pre-activation; AUX is that
+  pre-activation rounded to bf16.
+"""
+from __future__ import annotations
+
+import numpy as np
+
+MX_BLOCK = 32              # elements per E8M0 scale (OCP MX block size)
+E4M3_EMAX = 8              # exponent of the largest E4M3 binade (448 = 1.75 * 2^8)
+E4M3_MAX = 448.0
+E4M3_MANT_BITS = 3
+E4M3_EMIN = -6             # smallest normal exponent; subnormal step 2^-9
+E4M3_BIAS = 7
+E8M0_BIAS = 127
+BF16_MANT_BITS = 7
+BF16_EMIN = -126
+BF16_MAX = (2.0 - 2.0 ** -7) * 2.0 ** 127
+
+# --------------------------------------------------------------------------
+# Rounding to a binary floating-point format
+# --------------------------------------------------------------------------
+
+
+def round_to_binary_format(v, mant_bits: int, emin: int) -> np.ndarray:
+    """Round float64 values to the nearest value of a binary FP format, ties to even.
+
+    The format has ``mant_bits`` fraction bits and smallest normal exponent
+    ``emin``; below 2^emin it is subnormal with step 2^(emin - mant_bits).
+    It is unbounded above (overflow is the caller's business).  The sign is
+    kept, so a negative value that rounds to zero gives -0.0.
+    """
+    v = np.asarray(v, dtype=np.float64)
+    _, p = np.frexp(v)                    # v = m * 2^p with 0.5 <= |m| < 1
+    e = np.maximum(p - 1, emin)           # floor(log2|v|), held at emin for subnormals
+    quantum = np.ldexp(1.0, e - mant_bits)
+    # v / quantum is exact (division by a power of two); np.round is ties-to-even.
+    return np.round(v / quantum) * quantum
+
+
+def bf16_round(v) -> np.ndarray:
+    """float64 -> nearest bf16 value (ties to even), returned as float64.
+
+    Overflow goes to +-inf, as in IEEE round-to-nearest-even.
+    """
+    r = round_to_binary_format(v, BF16_MANT_BITS, BF16_EMIN)
+    v = np.asarray(v, dtype=np.float64)
+    r = np.where(np.abs(r) > BF16_MAX, np.copysign(np.inf, v), r)
+    return np.where(np.isnan(v), np.nan, r)
+
+
+def bf16_bits_to_f64(bits) -> np.ndarray:
+    """Decode bf16 bit patterns (uint16) to float64 (exact)."""
+    b = np.asarray(bits, dtype=np.uint16).astype(np.uint32) << np.uint32(16)
+    with np.errstate(invalid="ignore"):          # NaN patterns stay NaN
+        return b.view(np.float32).astype(np.float64)
+
+
+def f64_to_bf16_bits(v) -> np.ndarray:
+    """Round float64 to bf16 (ties to even) and return the uint16 bit patterns."""
+    r = bf16_round(v).astype(np.float32)          # exact: every bf16 value is an fp32 value
+    return (r.view(np.uint32) >> np.uint32(16)).astype(np.uint16)
+
+
+# --------------------------------------------------------------------------
+# E4M3 (OCP FP8 "E4M3") codec
+# --------------------------------------------------------------------------
+
+
+def e4m3_decode(codes) -> np.ndarray:
+    """Decode E4M3 bytes to float64: sign | 4-bit exponent (bias 7) | 3-bit mantissa.
+
+    Exponent field 0 is subnormal (m/8 * 2^-6); S.1111.111 is NaN; there is no
+    infinity.
+    """
+    c = np.asarray(codes, dtype=np.uint8).astype(np.int64)
+    sign = np.where(c & 0x80, -1.0, 1.0)
+    exp_field = (c >> 3) & 0xF
+    mant = (c & 0x7).astype(np.float64)
+    normal = np.ldexp(1.0 + mant / 8.0, exp_field - E4M3_BIAS)
+    subnormal = np.ldexp(mant / 8.0, E4M3_EMIN)
+    mag = np.where(exp_field == 0, subnormal, normal)
+    mag = np.where((exp_field == 0xF) & ((c & 0x7) == 0x7), np.nan, mag)
+    return sign * mag
+
+
+def e4m3_round_saturate(v) -> np.ndarray:
+    """Round float64 to the nearest E4M3 value (ties to even), then clamp to +-448.
+
+    Rounding first and clamping after gives the saturating conversion: every
+    |v| that would round above 448 becomes 448.
+    """
+    r = round_to_binary_format(v, E4M3_MANT_BITS, E4M3_EMIN)
+    return np.clip(r, -E4M3_MAX, E4M3_MAX)
+
+
+def e4m3_encode_value(r) -> np.ndarray:
+    """Bit pattern of an (already representable) E4M3 value; -0.0 -> 0x80."""
+    r = np.asarray(r, dtype=np.float64)
+    sign = np.signbit(r).astype(np.int64) << 7
+    a = np.abs(r)
+    _, p = np.frexp(a)
+    e = p - 1
+    is_sub = a < 2.0 ** E4M3_EMIN
+    sub_mant = np.round(a / 2.0 ** (E4M3_EMIN - E4M3_MANT_BITS)).astype(np.int64)
+    safe_e = np.where(is_sub | ~np.isfinite(a), 0, e)
+    norm_mant = np.round((a / np.ldexp(1.0, safe_e) - 1.0) * 8.0).astype(np.int64)
+    norm_field = (safe_e + E4M3_BIAS).astype(np.int64)
+    code = np.where(is_sub, sub_mant, (norm_field << 3) | norm_mant)
+    return (sign | code).astype(np.uint8)
+
+
+def e4m3_encode(v) -> np.ndarray:
+    """float64 -> E4M3 byte: round to nearest even, saturate to +-448, keep sign of zero."""
+    return e4m3_encode_value(e4m3_round_saturate(v))
+
+
+# --------------------------------------------------------------------------
+# MXFP8 quantisation
+# --------------------------------------------------------------------------
+
+
+def mx_scale_exponent(amax) -> np.ndarray:
+    """Shared exponent of an MX block: floor(log2 amax) - 8, clamped to [-127, 127].
+
+    floor(log2) is taken exactly from frexp (never from a log function).
+    amax == 0 gives -127 (reading: the smallest E8M0 scale).
+    """
+    amax = np.asarray(amax, dtype=np.float64)
+    _, p = np.frexp(amax)
+    e = np.clip((p - 1) - E4M3_EMAX, -E8M0_BIAS, E8M0_BIAS)
+    return np.where(amax == 0.0, -E8M0_BIAS, e).astype(np.int64)
+
+
+def quantize_mx(x_bits, axis: int):
+    """MXFP8-quantise a bf16 matrix along ``axis`` in blocks of 32.
+
+    ``x_bits``: uint16 bf16 patterns, shape [R, C].  Blocks are 32 consecutive
+    elements along ``axis`` (1: along a row; 0: down a column), so that axis
+    must have a length divisible by 32.
+
+    Returns ``(q, s)`` laid out with the blocked axis last and contiguous:
+      axis=1: q uint8 [R, C],  s uint8 [R, C/32]
+      axis=0: q uint8 [C, R],  s uint8 [C, R/32]   (the transposed copy)
+    where s is the E8M0 byte (exponent + 127) and q the E4M3 byte.
+    """
+    x = bf16_bits_to_f64(np.asarray(x_bits, dtype=np.uint16))
+    if axis == 0:
+        x = x.T                                   # put the blocked axis last
+    rows, n = x.shape
+    if n % MX_BLOCK:
+        raise ValueError(f"blocked axis length {n} is not a multiple of {MX_BLOCK}")
+    blocks = x.reshape(rows, n // MX_BLOCK, MX_BLOCK)
+    with np.errstate(invalid="ignore"):
+        amax = np.max(np.abs(blocks), axis=2)
+    bad = ~np.isfinite(amax)                      # block holds NaN or inf
+    amax_f = np.where(bad, 1.0, amax)
+    e = mx_scale_exponent(amax_f)
+    v = blocks * np.ldexp(1.0, -e)[:, :, None]    # exact: scaling by a power of two
+    q = e4m3_encode(v)
+    q = np.where(bad[:, :, None], np.uint8(0x7F), q)
+    s = np.where(bad, 0xFF, e + E8M0_BIAS).astype(np.uint8)
+    return q.reshape(rows, n).astype(np.uint8), s
+
+
+def quantize_rowwise(x_bits):
+    """Row-wise MXFP8: blocks of 32 along each row.  -> (q [R,C], s [R,C/32])."""
+    return quantize_mx(x_bits, axis=1)
+
+
+def quantize_colwise(x_bits):
+    """Column-wise MXFP8: blocks of 32 down each column, stored transposed.
+
+    -> (q [C,R], s [C,R/32]); row c of q is column c of X, so the copy is
+    K-contiguous when X's rows are the K axis of a later GEMM (the wgrad
+    operand).
+    """
+    return quantize_mx(x_bits, axis=0)
+
+
+def dequantize(q, s) -> np.ndarray:
+    """E4M3 bytes [R, C] with E8M0 bytes [R, C/32] -> float64 [R, C] (exact)."""
+    q = np.asarray(q, dtype=np.uint8)
+    s = np.asarray(s, dtype=np.uint8).astype(np.int64)
+    rows, n = q.shape
+    vals = e4m3_decode(q).reshape(rows, n // MX_BLOCK, MX_BLOCK)
+    scale = np.where(s == 0xFF, np.nan, np.ldexp(1.0, s - E8M0_BIAS))
+    return (vals * scale[:, :, None]).reshape(rows, n)
+
+
+# --------------------------------------------------------------------------
+# MXFP8 GEMM and epilogues
+# --------------------------------------------------------------------------
+
+
+def gelu_tanh(x) -> np.ndarray:
+    """GELU, tanh approximation: 0.5 x (1 + tanh(sqrt(2/pi) (x + 0.044715 x^3)))."""
+    x = np.asarray(x, dtype=np.float64)
+    return 0.5 * x * (1.0 + np.tanh(np.sqrt(2.0 / np.pi) * (x + 0.044715 * x ** 3)))
+
+
+def mx_gemm(qa, sa, qb, sb, bias_bits=None, gelu: bool = False):
+    """MXFP8 TN GEMM: pre = deq(A) . deq(B)^T (+ bias), then the epilogue.
+
+    qa [M,K], sa [M,K/32]; qb [N,K], sb [N,K/32] (both K-contiguous);
+    bias_bits: bf16 patterns [N] or None.
+
+    Returns a dict of float64 arrays:
+      pre   exact pre-activation (fp64 matmul of the exact dequantised operands)
+      d     bf16(pre), or bf16(gelu_tanh(pre)) when ``gelu``
+      aux   bf16(pre) when ``gelu``, else None
+      sigma sum_k |a_k b_k| (the error scale of the acceptance bound)
+    """
+    a = dequantize(qa, sa)
+    b = dequantize(qb, sb)
+    pre = a @ b.T
+    if bias_bits is not None:
+        pre = pre + bf16_bits_to_f64(bias_bits)[None, :]
+    sigma = np.abs(a) @ np.abs(b).T
+    if gelu:
+        return {"pre": pre, "d": bf16_round(gelu_tanh(pre)), "aux": bf16_round(pre), "sigma": sigma}
+    return {"pre": pre, "d": bf16_round(pre), "aux": None, "sigma": sigma}
+
+
+def mx_grouped_gemm(qx, sx, group_m, qw, sw, bias_bits=None, gelu: bool = False):
+    """Grouped MXFP8 GEMM (MoE experts): for each group g with m_g > 0,
+    D[rows of g] = epilogue(X_g . W_g^T (+ bias_g)).
+
+    qx [sum m, K], sx [sum m, K/32] hold the groups' rows back to back in group
+    order; qw [G, N, K], sw [G, N, K/32]; bias_bits [G, N] or None.  Empty
+    groups contribute nothing.  Returns dict of float64 [sum m, N] arrays as
+    ``mx_gemm`` does (aux None without gelu).
+    """
+    group_m = [int(m) for m in group_m]
+    total = sum(group_m)
+    n = qw.shape[1]
+    out = {"pre": np.zeros((total, n)), "d": np.zeros((total, n)),
+           "aux": np.zeros((total, n)) if gelu else None, "sigma": np.zeros((total, n))}
+    row = 0
+    for g, m in enumerate(group_m):
+        if m == 0:
+            continue
+        bias = None if bias_bits is None else bias_bits[g]
+        r = mx_gemm(qx[row:row + m], sx[row:row + m], qw[g], sw[g], bias, gelu)
+        for key in ("pre", "d", "sigma"):
+            out[key][row:row + m] = r[key]
+        if gelu:
+            out["aux"][row:row + m] = r["aux"]
+        row += m
+    return out
+
+
+# --------------------------------------------------------------------------
+# Acceptance bound
+# --------------------------------------------------------------------------
+
+REL_TOL = 2.0 ** -7
+SIGMA_TOL = 1e-5
+
+
+def gemm_error_bound(ref, sigma) -> np.ndarray:
+    """Per-element bound |gpu - ref| <= 2^-7 |ref| + 1e-5 sum_k |a_k b_k|."""
+    return REL_TOL * np.abs(ref) + SIGMA_TOL * np.asarray(sigma)

@@ -1,0 +1,102 @@
+"""Planted mistakes: break the oracle in a plausible way and check that a pin fails.
+
+Each test patches one piece of the oracle (on the CPU, for the duration of
+the test) and runs an existing pin, which must now raise AssertionError.
+"""
+import numpy as np
+import pytest
+
+from oracle import mx_oracle as O
+from tests import test_oracle_gemm as G
+from tests import test_oracle_quantize as Q
+
+
+def run_all_golden():
+    for blk in Q.parse_golden():
+        Q.test_golden_block_rowwise(blk)
+        Q.test_golden_block_colwise(blk)
+
+
+def test_golden_pins_pass_unpatched():
+    run_all_golden()
+
+
+def test_wrong_emax_is_caught(monkeypatch):
+    monkeypatch.setattr(O, "E4M3_EMAX", 7)
+    with pytest.raises(AssertionError):
+        run_all_golden()
+    with pytest.raises(AssertionError):
+        Q.test_scale_rule_exhaustive_against_brute_force()
+
+
+def test_ties_away_from_zero_is_caught(monkeypatch):
+    def round_half_away(v, mant_bits, emin):
+        v = np.asarray(v, dtype=np.float64)
+        _, p = np.frexp(v)
+        quantum = np.ldexp(1.0, np.maximum(p - 1, emin) - mant_bits)
+        return np.sign(v) * np.floor(np.abs(v) / quantum + 0.5) * quantum
+    monkeypatch.setattr(O, "round_to_binary_format", round_half_away)
+    with pytest.raises(AssertionError):
+        Q.test_e4m3_encode_equals_brute_force_nearest()
+    with pytest.raises(AssertionError):
+        run_all_golden()
+
+
+def test_lost_sign_of_zero_is_caught(monkeypatch):
+    orig = O.e4m3_encode_value
+    monkeypatch.setattr(O, "e4m3_encode_value", lambda r: orig(np.where(np.asarray(r) == 0, 0.0, r)))
+    with pytest.raises(AssertionError):
+        run_all_golden()
+    with pytest.raises(AssertionError):
+        Q.test_e4m3_encode_matches_library_saturating_cast()
+
+
+def test_scale_with_wrong_sign_is_caught(monkeypatch):
+    orig = O.mx_scale_exponent
+    monkeypatch.setattr(O, "mx_scale_exponent", lambda a: -orig(a))
+    with pytest.raises(AssertionError):
+        run_all_golden()
+
+
+def test_no_saturation_is_caught(monkeypatch):
+    monkeypatch.setattr(O, "E4M3_MAX", 1e9)
+    with pytest.raises(AssertionError):
+        run_all_golden()
+
+
+def test_wrong_scale_block_index_is_caught(monkeypatch):
+    def bad_dequantize(q, s):
+        q = np.asarray(q, dtype=np.uint8)
+        s = np.asarray(s, dtype=np.uint8).astype(np.int64)
+        scale = np.tile(np.ldexp(1.0, s - 127), (1, 32))        # k % nblocks instead of k // 32
+        return O.e4m3_decode(q) * scale
+    monkeypatch.setattr(O, "dequantize", bad_dequantize)
+    with pytest.raises(AssertionError):
+        G.test_tiny_gemm_exact_rational(8, 24, 64)
+
+
+def test_dropped_bias_is_caught(monkeypatch):
+    orig = O.mx_gemm
+    monkeypatch.setattr(O, "mx_gemm", lambda qa, sa, qb, sb, bias=None, gelu=False: orig(qa, sa, qb, sb, None, gelu))
+    with pytest.raises(AssertionError):
+        G.test_tiny_gemm_exact_rational(16, 16, 32)
+
+
+def test_transposed_b_is_caught(monkeypatch):
+    orig_deq = O.dequantize
+    calls = {"n": 0}
+
+    def deq_second_transposed(q, s):
+        calls["n"] += 1
+        d = orig_deq(q, s)
+        return d[::-1] if calls["n"] % 2 == 0 else d        # B's rows in the wrong order
+    monkeypatch.setattr(O, "dequantize", deq_second_transposed)
+    with pytest.raises(AssertionError):
+        G.test_transposed_operands_are_distinguished()
+
+
+def test_wrong_gelu_constant_is_caught(monkeypatch):
+    monkeypatch.setattr(O, "gelu_tanh",
+                        lambda x: 0.5 * x * (1 + np.tanh(np.sqrt(2 / np.pi) * (x + 0.0447 * x ** 3))))
+    with pytest.raises(AssertionError):
+        G.test_gelu_matches_library_and_identities()
