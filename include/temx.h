@@ -1,0 +1,169 @@
+/*
+ * temx — MXFP8 block-scaled quantisation and MXFP8 GEMM for GB300 (sm_103a).
+ *
+ * C ABI of libtemx.so.  Plain pointers and sizes only; every device buffer and
+ * the stream belong to the caller.  Calls are asynchronous on `stream` (a
+ * cudaStream_t passed as void*; NULL = the legacy default stream).  No call
+ * allocates device memory.
+ *
+ * Definitions the calls implement
+ * -------------------------------
+ * MXFP8 ("MXFP8 1D scaling", named in "HipKittens MXFP8 GEMM Support",
+ * ROCm/TransformerEngine PR #566, review thread; "E8M0 (power-of-2)" scales,
+ * ROCm/TransformerEngine README, "Blockwise FP8 GEMM support on ROCm"):
+ * every 32 consecutive elements along the quantised axis share one E8M0
+ * scale byte s = e + 127 with e = floor(log2 amax) - 8, clamped to
+ * [-127, 127] (OCP Microscaling Formats v1.0, FP32 -> MX conversion; amax = 0
+ * gives s = 0x00).  Each element becomes the E4M3 byte of x * 2^-e, rounded
+ * to nearest-even and saturated to +-448; a negative value that rounds to
+ * zero keeps its sign (0x80).  A block holding a NaN or an infinity gives
+ * s = 0xFF and every element 0x7F.
+ *
+ * Layouts
+ * -------
+ * Matrices are row-major.  A scale matrix for data [R x C] quantised along C
+ * is uint8 [R x ld_s] whose first C/32 bytes per row hold the scales; ld_s
+ * must be a multiple of 16 and >= C/32 (te_mx_scale_pitch gives the
+ * smallest).  Bytes past C/32 in a row are never written or read.
+ *
+ * Errors
+ * ------
+ * Every call validates its arguments on the host and returns a status before
+ * launching anything; te_mx_last_error() then holds a message (per thread).
+ * Kernels bound every wait; a wait that runs out sets a device status word
+ * that te_mx_device_status() reports (TE_MX_ERR_DEVICE_TIMEOUT).
+ */
+#ifndef TEMX_H
+#define TEMX_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#if defined(__GNUC__)
+#define TEMX_API __attribute__((visibility("default")))
+#else
+#define TEMX_API
+#endif
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum te_mx_status {
+    TE_MX_OK = 0,
+    TE_MX_ERR_INVALID_ARG = 1,       /* NULL where a buffer is required, negative size, bad enum */
+    TE_MX_ERR_UNSUPPORTED_SHAPE = 2, /* a size rule below is broken */
+    TE_MX_ERR_MISALIGNED = 3,        /* a pointer or pitch breaks its alignment rule */
+    TE_MX_ERR_WORKSPACE_TOO_SMALL = 4,
+    TE_MX_ERR_CUDA = 5,              /* a CUDA runtime/driver call failed (message has the name) */
+    TE_MX_ERR_DEVICE_TIMEOUT = 6,    /* a kernel gave up a bounded wait */
+    TE_MX_ERR_ARCH = 7               /* the current device is not sm_103 */
+} te_mx_status;
+
+/* GEMM epilogues ("BIAS and GELU AUX", HipKittens MXFP8 GEMM Support, PR
+ * description).  With bias: pre = acc + bias[n].  Without GELU: D = bf16(pre).
+ * With GELU: AUX = bf16(pre), D = bf16(0.5 pre (1 + tanh(sqrt(2/pi)(pre +
+ * 0.044715 pre^3)))) computed from the fp32 pre-activation. */
+typedef enum te_mx_epilogue {
+    TE_MX_EPI_NONE = 0,
+    TE_MX_EPI_BIAS = 1,
+    TE_MX_EPI_GELU_AUX = 2,
+    TE_MX_EPI_BIAS_GELU_AUX = 3
+} te_mx_epilogue;
+
+/* Smallest legal scale pitch for k quantised elements per row:
+ * round_up(k/32, 16) bytes. */
+TEMX_API size_t te_mx_scale_pitch(int64_t k);
+
+/* te_mx_quantize — MXFP8-quantise a bf16 matrix row-wise and/or column-wise in
+ * one pass over HBM (MXFP8 1D scaling; the column-wise copy is the transposed
+ * operand the wgrad GEMM consumes, cf. the cast_transpose kernels of
+ * ROCm/TransformerEngine README, "Experimental Triton Kernels on ROCm").
+ *
+ *   x       bf16 [rows x cols], row pitch ld_x elements (device).
+ *   q_row   uint8 [rows x cols] (pitch cols), E4M3 codes, blocks along a row;
+ *   s_row   uint8 [rows x ld_s_row] E8M0 bytes, s_row[r][j] scales
+ *           q_row[r][32j .. 32j+31].  Both NULL: row-wise output skipped.
+ *   q_col   uint8 [cols x rows] (pitch rows): q_col[c][r] is X[r][c], blocks of
+ *           32 consecutive rows of one column, i.e. the transpose quantised
+ *           along its rows;
+ *   s_col   uint8 [cols x ld_s_col], s_col[c][i] scales q_col[c][32i .. 32i+31].
+ *           Both NULL: column-wise output skipped.
+ * Rules: cols % 32 == 0; rows % 32 == 0 when q_col is given; rows, cols >= 0
+ * (0 is a no-op); x 16-byte aligned and ld_x % 8 == 0, ld_x >= cols; q_row,
+ * q_col 16-byte aligned; ld_s_* multiples of 16 and >= the block count.
+ * Output is bit-exact to the definition above. */
+TEMX_API te_mx_status te_mx_quantize(const void* x, int64_t rows, int64_t cols, int64_t ld_x,
+                            uint8_t* q_row, uint8_t* s_row, int64_t ld_s_row,
+                            uint8_t* q_col, uint8_t* s_col, int64_t ld_s_col,
+                            void* stream);
+
+/* te_mx_gemm — MXFP8 TN GEMM with fused epilogue (HipKittens MXFP8 GEMM
+ * Support, PR description: MXFP8 GEMM with BIAS and GELU AUX epilogues; the
+ * review thread's TN layout and its K % 128 rule for MXFP8 scaling):
+ *   acc[m][n] = sum_k (A[m][k] 2^(sA[m][k/32]-127)) (B[n][k] 2^(sB[n][k/32]-127)),
+ * accumulated in fp32 on the tensor cores, then the epilogue above.
+ *
+ *   A  uint8 E4M3 [M x K] (pitch K), sA uint8 [M x ld_sA];
+ *   B  uint8 E4M3 [N x K] (pitch K), sB uint8 [N x ld_sB]  (both K-contiguous);
+ *   bias  bf16 [N] or NULL (required for the *_BIAS* epilogues);
+ *   D     bf16 [M x N] (pitch N);  aux bf16 [M x N], required for GELU_AUX
+ *         epilogues, else ignored.
+ *   workspace / workspace_bytes: reserved; te_mx_gemm_workspace_size() is 0
+ *         and NULL/0 may be passed.
+ * Rules: K % 128 == 0, K >= 128; M, N >= 1 with N % 16 == 0 (M arbitrary);
+ * A, B, sA, sB, D, aux 16-byte aligned; ld_s* multiples of 16 >= K/32.
+ * Accuracy: |D - exact| <= 2^-7 |exact| + 1e-5 sum_k |a_k b_k| element-wise,
+ * exact = the epilogue of the fp64 product of the dequantised operands. */
+TEMX_API te_mx_status te_mx_gemm(const uint8_t* A, const uint8_t* sA, int64_t ld_sA,
+                        const uint8_t* B, const uint8_t* sB, int64_t ld_sB,
+                        int64_t M, int64_t N, int64_t K,
+                        const void* bias, int32_t epilogue,
+                        void* D, void* aux,
+                        void* workspace, size_t workspace_bytes,
+                        void* stream);
+
+/* te_mx_grouped_gemm — one launch over G groups (MoE experts) of the same
+ * GEMM ("Single-Launch Grouped GEMM Backends on ROCm", ROCm/TransformerEngine
+ * README; MXFP8 grouped GEMM), with ragged and possibly empty groups:
+ *   for g with m_g > 0: D[rows of g] = epilogue(X[rows of g] . W[g]^T + bias[g]).
+ *
+ *   group_m  int32 [G] on the DEVICE (as routing produces it), m_g >= 0;
+ *            group g owns rows [sum_{h<g} m_h, sum_{h<=g} m_h) of X, D, aux.
+ *   total_m  host upper bound on sum m_g: the row count of X, sX, D, aux.
+ *   X  uint8 [total_m x K], sX uint8 [total_m x ld_sX];
+ *   W  uint8 [G x N x K], sW uint8 [G*N x ld_sW] (group g's scales are rows
+ *      g*N .. g*N+N-1);  bias bf16 [G x N] or NULL.
+ * Rows past sum m_g are not written.  If sum m_g > total_m the call writes
+ * nothing past total_m and te_mx_device_status() reports TE_MX_ERR_INVALID_ARG.
+ * Rules as te_mx_gemm, plus 1 <= G <= 1024. */
+TEMX_API te_mx_status te_mx_grouped_gemm(int32_t num_groups, const int32_t* group_m, int64_t total_m,
+                                const uint8_t* X, const uint8_t* sX, int64_t ld_sX,
+                                const uint8_t* W, const uint8_t* sW, int64_t ld_sW,
+                                int64_t N, int64_t K,
+                                const void* bias, int32_t epilogue,
+                                void* D, void* aux,
+                                void* workspace, size_t workspace_bytes,
+                                void* stream);
+
+/* Workspace bytes te_mx_gemm / te_mx_grouped_gemm need: 0 for every shape
+ * (scale re-layout happens in shared memory; kept so a future layout change
+ * does not break the ABI). */
+TEMX_API size_t te_mx_gemm_workspace_size(int64_t M, int64_t N, int64_t K, int32_t num_groups);
+
+/* Synchronises the current device, returns and clears the device status word
+ * the kernels set (TE_MX_OK, TE_MX_ERR_DEVICE_TIMEOUT or
+ * TE_MX_ERR_INVALID_ARG), or TE_MX_ERR_CUDA if the synchronise fails. */
+TEMX_API te_mx_status te_mx_device_status(void);
+
+/* Message for the last non-OK status returned on this thread ("" if none). */
+TEMX_API const char* te_mx_last_error(void);
+
+/* Library version string. */
+TEMX_API const char* te_mx_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* TEMX_H */

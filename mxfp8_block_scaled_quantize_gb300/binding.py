@@ -1,0 +1,167 @@
+"""ctypes binding to libtemx.so (argument marshalling only).
+
+The ``te_mx_*`` functions take raw integer pointers and mirror include/temx.h;
+they raise ``TemxError`` on any status other than TE_MX_OK.  The torch-level
+helpers (``quantize``, ``gemm``, ``grouped_gemm``) only allocate outputs with
+torch and pass ``data_ptr()`` and the current stream; every step of the
+computation runs in the library's CUDA kernels.  There is no fallback: if the
+library cannot be loaded, every call raises.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+
+PKG = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(PKG, "libtemx.so")
+
+TE_MX_OK = 0
+STATUS_NAMES = {0: "TE_MX_OK", 1: "TE_MX_ERR_INVALID_ARG", 2: "TE_MX_ERR_UNSUPPORTED_SHAPE",
+                3: "TE_MX_ERR_MISALIGNED", 4: "TE_MX_ERR_WORKSPACE_TOO_SMALL", 5: "TE_MX_ERR_CUDA",
+                6: "TE_MX_ERR_DEVICE_TIMEOUT", 7: "TE_MX_ERR_ARCH"}
+EPI_NONE, EPI_BIAS, EPI_GELU_AUX, EPI_BIAS_GELU_AUX = 0, 1, 2, 3
+
+# (name, restype, argtypes) for every function declared in include/temx.h
+_I64, _I32, _P, _SZ = ctypes.c_int64, ctypes.c_int32, ctypes.c_void_p, ctypes.c_size_t
+SIGNATURES = {
+    "te_mx_scale_pitch": (_SZ, [_I64]),
+    "te_mx_quantize": (ctypes.c_int, [_P, _I64, _I64, _I64, _P, _P, _I64, _P, _P, _I64, _P]),
+    "te_mx_gemm": (ctypes.c_int, [_P, _P, _I64, _P, _P, _I64, _I64, _I64, _I64, _P, _I32, _P, _P, _P, _SZ, _P]),
+    "te_mx_grouped_gemm": (ctypes.c_int, [_I32, _P, _I64, _P, _P, _I64, _P, _P, _I64, _I64, _I64, _P, _I32,
+                                          _P, _P, _P, _SZ, _P]),
+    "te_mx_gemm_workspace_size": (_SZ, [_I64, _I64, _I64, _I32]),
+    "te_mx_device_status": (ctypes.c_int, []),
+    "te_mx_last_error": (ctypes.c_char_p, []),
+    "te_mx_version": (ctypes.c_char_p, []),
+}
+
+
+class TemxError(RuntimeError):
+    def __init__(self, status: int, message: str):
+        super().__init__(f"{STATUS_NAMES.get(status, status)}: {message}")
+        self.status = status
+
+
+_lib = None
+
+
+def lib() -> ctypes.CDLL:
+    """Load libtemx.so (built in-tree by ``_build.build()``); raises if missing."""
+    global _lib
+    if _lib is None:
+        if not os.path.exists(LIB_PATH):
+            raise ImportError(f"{LIB_PATH} is missing: build it with "
+                              "`python -m mxfp8_block_scaled_quantize_gb300._build`")
+        l = ctypes.CDLL(LIB_PATH)
+        for name, (res, args) in SIGNATURES.items():
+            f = getattr(l, name)
+            f.restype, f.argtypes = res, args
+        _lib = l
+    return _lib
+
+
+def _check(status: int) -> None:
+    if status != TE_MX_OK:
+        raise TemxError(status, lib().te_mx_last_error().decode())
+
+
+# ---------------------------------------------------------------- raw C ABI
+
+def te_mx_scale_pitch(k: int) -> int:
+    return lib().te_mx_scale_pitch(k)
+
+
+def te_mx_quantize(x, rows, cols, ld_x, q_row, s_row, ld_s_row, q_col, s_col, ld_s_col, stream) -> None:
+    _check(lib().te_mx_quantize(x, rows, cols, ld_x, q_row, s_row, ld_s_row, q_col, s_col, ld_s_col, stream))
+
+
+def te_mx_gemm(A, sA, ld_sA, B, sB, ld_sB, M, N, K, bias, epilogue, D, aux, workspace, workspace_bytes,
+               stream) -> None:
+    _check(lib().te_mx_gemm(A, sA, ld_sA, B, sB, ld_sB, M, N, K, bias, epilogue, D, aux, workspace,
+                            workspace_bytes, stream))
+
+
+def te_mx_grouped_gemm(num_groups, group_m, total_m, X, sX, ld_sX, W, sW, ld_sW, N, K, bias, epilogue, D, aux,
+                       workspace, workspace_bytes, stream) -> None:
+    _check(lib().te_mx_grouped_gemm(num_groups, group_m, total_m, X, sX, ld_sX, W, sW, ld_sW, N, K, bias,
+                                    epilogue, D, aux, workspace, workspace_bytes, stream))
+
+
+def te_mx_gemm_workspace_size(M, N, K, num_groups=0) -> int:
+    return lib().te_mx_gemm_workspace_size(M, N, K, num_groups)
+
+
+def te_mx_device_status() -> None:
+    _check(lib().te_mx_device_status())
+
+
+def te_mx_version() -> str:
+    return lib().te_mx_version().decode()
+
+
+# ---------------------------------------------------------------- torch helpers
+
+def _stream_ptr(stream=None) -> int:
+    import torch
+    s = stream if stream is not None else torch.cuda.current_stream()
+    return s.cuda_stream
+
+
+def _ptr(t) -> int:
+    return 0 if t is None else t.data_ptr()
+
+
+def quantize(x, rowwise: bool = True, colwise: bool = False, stream=None, out=None):
+    """MXFP8-quantise a 2-D bf16 CUDA tensor.  Returns a dict with q_row
+    [R,C], s_row [R, pitch(C)] and/or q_col [C,R], s_col [C, pitch(R)] (uint8)."""
+    import torch
+    assert x.dtype == torch.bfloat16 and x.dim() == 2 and x.is_cuda
+    rows, cols = x.shape
+    assert x.stride(1) == 1
+    o = dict(out or {})
+    if rowwise and "q_row" not in o:
+        o["q_row"] = torch.empty(rows, cols, dtype=torch.uint8, device=x.device)
+        o["s_row"] = torch.empty(rows, te_mx_scale_pitch(cols), dtype=torch.uint8, device=x.device)
+    if colwise and "q_col" not in o:
+        o["q_col"] = torch.empty(cols, rows, dtype=torch.uint8, device=x.device)
+        o["s_col"] = torch.empty(cols, te_mx_scale_pitch(rows), dtype=torch.uint8, device=x.device)
+    te_mx_quantize(x.data_ptr(), rows, cols, x.stride(0),
+                   _ptr(o.get("q_row")), _ptr(o.get("s_row")), o["s_row"].stride(0) if "s_row" in o else 0,
+                   _ptr(o.get("q_col")), _ptr(o.get("s_col")), o["s_col"].stride(0) if "s_col" in o else 0,
+                   _stream_ptr(stream))
+    return o
+
+
+def gemm(qa, sa, qb, sb, bias=None, gelu: bool = False, stream=None, out=None):
+    """D = epilogue(deq(qa) . deq(qb)^T (+ bias)) in bf16; returns (D, aux or None)."""
+    import torch
+    M, K = qa.shape
+    N = qb.shape[0]
+    epi = (EPI_BIAS if bias is not None else EPI_NONE) + (EPI_GELU_AUX if gelu else 0)
+    if out is None:
+        d = torch.empty(M, N, dtype=torch.bfloat16, device=qa.device)
+        aux = torch.empty(M, N, dtype=torch.bfloat16, device=qa.device) if gelu else None
+    else:
+        d, aux = out
+    te_mx_gemm(qa.data_ptr(), sa.data_ptr(), sa.stride(0), qb.data_ptr(), sb.data_ptr(), sb.stride(0),
+               M, N, K, _ptr(bias), epi, d.data_ptr(), _ptr(aux), 0, 0, _stream_ptr(stream))
+    return d, aux
+
+
+def grouped_gemm(group_m, qx, sx, qw, sw, bias=None, gelu: bool = False, stream=None, out=None):
+    """Grouped GEMM over experts: group_m int32 [G] on the device, qx [total_m, K],
+    qw [G, N, K], sw [G*N, pitch]; returns (D, aux or None) of [total_m, N]."""
+    import torch
+    total_m, K = qx.shape
+    G, N, _ = qw.shape
+    epi = (EPI_BIAS if bias is not None else EPI_NONE) + (EPI_GELU_AUX if gelu else 0)
+    if out is None:
+        d = torch.empty(total_m, N, dtype=torch.bfloat16, device=qx.device)
+        aux = torch.empty(total_m, N, dtype=torch.bfloat16, device=qx.device) if gelu else None
+    else:
+        d, aux = out
+    sw2 = sw.reshape(G * N, -1)
+    te_mx_grouped_gemm(G, group_m.data_ptr(), total_m, qx.data_ptr(), sx.data_ptr(), sx.stride(0),
+                       qw.data_ptr(), sw2.data_ptr(), sw2.stride(0), N, K, _ptr(bias), epi,
+                       d.data_ptr(), _ptr(aux), 0, 0, _stream_ptr(stream))
+    return d, aux

@@ -1,0 +1,289 @@
+// C ABI of libtemx.so: argument validation, device checks, tensor-map
+// encoding and status reporting.  The kernels live in quantize.cu / gemm.cu.
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include <cstdarg>
+#include <cstdio>
+#include <mutex>
+
+#include "ptx.cuh"
+#include "temx_internal.h"
+
+namespace temx {
+
+// Device status word: kernels record a bounded wait that gave up here.
+__device__ unsigned int g_device_status = 0;
+
+namespace {
+
+thread_local char t_last_error[512] = "";
+
+constexpr int kMaxDevices = 64;
+int g_sm_count[kMaxDevices];     // 0 = not queried yet
+int g_arch[kMaxDevices];         // major * 10 + minor
+unsigned int* g_status_ptr[kMaxDevices];
+std::mutex g_dev_mutex;
+
+using EncodeTiledFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
+                                   const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
+                                   const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                   CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+EncodeTiledFn g_encode = nullptr;
+std::once_flag g_encode_once;
+cudaError_t g_encode_err = cudaSuccess;
+
+te_mx_status get_encode(EncodeTiledFn* fn) {
+    std::call_once(g_encode_once, [] {
+        void* p = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        g_encode_err = cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000,
+                                                        cudaEnableDefault, &q);
+        if (g_encode_err == cudaSuccess && q == cudaDriverEntryPointSuccess)
+            g_encode = reinterpret_cast<EncodeTiledFn>(p);
+    });
+    if (!g_encode)
+        return set_error(TE_MX_ERR_CUDA, "cuTensorMapEncodeTiled unavailable (%s)",
+                         cudaGetErrorString(g_encode_err));
+    *fn = g_encode;
+    return TE_MX_OK;
+}
+
+// Current device must be sm_103 (the library is built for sm_103a only).
+te_mx_status check_device(int* dev_out) {
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return cuda_status(e, "cudaGetDevice");
+    if (dev < 0 || dev >= kMaxDevices) return set_error(TE_MX_ERR_CUDA, "device index %d out of range", dev);
+    std::lock_guard<std::mutex> lock(g_dev_mutex);
+    if (g_sm_count[dev] == 0) {
+        int major = 0, minor = 0, sms = 0;
+        if ((e = cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev)) != cudaSuccess ||
+            (e = cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev)) != cudaSuccess ||
+            (e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess)
+            return cuda_status(e, "cudaDeviceGetAttribute");
+        g_arch[dev] = major * 10 + minor;
+        void* sp = nullptr;
+        if (g_arch[dev] == 103 && (e = cudaGetSymbolAddress(&sp, g_device_status)) != cudaSuccess)
+            return cuda_status(e, "cudaGetSymbolAddress(status word)");
+        g_status_ptr[dev] = static_cast<unsigned int*>(sp);
+        g_sm_count[dev] = sms;
+    }
+    if (g_arch[dev] != 103)
+        return set_error(TE_MX_ERR_ARCH, "device %d is sm_%d; libtemx is built for sm_103a only", dev, g_arch[dev]);
+    if (dev_out) *dev_out = dev;
+    return TE_MX_OK;
+}
+
+bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+
+}  // namespace
+
+te_mx_status set_error(te_mx_status st, const char* fmt, ...) {
+    va_list ap;
+    va_start(ap, fmt);
+    vsnprintf(t_last_error, sizeof(t_last_error), fmt, ap);
+    va_end(ap);
+    return st;
+}
+
+te_mx_status cuda_status(cudaError_t e, const char* what) {
+    if (e == cudaSuccess) return TE_MX_OK;
+    if (e == cudaErrorNoKernelImageForDevice)
+        return set_error(TE_MX_ERR_ARCH, "%s: %s", what, cudaGetErrorString(e));
+    return set_error(TE_MX_ERR_CUDA, "%s: %s", what, cudaGetErrorString(e));
+}
+
+te_mx_status device_sm_count(int* sms) {
+    int dev = 0;
+    te_mx_status st = check_device(&dev);
+    if (st != TE_MX_OK) return st;
+    *sms = g_sm_count[dev];
+    return TE_MX_OK;
+}
+
+te_mx_status device_status_ptr(unsigned int** ptr) {
+    int dev = 0;
+    te_mx_status st = check_device(&dev);
+    if (st != TE_MX_OK) return st;
+    *ptr = g_status_ptr[dev];
+    return TE_MX_OK;
+}
+
+te_mx_status encode_tensor_map_2d(CUtensorMap* map, CUtensorMapDataType dtype, const void* base,
+                                  uint64_t dim0, uint64_t dim1, uint64_t stride1_bytes,
+                                  uint32_t box0, uint32_t box1, CUtensorMapSwizzle swizzle) {
+    EncodeTiledFn fn;
+    te_mx_status st = get_encode(&fn);
+    if (st != TE_MX_OK) return st;
+    const cuuint64_t dims[2] = {dim0, dim1};
+    const cuuint64_t strides[1] = {stride1_bytes};
+    const cuuint32_t box[2] = {box0, box1};
+    const cuuint32_t estr[2] = {1, 1};
+    CUresult r = fn(map, dtype, 2, const_cast<void*>(base), dims, strides, box, estr,
+                    CU_TENSOR_MAP_INTERLEAVE_NONE, swizzle, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                    CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    if (r != CUDA_SUCCESS)
+        return set_error(TE_MX_ERR_CUDA, "cuTensorMapEncodeTiled(2d) failed with %d (dims %llu x %llu, stride %llu)",
+                         int(r), (unsigned long long)dim0, (unsigned long long)dim1,
+                         (unsigned long long)stride1_bytes);
+    return TE_MX_OK;
+}
+
+te_mx_status encode_tensor_map_3d(CUtensorMap* map, CUtensorMapDataType dtype, const void* base,
+                                  uint64_t dim0, uint64_t dim1, uint64_t dim2,
+                                  uint64_t stride1_bytes, uint64_t stride2_bytes,
+                                  uint32_t box0, uint32_t box1, uint32_t box2,
+                                  CUtensorMapSwizzle swizzle) {
+    EncodeTiledFn fn;
+    te_mx_status st = get_encode(&fn);
+    if (st != TE_MX_OK) return st;
+    const cuuint64_t dims[3] = {dim0, dim1, dim2};
+    const cuuint64_t strides[2] = {stride1_bytes, stride2_bytes};
+    const cuuint32_t box[3] = {box0, box1, box2};
+    const cuuint32_t estr[3] = {1, 1, 1};
+    CUresult r = fn(map, dtype, 3, const_cast<void*>(base), dims, strides, box, estr,
+                    CU_TENSOR_MAP_INTERLEAVE_NONE, swizzle, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                    CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    if (r != CUDA_SUCCESS)
+        return set_error(TE_MX_ERR_CUDA, "cuTensorMapEncodeTiled(3d) failed with %d", int(r));
+    return TE_MX_OK;
+}
+
+}  // namespace temx
+
+using namespace temx;
+
+extern "C" {
+
+size_t te_mx_scale_pitch(int64_t k) {
+    if (k <= 0) return 0;
+    const int64_t blocks = (k + 31) / 32;
+    return size_t((blocks + 15) / 16 * 16);
+}
+
+const char* te_mx_last_error(void) { return t_last_error; }
+
+const char* te_mx_version(void) { return "temx 0.1 (sm_103a)"; }
+
+te_mx_status te_mx_quantize(const void* x, int64_t rows, int64_t cols, int64_t ld_x,
+                            uint8_t* q_row, uint8_t* s_row, int64_t ld_s_row,
+                            uint8_t* q_col, uint8_t* s_col, int64_t ld_s_col, void* stream) {
+    t_last_error[0] = '\0';
+    if (rows < 0 || cols < 0) return set_error(TE_MX_ERR_INVALID_ARG, "negative size %lld x %lld", (long long)rows, (long long)cols);
+    if ((q_row == nullptr) != (s_row == nullptr))
+        return set_error(TE_MX_ERR_INVALID_ARG, "q_row and s_row must both be given or both be NULL");
+    if ((q_col == nullptr) != (s_col == nullptr))
+        return set_error(TE_MX_ERR_INVALID_ARG, "q_col and s_col must both be given or both be NULL");
+    if (rows == 0 || cols == 0 || (!q_row && !q_col)) return TE_MX_OK;
+    if (!x) return set_error(TE_MX_ERR_INVALID_ARG, "x is NULL");
+    if (cols % 32) return set_error(TE_MX_ERR_UNSUPPORTED_SHAPE, "cols=%lld is not a multiple of 32", (long long)cols);
+    if (q_col && rows % 32)
+        return set_error(TE_MX_ERR_UNSUPPORTED_SHAPE, "column-wise output needs rows %% 32 == 0 (rows=%lld)", (long long)rows);
+    if (rows > (int64_t(1) << 31) - 64 || cols > (int64_t(1) << 31) - 64)
+        return set_error(TE_MX_ERR_UNSUPPORTED_SHAPE, "a dimension exceeds 2^31 - 64");
+    if (ld_x < cols || ld_x % 8) return set_error(TE_MX_ERR_MISALIGNED, "ld_x=%lld must be >= cols and a multiple of 8", (long long)ld_x);
+    if (!aligned(x, 16)) return set_error(TE_MX_ERR_MISALIGNED, "x is not 16-byte aligned");
+    if (q_row) {
+        if (!aligned(q_row, 16)) return set_error(TE_MX_ERR_MISALIGNED, "q_row is not 16-byte aligned");
+        if (ld_s_row % 16 || ld_s_row < cols / 32)
+            return set_error(TE_MX_ERR_MISALIGNED, "ld_s_row=%lld must be a multiple of 16 and >= cols/32", (long long)ld_s_row);
+    }
+    if (q_col) {
+        if (!aligned(q_col, 16)) return set_error(TE_MX_ERR_MISALIGNED, "q_col is not 16-byte aligned");
+        if (ld_s_col % 16 || ld_s_col < rows / 32)
+            return set_error(TE_MX_ERR_MISALIGNED, "ld_s_col=%lld must be a multiple of 16 and >= rows/32", (long long)ld_s_col);
+    }
+    te_mx_status st = check_device(nullptr);
+    if (st != TE_MX_OK) return st;
+    QuantizeArgs a{x, rows, cols, ld_x, q_row, s_row, ld_s_row, q_col, s_col, ld_s_col};
+    return quantize_launch(a, static_cast<cudaStream_t>(stream));
+}
+
+static te_mx_status validate_gemm_common(const uint8_t* A, const uint8_t* sA, int64_t ld_sA,
+                                         const uint8_t* B, const uint8_t* sB, int64_t ld_sB,
+                                         int64_t N, int64_t K, const void* bias, int32_t epi,
+                                         void* D, void* aux) {
+    if (epi < TE_MX_EPI_NONE || epi > TE_MX_EPI_BIAS_GELU_AUX)
+        return set_error(TE_MX_ERR_INVALID_ARG, "unknown epilogue %d", epi);
+    if (!A || !sA || !B || !sB || !D) return set_error(TE_MX_ERR_INVALID_ARG, "A, sA, B, sB and D are required");
+    const bool has_bias = epi == TE_MX_EPI_BIAS || epi == TE_MX_EPI_BIAS_GELU_AUX;
+    const bool gelu = epi == TE_MX_EPI_GELU_AUX || epi == TE_MX_EPI_BIAS_GELU_AUX;
+    if (has_bias && !bias) return set_error(TE_MX_ERR_INVALID_ARG, "bias epilogue without a bias pointer");
+    if (gelu && !aux) return set_error(TE_MX_ERR_INVALID_ARG, "GELU_AUX epilogue without an aux pointer");
+    if (K < 128 || K % 128) return set_error(TE_MX_ERR_UNSUPPORTED_SHAPE, "K=%lld must be a positive multiple of 128", (long long)K);
+    if (N < 16 || N % 16) return set_error(TE_MX_ERR_UNSUPPORTED_SHAPE, "N=%lld must be a positive multiple of 16", (long long)N);
+    if (K > (int64_t(1) << 30) || N > (int64_t(1) << 30)) return set_error(TE_MX_ERR_UNSUPPORTED_SHAPE, "N or K too large");
+    if (ld_sA % 16 || ld_sA < K / 32 || ld_sB % 16 || ld_sB < K / 32)
+        return set_error(TE_MX_ERR_MISALIGNED, "scale pitches must be multiples of 16 and >= K/32");
+    if (!aligned(A, 16) || !aligned(B, 16) || !aligned(sA, 16) || !aligned(sB, 16) || !aligned(D, 16) ||
+        (gelu && !aligned(aux, 16)) || (has_bias && !aligned(bias, 16)))
+        return set_error(TE_MX_ERR_MISALIGNED, "A, B, sA, sB, D, aux and bias must be 16-byte aligned");
+    return TE_MX_OK;
+}
+
+te_mx_status te_mx_gemm(const uint8_t* A, const uint8_t* sA, int64_t ld_sA,
+                        const uint8_t* B, const uint8_t* sB, int64_t ld_sB,
+                        int64_t M, int64_t N, int64_t K, const void* bias, int32_t epilogue,
+                        void* D, void* aux, void* workspace, size_t workspace_bytes, void* stream) {
+    (void)workspace; (void)workspace_bytes;
+    t_last_error[0] = '\0';
+    if (M < 0) return set_error(TE_MX_ERR_INVALID_ARG, "negative M");
+    if (M == 0) return TE_MX_OK;
+    if (M > (int64_t(1) << 31) - 256) return set_error(TE_MX_ERR_UNSUPPORTED_SHAPE, "M too large");
+    te_mx_status st = validate_gemm_common(A, sA, ld_sA, B, sB, ld_sB, N, K, bias, epilogue, D, aux);
+    if (st != TE_MX_OK) return st;
+    if ((st = check_device(nullptr)) != TE_MX_OK) return st;
+    GemmArgs a{};
+    a.A = A; a.sA = sA; a.ld_sA = ld_sA; a.B = B; a.sB = sB; a.ld_sB = ld_sB;
+    a.M = M; a.N = N; a.K = K; a.bias = bias;
+    a.has_bias = epilogue == TE_MX_EPI_BIAS || epilogue == TE_MX_EPI_BIAS_GELU_AUX;
+    a.gelu = epilogue == TE_MX_EPI_GELU_AUX || epilogue == TE_MX_EPI_BIAS_GELU_AUX;
+    a.D = D; a.aux = aux; a.groups = 0; a.group_m = nullptr;
+    return gemm_launch(a, static_cast<cudaStream_t>(stream));
+}
+
+te_mx_status te_mx_grouped_gemm(int32_t num_groups, const int32_t* group_m, int64_t total_m,
+                                const uint8_t* X, const uint8_t* sX, int64_t ld_sX,
+                                const uint8_t* W, const uint8_t* sW, int64_t ld_sW,
+                                int64_t N, int64_t K, const void* bias, int32_t epilogue,
+                                void* D, void* aux, void* workspace, size_t workspace_bytes,
+                                void* stream) {
+    (void)workspace; (void)workspace_bytes;
+    t_last_error[0] = '\0';
+    if (num_groups < 1 || num_groups > 1024) return set_error(TE_MX_ERR_INVALID_ARG, "num_groups=%d must be in [1, 1024]", num_groups);
+    if (!group_m) return set_error(TE_MX_ERR_INVALID_ARG, "group_m is NULL");
+    if (!aligned(group_m, 4)) return set_error(TE_MX_ERR_MISALIGNED, "group_m is not 4-byte aligned");
+    if (total_m < 0) return set_error(TE_MX_ERR_INVALID_ARG, "negative total_m");
+    if (total_m == 0) return TE_MX_OK;
+    if (total_m > (int64_t(1) << 31) - 256) return set_error(TE_MX_ERR_UNSUPPORTED_SHAPE, "total_m too large");
+    te_mx_status st = validate_gemm_common(X, sX, ld_sX, W, sW, ld_sW, N, K, bias, epilogue, D, aux);
+    if (st != TE_MX_OK) return st;
+    if (int64_t(num_groups) * N > (int64_t(1) << 31) - 256) return set_error(TE_MX_ERR_UNSUPPORTED_SHAPE, "G*N too large");
+    if ((st = check_device(nullptr)) != TE_MX_OK) return st;
+    GemmArgs a{};
+    a.A = X; a.sA = sX; a.ld_sA = ld_sX; a.B = W; a.sB = sW; a.ld_sB = ld_sW;
+    a.M = total_m; a.N = N; a.K = K; a.bias = bias;
+    a.has_bias = epilogue == TE_MX_EPI_BIAS || epilogue == TE_MX_EPI_BIAS_GELU_AUX;
+    a.gelu = epilogue == TE_MX_EPI_GELU_AUX || epilogue == TE_MX_EPI_BIAS_GELU_AUX;
+    a.D = D; a.aux = aux; a.groups = num_groups; a.group_m = group_m;
+    return gemm_launch(a, static_cast<cudaStream_t>(stream));
+}
+
+size_t te_mx_gemm_workspace_size(int64_t, int64_t, int64_t, int32_t) { return 0; }
+
+te_mx_status te_mx_device_status(void) {
+    t_last_error[0] = '\0';
+    cudaError_t e = cudaDeviceSynchronize();
+    if (e != cudaSuccess) return cuda_status(e, "cudaDeviceSynchronize");
+    unsigned int v = 0, zero = 0;
+    e = cudaMemcpyFromSymbol(&v, g_device_status, sizeof(v));
+    if (e != cudaSuccess) return cuda_status(e, "reading the device status word");
+    e = cudaMemcpyToSymbol(g_device_status, &zero, sizeof(zero));
+    if (e != cudaSuccess) return cuda_status(e, "clearing the device status word");
+    if (v == kStatusTimeout) return set_error(TE_MX_ERR_DEVICE_TIMEOUT, "a kernel gave up a bounded wait");
+    if (v == kStatusBadArg) return set_error(TE_MX_ERR_INVALID_ARG, "a kernel rejected device-side arguments (group sizes)");
+    return TE_MX_OK;
+}
+
+}  // extern "C"

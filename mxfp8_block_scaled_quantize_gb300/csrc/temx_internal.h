@@ -1,0 +1,56 @@
+// Private interface between the C ABI (api.cu) and the kernel launchers.
+#pragma once
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include <cstdint>
+
+#include "../../include/temx.h"
+
+namespace temx {
+
+struct QuantizeArgs {
+    const void* x;
+    int64_t rows, cols, ld_x;
+    uint8_t* q_row;
+    uint8_t* s_row;
+    int64_t ld_s_row;
+    uint8_t* q_col;
+    uint8_t* s_col;
+    int64_t ld_s_col;
+};
+
+struct GemmArgs {
+    const uint8_t* A;        // dense: [M x K]; grouped: X [total_m x K]
+    const uint8_t* sA;
+    int64_t ld_sA;
+    const uint8_t* B;        // dense: [N x K]; grouped: W [G x N x K]
+    const uint8_t* sB;
+    int64_t ld_sB;
+    int64_t M, N, K;         // grouped: M = total_m
+    const void* bias;        // bf16 [N] (grouped: [G x N]) or null
+    bool has_bias, gelu;
+    void* D;
+    void* aux;
+    int32_t groups;          // 0: dense GEMM
+    const int32_t* group_m;  // device int32 [groups] (grouped only)
+};
+
+te_mx_status quantize_launch(const QuantizeArgs& a, cudaStream_t stream);
+te_mx_status gemm_launch(const GemmArgs& a, cudaStream_t stream);
+
+// Helpers implemented in api.cu.
+te_mx_status set_error(te_mx_status st, const char* fmt, ...);
+te_mx_status cuda_status(cudaError_t e, const char* what);
+te_mx_status device_sm_count(int* sms);
+te_mx_status device_status_ptr(unsigned int** ptr);   // this device's status word
+te_mx_status encode_tensor_map_2d(CUtensorMap* map, CUtensorMapDataType dtype, const void* base,
+                                  uint64_t dim0, uint64_t dim1, uint64_t stride1_bytes,
+                                  uint32_t box0, uint32_t box1, CUtensorMapSwizzle swizzle);
+te_mx_status encode_tensor_map_3d(CUtensorMap* map, CUtensorMapDataType dtype, const void* base,
+                                  uint64_t dim0, uint64_t dim1, uint64_t dim2,
+                                  uint64_t stride1_bytes, uint64_t stride2_bytes,
+                                  uint32_t box0, uint32_t box1, uint32_t box2,
+                                  CUtensorMapSwizzle swizzle);
+
+}  // namespace temx

@@ -1,0 +1,72 @@
+"""The C-ABI library loads and exports every symbol include/temx.h declares
+(no GPU needed), and the host-side helpers behave as documented."""
+import os
+import re
+
+import pytest
+
+from mxfp8_block_scaled_quantize_gb300 import binding
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "temx.h")
+
+
+def declared_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(te_mx_\w+)\s*\(", text)))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    if not os.path.exists(binding.LIB_PATH):
+        from mxfp8_block_scaled_quantize_gb300 import _build
+        _build.build()
+    return binding.lib()
+
+
+def test_header_declares_the_three_entry_points():
+    names = declared_functions()
+    for n in ("te_mx_quantize", "te_mx_gemm", "te_mx_grouped_gemm"):
+        assert n in names
+
+
+def test_every_declared_symbol_is_exported(lib):
+    for name in declared_functions():
+        assert hasattr(lib, name), name
+    assert set(declared_functions()) == set(binding.SIGNATURES)
+
+
+def test_scale_pitch(lib):
+    assert binding.te_mx_scale_pitch(32) == 16
+    assert binding.te_mx_scale_pitch(1024) == 32
+    assert binding.te_mx_scale_pitch(7168) == 224
+    assert binding.te_mx_scale_pitch(8192 + 32) == 272
+    assert binding.te_mx_gemm_workspace_size(4096, 4096, 4096, 0) == 0
+
+
+def test_version(lib):
+    assert "sm_103a" in binding.te_mx_version()
+
+
+def test_host_validation_rejects_bad_arguments_before_any_launch(lib):
+    # these fail argument checks on the host, so they need no GPU
+    with pytest.raises(binding.TemxError, match="INVALID_ARG"):
+        binding.te_mx_quantize(16, 32, 32, 32, 16, 0, 16, 0, 0, 0, 0)      # q_row without s_row
+    with pytest.raises(binding.TemxError, match="UNSUPPORTED_SHAPE"):
+        binding.te_mx_quantize(16, 32, 48, 48, 16, 16, 16, 0, 0, 0, 0)     # cols % 32
+    with pytest.raises(binding.TemxError, match="UNSUPPORTED_SHAPE"):
+        binding.te_mx_quantize(16, 48, 32, 32, 0, 0, 0, 16, 16, 16, 0)     # colwise rows % 32
+    with pytest.raises(binding.TemxError, match="MISALIGNED"):
+        binding.te_mx_quantize(8, 32, 32, 32, 16, 16, 16, 0, 0, 0, 0)      # x not 16-aligned
+    with pytest.raises(binding.TemxError, match="UNSUPPORTED_SHAPE"):
+        binding.te_mx_gemm(16, 16, 16, 16, 16, 16, 128, 128, 96, 0, 0, 16, 0, 0, 0, 0)   # K % 128
+    with pytest.raises(binding.TemxError, match="INVALID_ARG"):
+        binding.te_mx_gemm(16, 16, 16, 16, 16, 16, 128, 128, 128, 0, 1, 16, 0, 0, 0, 0)  # bias missing
+    with pytest.raises(binding.TemxError, match="INVALID_ARG"):
+        binding.te_mx_gemm(16, 16, 16, 16, 16, 16, 128, 128, 128, 0, 2, 16, 0, 0, 0, 0)  # aux missing
+    with pytest.raises(binding.TemxError, match="INVALID_ARG"):
+        binding.te_mx_grouped_gemm(0, 16, 128, 16, 16, 16, 16, 16, 16, 128, 128, 0, 0, 16, 0, 0, 0, 0)
+    # zero-sized problems are no-ops
+    binding.te_mx_quantize(0, 0, 64, 64, 0, 0, 0, 0, 0, 0, 0)
+    binding.te_mx_gemm(16, 16, 16, 16, 16, 16, 0, 128, 128, 0, 0, 16, 0, 0, 0, 0)
