@@ -57,6 +57,27 @@ BF16_EMIN = -126
 BF16_MAX = (2.0 - 2.0 ** -7) * 2.0 ** 127
 
 # --------------------------------------------------------------------------
+# Exact exponent helpers
+# --------------------------------------------------------------------------
+# Every nonzero value handled here is a normal IEEE-754 double (the smallest
+# magnitudes are bf16 subnormals, about 2^-133, far above 2^-1022), so
+# floor(log2 |v|) is the double's unbiased exponent field and 2^e is the double
+# with exponent field e + 1023 and a zero fraction.
+
+
+def floor_log2(v) -> np.ndarray:
+    """floor(log2 |v|) for normal doubles (int64); -1023 for 0."""
+    bits = np.asarray(v, dtype=np.float64).view(np.uint64)
+    return ((bits >> np.uint64(52)) & np.uint64(0x7FF)).astype(np.int64) - 1023
+
+
+def pow2(e) -> np.ndarray:
+    """2.0 ** e for integer e in [-1022, 1023], exactly."""
+    e = np.asarray(e, dtype=np.int64)
+    return ((e + 1023).astype(np.uint64) << np.uint64(52)).view(np.float64)
+
+
+# --------------------------------------------------------------------------
 # Rounding to a binary floating-point format
 # --------------------------------------------------------------------------
 
@@ -70,9 +91,8 @@ def round_to_binary_format(v, mant_bits: int, emin: int) -> np.ndarray:
     kept, so a negative value that rounds to zero gives -0.0.
     """
     v = np.asarray(v, dtype=np.float64)
-    _, p = np.frexp(v)                    # v = m * 2^p with 0.5 <= |m| < 1
-    e = np.maximum(p - 1, emin)           # floor(log2|v|), held at emin for subnormals
-    quantum = np.ldexp(1.0, e - mant_bits)
+    e = np.maximum(floor_log2(v), emin)   # held at emin for subnormals (and zero)
+    quantum = pow2(e - mant_bits)
     # v / quantum is exact (division by a power of two); np.round is ties-to-even.
     return np.round(v / quantum) * quantum
 
@@ -138,12 +158,11 @@ def e4m3_encode_value(r) -> np.ndarray:
     r = np.asarray(r, dtype=np.float64)
     sign = np.signbit(r).astype(np.int64) << 7
     a = np.abs(r)
-    _, p = np.frexp(a)
-    e = p - 1
+    e = floor_log2(a)
     is_sub = a < 2.0 ** E4M3_EMIN
     sub_mant = np.round(a / 2.0 ** (E4M3_EMIN - E4M3_MANT_BITS)).astype(np.int64)
     safe_e = np.where(is_sub | ~np.isfinite(a), 0, e)
-    norm_mant = np.round((a / np.ldexp(1.0, safe_e) - 1.0) * 8.0).astype(np.int64)
+    norm_mant = np.round((a / pow2(safe_e) - 1.0) * 8.0).astype(np.int64)
     norm_field = (safe_e + E4M3_BIAS).astype(np.int64)
     code = np.where(is_sub, sub_mant, (norm_field << 3) | norm_mant)
     return (sign | code).astype(np.uint8)
@@ -162,12 +181,11 @@ def e4m3_encode(v) -> np.ndarray:
 def mx_scale_exponent(amax) -> np.ndarray:
     """Shared exponent of an MX block: floor(log2 amax) - 8, clamped to [-127, 127].
 
-    floor(log2) is taken exactly from frexp (never from a log function).
+    floor(log2) is taken exactly from the exponent field (never from a log function).
     amax == 0 gives -127 (reading: the smallest E8M0 scale).
     """
     amax = np.asarray(amax, dtype=np.float64)
-    _, p = np.frexp(amax)
-    e = np.clip((p - 1) - E4M3_EMAX, -E8M0_BIAS, E8M0_BIAS)
+    e = np.clip(floor_log2(amax) - E4M3_EMAX, -E8M0_BIAS, E8M0_BIAS)
     return np.where(amax == 0.0, -E8M0_BIAS, e).astype(np.int64)
 
 
@@ -195,7 +213,7 @@ def quantize_mx(x_bits, axis: int):
     bad = ~np.isfinite(amax)                      # block holds NaN or inf
     amax_f = np.where(bad, 1.0, amax)
     e = mx_scale_exponent(amax_f)
-    v = blocks * np.ldexp(1.0, -e)[:, :, None]    # exact: scaling by a power of two
+    v = blocks * pow2(-e)[:, :, None]             # exact: scaling by a power of two
     q = e4m3_encode(v)
     q = np.where(bad[:, :, None], np.uint8(0x7F), q)
     s = np.where(bad, 0xFF, e + E8M0_BIAS).astype(np.uint8)
@@ -223,7 +241,7 @@ def dequantize(q, s) -> np.ndarray:
     s = np.asarray(s, dtype=np.uint8).astype(np.int64)
     rows, n = q.shape
     vals = e4m3_decode(q).reshape(rows, n // MX_BLOCK, MX_BLOCK)
-    scale = np.where(s == 0xFF, np.nan, np.ldexp(1.0, s - E8M0_BIAS))
+    scale = np.where(s == 0xFF, np.nan, pow2(s - E8M0_BIAS))
     return (vals * scale[:, :, None]).reshape(rows, n)
 
 
