@@ -1,0 +1,300 @@
+"""GPU parity of te_mx_gemm / te_mx_grouped_gemm against the fp64 oracle.
+
+Acceptance (element-wise, no exceptions): |gpu - oracle| <= 2^-7 |oracle| +
+1e-5 sum_k |a_k b_k|, oracle = the epilogue of the fp64 product of the same
+dequantised operands (rounded to bf16).  Operands for the small cases are
+quantised by the oracle and uploaded, so these tests do not depend on the GPU
+quantiser; the full-size cases run the GPU quantiser and check its sampled
+rows bit-exactly first.  Scale-pitch padding is filled with 0xFF (an E8M0
+NaN) to prove it is never used, and every output has a canary tail.
+"""
+import numpy as np
+import pytest
+import torch
+
+from mxfp8_block_scaled_quantize_gb300 import binding, workloads
+from oracle import mx_oracle as O
+from tests import _util as U
+
+pytestmark = pytest.mark.gpu
+
+
+def rand_bits(shape, seed, std=1.0, outlier_cols=None):
+    g = torch.Generator().manual_seed(seed)
+    x = torch.randn(*shape, generator=g) * std
+    if outlier_cols is not None:
+        x[..., outlier_cols] *= 64.0
+    return U.bf16_bits(x.to(torch.bfloat16))
+
+
+def oracle_rowwise(bits, chunk=4096):
+    qs, ss = [], []
+    for r0 in range(0, bits.shape[0], chunk):
+        q, s = O.quantize_rowwise(bits[r0:r0 + chunk])
+        qs.append(q); ss.append(s)
+    return np.concatenate(qs), np.concatenate(ss)
+
+
+def upload(q, s):
+    """Oracle codes/scales -> device tensors; scale padding = 0xFF."""
+    pitch = binding.te_mx_scale_pitch(q.shape[1])
+    sp = np.full((q.shape[0], pitch), 0xFF, np.uint8)
+    sp[:, : s.shape[1]] = s
+    return torch.from_numpy(q).cuda(), torch.from_numpy(sp).cuda()
+
+
+def run_gemm(qa, sa, qb, sb, bias_bits=None, gelu=False):
+    M, N = qa.shape[0], qb.shape[0]
+    d, dbuf = U.guarded_bf16(M, N)
+    aux, abuf = U.guarded_bf16(M, N) if gelu else (None, None)
+    bias = U.from_bits(bias_bits).cuda() if bias_bits is not None else None
+    binding.gemm(qa, sa, qb, sb, bias=bias, gelu=gelu, out=(d, aux))
+    binding.te_mx_device_status()
+    U.check_guard(dbuf, M * N)
+    if gelu:
+        U.check_guard(abuf, M * N)
+    return d, aux
+
+
+def to_f64(t):
+    return t.float().cpu().numpy().astype(np.float64)
+
+
+def assert_within_bound(got, ref, sigma, what):
+    err = np.abs(got - ref)
+    bound = O.gemm_error_bound(ref, sigma)
+    bad = ~(err <= bound)
+    if bad.any():
+        i = tuple(np.argwhere(bad)[0])
+        raise AssertionError(f"{what}: {int(bad.sum())} of {bad.size} outside the bound; first {i}: "
+                             f"gpu {got[i]!r} oracle {ref[i]!r} bound {bound[i]!r}")
+
+
+def check_dense(M, N, K, bias, gelu, seed, b_std=0.05):
+    a_bits = rand_bits((M, K), seed, outlier_cols=[3, K // 2])
+    b_bits = rand_bits((N, K), seed + 1, std=b_std)
+    qa, sa = O.quantize_rowwise(a_bits)
+    qb, sb = O.quantize_rowwise(b_bits)
+    bias_bits = rand_bits((N,), seed + 2, std=0.5) if bias else None
+    d, aux = run_gemm(*upload(qa, sa), *upload(qb, sb), bias_bits, gelu)
+    ref = O.mx_gemm(qa, sa, qb, sb, bias_bits, gelu)
+    assert_within_bound(to_f64(d), ref["d"], ref["sigma"], "D")
+    if gelu:
+        assert_within_bound(to_f64(aux), ref["aux"], ref["sigma"], "AUX")
+
+
+@pytest.mark.parametrize("m,k", [(128, 256), (200, 640)])
+def test_identity_b_is_bit_exact(m, k):
+    # B = I: every B block is one 1.0 -> D must equal the dequantised A exactly
+    qa, sa = O.quantize_rowwise(rand_bits((m, k), 40, std=3.0))
+    qb, sb = O.quantize_rowwise(O.f64_to_bf16_bits(np.eye(k)))
+    d, _ = run_gemm(*upload(qa, sa), *upload(qb, sb))
+    want = O.dequantize(qa, sa)
+    got = to_f64(d)
+    if not np.array_equal(got, want):
+        bad = np.argwhere(got != want)
+        i = tuple(bad[0])
+        raise AssertionError(f"{len(bad)} mismatches, first {i}: gpu {got[i]} want {want[i]}")
+
+
+def test_single_nonzero_block_scales():
+    # one nonzero K-block per row of A with distinct scales: checks that each
+    # row and each K-block reads its own scale byte
+    m, n, k = 128, 256, 512
+    a = np.zeros((m, k))
+    rng = np.random.default_rng(1)
+    for r in range(m):
+        blk = r % (k // 32)
+        a[r, 32 * blk:32 * blk + 32] = rng.standard_normal(32) * 2.0 ** (r % 17 - 8)
+    b = rng.standard_normal((n, k)) * 2.0 ** (np.arange(n) % 13 - 6)[:, None]
+    qa, sa = O.quantize_rowwise(O.f64_to_bf16_bits(a))
+    qb, sb = O.quantize_rowwise(O.f64_to_bf16_bits(b))
+    d, _ = run_gemm(*upload(qa, sa), *upload(qb, sb))
+    ref = O.mx_gemm(qa, sa, qb, sb)
+    assert_within_bound(to_f64(d), ref["d"], ref["sigma"], "D")
+
+
+@pytest.mark.parametrize("M,N,K,bias,gelu", [
+    (128, 256, 128, False, False),
+    (256, 256, 256, True, False),
+    (200, 96, 384, False, True),
+    (333, 528, 640, True, True),
+    (1, 16, 128, True, False),
+    (130, 272, 1024, False, False),
+    (1024, 1024, 2048, True, True),
+    (640, 3072, 1024, True, False),
+])
+def test_dense_vs_oracle(M, N, K, bias, gelu):
+    check_dense(M, N, K, bias, gelu, seed=M + N + K)
+
+
+def test_gelu_of_zero_and_of_bias():
+    # A = 0: pre = bias, D = GELU(bias), AUX = bias; with no bias D = AUX = 0
+    m, n, k = 128, 256, 256
+    qa, sa = O.quantize_rowwise(np.zeros((m, k), np.uint16))
+    qb, sb = O.quantize_rowwise(rand_bits((n, k), 50))
+    bias_bits = rand_bits((n,), 51, std=2.0)
+    d, aux = run_gemm(*upload(qa, sa), *upload(qb, sb), None, True)
+    assert not to_f64(d).any() and not to_f64(aux).any()
+    d, aux = run_gemm(*upload(qa, sa), *upload(qb, sb), bias_bits, True)
+    ref = O.mx_gemm(qa, sa, qb, sb, bias_bits, True)
+    assert np.array_equal(to_f64(aux), ref["aux"])
+    assert np.all(np.abs(to_f64(d) - ref["d"]) <= 2.0 ** -7 * np.abs(ref["d"]))
+
+
+def test_tiny_workload_end_to_end():
+    d = workloads.make_tiny()
+    a, b = d["A"].cuda(), d["B"].cuda()
+    qa = binding.quantize(a, rowwise=True, colwise=True)
+    qb = binding.quantize(b, rowwise=True, colwise=False)
+    ra, rb = O.quantize_rowwise(U.bf16_bits(d["A"])), O.quantize_rowwise(U.bf16_bits(d["B"]))
+    ca = O.quantize_colwise(U.bf16_bits(d["A"]))
+    U.assert_bytes_equal(qa["q_row"].cpu().numpy(), ra[0], "A row codes")
+    U.assert_bytes_equal(qa["s_row"].cpu().numpy()[:, :8], ra[1], "A row scales")
+    U.assert_bytes_equal(qa["q_col"].cpu().numpy(), ca[0], "A col codes")
+    U.assert_bytes_equal(qa["s_col"].cpu().numpy()[:, :8], ca[1], "A col scales")
+    U.assert_bytes_equal(qb["q_row"].cpu().numpy(), rb[0], "B row codes")
+    bias_bits = U.bf16_bits(d["bias"])
+    out, _ = binding.gemm(qa["q_row"], qa["s_row"], qb["q_row"], qb["s_row"], bias=d["bias"].cuda())
+    binding.te_mx_device_status()
+    ref = O.mx_gemm(ra[0], ra[1], rb[0], rb[1], bias_bits)
+    assert_within_bound(to_f64(out), ref["d"], ref["sigma"], "D")
+
+
+# ---------------------------------------------------------------- grouped
+
+def run_grouped(group_m, total_m, N, K, bias, gelu, seed):
+    G = len(group_m)
+    x_bits = rand_bits((total_m, K), seed)
+    w_bits = rand_bits((G, N, K), seed + 1, std=0.05)
+    qx, sx = O.quantize_rowwise(x_bits)
+    qw, sw = O.quantize_rowwise(w_bits.reshape(G * N, K))
+    bias_bits = rand_bits((G, N), seed + 2, std=0.5) if bias else None
+    dqx, dsx = upload(qx, sx)
+    dqw, dsw = upload(qw, sw)
+    gm = torch.tensor(group_m, dtype=torch.int32, device="cuda")
+    d, dbuf = U.guarded_bf16(total_m, N)
+    aux, abuf = U.guarded_bf16(total_m, N) if gelu else (None, None)
+    bias_t = U.from_bits(bias_bits).cuda() if bias else None
+    binding.grouped_gemm(gm, dqx, dsx, dqw.view(G, N, K), dsw, bias=bias_t, gelu=gelu, out=(d, aux))
+    return (qx, sx, qw.reshape(G, N, K), sw.reshape(G, N, -1), bias_bits), (d, dbuf, aux, abuf)
+
+
+@pytest.mark.parametrize("group_m,N,K,bias,gelu", [
+    ([0, 5, 130, 0, 256, 77], 160, 256, True, True),
+    ([300], 256, 512, False, False),
+    ([1, 0, 0, 129, 127, 128, 0, 2], 272, 384, True, False),
+])
+def test_grouped_vs_oracle(group_m, N, K, bias, gelu):
+    used = sum(group_m)
+    total_m = used + 40                                  # 40 spare rows stay untouched
+    (qx, sx, qw, sw, bias_bits), (d, dbuf, aux, abuf) = run_grouped(group_m, total_m, N, K, bias, gelu, 7 * N + K)
+    binding.te_mx_device_status()
+    ref = O.mx_grouped_gemm(qx[:used], sx[:used], group_m, qw, sw, bias_bits, gelu)
+    dd = to_f64(d)
+    assert_within_bound(dd[:used], ref["d"], ref["sigma"], "D")
+    canary = 0xA5A5
+    assert np.all(U.bf16_bits(d[used:]) == canary), "rows past sum(m) were written"
+    U.check_guard(dbuf, total_m * N)
+    if gelu:
+        assert_within_bound(to_f64(aux)[:used], ref["aux"], ref["sigma"], "AUX")
+        assert np.all(U.bf16_bits(aux[used:]) == canary)
+
+
+def test_grouped_all_empty():
+    (_, _, _, _, _), (d, dbuf, _, _) = run_grouped([0, 0, 0], 64, 128, 128, False, False, 3)
+    binding.te_mx_device_status()
+    assert np.all(U.bf16_bits(d) == 0xA5A5)
+
+
+def test_grouped_sizes_beyond_total_are_reported_and_clamped():
+    (_, _, _, _, _), (d, dbuf, _, _) = run_grouped([100, 100], 150, 128, 128, False, False, 5)
+    with pytest.raises(binding.TemxError, match="INVALID_ARG"):
+        binding.te_mx_device_status()
+    U.check_guard(dbuf, 150 * 128)
+    binding.te_mx_device_status()          # the status word was cleared
+
+
+# ---------------------------------------------------------------- full-size workloads (sampled rows)
+
+def sample_rows(n, k, seed, tile=128):
+    rng = np.random.default_rng(seed)
+    rows = set(rng.choice(n, k, replace=False).tolist())
+    rows |= {0, n - 1, min(n - 1, tile - 1), min(n - 1, tile)}
+    return np.array(sorted(rows))
+
+
+def check_sampled(d, aux, rows, qa_rows, sa_rows, qb, sb, bias_bits, gelu, what):
+    ref = O.mx_gemm(qa_rows, sa_rows, qb, sb, bias_bits, gelu)
+    ri = torch.from_numpy(rows).cuda()
+    assert_within_bound(to_f64(d[ri]), ref["d"], ref["sigma"], what + " D")
+    if gelu:
+        assert_within_bound(to_f64(aux[ri]), ref["aux"], ref["sigma"], what + " AUX")
+
+
+def fprop_check(x_cpu, w_cpu, bias_cpu, gelu, seed, what):
+    x, w = x_cpu.cuda(), w_cpu.cuda()
+    qx = binding.quantize(x, rowwise=True)
+    qw = binding.quantize(w, rowwise=True)
+    d, aux = binding.gemm(qx["q_row"], qx["s_row"], qw["q_row"], qw["s_row"],
+                          bias=None if bias_cpu is None else bias_cpu.cuda(), gelu=gelu)
+    binding.te_mx_device_status()
+    rows = sample_rows(x_cpu.shape[0], 24, seed)
+    qa, sa = O.quantize_rowwise(U.bf16_bits(x_cpu[torch.from_numpy(rows)]))
+    U.assert_bytes_equal(qx["q_row"][torch.from_numpy(rows).cuda()].cpu().numpy(), qa, what + " X codes")
+    qb, sb = oracle_rowwise(U.bf16_bits(w_cpu))
+    check_sampled(d, aux, rows, qa, sa, qb, sb, None if bias_cpu is None else U.bf16_bits(bias_cpu), gelu, what)
+
+
+def wgrad_check(dy_cpu, x_cpu, seed, what):
+    # dW[N_out x K_in] = dY^T X over T tokens: A = colwise(dY) [N_out x T], B = colwise(X) [K_in x T]
+    dy, x = dy_cpu.cuda(), x_cpu.cuda()
+    qdy = binding.quantize(dy, rowwise=False, colwise=True)
+    qx = binding.quantize(x, rowwise=False, colwise=True)
+    dw, _ = binding.gemm(qdy["q_col"], qdy["s_col"], qx["q_col"], qx["s_col"])
+    binding.te_mx_device_status()
+    rows = sample_rows(dy_cpu.shape[1], 16, seed)
+    qa, sa = O.quantize_colwise(U.bf16_bits(dy_cpu[:, torch.from_numpy(rows)]))
+    qb, sb = O.quantize_colwise(U.bf16_bits(x_cpu))
+    check_sampled(dw, None, rows, qa, sa, qb, sb, None, False, what)
+
+
+def test_full_size_qkv():
+    d = workloads.make_qkv()
+    fprop_check(d["X"], d["W"], d["bias"], False, 1, "qkv fprop")
+
+
+def test_full_size_fc1_fprop_and_wgrad():
+    d = workloads.make_fc1()
+    fprop_check(d["X"], d["W"], d["bias"], True, 2, "fc1 fprop")
+    wgrad_check(d["dY"], d["X"], 3, "fc1 wgrad")
+
+
+def test_full_size_ffn_fprop_and_wgrad():
+    d = workloads.make_ffn()
+    fprop_check(d["X"], d["W"], d["bias"], True, 4, "ffn fprop")
+    wgrad_check(d["dY"], d["X"], 5, "ffn wgrad")
+
+
+def test_full_size_moe_grouped():
+    d = workloads.make_moe()
+    counts = d["group_m"].numpy()
+    G, N, K = 128, 1536, 4096
+    x, w = d["X"].cuda(), d["W"].cuda()
+    qx = binding.quantize(x, rowwise=True)
+    qw = binding.quantize(w.view(G * N, K), rowwise=True)
+    gm = d["group_m"].cuda()
+    out, aux = binding.grouped_gemm(gm, qx["q_row"], qx["s_row"], qw["q_row"].view(G, N, K), qw["s_row"],
+                                    gelu=True)
+    binding.te_mx_device_status()
+    starts = np.concatenate([[0], np.cumsum(counts)])
+    nonempty = np.nonzero(counts)[0]
+    picks = {int(nonempty[np.argmax(counts[nonempty])]), int(nonempty[np.argmin(counts[nonempty])]),
+             int(nonempty[0]), int(nonempty[-1])}
+    picks |= set(np.random.default_rng(6).choice(nonempty, 3, replace=False).tolist())
+    for g in sorted(picks):
+        r0, r1 = int(starts[g]), int(starts[g + 1])
+        rows = np.unique(np.concatenate([[r0, r1 - 1], np.random.default_rng(g).integers(r0, r1, 6)]))
+        qa, sa = O.quantize_rowwise(U.bf16_bits(d["X"][torch.from_numpy(rows)]))
+        qb, sb = O.quantize_rowwise(U.bf16_bits(d["W"][g]))
+        check_sampled(out, aux, rows, qa, sa, qb, sb, None, True, f"moe group {g} (m={counts[g]})")
