@@ -1,0 +1,446 @@
+"""Benchmark of the FP8-Linear hot path (MXFP8 quantise + MXFP8 GEMMs) on GB300.
+
+One step = the whole hot path once over one batch of synthetic input:
+  dense FFN layer (8192 tokens, hidden 7168, ffn 18432):
+    quantise X [8192x7168] row+col, W [18432x7168] row, dY [8192x18432] row+col;
+    fprop  D, AUX = GELU-tanh(X W^T + b)       (M=8192,  N=18432, K=7168)
+    wgrad  dW = dY^T X on column-wise operands (M=18432, N=7168,  K=8192)
+  MoE expert layer (16384 tokens, top-8 of 128 experts, Zipf(1.1) routing):
+    quantise X [131072x4096] row, W [128*1536x4096] row;
+    grouped D, AUX = GELU-tanh(X_e W_e^T) over the ragged groups, one launch.
+value = the step's GEMM FLOPs / step time (TFLOP/s; quantisation time included).
+
+`--impl reference` times the CPU oracle on a bounded sample of the same step.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+import numpy as np
+import torch
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "MXFP8 GEMM TFLOPS & quantize GB/s at 1 GB300, as % of FP8/HBM roofline"
+UNIT = "TFLOP/s"
+WORKLOAD = ("ffn fprop+wgrad (tokens 8192, hidden 7168, ffn 18432) + moe grouped "
+            "(16384 tokens top-8 of 128 experts, 1536x4096), with all MXFP8 quantisation")
+
+
+def load_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            p = json.load(f)
+        return {"hbm_gbs": p["hbm_gbs"], "bf16": p["bf16_tflops"],
+                "bf16_sustained": p.get("bf16_tflops_sustained", p["bf16_tflops"]), "source": "measured"}
+    except Exception:
+        return {"hbm_gbs": 6800.0, "bf16": 1900.0, "bf16_sustained": 1700.0, "source": "fallback"}
+
+
+# ----------------------------------------------------------------------------- clocks
+
+class ClockSampler:
+    FIELDS = ["clocks.sm", "clocks.max.sm", "power.draw", "clocks_event_reasons.active",
+              "clocks_event_reasons.hw_slowdown", "clocks_event_reasons.hw_thermal_slowdown",
+              "clocks_event_reasons.sw_thermal_slowdown", "clocks_event_reasons.sw_power_cap"]
+
+    def __init__(self, device_index: int):
+        self.dev = device_index
+        self.proc = None
+        self.lines = []
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.dev), "--query-gpu=" + ",".join(self.FIELDS),
+                 "--format=csv,noheader,nounits", "-lms", "50"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.thread = threading.Thread(target=self._read, daemon=True)
+            self.thread.start()
+        except Exception:
+            self.proc = None
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except Exception:
+            self.proc.kill()
+        sm, smax, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ln in self.lines:
+            parts = [x.strip() for x in ln.split(",")]
+            if len(parts) < 8:
+                continue
+            try:
+                sm.append(float(parts[0]))
+                smax.append(float(parts[1]))
+            except ValueError:
+                continue
+            for name, val in zip(names, parts[4:8]):
+                if val.lower() == "active":
+                    reasons.add(name)
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(smax) if smax else None,
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+# ----------------------------------------------------------------------------- workload
+
+def build_inputs(dev):
+    from mxfp8_block_scaled_quantize_gb300 import workloads
+    ffn = workloads.make_ffn()
+    moe = workloads.make_moe()
+    host = {"ffn_X": ffn["X"], "ffn_W": ffn["W"], "ffn_b": ffn["bias"], "ffn_dY": ffn["dY"],
+            "moe_X": moe["X"], "moe_W": moe["W"].view(128 * 1536, 4096), "moe_m": moe["group_m"]}
+    return host
+
+
+class Step:
+    """Device buffers and the launch sequence of one step (all on one stream)."""
+
+    def __init__(self, host, dev):
+        import mxfp8_block_scaled_quantize_gb300 as temx
+        self.temx = temx
+        self.d = {k: v.to(dev) for k, v in host.items()}
+        d = self.d
+        e = lambda *s, dt=torch.uint8: torch.empty(*s, dtype=dt, device=dev)
+        pitch = temx.te_mx_scale_pitch
+        T, H, F = 8192, 7168, 18432
+        self.o = o = {}
+        o["x_row"] = {"q_row": e(T, H), "s_row": e(T, pitch(H)), "q_col": e(H, T), "s_col": e(H, pitch(T))}
+        o["w_row"] = {"q_row": e(F, H), "s_row": e(F, pitch(H))}
+        o["dy"] = {"q_row": e(T, F), "s_row": e(T, pitch(F)), "q_col": e(F, T), "s_col": e(F, pitch(T))}
+        o["fprop"] = (e(T, F, dt=torch.bfloat16), e(T, F, dt=torch.bfloat16))
+        o["wgrad"] = (e(F, H, dt=torch.bfloat16), None)
+        MT, G, N, K = 131072, 128, 1536, 4096
+        o["mx"] = {"q_row": e(MT, K), "s_row": e(MT, pitch(K))}
+        o["mw"] = {"q_row": e(G * N, K), "s_row": e(G * N, pitch(K))}
+        o["moe"] = (e(MT, N, dt=torch.bfloat16), e(MT, N, dt=torch.bfloat16))
+        counts = host["moe_m"].numpy()
+        self.flops = {"gemm_fprop": 2.0 * T * F * H, "gemm_wgrad": 2.0 * F * H * T,
+                      "gemm_grouped": 2.0 * float(counts.sum()) * N * K}
+        qb = lambda r, c, both: (2.0 + (2 if both else 1) * (1 + 1 / 32)) * r * c
+        self.bytes = {"quant_ffn_x": qb(T, H, True), "quant_ffn_w": qb(F, H, False),
+                      "quant_ffn_dy": qb(T, F, True), "quant_moe_x": qb(MT, K, False),
+                      "quant_moe_w": qb(G * N, K, False)}
+        self.kernels = [
+            ("quant_ffn_x", lambda: temx.quantize(d["ffn_X"], True, True, out=o["x_row"])),
+            ("quant_ffn_w", lambda: temx.quantize(d["ffn_W"], True, False, out=o["w_row"])),
+            ("quant_ffn_dy", lambda: temx.quantize(d["ffn_dY"], True, True, out=o["dy"])),
+            ("gemm_fprop", lambda: temx.gemm(o["x_row"]["q_row"], o["x_row"]["s_row"], o["w_row"]["q_row"],
+                                             o["w_row"]["s_row"], bias=d["ffn_b"], gelu=True, out=o["fprop"])),
+            ("gemm_wgrad", lambda: temx.gemm(o["dy"]["q_col"], o["dy"]["s_col"], o["x_row"]["q_col"],
+                                             o["x_row"]["s_col"], out=o["wgrad"])),
+            ("quant_moe_x", lambda: temx.quantize(d["moe_X"], True, False, out=o["mx"])),
+            ("quant_moe_w", lambda: temx.quantize(d["moe_W"], True, False, out=o["mw"])),
+            ("gemm_grouped", lambda: temx.grouped_gemm(d["moe_m"], o["mx"]["q_row"], o["mx"]["s_row"],
+                                                       o["mw"]["q_row"].view(G, N, K), o["mw"]["s_row"],
+                                                       gelu=True, out=o["moe"])),
+        ]
+        self.outputs = [o["fprop"][0], o["fprop"][1], o["wgrad"][0], o["moe"][0], o["moe"][1]]
+
+    def run(self, events=None):
+        for i, (_, fn) in enumerate(self.kernels):
+            if events is not None:
+                events[i][0].record()
+            fn()
+            if events is not None:
+                events[i][1].record()
+
+
+def time_device(step, steps, warmup, sampler):
+    for _ in range(warmup):
+        step.run()
+    step.temx.te_mx_device_status()
+    n = len(step.kernels)
+    evs = [[(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(n)]
+           for _ in range(steps)]
+    start, stop = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    barrier()
+    torch.cuda.synchronize()
+    sampler.start()
+    time.sleep(0.3)
+    start.record()
+    for s in range(steps):
+        step.run(evs[s])
+    stop.record()
+    torch.cuda.synchronize()
+    clocks = sampler.stop()
+    barrier()
+    step.temx.te_mx_device_status()
+    total_ms = start.elapsed_time(stop)
+    per_kernel = {}
+    for i, (name, _) in enumerate(step.kernels):
+        per_kernel[name] = sum(evs[s][i][0].elapsed_time(evs[s][i][1]) for s in range(steps)) / steps
+    return total_ms, per_kernel, clocks
+
+
+def time_e2e(step, host, steps, warmup):
+    """Same step through the public API with host buffers: every step copies
+    its inputs host->device from pinned memory and its outputs back."""
+    pinned_in = {k: v.pin_memory() for k, v in host.items()}
+    pinned_out = [torch.empty(t.shape, dtype=t.dtype).pin_memory() for t in step.outputs]
+    h2d = sum(t.numel() * t.element_size() for t in pinned_in.values())
+    d2h = sum(t.numel() * t.element_size() for t in pinned_out)
+
+    def one():
+        for k, v in pinned_in.items():
+            step.d[k].copy_(v, non_blocking=True)
+        step.run()
+        for dst, src in zip(pinned_out, step.outputs):
+            dst.copy_(src, non_blocking=True)
+
+    for _ in range(max(1, warmup // 2)):
+        one()
+    barrier()
+    torch.cuda.synchronize()
+    t0 = time.perf_counter()
+    for _ in range(steps):
+        one()
+    torch.cuda.synchronize()
+    dt = time.perf_counter() - t0
+    barrier()
+    return dt * 1e3 / steps, h2d, d2h
+
+
+# ----------------------------------------------------------------------------- CPU oracle leg
+
+def oracle_sample_step(host, rng_seed=0):
+    """A bounded sample of one step on the host cores with the CPU oracle:
+    1/256 of each quantisation (whole 32-row bands) and a 256x256 output block
+    (full K) of each GEMM.  Returns (GEMM FLOPs done, seconds)."""
+    from oracle import mx_oracle as O
+    bits = lambda t: t.contiguous().view(torch.int16).numpy().view(np.uint16)
+    t0 = time.perf_counter()
+    # quantisation: 1/256 of the step's elements (rows in 32-row bands)
+    for key, both in (("ffn_X", True), ("ffn_W", False), ("ffn_dY", True), ("moe_X", False), ("moe_W", False)):
+        x = host[key]
+        r = max(32, x.shape[0] // 256 // 32 * 32)
+        b = bits(x[:r])
+        O.quantize_rowwise(b)
+        if both:
+            O.quantize_colwise(b)
+    flops = 0.0
+    # fprop block: 256 rows of X x 256 rows of W, K = 7168, bias + GELU
+    qa, sa = O.quantize_rowwise(bits(host["ffn_X"][:256]))
+    qb, sb = O.quantize_rowwise(bits(host["ffn_W"][:256]))
+    O.mx_gemm(qa, sa, qb, sb, bits(host["ffn_b"][:256]), gelu=True)
+    flops += 2.0 * 256 * 256 * 7168
+    # wgrad block: 256 columns of dY x 256 columns of X, K = 8192 tokens
+    qa, sa = O.quantize_colwise(bits(host["ffn_dY"][:, :256]))
+    qb, sb = O.quantize_colwise(bits(host["ffn_X"][:, :256]))
+    O.mx_gemm(qa, sa, qb, sb)
+    flops += 2.0 * 256 * 256 * 8192
+    # grouped block: 256 rows of one expert x 256 of its weight rows, K = 4096, GELU
+    qa, sa = O.quantize_rowwise(bits(host["moe_X"][:256]))
+    qb, sb = O.quantize_rowwise(bits(host["moe_W"][:256]))
+    O.mx_gemm(qa, sa, qb, sb, None, gelu=True)
+    flops += 2.0 * 256 * 256 * 4096
+    return flops, time.perf_counter() - t0
+
+
+SAMPLE_DESC = ("per sample: 1/256 of every quantisation of the step (32-row bands, row- and column-wise "
+               "as in the step) + a 256x256 output block (full K) of the fprop, wgrad and grouped GEMMs "
+               "with their epilogues; value = sampled GEMM FLOPs / sample time")
+
+
+def cpu_baseline(host, budget_s=15.0):
+    flops, secs, n = 0.0, 0.0, 0
+    while secs < budget_s or n < 1:
+        f, s = oracle_sample_step(host)
+        flops += f; secs += s; n += 1
+    return {"value": flops / secs / 1e12, "unit": UNIT, "cores": os.cpu_count(), "kind": "oracle",
+            "sample": f"{n} samples, {secs:.1f} s; " + SAMPLE_DESC +
+                      "; numpy fp64 (matmul on the BLAS threads of all host cores, the rest single-threaded)"}
+
+
+# ----------------------------------------------------------------------------- distributed
+
+_dist = False
+
+
+def barrier():
+    if _dist:
+        torch.distributed.barrier()
+
+
+def dist_max(x: float) -> float:
+    if not _dist:
+        return x
+    t = torch.tensor([x], dtype=torch.float64, device="cuda")
+    torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+    return float(t.item())
+
+
+CASES = {
+    "quant_both": "ffn X [8192x7168] row- and column-wise",
+    "quant_row": "ffn W [18432x7168] row-wise",
+    "gemm_fc1": "fc1 fprop 4096x4096x1024, bias + GELU + AUX",
+    "gemm_ffn": "ffn fprop 8192x18432x7168, bias + GELU + AUX",
+    "gemm_wgrad": "ffn wgrad 18432x7168x8192 on column-wise operands",
+    "gemm_moe": "moe grouped 128 experts x 1536 x 4096, GELU + AUX",
+}
+
+
+def run_case(case: str, reps: int):
+    """Run one kernel of the step `reps` times (for profilers); prints per-launch ms."""
+    import mxfp8_block_scaled_quantize_gb300 as temx
+    from mxfp8_block_scaled_quantize_gb300 import workloads
+    dev = torch.device("cuda", 0)
+    if case in ("quant_both", "quant_row", "gemm_ffn", "gemm_wgrad"):
+        w = workloads.make_ffn()
+    elif case == "gemm_fc1":
+        w = workloads.make_fc1()
+    else:
+        w = workloads.make_moe()
+    if case == "quant_both":
+        x = w["X"].to(dev)
+        fn = lambda: temx.quantize(x, True, True)
+    elif case == "quant_row":
+        x = w["W"].to(dev)
+        fn = lambda: temx.quantize(x, True, False)
+    elif case in ("gemm_fc1", "gemm_ffn"):
+        qx = temx.quantize(w["X"].to(dev), True, False)
+        qw = temx.quantize(w["W"].to(dev), True, False)
+        b = w["bias"].to(dev)
+        fn = lambda: temx.gemm(qx["q_row"], qx["s_row"], qw["q_row"], qw["s_row"], bias=b, gelu=True)
+    elif case == "gemm_wgrad":
+        qd = temx.quantize(w["dY"].to(dev), False, True)
+        qx = temx.quantize(w["X"].to(dev), False, True)
+        fn = lambda: temx.gemm(qd["q_col"], qd["s_col"], qx["q_col"], qx["s_col"])
+    else:
+        qx = temx.quantize(w["X"].to(dev), True, False)
+        qw = temx.quantize(w["W"].view(128 * 1536, 4096).to(dev), True, False)
+        gm = w["group_m"].to(dev)
+        fn = lambda: temx.grouped_gemm(gm, qx["q_row"], qx["s_row"], qw["q_row"].view(128, 1536, 4096),
+                                       qw["s_row"], gelu=True)
+    torch.cuda.synchronize()
+    times = []
+    for _ in range(reps):
+        a, b_ = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record(); fn(); b_.record()
+        torch.cuda.synchronize()
+        times.append(a.elapsed_time(b_))
+    temx.te_mx_device_status()
+    print(json.dumps({"case": case, "desc": CASES[case], "ms": times}))
+
+
+def main():
+    global _dist
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=100)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", default="temx", choices=["temx", "reference"])
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--case", choices=sorted(CASES), help="run one kernel of the step (for profilers)")
+    ap.add_argument("--reps", type=int, default=3)
+    args = ap.parse_args()
+    if args.case:
+        run_case(args.case, args.reps)
+        return
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+
+    if args.impl == "reference":
+        if rank != 0:
+            return
+        host = build_inputs("cpu")
+        for _ in range(args.warmup):
+            oracle_sample_step(host)
+        flops, secs = 0.0, 0.0
+        for _ in range(args.steps):
+            f, s = oracle_sample_step(host)
+            flops += f; secs += s
+        v = flops / secs / 1e12
+        print(json.dumps({
+            "impl": "reference", "metric": METRIC, "value": v, "unit": UNIT, "n_gpus": 1,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": secs * 1e3 / args.steps,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+            "data": "synthetic (seeded generators)", "config": {"workload": WORKLOAD, "sample": SAMPLE_DESC},
+            "cpu_baseline": {"value": v, "unit": UNIT, "cores": os.cpu_count(), "kind": "oracle", "sample": SAMPLE_DESC},
+            "e2e": {"value": v, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}))
+        return
+
+    if world > 1:
+        torch.distributed.init_process_group("nccl")
+        _dist = True
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    import mxfp8_block_scaled_quantize_gb300 as temx
+    temx.binding.lib()
+    peaks = load_peaks()
+    host = build_inputs(dev)
+    step = Step(host, dev)
+    sampler = ClockSampler(local)
+    total_ms, per_kernel, clocks = time_device(step, args.steps, args.warmup, sampler)
+    ms_step = dist_max(total_ms / args.steps)
+    gemm_flops = sum(step.flops.values())
+    value = world * gemm_flops / (ms_step * 1e-3) / 1e12
+
+    fp8_peak = 2.0 * peaks["bf16_sustained"]          # nominal fp8:bf16 = 2
+    fp8_burst = 2.0 * peaks["bf16"]
+    kern = {}
+    for name, ms in per_kernel.items():
+        if name in step.flops:
+            ach = step.flops[name] / (ms * 1e-3) / 1e12
+            kern[name] = {"us": ms * 1e3, "achieved": ach, "unit": "TFLOP/s", "frac": ach / fp8_peak,
+                          "frac_of_burst": ach / fp8_burst, "flops": step.flops[name]}
+        else:
+            ach = step.bytes[name] / (ms * 1e-3) / 1e9
+            kern[name] = {"us": ms * 1e3, "achieved": ach, "unit": "GB/s", "frac": ach / peaks["hbm_gbs"],
+                          "bytes": step.bytes[name]}
+    dom = max(per_kernel, key=per_kernel.get)
+    dk = kern[dom]
+    traffic = None
+    roofline = {"kernel": dom, "bound": "tensor" if dk["unit"] == "TFLOP/s" else "hbm",
+                "achieved": dk["achieved"], "peak": fp8_peak if dk["unit"] == "TFLOP/s" else peaks["hbm_gbs"],
+                "unit": dk["unit"], "frac": dk["frac"], "traffic": traffic,
+                "peak_source": (f"{peaks['source']}: 2 x bf16 sustained {peaks['bf16_sustained']} TFLOP/s"
+                                if dk["unit"] == "TFLOP/s" else f"{peaks['source']}: HBM copy {peaks['hbm_gbs']} GB/s")}
+    qbytes = sum(step.bytes.values())
+    qms = sum(per_kernel[n] for n in step.bytes)
+    gms = sum(per_kernel[n] for n in step.flops)
+
+    e2e_ms, h2d, d2h = time_e2e(step, host, max(3, args.steps // 4), args.warmup)
+    e2e_ms = dist_max(e2e_ms)
+    out = {
+        "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": ms_step, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "e4m3 x e4m3 -> fp32 accumulate, bf16 in/out",
+        "data": "synthetic (seeded generators, shapes and distributions of the workloads)",
+        "config": {"workload": WORKLOAD, "parallelism": "replicas" if world > 1 else "single GPU",
+                   "l2": "inputs larger than L2 (every operand > 126 MB except bias/group sizes)"},
+        "gemm_tflops": gemm_flops / (gms * 1e-3) / 1e12, "gemm_frac": gemm_flops / (gms * 1e-3) / 1e12 / fp8_peak,
+        "quantize_gbs": qbytes / (qms * 1e-3) / 1e9, "quantize_frac": qbytes / (qms * 1e-3) / 1e9 / peaks["hbm_gbs"],
+        "kernels": kern, "roofline": roofline, "clocks": clocks,
+        "gpu_launches": len(step.kernels) * args.steps,
+        "e2e": {"value": world * gemm_flops / (e2e_ms * 1e-3) / 1e12, "unit": UNIT,
+                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
+    }
+    if rank == 0 and not args.no_cpu_baseline:
+        out["cpu_baseline"] = cpu_baseline({k: v.cpu() if v.is_cuda else v for k, v in host.items()})
+    if rank == 0:
+        print(json.dumps(out))
+    if _dist:
+        torch.distributed.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()
