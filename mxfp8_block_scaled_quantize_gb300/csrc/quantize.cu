@@ -8,17 +8,17 @@
 //   q = E4M3_rn_satfinite(x * 2^(127 - s))
 // and a block holding NaN/inf gets s = 0xFF, q = 0x7F.
 //
-// Work decomposition.  The input is cut into units of 32 rows x 64 columns
-// (4 KB of bf16).  Every warp runs its own pipeline: lane 0 keeps
-// kStages units in flight with TMA (128-byte swizzle, so both the row reads
-// and the column reads below are bank-conflict free), and the warp consumes
-// them in order.  Per unit:
-//   row-wise:    lane r owns row r: two 32-element blocks, 2 x 32 bytes of
-//                codes and 2 scale bytes;
-//   column-wise: lane l owns columns 2l, 2l+1: one 32-row block each, stored
-//                as 32 contiguous bytes of the transposed copy plus one scale
-//                byte each.
-// Warps never wait on each other, so there is no CTA-wide barrier.
+// Work decomposition.  The input is cut into units of 64 rows x 64 columns
+// (8 KB of bf16).  Every warp runs its own pipeline over a kStages-deep ring:
+// lane 0 loads units with TMA (128-byte swizzle, so both the row reads and the
+// column reads below are bank-conflict free) and the whole warp consumes them:
+//   column-wise: lane l owns columns 2l and 2l+1 (two 32-row blocks each);
+//   row-wise:    lane l owns rows l and l+32 (two 32-column blocks each).
+// Once every lane has read the unit, the codes (64 x 64 bytes per orientation)
+// are written into the same 8 KB of shared memory with a 64-byte swizzle and
+// leave with two TMA tensor stores, so global writes are whole lines instead
+// of 32 scattered sectors per instruction.  Scale bytes (2 per row or column
+// per unit) are stored directly.  Warps never wait on each other.
 #include <cuda_runtime.h>
 
 #include "ptx.cuh"
@@ -28,23 +28,21 @@ namespace temx {
 
 namespace {
 
-constexpr int kRows = 32;                    // unit height (= one column-wise block)
+constexpr int kRows = 64;                    // unit height (two column-wise blocks)
 constexpr int kCols = 64;                    // unit width in bf16 (= 128-byte swizzle row)
 constexpr int kUnitBytes = kRows * kCols * 2;
-constexpr int kWarps = 16;
-constexpr int kStages = 3;
+constexpr int kWarps = 12;
+constexpr int kStages = 2;
 constexpr int kSmemBytes = kWarps * kStages * kUnitBytes + 1024;
 
 struct QuantizeParams {
     int64_t rows, cols;
-    uint8_t* q_row;
     uint8_t* s_row;
     int64_t ld_s_row;
-    uint8_t* q_col;
     uint8_t* s_col;
     int64_t ld_s_col;
     int64_t col_units;     // ceil(cols / 64)
-    int64_t units;         // ceil(rows / 32) * col_units
+    int64_t units;         // ceil(rows / 64) * col_units
     unsigned int* status;  // device status word
 };
 
@@ -85,92 +83,80 @@ __device__ __forceinline__ uint32_t quant4(uint32_t w0, uint32_t w1, float m) {
     return a | (b << 16);
 }
 
-// Row-wise blocks of one unit: lane = row within the unit.
-__device__ __forceinline__ void unit_rowwise(const uint8_t* tile, int lane, int64_t r, int64_t c0,
-                                             const QuantizeParams& p) {
+// Largest |x| of 2n words of bf16 pairs, as bf16 bits (tree of max.u16x2).
+template <int kWords>
+__device__ __forceinline__ uint32_t amax_words(const uint32_t* w) {
+    uint32_t m[kWords / 2];
+#pragma unroll
+    for (int i = 0; i < kWords / 2; ++i) m[i] = max_u16x2(w[2 * i] & 0x7FFF7FFFu, w[2 * i + 1] & 0x7FFF7FFFu);
+#pragma unroll
+    for (int s = kWords / 4; s >= 1; s >>= 1)
+#pragma unroll
+        for (int i = 0; i < s; ++i) m[i] = max_u16x2(m[i], m[i + s]);
+    return m[0];                          // two maxima, one per 16-bit half
+}
+
+// One row of a unit (64 bf16 at shared address `row_addr`, 128-byte swizzle
+// phase `sw`): two row-wise blocks -> codes[2][8] words, scale bytes sb[2].
+__device__ __forceinline__ void row_blocks(uint32_t row_addr, int sw, uint32_t (&codes)[2][8], uint32_t (&sb)[2]) {
     uint32_t w[32];
 #pragma unroll
     for (int j = 0; j < 8; ++j) {
-        const uint4 v = *reinterpret_cast<const uint4*>(tile + lane * 128 + ((j ^ (lane & 7)) << 4));
+        const uint4 v = lds128(row_addr + ((j ^ sw) << 4));
         w[4 * j + 0] = v.x; w[4 * j + 1] = v.y; w[4 * j + 2] = v.z; w[4 * j + 3] = v.w;
     }
-    uint32_t sb[2];
 #pragma unroll
     for (int blk = 0; blk < 2; ++blk) {
-        uint32_t m2 = 0;
-#pragma unroll
-        for (int i = 0; i < 16; ++i) m2 = max_u16x2(m2, w[16 * blk + i] & 0x7FFF7FFFu);
-        const uint32_t amax = max(m2 & 0xFFFFu, m2 >> 16);
-        sb[blk] = scale_byte(amax);
+        const uint32_t m2 = amax_words<16>(w + 16 * blk);
+        sb[blk] = scale_byte(max(m2 & 0xFFFFu, m2 >> 16));
         const float m = inv_scale(sb[blk]);
-        uint32_t o[8];
 #pragma unroll
-        for (int i = 0; i < 8; ++i) o[i] = quant4(w[16 * blk + 2 * i], w[16 * blk + 2 * i + 1], m);
+        for (int i = 0; i < 8; ++i) codes[blk][i] = quant4(w[16 * blk + 2 * i], w[16 * blk + 2 * i + 1], m);
         if (sb[blk] == 0xFFu) {
 #pragma unroll
-            for (int i = 0; i < 8; ++i) o[i] = 0x7F7F7F7Fu;
+            for (int i = 0; i < 8; ++i) codes[blk][i] = 0x7F7F7F7Fu;
         }
-        const int64_t c = c0 + 32 * blk;
-        if (r < p.rows && c < p.cols) {
-            uint8_t* dst = p.q_row + r * p.cols + c;
-            st_global_v4(dst, o[0], o[1], o[2], o[3]);
-            st_global_v4(dst + 16, o[4], o[5], o[6], o[7]);
-        }
-    }
-    if (r < p.rows) {
-        uint8_t* ds = p.s_row + r * p.ld_s_row + (c0 >> 5);
-        if (c0 + 32 < p.cols) st_global_u16(ds, sb[0] | (sb[1] << 8));
-        else st_global_u8(ds, sb[0]);
     }
 }
 
-// Column-wise blocks of one unit: lane l owns columns 2l and 2l+1.
-__device__ __forceinline__ void unit_colwise(const uint8_t* tile, int lane, int64_t r0, int64_t c0,
-                                             const QuantizeParams& p) {
+// Columns 2l and 2l+1 over the 32 rows from `row0` (a multiple of 8):
+// codes lo[8] / hi[8] (32 bytes each, rows in order) and their scale bytes.
+__device__ __forceinline__ void col_blocks(uint32_t tile, int row0, int lane, uint32_t (&lo)[8], uint32_t (&hi)[8],
+                                           uint32_t& s_lo, uint32_t& s_hi) {
     uint32_t w[32];
-    const int chunk = lane >> 2, in_chunk = (lane & 3) << 2;
+    const uint32_t base = tile + row0 * 128 + ((lane & 3) << 2);
+    const int chunk = lane >> 2;
 #pragma unroll
-    for (int r = 0; r < 32; ++r)
-        w[r] = *reinterpret_cast<const uint32_t*>(tile + r * 128 + ((chunk ^ (r & 7)) << 4) + in_chunk);
-    uint32_t m2 = 0;
-#pragma unroll
-    for (int r = 0; r < 32; ++r) m2 = max_u16x2(m2, w[r] & 0x7FFF7FFFu);
-    const uint32_t s_lo = scale_byte(m2 & 0xFFFFu), s_hi = scale_byte(m2 >> 16);
+    for (int r = 0; r < 32; ++r) w[r] = lds32(base + r * 128 + ((chunk ^ (r & 7)) << 4));
+    const uint32_t m2 = amax_words<32>(w);
+    s_lo = scale_byte(m2 & 0xFFFFu);
+    s_hi = scale_byte(m2 >> 16);
     const float m_lo = inv_scale(s_lo), m_hi = inv_scale(s_hi);
-    uint32_t o_lo[8], o_hi[8];
 #pragma unroll
     for (int i = 0; i < 8; ++i) {
         const uint32_t a0 = w[4 * i], a1 = w[4 * i + 1], a2 = w[4 * i + 2], a3 = w[4 * i + 3];
-        o_lo[i] = cvt_e4m3x2(__fmul_rn(bf16_lo(a0), m_lo), __fmul_rn(bf16_lo(a1), m_lo)) |
-                  (cvt_e4m3x2(__fmul_rn(bf16_lo(a2), m_lo), __fmul_rn(bf16_lo(a3), m_lo)) << 16);
-        o_hi[i] = cvt_e4m3x2(__fmul_rn(bf16_hi(a0), m_hi), __fmul_rn(bf16_hi(a1), m_hi)) |
-                  (cvt_e4m3x2(__fmul_rn(bf16_hi(a2), m_hi), __fmul_rn(bf16_hi(a3), m_hi)) << 16);
+        lo[i] = cvt_e4m3x2(__fmul_rn(bf16_lo(a0), m_lo), __fmul_rn(bf16_lo(a1), m_lo)) |
+                (cvt_e4m3x2(__fmul_rn(bf16_lo(a2), m_lo), __fmul_rn(bf16_lo(a3), m_lo)) << 16);
+        hi[i] = cvt_e4m3x2(__fmul_rn(bf16_hi(a0), m_hi), __fmul_rn(bf16_hi(a1), m_hi)) |
+                (cvt_e4m3x2(__fmul_rn(bf16_hi(a2), m_hi), __fmul_rn(bf16_hi(a3), m_hi)) << 16);
     }
     if (s_lo == 0xFFu) {
 #pragma unroll
-        for (int i = 0; i < 8; ++i) o_lo[i] = 0x7F7F7F7Fu;
+        for (int i = 0; i < 8; ++i) lo[i] = 0x7F7F7F7Fu;
     }
     if (s_hi == 0xFFu) {
 #pragma unroll
-        for (int i = 0; i < 8; ++i) o_hi[i] = 0x7F7F7F7Fu;
-    }
-    const int64_t c = c0 + 2 * lane;
-    if (c < p.cols) {   // cols % 32 == 0, so c and c + 1 are valid together
-        uint8_t* d0 = p.q_col + c * p.rows + r0;
-        uint8_t* d1 = d0 + p.rows;
-        st_global_v4(d0, o_lo[0], o_lo[1], o_lo[2], o_lo[3]);
-        st_global_v4(d0 + 16, o_lo[4], o_lo[5], o_lo[6], o_lo[7]);
-        st_global_v4(d1, o_hi[0], o_hi[1], o_hi[2], o_hi[3]);
-        st_global_v4(d1 + 16, o_hi[4], o_hi[5], o_hi[6], o_hi[7]);
-        uint8_t* s0 = p.s_col + c * p.ld_s_col + (r0 >> 5);
-        st_global_u8(s0, s_lo);
-        st_global_u8(s0 + p.ld_s_col, s_hi);
+        for (int i = 0; i < 8; ++i) hi[i] = 0x7F7F7F7Fu;
     }
 }
 
+// Byte offset of 16-byte chunk c of 64-byte row r in a 64-byte-swizzled tile.
+__device__ __forceinline__ uint32_t sw64(int r, int c) { return uint32_t(r * 64 + ((c ^ ((r >> 1) & 3)) << 4)); }
+
 template <bool kRowwise, bool kColwise>
 __global__ void __launch_bounds__(kWarps * 32, 1)
-quantize_kernel(const __grid_constant__ CUtensorMap x_map, const QuantizeParams p) {
+quantize_kernel(const __grid_constant__ CUtensorMap x_map, const __grid_constant__ CUtensorMap qrow_map,
+                const __grid_constant__ CUtensorMap qcol_map, const QuantizeParams p) {
     extern __shared__ uint8_t smem_raw[];
     __shared__ __align__(8) uint64_t bars[kWarps][kStages];
 
@@ -180,17 +166,19 @@ quantize_kernel(const __grid_constant__ CUtensorMap x_map, const QuantizeParams 
     const int64_t nwarps = int64_t(gridDim.x) * kWarps;
     if (gwarp >= p.units) return;
     const int64_t n_mine = (p.units - gwarp + nwarps - 1) / nwarps;
-    uint8_t* ring = smem + warp * (kStages * kUnitBytes);
+    const uint32_t ring = smem_u32(smem + warp * (kStages * kUnitBytes));
 
     if (lane == 0) {
         tma_prefetch_desc(&x_map);
+        if (kRowwise) tma_prefetch_desc(&qrow_map);
+        if (kColwise) tma_prefetch_desc(&qcol_map);
         for (int s = 0; s < kStages; ++s) mbar_init(smem_u32(&bars[warp][s]), 1);
         fence_mbarrier_init();
         for (int s = 0; s < kStages && s < n_mine; ++s) {
             const int64_t u = gwarp + s * nwarps;
             const uint32_t bar = smem_u32(&bars[warp][s]);
             mbar_arrive_expect_tx(bar, kUnitBytes);
-            tma_load_2d(smem_u32(ring + s * kUnitBytes), &x_map, bar,
+            tma_load_2d(ring + s * kUnitBytes, &x_map, bar,
                         int32_t((u % p.col_units) * kCols), int32_t((u / p.col_units) * kRows));
         }
     }
@@ -201,30 +189,95 @@ quantize_kernel(const __grid_constant__ CUtensorMap x_map, const QuantizeParams 
         const uint32_t parity = uint32_t((i / kStages) & 1);
         const uint32_t bar = smem_u32(&bars[warp][s]);
         if (!mbar_wait(bar, parity, p.status)) break;
-        const uint8_t* tile = ring + s * kUnitBytes;
+        const uint32_t tile = ring + s * kUnitBytes;
         const int64_t u = gwarp + i * nwarps;
         const int64_t r0 = (u / p.col_units) * kRows, c0 = (u % p.col_units) * kCols;
-        if (kRowwise) unit_rowwise(tile, lane, r0 + lane, c0, p);
-        if (kColwise) unit_colwise(tile, lane, r0, c0, p);
-        __syncwarp();
-        if (lane == 0 && i + kStages < n_mine) {
-            fence_proxy_async_smem();          // our generic reads before the async refill
-            const int64_t un = gwarp + (i + kStages) * nwarps;
-            mbar_arrive_expect_tx(bar, kUnitBytes);
-            tma_load_2d(smem_u32(ring + s * kUnitBytes), &x_map, bar,
-                        int32_t((un % p.col_units) * kCols), int32_t((un / p.col_units) * kRows));
+
+        uint32_t cc[2][2][8];             // column codes [half][column 2l / 2l+1][words]
+        uint32_t rc[2][2][8];             // row codes [row l / l+32][block][words]
+        if (kColwise) {
+            const bool second = r0 + 32 < p.rows;          // rows % 32 == 0 here
+            uint32_t s_lo[2] = {0, 0}, s_hi[2] = {0, 0};
+            col_blocks(tile, 0, lane, cc[0][0], cc[0][1], s_lo[0], s_hi[0]);
+            col_blocks(tile, 32, lane, cc[1][0], cc[1][1], s_lo[1], s_hi[1]);
+            const int64_t c = c0 + 2 * lane;
+            if (c < p.cols) {                              // cols % 32 == 0: c + 1 valid too
+                uint8_t* sp = p.s_col + c * p.ld_s_col + (r0 >> 5);
+                if (second) {
+                    st_global_u16(sp, s_lo[0] | (s_lo[1] << 8));
+                    st_global_u16(sp + p.ld_s_col, s_hi[0] | (s_hi[1] << 8));
+                } else {
+                    st_global_u8(sp, s_lo[0]);
+                    st_global_u8(sp + p.ld_s_col, s_hi[0]);
+                }
+            }
         }
+        if (kRowwise) {
+#pragma unroll
+            for (int rr = 0; rr < 2; ++rr) {
+                uint32_t sb[2];
+                row_blocks(tile + (lane + 32 * rr) * 128, lane & 7, rc[rr], sb);
+                const int64_t r = r0 + lane + 32 * rr;
+                if (r < p.rows) {
+                    uint8_t* sp = p.s_row + r * p.ld_s_row + (c0 >> 5);
+                    if (c0 + 32 < p.cols) st_global_u16(sp, sb[0] | (sb[1] << 8));
+                    else st_global_u8(sp, sb[0]);
+                }
+            }
+        }
+        __syncwarp();                     // every lane has read the unit: reuse it for the codes
+        if (kRowwise) {
+#pragma unroll
+            for (int rr = 0; rr < 2; ++rr) {
+                const int r = lane + 32 * rr;
+#pragma unroll
+                for (int c = 0; c < 4; ++c) {
+                    const uint32_t* w = rc[rr][c >> 1] + 4 * (c & 1);
+                    sts128(tile + sw64(r, c), w[0], w[1], w[2], w[3]);
+                }
+            }
+        }
+        if (kColwise) {
+#pragma unroll
+            for (int j = 0; j < 2; ++j) {
+                const int cl = 2 * lane + j;
+#pragma unroll
+                for (int h = 0; h < 2; ++h)
+#pragma unroll
+                    for (int t = 0; t < 2; ++t) {
+                        const uint32_t* w = cc[h][j] + 4 * t;
+                        sts128(tile + 4096 + sw64(cl, 2 * h + t), w[0], w[1], w[2], w[3]);
+                    }
+            }
+        }
+        fence_proxy_async_smem();         // make the staged codes visible to the TMA engine
+        __syncwarp();
+        if (lane == 0) {
+            if (kRowwise) tma_store_2d(&qrow_map, tile, int32_t(c0), int32_t(r0));
+            if (kColwise) tma_store_2d(&qcol_map, tile + 4096, int32_t(r0), int32_t(c0));
+            bulk_commit();
+            if (i + kStages < n_mine) {
+                bulk_wait_read_all();     // the stores have read the tile: refill it
+                const int64_t un = gwarp + (i + kStages) * nwarps;
+                mbar_arrive_expect_tx(bar, kUnitBytes);
+                tma_load_2d(tile, &x_map, bar, int32_t((un % p.col_units) * kCols),
+                            int32_t((un / p.col_units) * kRows));
+            }
+        }
+        __syncwarp();
     }
+    if (lane == 0) bulk_wait_all();
 }
 
 template <bool R, bool C>
-cudaError_t launch(const CUtensorMap& map, const QuantizeParams& p, int sms, cudaStream_t stream) {
+cudaError_t launch(const CUtensorMap& xm, const CUtensorMap& qr, const CUtensorMap& qc, const QuantizeParams& p,
+                   int sms, cudaStream_t stream) {
     auto k = quantize_kernel<R, C>;
     cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
     if (e != cudaSuccess) return e;
     const int64_t want = (p.units + kWarps - 1) / kWarps;
     const int grid = int(want < sms ? want : sms);
-    k<<<grid, kWarps * 32, kSmemBytes, stream>>>(map, p);
+    k<<<grid, kWarps * 32, kSmemBytes, stream>>>(xm, qr, qc, p);
     return cudaGetLastError();
 }
 
@@ -234,16 +287,24 @@ te_mx_status quantize_launch(const QuantizeArgs& a, cudaStream_t stream) {
     const bool rowwise = a.q_row != nullptr, colwise = a.q_col != nullptr;
     if (a.rows == 0 || a.cols == 0 || (!rowwise && !colwise)) return TE_MX_OK;
 
-    CUtensorMap map;
-    te_mx_status st = encode_tensor_map_2d(&map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, a.x,
+    CUtensorMap xm, qr, qc;
+    te_mx_status st = encode_tensor_map_2d(&xm, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, a.x,
                                            uint64_t(a.cols), uint64_t(a.rows), uint64_t(a.ld_x) * 2,
                                            kCols, kRows, CU_TENSOR_MAP_SWIZZLE_128B);
     if (st != TE_MX_OK) return st;
+    qr = xm;
+    qc = xm;
+    if (rowwise && (st = encode_tensor_map_2d(&qr, CU_TENSOR_MAP_DATA_TYPE_UINT8, a.q_row, uint64_t(a.cols),
+                                              uint64_t(a.rows), uint64_t(a.cols), kCols, kRows,
+                                              CU_TENSOR_MAP_SWIZZLE_64B)) != TE_MX_OK) return st;
+    if (colwise && (st = encode_tensor_map_2d(&qc, CU_TENSOR_MAP_DATA_TYPE_UINT8, a.q_col, uint64_t(a.rows),
+                                              uint64_t(a.cols), uint64_t(a.rows), kRows, kCols,
+                                              CU_TENSOR_MAP_SWIZZLE_64B)) != TE_MX_OK) return st;
 
     QuantizeParams p;
     p.rows = a.rows; p.cols = a.cols;
-    p.q_row = a.q_row; p.s_row = a.s_row; p.ld_s_row = a.ld_s_row;
-    p.q_col = a.q_col; p.s_col = a.s_col; p.ld_s_col = a.ld_s_col;
+    p.s_row = a.s_row; p.ld_s_row = a.ld_s_row;
+    p.s_col = a.s_col; p.ld_s_col = a.ld_s_col;
     p.col_units = (a.cols + kCols - 1) / kCols;
     p.units = ((a.rows + kRows - 1) / kRows) * p.col_units;
     st = device_status_ptr(&p.status);
@@ -253,9 +314,9 @@ te_mx_status quantize_launch(const QuantizeArgs& a, cudaStream_t stream) {
     st = device_sm_count(&sms);
     if (st != TE_MX_OK) return st;
     cudaError_t e;
-    if (rowwise && colwise) e = launch<true, true>(map, p, sms, stream);
-    else if (rowwise) e = launch<true, false>(map, p, sms, stream);
-    else e = launch<false, true>(map, p, sms, stream);
+    if (rowwise && colwise) e = launch<true, true>(xm, qr, qc, p, sms, stream);
+    else if (rowwise) e = launch<true, false>(xm, qr, qc, p, sms, stream);
+    else e = launch<false, true>(xm, qr, qc, p, sms, stream);
     return cuda_status(e, "quantize kernel launch");
 }
 
