@@ -9,17 +9,30 @@
 // for MoE experts (ROCm/TransformerEngine README, "Single-Launch Grouped GEMM
 // Backends on ROCm").
 //
-// Kernel structure (one persistent CTA per SM, 10 warps):
-//   warp 0      TMA producer: A/B tiles (128-byte swizzle) and, every 4th
-//               K-step, the row-major scale tiles, into a kStages-deep ring;
-//   warp 1      TMEM owner and MMA issuer: turns each raw scale tile into the
-//               scale-factor layout in shared memory (an in-place 4x4 word
-//               transpose), copies it to TMEM with tcgen05.cp and issues 4
-//               block-scaled MMAs (K = 32 each) per 128-wide K-step;
-//   warps 2..9  epilogue: each takes one 32-lane quarter x 128 columns of the
-//               128 x 256 accumulator into registers, releases TMEM at once
-//               (so the next tile's MMAs overlap this tile's epilogue), then
-//               applies bias / GELU and stores bf16 D (and AUX).
+// Kernel structure (persistent, one CTA per SM, 11 warps), in two shapes:
+//   kPair = 1: one CTA computes a 128 x 256 tile (cta_group::1);
+//   kPair = 2: a cluster of two CTAs computes a 256 x 256 tile with
+//              cta_group::2 MMAs: each CTA holds 128 rows of A and 128 rows of
+//              B, the even CTA issues the MMAs and each CTA's TMEM receives
+//              its 128 x 256 accumulator.  Per SM this halves the B bytes a
+//              K-step needs, which is what limits the single-CTA shape (the
+//              ingress of an SM is ~53 B/clk; 48 KB per 512-cycle K-step does
+//              not fit).
+//   warp 0      TMA producer: A/B tiles (128-byte swizzle) into a kStages ring
+//               (completion on the MMA CTA's barrier) and, every 4th K-step,
+//               the row-major scale tiles (completion on the CTA's own barrier);
+//   warp 1      TMEM owner; in the MMA CTA one lane issues 4 block-scaled MMAs
+//               (K = 32 each) per 128-wide K-step and nothing else (a tcgen05
+//               instruction costs ~80-90 issue cycles, so the MMA thread has
+//               no slack for the scale copies);
+//   warp 10     scale-factor warp: turns each landed scale tile into the
+//               tcgen05 scale-factor layout in place (a 4x4 word transpose),
+//               copies the group's scale factors into TMEM (tcgen05.cp, from the
+//               MMA CTA for a pair) and commits them to the MMA warp;
+//   warps 2..9  epilogue: each takes one 32-lane quarter x 128 columns of its
+//               CTA's 128 x 256 accumulator into registers, releases TMEM at
+//               once (so the next tile's MMAs overlap this tile's epilogue),
+//               then applies bias / GELU and stores bf16 D (and AUX).
 // Every mbarrier wait is bounded; a wait that gives up aborts the CTA cleanly
 // and sets the device status word.
 #include <cuda_runtime.h>
@@ -31,43 +44,58 @@ namespace temx {
 
 namespace {
 
-constexpr int kBM = 128;                 // tile rows (TMEM lanes)
+constexpr int kBM = 128;                 // accumulator rows per CTA (TMEM lanes)
 constexpr int kBN = 256;                 // tile columns (accumulator columns)
 constexpr int kBK = 128;                 // K per pipeline stage (bytes of E4M3)
-constexpr int kStages = 4;
-constexpr int kThreads = 320;
+constexpr int kThreads = 352;
 constexpr int kEpiWarps = 8;
+constexpr int kSfWarp = 10;
 constexpr int kGroupM = 16;              // m-tiles per raster band (L2 reuse of B)
 constexpr int kMaxGroups = 1024;
-
-constexpr int kABytes = kBM * kBK;       // 16 KB
-constexpr int kBBytes = kBN * kBK;       // 32 KB
 constexpr int kSFABytes = kBM * 16;      // 128 rows x 16 scale bytes (4 K-steps)
-constexpr int kSFBBytes = kBN * 16;
-constexpr int kStageBytes = kABytes + kBBytes + kSFABytes + kSFBBytes;   // 55296
-constexpr int kSmemDyn = kStages * kStageBytes + 1024;
+constexpr int kSFBBytes = kBN * 16;      // every CTA holds all 256 B rows' scales
+constexpr int kSfGroupBytes = kSFABytes + kSFBBytes;   // one scale group (4 K-steps)
+constexpr int kSfRing = 3;               // scale-group slots in shared memory
+constexpr int kSfAhead = 2;              // scale groups loaded ahead of the one being prepared
+constexpr int kSfTmemGroups = 4;         // scale groups resident in TMEM
 
-// TMEM columns: accumulator [0, 256); scale-factor slots from 256, 8 slots of
-// 12 columns (4 for A's 128 rows, 8 for B's 256 rows).
+template <int kPair>
+struct Cfg {
+    static constexpr int kTileM = kBM * kPair;            // rows of one (pair) tile
+    static constexpr int kBRows = kBN / kPair;            // B rows loaded per CTA
+    static constexpr int kABytes = kBM * kBK;             // 16 KB
+    static constexpr int kBBytes = kBRows * kBK;          // 32 KB or 16 KB
+    static constexpr int kStages = kPair == 2 ? 6 : 4;
+    static constexpr int kStageBytes = kABytes + kBBytes;
+    static constexpr int kSmemDyn = kStages * kStageBytes + kSfRing * kSfGroupBytes + 1024;
+    // Instruction descriptor, kind::mxf8f6f4 with block scaling: E4M3 A and B
+    // (format 0), both K-major, N >> 3 at bit 17, UE8M0 scales (bit 23),
+    // M >> 4 at bit 24; scale-factor byte ids at bits 4..5 (B) and 29..30 (A).
+    static constexpr uint32_t kIdescBase =
+        (uint32_t(kBN >> 3) << 17) | (1u << 23) | (uint32_t(kTileM >> 4) << 24);
+};
+static_assert(Cfg<1>::kStageBytes % 1024 == 0 && Cfg<2>::kStageBytes % 1024 == 0, "stage alignment");
+
+__device__ __forceinline__ uint32_t idesc_sf(uint32_t base, uint32_t sf_id) {
+    return base | (sf_id << 4) | (sf_id << 29);
+}
+
+// TMEM columns: accumulator [0, 256); scale-factor slots from 256, 16 slots
+// of 12 columns (4 for A's 128 rows, 8 for B's 256 rows): K-step c of scale
+// group j uses slot (j % 4) * 4 + c.  The scale-factor warp copies group j
+// only after the MMAs of group j - 3 completed, so a slot is never rewritten
+// while an MMA may still read it.
 constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kSfCol0 = 256;
 constexpr uint32_t kSfSlotCols = 12;
-constexpr uint32_t kSfSlots = 8;
-
-// Instruction descriptor, kind::mxf8f6f4 with block scaling: E4M3 A and B
-// (format 0), both K-major, N >> 3 at bit 17, UE8M0 scales (bit 23),
-// M >> 4 at bit 24; scale-factor byte ids at bits 4..5 (B) and 29..30 (A).
-constexpr uint32_t kIdescBase = (uint32_t(kBN >> 3) << 17) | (1u << 23) | (uint32_t(kBM >> 4) << 24);
-__device__ __forceinline__ uint32_t idesc_for(uint32_t sf_id) {
-    return kIdescBase | (sf_id << 4) | (sf_id << 29);
-}
+constexpr uint32_t kSfSlots = 16;
 
 struct GemmParams {
     int64_t M;               // dense: rows of A/D; grouped: total_m (rows of X/D)
     int32_t N, K;
     int32_t k_iters;         // K / 128
     int32_t n_tiles;         // ceil(N / 256)
-    int32_t m_tiles;         // dense: ceil(M / 128)
+    int32_t m_tiles;         // dense: ceil(M / tile rows)
     int64_t total_tiles;     // dense only
     int32_t groups;          // 0: dense
     const int32_t* group_m;  // device
@@ -81,19 +109,24 @@ struct GemmParams {
 __device__ __forceinline__ int64_t imin64(int64_t a, int64_t b) { return a < b ? a : b; }
 
 struct Tile {
-    int32_t a_row;           // first A row (TMA coordinate)
+    int32_t a_row;           // first row of the (pair) tile
     int32_t row_end;         // rows >= row_end are not stored
     int32_t n0;              // first output column
-    int32_t b_row;           // first B row (TMA coordinate)
+    int32_t b_row;           // first B row of the tile
     int32_t group;           // bias / B group
 };
 
 // Shared state besides the stage ring.
+template <int kStages>
 struct __align__(16) SharedState {
-    uint64_t full[kStages];
-    uint64_t empty[kStages];
+    uint64_t full[kStages];                // A/B bytes landed (used in the MMA CTA)
+    uint64_t empty[kStages];               // stage consumed by the MMAs (each CTA)
+    uint64_t sf_full[kSfRing];             // this CTA's scale group landed in its ring slot
+    uint64_t sf_ready[kSfRing];            // the group's scale factors are in TMEM (each CTA of a pair)
+    uint64_t sf_peer[kSfRing];             // (MMA CTA of a pair) the peer's scale group is in copy layout
+    uint64_t grp_done[kSfTmemGroups];      // (MMA CTA) the MMAs of a scale group completed
     uint64_t tmem_full;
-    uint64_t tmem_empty;
+    uint64_t tmem_empty;                   // (MMA CTA) accumulator drained by every epilogue warp
     uint32_t tmem_base;
     int32_t abort;
     int64_t grouped_tiles;                 // total tiles of a grouped launch
@@ -105,7 +138,8 @@ struct __align__(16) SharedState {
 // a band, so the CTAs running at one time share a few A row-bands and B
 // column-bands in L2.  Grouped: group-major, then n-major over the group's
 // m-tiles.  `hint` carries the group found last time (tiles increase).
-__device__ __forceinline__ Tile map_tile(const GemmParams& p, const SharedState& sh, int64_t t, int32_t& hint) {
+template <int kTileM, typename SH>
+__device__ __forceinline__ Tile map_tile(const GemmParams& p, const SH& sh, int64_t t, int32_t& hint) {
     Tile tl;
     if (p.groups == 0) {
         const int64_t per_band = int64_t(kGroupM) * p.n_tiles;
@@ -115,8 +149,8 @@ __device__ __forceinline__ Tile map_tile(const GemmParams& p, const SharedState&
         const int64_t local = t - band * per_band;
         const int32_t mt = first_m + int32_t(local % gm);
         const int32_t nt = int32_t(local / gm);
-        tl.a_row = mt * kBM;
-        tl.row_end = int32_t(imin64(p.M, int64_t(tl.a_row) + kBM));
+        tl.a_row = mt * kTileM;
+        tl.row_end = int32_t(imin64(p.M, int64_t(tl.a_row) + kTileM));
         tl.n0 = nt * kBN;
         tl.b_row = tl.n0;
         tl.group = 0;
@@ -126,10 +160,10 @@ __device__ __forceinline__ Tile map_tile(const GemmParams& p, const SharedState&
         hint = g;
         const int32_t local = int32_t(t - sh.tile_start[g]);
         const int32_t rows = sh.row_start[g + 1] - sh.row_start[g];
-        const int32_t mtg = (rows + kBM - 1) / kBM;
+        const int32_t mtg = (rows + kTileM - 1) / kTileM;
         const int32_t mt = local % mtg, nt = local / mtg;
-        tl.a_row = sh.row_start[g] + mt * kBM;
-        tl.row_end = min(sh.row_start[g + 1], tl.a_row + kBM);
+        tl.a_row = sh.row_start[g] + mt * kTileM;
+        tl.row_end = min(sh.row_start[g + 1], tl.a_row + kTileM);
         tl.n0 = nt * kBN;
         tl.b_row = g * p.N + tl.n0;
         tl.group = g;
@@ -141,7 +175,8 @@ __device__ __forceinline__ Tile map_tile(const GemmParams& p, const SharedState&
 // owns rows [row_start[g], row_start[g+1]) and linear tiles [tile_start[g],
 // tile_start[g+1]).  Sizes are clamped so that no group reaches past total_m;
 // a negative size or a sum above total_m sets the status word.
-__device__ void group_prefix(const GemmParams& p, SharedState& sh, int lane) {
+template <int kTileM, typename SH>
+__device__ void group_prefix(const GemmParams& p, SH& sh, int lane) {
     const int G = p.groups;
     const int per = (G + 31) / 32;
     const int lo = min(G, lane * per), hi = min(G, lo + per);
@@ -162,7 +197,7 @@ __device__ void group_prefix(const GemmParams& p, SharedState& sh, int lane) {
         const int32_t m = max(p.group_m[g], 0);
         const int64_t start = imin64(row, p.M), end = imin64(row + m, p.M);
         sh.row_start[g] = int32_t(start);
-        tsum += (end - start + kBM - 1) / kBM * p.n_tiles;
+        tsum += (end - start + kTileM - 1) / kTileM * p.n_tiles;
         row += m;
     }
     if (hi == G && lo < hi) sh.row_start[G] = int32_t(imin64(row, p.M));
@@ -178,7 +213,7 @@ __device__ void group_prefix(const GemmParams& p, SharedState& sh, int lane) {
         const int32_t m = max(p.group_m[g], 0);
         const int64_t start = imin64(row, p.M), end = imin64(row + m, p.M);
         sh.tile_start[g] = int32_t(t0);
-        t0 += (end - start + kBM - 1) / kBM * p.n_tiles;
+        t0 += (end - start + kTileM - 1) / kTileM * p.n_tiles;
         row += m;
     }
     if (lane == 31) {
@@ -189,7 +224,8 @@ __device__ void group_prefix(const GemmParams& p, SharedState& sh, int lane) {
 }
 
 // Bounded mbarrier wait that also returns false once another role aborted.
-__device__ __forceinline__ bool wait_or_abort(uint32_t bar, uint32_t parity, SharedState& sh,
+template <typename SH>
+__device__ __forceinline__ bool wait_or_abort(uint32_t bar, uint32_t parity, SH& sh,
                                               unsigned int* status) {
     if (mbar_try_wait(bar, parity)) return true;
     const unsigned long long t0 = globaltimer_ns();
@@ -209,26 +245,20 @@ __device__ __forceinline__ bool wait_or_abort(uint32_t bar, uint32_t parity, Sha
 // K-step c) -> scale-factor layout for tcgen05.cp 32x128b: for each 128-row
 // atom and K-step c, 512 bytes where byte j*16 + i*4 + b is scale byte b of
 // row 32i + j.  In place; the whole warp reads before anyone writes.
-__device__ __forceinline__ void sf_to_tmem_layout(uint8_t* sf, int atoms, int lane) {
+__device__ __forceinline__ void sf_to_tmem_layout(uint32_t sf, int lane) {
     uint4 v[3][4];
 #pragma unroll
-    for (int a = 0; a < 3; ++a) {
-        if (a < atoms) {
+    for (int a = 0; a < 3; ++a)
 #pragma unroll
-            for (int i = 0; i < 4; ++i)
-                v[a][i] = *reinterpret_cast<const uint4*>(sf + a * 2048 + (32 * i + lane) * 16);
-        }
-    }
+        for (int i = 0; i < 4; ++i) v[a][i] = lds128(sf + a * 2048 + (32 * i + lane) * 16);
     __syncwarp();
 #pragma unroll
     for (int a = 0; a < 3; ++a) {
-        if (a < atoms) {
-            uint8_t* base = sf + a * 2048 + lane * 16;
-            *reinterpret_cast<uint4*>(base + 0 * 512) = make_uint4(v[a][0].x, v[a][1].x, v[a][2].x, v[a][3].x);
-            *reinterpret_cast<uint4*>(base + 1 * 512) = make_uint4(v[a][0].y, v[a][1].y, v[a][2].y, v[a][3].y);
-            *reinterpret_cast<uint4*>(base + 2 * 512) = make_uint4(v[a][0].z, v[a][1].z, v[a][2].z, v[a][3].z);
-            *reinterpret_cast<uint4*>(base + 3 * 512) = make_uint4(v[a][0].w, v[a][1].w, v[a][2].w, v[a][3].w);
-        }
+        const uint32_t base = sf + a * 2048 + lane * 16;
+        sts128(base + 0 * 512, v[a][0].x, v[a][1].x, v[a][2].x, v[a][3].x);
+        sts128(base + 1 * 512, v[a][0].y, v[a][1].y, v[a][2].y, v[a][3].y);
+        sts128(base + 2 * 512, v[a][0].z, v[a][1].z, v[a][2].z, v[a][3].z);
+        sts128(base + 3 * 512, v[a][0].w, v[a][1].w, v[a][2].w, v[a][3].w);
     }
 }
 
@@ -283,22 +313,38 @@ __device__ __forceinline__ void store_chunk(const uint32_t* acc, const GemmParam
     st_global_v4(p.D + off + 8, o[4], o[5], o[6], o[7]);
 }
 
+template <int kPair>
 __global__ void __launch_bounds__(kThreads, 1)
 gemm_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_constant__ CUtensorMap map_b,
             const __grid_constant__ CUtensorMap map_sfa, const __grid_constant__ CUtensorMap map_sfb,
             const GemmParams p) {
+    using C = Cfg<kPair>;
+    using SH = SharedState<C::kStages>;
     extern __shared__ uint8_t smem_raw[];
-    __shared__ SharedState sh;
+    __shared__ SH sh;
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const uint32_t rank = kPair == 2 ? cluster_ctarank() : 0u;     // 0 = the MMA CTA
+    const int64_t unit = kPair == 2 ? blockIdx.x / 2 : blockIdx.x;  // cluster (pair) index
+    const int64_t units = kPair == 2 ? gridDim.x / 2 : gridDim.x;
+    // Barriers of the MMA CTA as seen from this CTA (cluster addresses for pairs).
+    auto leader = [&](const uint64_t& bar) -> uint32_t {
+        return kPair == 2 ? mapa_shared(smem_u32(&bar), 0) : smem_u32(&bar);
+    };
 
     if (threadIdx.x == 0) {
-        for (int s = 0; s < kStages; ++s) {
-            mbar_init(smem_u32(&sh.full[s]), 1);
+        for (int s = 0; s < C::kStages; ++s) {
+            mbar_init(smem_u32(&sh.full[s]), kPair);
             mbar_init(smem_u32(&sh.empty[s]), 1);
         }
+        for (int s = 0; s < kSfRing; ++s) {
+            mbar_init(smem_u32(&sh.sf_full[s]), 1);
+            mbar_init(smem_u32(&sh.sf_ready[s]), 1);
+            mbar_init(smem_u32(&sh.sf_peer[s]), 1);
+        }
+        for (int s = 0; s < kSfTmemGroups; ++s) mbar_init(smem_u32(&sh.grp_done[s]), 1);
         mbar_init(smem_u32(&sh.tmem_full), 1);
-        mbar_init(smem_u32(&sh.tmem_empty), kEpiWarps);
+        mbar_init(smem_u32(&sh.tmem_empty), kEpiWarps * kPair);
         sh.abort = 0;
         sh.grouped_tiles = 0;
         fence_mbarrier_init();
@@ -308,95 +354,191 @@ gemm_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_constant__ C
         tma_prefetch_desc(&map_sfb);
     }
     if (warp == 1) {
-        tmem_alloc(smem_u32(&sh.tmem_base), kTmemCols);
-        tmem_relinquish();
+        if constexpr (kPair == 2) {
+            tmem_alloc_pair(smem_u32(&sh.tmem_base), kTmemCols);
+            tmem_relinquish_pair();
+        } else {
+            tmem_alloc(smem_u32(&sh.tmem_base), kTmemCols);
+            tmem_relinquish();
+        }
         tc_fence_before();
     }
-    if (p.groups > 0 && warp == 2) group_prefix(p, sh, lane);
+    if (p.groups > 0 && warp == 2) group_prefix<C::kTileM>(p, sh, lane);
     __syncthreads();
+    if constexpr (kPair == 2) cluster_sync();      // peer barriers initialised before any remote use
     tc_fence_after();
     const uint32_t tmem = sh.tmem_base;
     const int64_t total = p.groups > 0 ? sh.grouped_tiles : p.total_tiles;
 
     if (warp == 0) {
-        // ------------------------------------------------ TMA producer
+        // ------------------------------------------------ TMA producer (every CTA)
         if (lane == 0) {
             int32_t hint = 0;
             uint32_t stage = 0, phase = 0;
-            for (int64_t t = blockIdx.x; t < total; t += gridDim.x) {
-                const Tile tl = map_tile(p, sh, t, hint);
-                bool ok = true;
-                for (int32_t k = 0; k < p.k_iters && ok; ++k) {
+            bool ok = true;
+            for (int64_t t = unit; t < total && ok; t += units) {
+                const Tile tl = map_tile<C::kTileM>(p, sh, t, hint);
+                const int32_t a_row = tl.a_row + int32_t(rank) * kBM;
+                const int32_t b_row = tl.b_row + int32_t(rank) * C::kBRows;
+                for (int32_t k = 0; k < p.k_iters; ++k) {
                     if (!wait_or_abort(smem_u32(&sh.empty[stage]), phase ^ 1u, sh, p.status)) { ok = false; break; }
-                    uint8_t* st = smem + stage * kStageBytes;
-                    const uint32_t full = smem_u32(&sh.full[stage]);
-                    const bool sf = (k & 3) == 0;
-                    mbar_arrive_expect_tx(full, kABytes + kBBytes + (sf ? kSFABytes + kSFBBytes : 0));
-                    tma_load_2d(smem_u32(st), &map_a, full, k * kBK, tl.a_row);
-                    tma_load_2d(smem_u32(st + kABytes), &map_b, full, k * kBK, tl.b_row);
-                    if (sf) {
-                        tma_load_2d(smem_u32(st + kABytes + kBBytes), &map_sfa, full, k * 4, tl.a_row);
-                        tma_load_2d(smem_u32(st + kABytes + kBBytes + kSFABytes), &map_sfb, full, k * 4, tl.b_row);
+                    uint8_t* st = smem + stage * C::kStageBytes;
+                    const uint32_t full = leader(sh.full[stage]);
+                    if constexpr (kPair == 2) {
+                        if (rank == 0) mbar_arrive_expect_tx(smem_u32(&sh.full[stage]), C::kABytes + C::kBBytes);
+                        else mbar_arrive_expect_tx_cluster_relaxed(full, C::kABytes + C::kBBytes);
+                        tma_load_2d_pair(smem_u32(st), &map_a, full, k * kBK, a_row);
+                        tma_load_2d_pair(smem_u32(st + C::kABytes), &map_b, full, k * kBK, b_row);
+                    } else {
+                        mbar_arrive_expect_tx(full, C::kABytes + C::kBBytes);
+                        tma_load_2d(smem_u32(st), &map_a, full, k * kBK, a_row);
+                        tma_load_2d(smem_u32(st + C::kABytes), &map_b, full, k * kBK, b_row);
                     }
-                    if (++stage == kStages) { stage = 0; phase ^= 1u; }
+                    if (++stage == C::kStages) { stage = 0; phase ^= 1u; }
                 }
-                if (!ok) break;
             }
         }
     } else if (warp == 1) {
-        // ------------------------------------------------ MMA issuer
-        uint32_t stage = 0, phase = 0, gk = 0;
-        int32_t local = 0;
-        bool ok = true;
-        for (int64_t t = blockIdx.x; t < total && ok; t += gridDim.x, ++local) {
-            if (local > 0) {
-                if (!wait_or_abort(smem_u32(&sh.tmem_empty), uint32_t(local - 1) & 1u, sh, p.status)) break;
-                tc_fence_after();
-            }
-            for (int32_t k = 0; k < p.k_iters; ++k) {
-                if (!wait_or_abort(smem_u32(&sh.full[stage]), phase, sh, p.status)) { ok = false; break; }
-                uint8_t* st = smem + stage * kStageBytes;
-                uint8_t* sfa = st + kABytes + kBBytes;
-                if ((k & 3) == 0) {
-                    sf_to_tmem_layout(sfa, 3, lane);          // A atom + 2 B atoms (contiguous)
-                    fence_proxy_async_smem();
-                    __syncwarp();
-                    if (lane == 0) {
-                        tc_fence_after();
-                        const int nchunks = min(4, p.k_iters - k);
-                        for (int c = 0; c < nchunks; ++c) {
-                            const uint32_t col = tmem + kSfCol0 + ((gk + c) % kSfSlots) * kSfSlotCols;
-                            tc_cp_32x128b_warpx4(col + 0, smem_desc(smem_u32(sfa + c * 512), 0, 128, 0));
-                            tc_cp_32x128b_warpx4(col + 4, smem_desc(smem_u32(sfa + 2048 + c * 512), 0, 128, 0));
-                            tc_cp_32x128b_warpx4(col + 8, smem_desc(smem_u32(sfa + 4096 + c * 512), 0, 128, 0));
-                        }
-                    }
-                }
-                if (lane == 0) {
+        // ------------------------------------------------ MMA issuer (one lane of the MMA CTA)
+        if (lane == 0 && rank == 0) {
+            uint32_t stage = 0, phase = 0, grp = 0;   // grp: global index of the current scale group
+            int32_t local = 0;
+            bool ok = true;
+            for (int64_t t = unit; t < total && ok; t += units, ++local) {
+                if (local > 0) {
+                    if (!wait_or_abort(smem_u32(&sh.tmem_empty), uint32_t(local - 1) & 1u, sh, p.status)) break;
                     tc_fence_after();
-                    const uint32_t sf_col = tmem + kSfCol0 + (gk % kSfSlots) * kSfSlotCols;
-                    const uint32_t a_base = smem_u32(st), b_base = smem_u32(st + kABytes);
+                }
+                for (int32_t k = 0; k < p.k_iters; ++k) {
+                    if (!wait_or_abort(smem_u32(&sh.full[stage]), phase, sh, p.status)) { ok = false; break; }
+                    uint8_t* st = smem + stage * C::kStageBytes;
+                    if ((k & 3) == 0) {
+                        if (!wait_or_abort(smem_u32(&sh.sf_ready[grp % kSfRing]), (grp / kSfRing) & 1u, sh, p.status)) {
+                            ok = false;
+                            break;
+                        }
+                        tc_fence_after();
+                    }
+                    const uint32_t sf_col =
+                        tmem + kSfCol0 + ((grp % kSfTmemGroups) * 4 + uint32_t(k & 3)) * kSfSlotCols;
+                    const uint64_t a_desc = smem_desc(smem_u32(st), 16, 1024, 2);
+                    const uint64_t b_desc = smem_desc(smem_u32(st + C::kABytes), 16, 1024, 2);
 #pragma unroll
                     for (int kk = 0; kk < 4; ++kk) {
-                        mma_mxf8(tmem, smem_desc(a_base + kk * 32, 16, 1024, 2), smem_desc(b_base + kk * 32, 16, 1024, 2),
-                                 idesc_for(uint32_t(kk)), sf_col, sf_col + 4, (k | kk) != 0 ? 1u : 0u);
+                        // +32 bytes along K inside the 128-byte swizzled row = +2 in the address field
+                        const uint32_t idesc = idesc_sf(C::kIdescBase, uint32_t(kk));
+                        const uint32_t acc = (k | kk) != 0 ? 1u : 0u;
+                        if constexpr (kPair == 2)
+                            mma_mxf8_pair(tmem, a_desc + 2 * kk, b_desc + 2 * kk, idesc, sf_col, sf_col + 4, acc);
+                        else
+                            mma_mxf8(tmem, a_desc + 2 * kk, b_desc + 2 * kk, idesc, sf_col, sf_col + 4, acc);
                     }
-                    tc_commit(smem_u32(&sh.empty[stage]));
+                    if constexpr (kPair == 2) tc_commit_pair_mc(smem_u32(&sh.empty[stage]), 0x3);
+                    else tc_commit(smem_u32(&sh.empty[stage]));
+                    if ((k & 3) == 3 || k == p.k_iters - 1) {      // last K-step of the scale group
+                        if constexpr (kPair == 2) tc_commit_pair_mc(smem_u32(&sh.grp_done[grp % kSfTmemGroups]), 0x1);
+                        else tc_commit(smem_u32(&sh.grp_done[grp % kSfTmemGroups]));
+                        ++grp;
+                    }
+                    if (++stage == C::kStages) { stage = 0; phase ^= 1u; }
                 }
-                __syncwarp();
-                ++gk;
-                if (++stage == kStages) { stage = 0; phase ^= 1u; }
+                if (!ok) break;
+                if constexpr (kPair == 2) tc_commit_pair_mc(smem_u32(&sh.tmem_full), 0x3);
+                else tc_commit(smem_u32(&sh.tmem_full));
             }
-            if (!ok) break;
-            if (lane == 0) tc_commit(smem_u32(&sh.tmem_full));
-            __syncwarp();
+        }
+    } else if (warp == kSfWarp) {
+        // ------------------------------------------------ scale-factor layout (every CTA)
+        // Scale groups (4 K-steps each, the last of a tile possibly shorter)
+        // go through a kSfRing-slot ring: lane 0 loads group j + kSfAhead
+        // while group j is prepared.  Group j is copied into TMEM only after
+        // the MMAs of group j - 3 completed (grp_done); that keeps its TMEM
+        // slots free and also means the MMA warp has passed its wait on
+        // sf_ready of group j - 3, the previous user of this ring slot.  A ring
+        // slot is reloaded only after the copies of its previous group landed
+        // (sf_ready).  So every barrier phase here is observed by its waiter
+        // before the barrier can complete again.
+        uint8_t* ring = smem + C::kStages * C::kStageBytes;
+        const int32_t ngroups = (p.k_iters + 3) / 4;
+        int64_t lt = unit;                // next group to load: tile lt, group lg
+        int32_t lg = 0, lhint = 0;
+        uint32_t jl = 0;                  // its global index
+        Tile ltl{};
+        if (lt < total) ltl = map_tile<C::kTileM>(p, sh, lt, lhint);
+        bool ok = true;
+        auto load_next = [&]() -> bool {  // lane 0
+            if (lt >= total) return true;
+            const uint32_t slot = jl % kSfRing;
+            if (jl >= kSfRing &&
+                !wait_or_abort(smem_u32(&sh.sf_ready[slot]), ((jl / kSfRing) - 1) & 1u, sh, p.status))
+                return false;
+            const uint32_t bar = smem_u32(&sh.sf_full[slot]);
+            const uint32_t dst = smem_u32(ring + slot * kSfGroupBytes);
+            mbar_arrive_expect_tx(bar, kSfGroupBytes);
+            tma_load_2d(dst, &map_sfa, bar, lg * 16, ltl.a_row + int32_t(rank) * kBM);
+            tma_load_2d(dst + kSFABytes, &map_sfb, bar, lg * 16, ltl.b_row);
+            ++jl;
+            if (++lg == ngroups) {
+                lg = 0;
+                lt += units;
+                if (lt < total) ltl = map_tile<C::kTileM>(p, sh, lt, lhint);
+            }
+            return true;
+        };
+        if (lane == 0)
+            for (int i = 0; i < kSfAhead && ok; ++i) ok = load_next();
+        ok = __shfl_sync(0xFFFFFFFFu, ok, 0);
+        uint32_t j = 0;
+        for (int64_t t = unit; t < total && ok; t += units) {
+            for (int32_t g = 0; g < ngroups && ok; ++g, ++j) {
+                const uint32_t slot = j % kSfRing, bit = (j / kSfRing) & 1u;
+                if (!wait_or_abort(smem_u32(&sh.sf_full[slot]), bit, sh, p.status)) { ok = false; break; }
+                const uint32_t sf = smem_u32(ring + slot * kSfGroupBytes);
+                sf_to_tmem_layout(sf, lane);
+                fence_proxy_async_smem();
+                __syncwarp();
+                if (lane == 0) {
+                    if (kPair == 2 && rank != 0) {
+                        mbar_arrive_cluster(leader(sh.sf_peer[slot]));
+                    } else {
+                        if (kPair == 2) ok = wait_or_abort(smem_u32(&sh.sf_peer[slot]), bit, sh, p.status);
+                        if (ok && j >= 3)
+                            ok = wait_or_abort(smem_u32(&sh.grp_done[(j - 3) % kSfTmemGroups]),
+                                               ((j - 3) / kSfTmemGroups) & 1u, sh, p.status);
+                        if (ok) {
+                            tc_fence_after();
+                            const int nchunks = min(4, p.k_iters - 4 * g);
+                            for (int c = 0; c < nchunks; ++c) {
+                                const uint32_t col = tmem + kSfCol0 + ((j % kSfTmemGroups) * 4 + c) * kSfSlotCols;
+                                const uint64_t d0 = smem_desc(sf + c * 512, 0, 128, 0);
+                                const uint64_t d1 = smem_desc(sf + 2048 + c * 512, 0, 128, 0);
+                                const uint64_t d2 = smem_desc(sf + 4096 + c * 512, 0, 128, 0);
+                                if constexpr (kPair == 2) {
+                                    tc_cp_32x128b_warpx4_pair(col + 0, d0);
+                                    tc_cp_32x128b_warpx4_pair(col + 4, d1);
+                                    tc_cp_32x128b_warpx4_pair(col + 8, d2);
+                                } else {
+                                    tc_cp_32x128b_warpx4(col + 0, d0);
+                                    tc_cp_32x128b_warpx4(col + 4, d1);
+                                    tc_cp_32x128b_warpx4(col + 8, d2);
+                                }
+                            }
+                            // sf_ready completes once these copies landed (in both CTAs of a pair)
+                            if constexpr (kPair == 2) tc_commit_pair_mc(smem_u32(&sh.sf_ready[slot]), 0x3);
+                            else tc_commit(smem_u32(&sh.sf_ready[slot]));
+                        }
+                    }
+                    if (ok) ok = load_next();
+                }
+                ok = __shfl_sync(0xFFFFFFFFu, ok, 0);
+            }
         }
     } else {
-        // ------------------------------------------------ epilogue
+        // ------------------------------------------------ epilogue (every CTA)
         const int e = warp - 2, q = warp & 3, h = e >> 2;
         int32_t hint = 0, local = 0;
-        for (int64_t t = blockIdx.x; t < total; t += gridDim.x, ++local) {
-            const Tile tl = map_tile(p, sh, t, hint);
+        for (int64_t t = unit; t < total; t += units, ++local) {
+            const Tile tl = map_tile<C::kTileM>(p, sh, t, hint);
             if (!wait_or_abort(smem_u32(&sh.tmem_full), uint32_t(local) & 1u, sh, p.status)) break;
             tc_fence_after();
             uint32_t acc0[64], acc1[64];
@@ -406,8 +548,11 @@ gemm_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_constant__ C
             tmem_ld_wait();
             tc_fence_before();
             __syncwarp();
-            if (lane == 0) mbar_arrive(smem_u32(&sh.tmem_empty));
-            const int64_t row = int64_t(tl.a_row) + 32 * q + lane;
+            if (lane == 0) {
+                if constexpr (kPair == 2) mbar_arrive_cluster(leader(sh.tmem_empty));
+                else mbar_arrive(smem_u32(&sh.tmem_empty));
+            }
+            const int64_t row = int64_t(tl.a_row) + int64_t(rank) * kBM + 32 * q + lane;
             if (row < tl.row_end) {
                 const uint16_t* bias = p.has_bias ? p.bias + int64_t(tl.group) * p.N : nullptr;
                 const int32_t nb = tl.n0 + 128 * h;
@@ -422,15 +567,17 @@ gemm_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_constant__ C
     }
 
     __syncthreads();
+    if constexpr (kPair == 2) cluster_sync();      // no CTA leaves while its peer may still signal it
     if (warp == 1) {
         tc_fence_after();
-        tmem_dealloc(tmem, kTmemCols);
+        if constexpr (kPair == 2) tmem_dealloc_pair(tmem, kTmemCols);
+        else tmem_dealloc(tmem, kTmemCols);
     }
 }
 
-}  // namespace
-
-te_mx_status gemm_launch(const GemmArgs& a, cudaStream_t stream) {
+template <int kPair>
+te_mx_status launch_gemm(const GemmArgs& a, int sms, unsigned int* status, cudaStream_t stream) {
+    using C = Cfg<kPair>;
     const bool grouped = a.groups > 0;
     const uint64_t b_rows = grouped ? uint64_t(a.groups) * uint64_t(a.N) : uint64_t(a.N);
     const uint64_t sf_cols = uint64_t(a.K / 32) < 16 ? 16 : uint64_t(a.K / 32);
@@ -439,7 +586,7 @@ te_mx_status gemm_launch(const GemmArgs& a, cudaStream_t stream) {
     if ((st = encode_tensor_map_2d(&ma, CU_TENSOR_MAP_DATA_TYPE_UINT8, a.A, uint64_t(a.K), uint64_t(a.M),
                                    uint64_t(a.K), kBK, kBM, CU_TENSOR_MAP_SWIZZLE_128B)) != TE_MX_OK) return st;
     if ((st = encode_tensor_map_2d(&mb, CU_TENSOR_MAP_DATA_TYPE_UINT8, a.B, uint64_t(a.K), b_rows,
-                                   uint64_t(a.K), kBK, kBN, CU_TENSOR_MAP_SWIZZLE_128B)) != TE_MX_OK) return st;
+                                   uint64_t(a.K), kBK, C::kBRows, CU_TENSOR_MAP_SWIZZLE_128B)) != TE_MX_OK) return st;
     if ((st = encode_tensor_map_2d(&msa, CU_TENSOR_MAP_DATA_TYPE_UINT8, a.sA, sf_cols, uint64_t(a.M),
                                    uint64_t(a.ld_sA), 16, kBM, CU_TENSOR_MAP_SWIZZLE_NONE)) != TE_MX_OK) return st;
     if ((st = encode_tensor_map_2d(&msb, CU_TENSOR_MAP_DATA_TYPE_UINT8, a.sB, sf_cols, b_rows,
@@ -451,7 +598,7 @@ te_mx_status gemm_launch(const GemmArgs& a, cudaStream_t stream) {
     p.K = int32_t(a.K);
     p.k_iters = int32_t(a.K / kBK);
     p.n_tiles = int32_t((a.N + kBN - 1) / kBN);
-    p.m_tiles = int32_t((a.M + kBM - 1) / kBM);
+    p.m_tiles = int32_t((a.M + C::kTileM - 1) / C::kTileM);
     p.total_tiles = grouped ? 0 : int64_t(p.m_tiles) * p.n_tiles;
     p.groups = a.groups;
     p.group_m = a.group_m;
@@ -460,16 +607,52 @@ te_mx_status gemm_launch(const GemmArgs& a, cudaStream_t stream) {
     p.aux = static_cast<uint16_t*>(a.aux);
     p.has_bias = a.has_bias;
     p.gelu = a.gelu;
-    if ((st = device_status_ptr(&p.status)) != TE_MX_OK) return st;
+    p.status = status;
 
+    const int64_t slots = sms / kPair;                     // CTAs (pairs) resident at once
+    int64_t units = grouped ? slots : (p.total_tiles < slots ? p.total_tiles : slots);
+    if (units < 1) units = 1;
+    auto kern = gemm_kernel<kPair>;
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemDyn);
+    if (e != cudaSuccess) return cuda_status(e, "cudaFuncSetAttribute(gemm)");
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(unsigned(units * kPair));
+    cfg.blockDim = dim3(kThreads);
+    cfg.dynamicSmemBytes = C::kSmemDyn;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = kPair;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    if constexpr (kPair == 2) {
+        // persistent grid: never more pairs than can be resident together
+        int max_clusters = 0;
+        e = cudaOccupancyMaxActiveClusters(&max_clusters, kern, &cfg);
+        if (e != cudaSuccess) return cuda_status(e, "cudaOccupancyMaxActiveClusters(gemm)");
+        if (max_clusters < 1) return set_error(TE_MX_ERR_CUDA, "no CTA pair of the GEMM fits on this device");
+        if (units > max_clusters) units = max_clusters;
+        cfg.gridDim = dim3(unsigned(units * kPair));
+    }
+    e = cudaLaunchKernelEx(&cfg, kern, ma, mb, msa, msb, p);
+    return cuda_status(e, "gemm kernel launch");
+}
+
+}  // namespace
+
+te_mx_status gemm_launch(const GemmArgs& a, cudaStream_t stream) {
+    unsigned int* status = nullptr;
+    te_mx_status st = device_status_ptr(&status);
+    if (st != TE_MX_OK) return st;
     int sms = 0;
     if ((st = device_sm_count(&sms)) != TE_MX_OK) return st;
-    int64_t grid = grouped ? sms : (p.total_tiles < sms ? p.total_tiles : sms);
-    if (grid < 1) grid = 1;
-    cudaError_t e = cudaFuncSetAttribute(gemm_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemDyn);
-    if (e != cudaSuccess) return cuda_status(e, "cudaFuncSetAttribute(gemm)");
-    gemm_kernel<<<int(grid), kThreads, kSmemDyn, stream>>>(ma, mb, msa, msb, p);
-    return cuda_status(cudaGetLastError(), "gemm kernel launch");
+    // CTA pairs once there are enough 256-row tiles to fill the GPU; single
+    // CTAs for small problems (finer tiles, more of them).
+    const int64_t pair_tiles = ((a.M + 255) / 256) * ((a.N + kBN - 1) / kBN);
+    const bool pair = a.groups > 0 ? a.M >= 256 * 8 : pair_tiles >= sms / 2;
+    return pair ? launch_gemm<2>(a, sms, status, stream) : launch_gemm<1>(a, sms, status, stream);
 }
 
 }  // namespace temx

@@ -128,6 +128,29 @@ def test_dense_vs_oracle(M, N, K, bias, gelu):
     check_dense(M, N, K, bias, gelu, seed=M + N + K)
 
 
+# Shapes with at least 76 tiles of 256 x 256 run on CTA pairs (cta_group::2).
+@pytest.mark.parametrize("M,N,K,bias,gelu", [
+    (2048, 2560, 256, True, True),
+    (2000, 2624, 640, False, False),
+    (2304, 2304, 384, True, False),
+])
+def test_dense_pair_tiles_vs_oracle(M, N, K, bias, gelu):
+    check_dense(M, N, K, bias, gelu, seed=M + N + K + 1)
+
+
+def test_identity_b_pair_tiles_is_bit_exact():
+    m, k = 2048, 2560
+    qa, sa = O.quantize_rowwise(rand_bits((m, k), 41, std=3.0))
+    qb, sb = O.quantize_rowwise(O.f64_to_bf16_bits(np.eye(k)))
+    d, _ = run_gemm(*upload(qa, sa), *upload(qb, sb))
+    want = O.dequantize(qa, sa)
+    got = to_f64(d)
+    if not np.array_equal(got, want):
+        bad = np.argwhere(got != want)
+        i = tuple(bad[0])
+        raise AssertionError(f"{len(bad)} mismatches, first {i}: gpu {got[i]} want {want[i]}")
+
+
 def test_gelu_of_zero_and_of_bias():
     # A = 0: pre = bias, D = GELU(bias), AUX = bias; with no bias D = AUX = 0
     m, n, k = 128, 256, 256
@@ -182,6 +205,7 @@ def run_grouped(group_m, total_m, N, K, bias, gelu, seed):
 
 @pytest.mark.parametrize("group_m,N,K,bias,gelu", [
     ([0, 5, 130, 0, 256, 77], 160, 256, True, True),
+    ([700, 0, 1, 513, 900, 0, 300], 256, 256, True, True),        # >= 2048 rows: CTA pairs
     ([300], 256, 512, False, False),
     ([1, 0, 0, 129, 127, 128, 0, 2], 272, 384, True, False),
 ])
