@@ -126,7 +126,8 @@ struct __align__(16) SharedState {
     uint64_t sf_peer[kSfRing];             // (MMA CTA of a pair) the peer's scale group is in copy layout
     uint64_t grp_done[kSfTmemGroups];      // (MMA CTA) the MMAs of a scale group completed
     uint64_t tmem_full;
-    uint64_t tmem_empty;                   // (MMA CTA) accumulator drained by every epilogue warp
+    uint64_t tmem_empty;                   // (MMA CTA) accumulator drained by the epilogue of every CTA
+    uint64_t epi_drained;                  // this CTA's 8 epilogue warps hold their accumulator rows
     uint32_t tmem_base;
     int32_t abort;
     int64_t grouped_tiles;                 // total tiles of a grouped launch
@@ -344,7 +345,8 @@ gemm_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_constant__ C
         }
         for (int s = 0; s < kSfTmemGroups; ++s) mbar_init(smem_u32(&sh.grp_done[s]), 1);
         mbar_init(smem_u32(&sh.tmem_full), 1);
-        mbar_init(smem_u32(&sh.tmem_empty), kEpiWarps * kPair);
+        mbar_init(smem_u32(&sh.tmem_empty), kPair);
+        mbar_init(smem_u32(&sh.epi_drained), kEpiWarps);
         sh.abort = 0;
         sh.grouped_tiles = 0;
         fence_mbarrier_init();
@@ -547,21 +549,36 @@ gemm_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_constant__ C
             tmem_ld_32x32b_x64(taddr + 64, acc1);
             tmem_ld_wait();
             tc_fence_before();
+            // Once all 8 epilogue warps hold their registers, one relaxed arrive
+            // per CTA releases the accumulator (the reads retired at wait::ld;
+            // a release here would wait for this warp's earlier global stores).
             __syncwarp();
-            if (lane == 0) {
-                if constexpr (kPair == 2) mbar_arrive_cluster(leader(sh.tmem_empty));
-                else mbar_arrive(smem_u32(&sh.tmem_empty));
+            if (lane == 0) mbar_arrive(smem_u32(&sh.epi_drained));
+            if (warp == 2 && lane == 0) {
+                if (wait_or_abort(smem_u32(&sh.epi_drained), uint32_t(local) & 1u, sh, p.status)) {
+                    if constexpr (kPair == 2) mbar_arrive_cluster_relaxed(leader(sh.tmem_empty));
+                    else mbar_arrive(smem_u32(&sh.tmem_empty));
+                }
             }
             const int64_t row = int64_t(tl.a_row) + int64_t(rank) * kBM + 32 * q + lane;
             if (row < tl.row_end) {
                 const uint16_t* bias = p.has_bias ? p.bias + int64_t(tl.group) * p.N : nullptr;
                 const int32_t nb = tl.n0 + 128 * h;
+                // The next tile's operands stream in while these stores go out;
+                // a burst of D/AUX stores at the start of that tile slows its
+                // loads, so the 8 chunks are spread over about half of the
+                // tile's mainloop (~700 cycles per K-step).
+                const uint32_t gap_ns = uint32_t(p.k_iters) * 20u;
 #pragma unroll
-                for (int j = 0; j < 4; ++j)
+                for (int j = 0; j < 4; ++j) {
                     if (nb + 16 * j < p.N) store_chunk(acc0 + 16 * j, p, bias, row, nb + 16 * j);
+                    __nanosleep(gap_ns);
+                }
 #pragma unroll
-                for (int j = 0; j < 4; ++j)
+                for (int j = 0; j < 4; ++j) {
                     if (nb + 64 + 16 * j < p.N) store_chunk(acc1 + 16 * j, p, bias, row, nb + 64 + 16 * j);
+                    if (j < 3) __nanosleep(gap_ns);
+                }
             }
         }
     }

@@ -281,6 +281,11 @@ __device__ __forceinline__ void mbar_arrive_expect_tx_cluster_relaxed(uint32_t c
     asm volatile("mbarrier.arrive.expect_tx.relaxed.cluster.shared::cluster.b64 _, [%0], %1;"
                  :: "r"(cluster_addr), "r"(bytes) : "memory");
 }
+// Relaxed arrive on a (possibly remote) mbarrier: orders nothing, so it does
+// not wait for this thread's outstanding global stores.
+__device__ __forceinline__ void mbar_arrive_cluster_relaxed(uint32_t cluster_addr) {
+    asm volatile("mbarrier.arrive.relaxed.cluster.shared::cluster.b64 _, [%0];" :: "r"(cluster_addr) : "memory");
+}
 // TMA load into this CTA's shared memory whose completion is signalled on an
 // mbarrier of either CTA of the pair.
 __device__ __forceinline__ void tma_load_2d_pair(uint32_t dst, const CUtensorMap* desc, uint32_t bar_cluster,
