@@ -15,6 +15,7 @@ value = the step's GEMM FLOPs / step time (TFLOP/s; quantisation time included).
 from __future__ import annotations
 
 import argparse
+import hashlib
 import json
 import os
 import statistics
@@ -44,6 +45,32 @@ def load_peaks():
                 "bf16_sustained": p.get("bf16_tflops_sustained", p["bf16_tflops"]), "source": "measured"}
     except Exception:
         return {"hbm_gbs": 6800.0, "bf16": 1900.0, "bf16_sustained": 1700.0, "source": "fallback"}
+
+
+KERNEL_SOURCES = {"gemm": ["gemm.cu", "ptx.cuh"], "quant": ["quantize.cu", "ptx.cuh"]}
+
+
+def source_sha256(kernel_name: str) -> str:
+    """Hash of the sources that build the kernel behind a bench kernel name."""
+    h = hashlib.sha256()
+    for f in KERNEL_SOURCES[kernel_name.split("_")[0]]:
+        with open(os.path.join(ROOT, "mxfp8_block_scaled_quantize_gb300", "csrc", f), "rb") as fh:
+            h.update(fh.read())
+    return h.hexdigest()
+
+
+def measured_traffic(kernel_name: str):
+    """DRAM bytes (read + write) per launch from profiles/traffic.json, recorded
+    by ncu for this workload; None unless the kernel's sources are unchanged
+    since that capture."""
+    try:
+        with open(os.path.join(ROOT, "profiles", "traffic.json")) as f:
+            entry = json.load(f).get(kernel_name)
+    except (OSError, ValueError):
+        return None
+    if not entry or entry.get("source_sha256") != source_sha256(kernel_name):
+        return None
+    return entry["bytes_per_launch"]
 
 
 # ----------------------------------------------------------------------------- clocks
@@ -280,11 +307,18 @@ def barrier():
 
 
 def dist_max(x: float) -> float:
+    """Max of x over all ranks (replicas report the slowest rank's time)."""
     if not _dist:
         return x
-    t = torch.tensor([x], dtype=torch.float64, device="cuda")
+    dev = "cuda" if torch.distributed.get_backend() == "nccl" else "cpu"
+    t = torch.tensor([x], dtype=torch.float64, device=dev)
     torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
     return float(t.item())
+
+
+def whole_job_tflops(flops_per_rank: float, world: int, ms_step_max: float) -> float:
+    """Whole-job throughput of `world` replicas: all ranks' FLOPs / the slowest rank's step time."""
+    return world * flops_per_rank / (ms_step_max * 1e-3) / 1e12
 
 
 CASES = {
@@ -392,7 +426,7 @@ def main():
     total_ms, per_kernel, clocks = time_device(step, args.steps, args.warmup, sampler)
     ms_step = dist_max(total_ms / args.steps)
     gemm_flops = sum(step.flops.values())
-    value = world * gemm_flops / (ms_step * 1e-3) / 1e12
+    value = whole_job_tflops(gemm_flops, world, ms_step)
 
     fp8_peak = 2.0 * peaks["bf16_sustained"]          # nominal fp8:bf16 = 2
     fp8_burst = 2.0 * peaks["bf16"]
@@ -408,7 +442,7 @@ def main():
                           "bytes": step.bytes[name]}
     dom = max(per_kernel, key=per_kernel.get)
     dk = kern[dom]
-    traffic = None
+    traffic = measured_traffic(dom)
     roofline = {"kernel": dom, "bound": "tensor" if dk["unit"] == "TFLOP/s" else "hbm",
                 "achieved": dk["achieved"], "peak": fp8_peak if dk["unit"] == "TFLOP/s" else peaks["hbm_gbs"],
                 "unit": dk["unit"], "frac": dk["frac"], "traffic": traffic,
@@ -431,7 +465,7 @@ def main():
         "quantize_gbs": qbytes / (qms * 1e-3) / 1e9, "quantize_frac": qbytes / (qms * 1e-3) / 1e9 / peaks["hbm_gbs"],
         "kernels": kern, "roofline": roofline, "clocks": clocks,
         "gpu_launches": len(step.kernels) * args.steps,
-        "e2e": {"value": world * gemm_flops / (e2e_ms * 1e-3) / 1e12, "unit": UNIT,
+        "e2e": {"value": whole_job_tflops(gemm_flops, world, e2e_ms), "unit": UNIT,
                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
     }
     if rank == 0 and not args.no_cpu_baseline:

@@ -156,6 +156,16 @@ TEMX_API size_t te_mx_gemm_workspace_size(int64_t M, int64_t N, int64_t K, int32
  * TE_MX_ERR_INVALID_ARG), or TE_MX_ERR_CUDA if the synchronise fails. */
 TEMX_API te_mx_status te_mx_device_status(void);
 
+/* te_mx_selftest_timeout — check of the failure-detection path (no part of the
+ * computation): launches one CTA that waits on an mbarrier that nothing ever
+ * arrives at, with the same bounded wait the kernels use but a limit of
+ * `limit_us` microseconds (1 .. 2,000,000).  The wait gives up, records
+ * TE_MX_ERR_DEVICE_TIMEOUT in the device status word and the kernel returns
+ * normally, so the CUDA context stays usable; the next te_mx_device_status()
+ * reports the timeout (and clears it).  Returns TE_MX_ERR_INVALID_ARG for a
+ * limit outside the range. */
+TEMX_API te_mx_status te_mx_selftest_timeout(uint32_t limit_us, void* stream);
+
 /* Message for the last non-OK status returned on this thread ("" if none). */
 TEMX_API const char* te_mx_last_error(void);
 

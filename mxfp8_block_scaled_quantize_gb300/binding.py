@@ -31,6 +31,7 @@ SIGNATURES = {
                                           _P, _P, _P, _SZ, _P]),
     "te_mx_gemm_workspace_size": (_SZ, [_I64, _I64, _I64, _I32]),
     "te_mx_device_status": (ctypes.c_int, []),
+    "te_mx_selftest_timeout": (ctypes.c_int, [ctypes.c_uint32, _P]),
     "te_mx_last_error": (ctypes.c_char_p, []),
     "te_mx_version": (ctypes.c_char_p, []),
 }
@@ -93,6 +94,10 @@ def te_mx_gemm_workspace_size(M, N, K, num_groups=0) -> int:
 
 def te_mx_device_status() -> None:
     _check(lib().te_mx_device_status())
+
+
+def te_mx_selftest_timeout(limit_us: int, stream=None) -> None:
+    _check(lib().te_mx_selftest_timeout(limit_us, 0 if stream is None else stream))
 
 
 def te_mx_version() -> str:

@@ -17,6 +17,17 @@ __device__ unsigned int g_device_status = 0;
 
 namespace {
 
+// Failure-detection self-test: one thread waits on an mbarrier that never
+// completes; the bounded wait gives up after `limit_ns` and records a timeout.
+__global__ void selftest_timeout_kernel(unsigned int* status, unsigned long long limit_ns) {
+    __shared__ __align__(8) uint64_t bar;
+    if (threadIdx.x != 0) return;
+    const uint32_t b = smem_u32(&bar);
+    mbar_init(b, 1);
+    fence_mbarrier_init();
+    mbar_wait(b, 0, status, limit_ns);     // phase 0 never completes: nothing arrives
+}
+
 thread_local char t_last_error[512] = "";
 
 constexpr int kMaxDevices = 64;
@@ -271,6 +282,18 @@ te_mx_status te_mx_grouped_gemm(int32_t num_groups, const int32_t* group_m, int6
 }
 
 size_t te_mx_gemm_workspace_size(int64_t, int64_t, int64_t, int32_t) { return 0; }
+
+te_mx_status te_mx_selftest_timeout(uint32_t limit_us, void* stream) {
+    t_last_error[0] = '\0';
+    if (limit_us < 1 || limit_us > 2000000u)
+        return set_error(TE_MX_ERR_INVALID_ARG, "limit_us=%u must be in [1, 2000000]", limit_us);
+    unsigned int* status = nullptr;
+    te_mx_status st = device_status_ptr(&status);
+    if (st != TE_MX_OK) return st;
+    selftest_timeout_kernel<<<1, 32, 0, static_cast<cudaStream_t>(stream)>>>(
+        status, static_cast<unsigned long long>(limit_us) * 1000ull);
+    return cuda_status(cudaGetLastError(), "selftest kernel launch");
+}
 
 te_mx_status te_mx_device_status(void) {
     t_last_error[0] = '\0';
