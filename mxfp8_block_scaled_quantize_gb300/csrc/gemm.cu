@@ -65,9 +65,13 @@ struct Cfg {
     static constexpr int kBRows = kBN / kPair;            // B rows loaded per CTA
     static constexpr int kABytes = kBM * kBK;             // 16 KB
     static constexpr int kBBytes = kBRows * kBK;          // 32 KB or 16 KB
-    static constexpr int kStages = kPair == 2 ? 6 : 4;
+    static constexpr int kStages = kPair == 2 ? 5 : 4;
     static constexpr int kStageBytes = kABytes + kBBytes;
-    static constexpr int kSmemDyn = kStages * kStageBytes + kSfRing * kSfGroupBytes + 1024;
+    // CTA pairs stage the epilogue's bf16 rows in shared memory (4 KB per
+    // epilogue warp) so that global stores are written as whole lines.
+    static constexpr bool kStagedStores = kPair == 2;
+    static constexpr int kEpiStageBytes = kStagedStores ? kEpiWarps * 4096 : 0;
+    static constexpr int kSmemDyn = kStages * kStageBytes + kSfRing * kSfGroupBytes + kEpiStageBytes + 1024;
     // Instruction descriptor, kind::mxf8f6f4 with block scaling: E4M3 A and B
     // (format 0), both K-major, N >> 3 at bit 17, UE8M0 scales (bit 23),
     // M >> 4 at bit 24; scale-factor byte ids at bits 4..5 (B) and 29..30 (A).
@@ -312,6 +316,56 @@ __device__ __forceinline__ void store_chunk(const uint32_t* acc, const GemmParam
     for (int i = 0; i < 8; ++i) o[i] = pack_bf16x2(v[2 * i], v[2 * i + 1]);
     st_global_v4(p.D + off, o[0], o[1], o[2], o[3]);
     st_global_v4(p.D + off + 8, o[4], o[5], o[6], o[7]);
+}
+
+// 64 accumulator columns of one row per lane (32 rows per warp) -> bias /
+// GELU -> bf16, written as whole 128-byte lines: each lane puts its row's 128
+// bytes into the warp's staging tile (16-byte chunks XOR-swizzled by row, so
+// neither the writes nor the reads conflict), then every store instruction
+// writes 4 complete rows.
+__device__ __forceinline__ void store_64_staged(uint32_t* acc, const GemmParams& p, const uint16_t* bias,
+                                                int64_t row0, int64_t row_end, int32_t n, uint32_t stage,
+                                                int lane) {
+    float* v = reinterpret_cast<float*>(acc);
+    if (p.has_bias) {
+#pragma unroll
+        for (int c = 0; c < 8; ++c) {
+            if (n + 8 * c < p.N) {
+                const uint4 b = __ldg(reinterpret_cast<const uint4*>(bias + n + 8 * c));
+                const uint32_t bw[4] = {b.x, b.y, b.z, b.w};
+#pragma unroll
+                for (int i = 0; i < 4; ++i) {
+                    v[8 * c + 2 * i] += __uint_as_float(bw[i] << 16);
+                    v[8 * c + 2 * i + 1] += __uint_as_float(bw[i] & 0xFFFF0000u);
+                }
+            }
+        }
+    }
+    const int passes = p.gelu ? 2 : 1;
+    for (int pass = 0; pass < passes; ++pass) {
+        const bool is_aux = p.gelu && pass == 0;
+        if (p.gelu && pass == 1) {
+#pragma unroll
+            for (int i = 0; i < 64; ++i) v[i] = gelu_tanh_f(v[i]);
+        }
+#pragma unroll
+        for (int c = 0; c < 8; ++c) {
+            const uint32_t w0 = pack_bf16x2(v[8 * c + 0], v[8 * c + 1]), w1 = pack_bf16x2(v[8 * c + 2], v[8 * c + 3]);
+            const uint32_t w2 = pack_bf16x2(v[8 * c + 4], v[8 * c + 5]), w3 = pack_bf16x2(v[8 * c + 6], v[8 * c + 7]);
+            sts128(stage + lane * 128 + ((c ^ (lane & 7)) << 4), w0, w1, w2, w3);
+        }
+        __syncwarp();
+        uint16_t* out = is_aux ? p.aux : p.D;
+        const int c = lane & 7;
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+            const int r = 4 * i + (lane >> 3);
+            const uint4 w = lds128(stage + r * 128 + ((c ^ (r & 7)) << 4));
+            if (row0 + r < row_end && n + 8 * c < p.N)
+                st_global_v4(out + (row0 + r) * p.N + n + 8 * c, w.x, w.y, w.z, w.w);
+        }
+        __syncwarp();
+    }
 }
 
 template <int kPair>
@@ -561,7 +615,17 @@ gemm_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_constant__ C
                 }
             }
             const int64_t row = int64_t(tl.a_row) + int64_t(rank) * kBM + 32 * q + lane;
-            if (row < tl.row_end) {
+            if constexpr (C::kStagedStores) {
+                const int64_t row0 = row - lane;
+                if (row0 < tl.row_end) {             // warp-uniform: some row of this warp is stored
+                    const uint16_t* bias = p.has_bias ? p.bias + int64_t(tl.group) * p.N : nullptr;
+                    const int32_t nb = tl.n0 + 128 * h;
+                    const uint32_t stage = smem_u32(smem + C::kStages * C::kStageBytes + kSfRing * kSfGroupBytes) +
+                                           uint32_t(e) * 4096u;
+                    if (nb < p.N) store_64_staged(acc0, p, bias, row0, tl.row_end, nb, stage, lane);
+                    if (nb + 64 < p.N) store_64_staged(acc1, p, bias, row0, tl.row_end, nb + 64, stage, lane);
+                }
+            } else if (row < tl.row_end) {
                 const uint16_t* bias = p.has_bias ? p.bias + int64_t(tl.group) * p.N : nullptr;
                 const int32_t nb = tl.n0 + 128 * h;
                 // The next tile's operands stream in while these stores go out;
