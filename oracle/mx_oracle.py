@@ -29,7 +29,11 @@ Sources of the definitions
   infinities, S.1111.111 is NaN, largest normal 448).
 * GELU-tanh: the tanh approximation of GELU named on the TE "Getting
   Started" page (``approximate=True``), 0.5 x (1 + tanh(sqrt(2/pi) (x +
-  0.044715 x^3))).
+  0.044715 x^3))); its derivative (dGELU) for the backward epilogue named in
+  ROCm/TransformerEngine README, "Blockwise FP8 GEMM support on ROCm"
+  (bias/beta/DGELU epilogues).
+* Bias gradient: the column sums of the output gradient (the cast_transpose_bgrad
+  kernels of ROCm/TransformerEngine README, "Experimental Triton Kernels on ROCm").
 
 Readings where the sources are silent (each one is listed in the design notes):
 * amax == 0: the scale byte is 0x00 (2^-127, the smallest E8M0 value); every
@@ -254,6 +258,36 @@ def gelu_tanh(x) -> np.ndarray:
     """GELU, tanh approximation: 0.5 x (1 + tanh(sqrt(2/pi) (x + 0.044715 x^3)))."""
     x = np.asarray(x, dtype=np.float64)
     return 0.5 * x * (1.0 + np.tanh(np.sqrt(2.0 / np.pi) * (x + 0.044715 * x ** 3)))
+
+
+def dgelu_tanh(x) -> np.ndarray:
+    """d/dx of gelu_tanh: 0.5 (1 + tanh u) + 0.5 x (1 - tanh^2 u) u',
+    u = sqrt(2/pi) (x + 0.044715 x^3), u' = sqrt(2/pi) (1 + 3 * 0.044715 x^2)."""
+    x = np.asarray(x, dtype=np.float64)
+    c = np.sqrt(2.0 / np.pi)
+    t = np.tanh(c * (x + 0.044715 * x ** 3))
+    return 0.5 * (1.0 + t) + 0.5 * x * (1.0 - t * t) * c * (1.0 + 3.0 * 0.044715 * x ** 2)
+
+
+def mx_gemm_dgelu(qa, sa, qb, sb, aux_bits):
+    """MXFP8 TN GEMM with the dGELU epilogue: D = bf16(acc * dgelu_tanh(aux)),
+    acc = deq(A) . deq(B)^T, aux the bf16 pre-activation saved by the forward
+    GEMM (an input here).  Returns dict with d, ref (unrounded), sigma (scaled by
+    |dgelu(aux)|, the error scale of the bound)."""
+    a = dequantize(qa, sa)
+    b = dequantize(qb, sb)
+    g = dgelu_tanh(bf16_bits_to_f64(aux_bits))
+    acc = a @ b.T
+    sigma = (np.abs(a) @ np.abs(b).T) * np.abs(g)
+    ref = acc * g
+    return {"pre": ref, "d": bf16_round(ref), "sigma": sigma}
+
+
+def column_sums(x_bits):
+    """Bias gradient: sum over rows of a bf16 matrix (fp64, exact for the
+    sizes here).  Returns (sums, sum of |x| per column)."""
+    x = bf16_bits_to_f64(x_bits)
+    return x.sum(axis=0), np.abs(x).sum(axis=0)
 
 
 def mx_gemm(qa, sa, qb, sb, bias_bits=None, gelu: bool = False):
