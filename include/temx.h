@@ -68,7 +68,13 @@ typedef enum te_mx_epilogue {
     TE_MX_EPI_NONE = 0,
     TE_MX_EPI_BIAS = 1,
     TE_MX_EPI_GELU_AUX = 2,
-    TE_MX_EPI_BIAS_GELU_AUX = 3
+    TE_MX_EPI_BIAS_GELU_AUX = 3,
+    /* Backward of GELU (the DGELU epilogue of "Blockwise FP8 GEMM support on
+     * ROCm", ROCm/TransformerEngine README): `aux` is an INPUT holding the bf16
+     * pre-activation saved by the forward GELU_AUX GEMM, and
+     * D = bf16(acc * gelu'(aux)), gelu' the derivative of the tanh form.
+     * bias must be NULL. */
+    TE_MX_EPI_DGELU = 4
 } te_mx_epilogue;
 
 /* Smallest legal scale pitch for k quantised elements per row:
@@ -107,8 +113,8 @@ TEMX_API te_mx_status te_mx_quantize(const void* x, int64_t rows, int64_t cols, 
  *   A  uint8 E4M3 [M x K] (pitch K), sA uint8 [M x ld_sA];
  *   B  uint8 E4M3 [N x K] (pitch K), sB uint8 [N x ld_sB]  (both K-contiguous);
  *   bias  bf16 [N] or NULL (required for the *_BIAS* epilogues);
- *   D     bf16 [M x N] (pitch N);  aux bf16 [M x N], required for GELU_AUX
- *         epilogues, else ignored.
+ *   D     bf16 [M x N] (pitch N);  aux bf16 [M x N]: written by the GELU_AUX
+ *         epilogues, read by DGELU, else ignored.
  *   workspace / workspace_bytes: reserved; te_mx_gemm_workspace_size() is 0
  *         and NULL/0 may be passed.
  * Rules: K % 128 == 0, K >= 128; M, N >= 1 with N % 16 == 0 (M arbitrary);

@@ -19,7 +19,7 @@ TE_MX_OK = 0
 STATUS_NAMES = {0: "TE_MX_OK", 1: "TE_MX_ERR_INVALID_ARG", 2: "TE_MX_ERR_UNSUPPORTED_SHAPE",
                 3: "TE_MX_ERR_MISALIGNED", 4: "TE_MX_ERR_WORKSPACE_TOO_SMALL", 5: "TE_MX_ERR_CUDA",
                 6: "TE_MX_ERR_DEVICE_TIMEOUT", 7: "TE_MX_ERR_ARCH"}
-EPI_NONE, EPI_BIAS, EPI_GELU_AUX, EPI_BIAS_GELU_AUX = 0, 1, 2, 3
+EPI_NONE, EPI_BIAS, EPI_GELU_AUX, EPI_BIAS_GELU_AUX, EPI_DGELU = 0, 1, 2, 3, 4
 
 # (name, restype, argtypes) for every function declared in include/temx.h
 _I64, _I32, _P, _SZ = ctypes.c_int64, ctypes.c_int32, ctypes.c_void_p, ctypes.c_size_t
@@ -137,12 +137,20 @@ def quantize(x, rowwise: bool = True, colwise: bool = False, stream=None, out=No
     return o
 
 
-def gemm(qa, sa, qb, sb, bias=None, gelu: bool = False, stream=None, out=None):
-    """D = epilogue(deq(qa) . deq(qb)^T (+ bias)) in bf16; returns (D, aux or None)."""
+def gemm(qa, sa, qb, sb, bias=None, gelu: bool = False, stream=None, out=None, dgelu_aux=None):
+    """D = epilogue(deq(qa) . deq(qb)^T (+ bias)) in bf16; returns (D, aux or None).
+    With ``dgelu_aux`` (bf16 [M, N], the forward pre-activation) the epilogue is
+    D = bf16(acc * gelu'(dgelu_aux))."""
     import torch
     M, K = qa.shape
     N = qb.shape[0]
     epi = (EPI_BIAS if bias is not None else EPI_NONE) + (EPI_GELU_AUX if gelu else 0)
+    if dgelu_aux is not None:
+        assert bias is None and not gelu
+        d = torch.empty(M, N, dtype=torch.bfloat16, device=qa.device) if out is None else out[0]
+        te_mx_gemm(qa.data_ptr(), sa.data_ptr(), sa.stride(0), qb.data_ptr(), sb.data_ptr(), sb.stride(0),
+                   M, N, K, 0, EPI_DGELU, d.data_ptr(), dgelu_aux.data_ptr(), 0, 0, _stream_ptr(stream))
+        return d, None
     if out is None:
         d = torch.empty(M, N, dtype=torch.bfloat16, device=qa.device)
         aux = torch.empty(M, N, dtype=torch.bfloat16, device=qa.device) if gelu else None
@@ -153,13 +161,22 @@ def gemm(qa, sa, qb, sb, bias=None, gelu: bool = False, stream=None, out=None):
     return d, aux
 
 
-def grouped_gemm(group_m, qx, sx, qw, sw, bias=None, gelu: bool = False, stream=None, out=None):
+def grouped_gemm(group_m, qx, sx, qw, sw, bias=None, gelu: bool = False, stream=None, out=None, dgelu_aux=None):
     """Grouped GEMM over experts: group_m int32 [G] on the device, qx [total_m, K],
-    qw [G, N, K], sw [G*N, pitch]; returns (D, aux or None) of [total_m, N]."""
+    qw [G, N, K], sw [G*N, pitch]; returns (D, aux or None) of [total_m, N].
+    With ``dgelu_aux`` the epilogue is the GELU backward (see ``gemm``)."""
     import torch
     total_m, K = qx.shape
     G, N, _ = qw.shape
     epi = (EPI_BIAS if bias is not None else EPI_NONE) + (EPI_GELU_AUX if gelu else 0)
+    if dgelu_aux is not None:
+        assert bias is None and not gelu
+        d = torch.empty(total_m, N, dtype=torch.bfloat16, device=qx.device) if out is None else out[0]
+        sw2 = sw.reshape(G * N, -1)
+        te_mx_grouped_gemm(G, group_m.data_ptr(), total_m, qx.data_ptr(), sx.data_ptr(), sx.stride(0),
+                           qw.data_ptr(), sw2.data_ptr(), sw2.stride(0), N, K, 0, EPI_DGELU,
+                           d.data_ptr(), dgelu_aux.data_ptr(), 0, 0, _stream_ptr(stream))
+        return d, None
     if out is None:
         d = torch.empty(total_m, N, dtype=torch.bfloat16, device=qx.device)
         aux = torch.empty(total_m, N, dtype=torch.bfloat16, device=qx.device) if gelu else None

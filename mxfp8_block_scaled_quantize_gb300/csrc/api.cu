@@ -215,13 +215,14 @@ static te_mx_status validate_gemm_common(const uint8_t* A, const uint8_t* sA, in
                                          const uint8_t* B, const uint8_t* sB, int64_t ld_sB,
                                          int64_t N, int64_t K, const void* bias, int32_t epi,
                                          void* D, void* aux) {
-    if (epi < TE_MX_EPI_NONE || epi > TE_MX_EPI_BIAS_GELU_AUX)
+    if (epi < TE_MX_EPI_NONE || epi > TE_MX_EPI_DGELU)
         return set_error(TE_MX_ERR_INVALID_ARG, "unknown epilogue %d", epi);
     if (!A || !sA || !B || !sB || !D) return set_error(TE_MX_ERR_INVALID_ARG, "A, sA, B, sB and D are required");
     const bool has_bias = epi == TE_MX_EPI_BIAS || epi == TE_MX_EPI_BIAS_GELU_AUX;
-    const bool gelu = epi == TE_MX_EPI_GELU_AUX || epi == TE_MX_EPI_BIAS_GELU_AUX;
+    const bool gelu = epi == TE_MX_EPI_GELU_AUX || epi == TE_MX_EPI_BIAS_GELU_AUX || epi == TE_MX_EPI_DGELU;
     if (has_bias && !bias) return set_error(TE_MX_ERR_INVALID_ARG, "bias epilogue without a bias pointer");
-    if (gelu && !aux) return set_error(TE_MX_ERR_INVALID_ARG, "GELU_AUX epilogue without an aux pointer");
+    if (gelu && !aux) return set_error(TE_MX_ERR_INVALID_ARG, "GELU epilogue without an aux pointer");
+    if (epi == TE_MX_EPI_DGELU && bias) return set_error(TE_MX_ERR_INVALID_ARG, "DGELU epilogue takes no bias");
     if (K < 128 || K % 128) return set_error(TE_MX_ERR_UNSUPPORTED_SHAPE, "K=%lld must be a positive multiple of 128", (long long)K);
     if (N < 16 || N % 16) return set_error(TE_MX_ERR_UNSUPPORTED_SHAPE, "N=%lld must be a positive multiple of 16", (long long)N);
     if (K > (int64_t(1) << 30) || N > (int64_t(1) << 30)) return set_error(TE_MX_ERR_UNSUPPORTED_SHAPE, "N or K too large");
@@ -250,6 +251,7 @@ te_mx_status te_mx_gemm(const uint8_t* A, const uint8_t* sA, int64_t ld_sA,
     a.M = M; a.N = N; a.K = K; a.bias = bias;
     a.has_bias = epilogue == TE_MX_EPI_BIAS || epilogue == TE_MX_EPI_BIAS_GELU_AUX;
     a.gelu = epilogue == TE_MX_EPI_GELU_AUX || epilogue == TE_MX_EPI_BIAS_GELU_AUX;
+    a.dgelu = epilogue == TE_MX_EPI_DGELU;
     a.D = D; a.aux = aux; a.groups = 0; a.group_m = nullptr;
     return gemm_launch(a, static_cast<cudaStream_t>(stream));
 }
@@ -277,6 +279,7 @@ te_mx_status te_mx_grouped_gemm(int32_t num_groups, const int32_t* group_m, int6
     a.M = total_m; a.N = N; a.K = K; a.bias = bias;
     a.has_bias = epilogue == TE_MX_EPI_BIAS || epilogue == TE_MX_EPI_BIAS_GELU_AUX;
     a.gelu = epilogue == TE_MX_EPI_GELU_AUX || epilogue == TE_MX_EPI_BIAS_GELU_AUX;
+    a.dgelu = epilogue == TE_MX_EPI_DGELU;
     a.D = D; a.aux = aux; a.groups = num_groups; a.group_m = group_m;
     return gemm_launch(a, static_cast<cudaStream_t>(stream));
 }

@@ -106,7 +106,7 @@ struct GemmParams {
     const uint16_t* bias;    // bf16 bits, [N] or [G x N]
     uint16_t* D;
     uint16_t* aux;
-    bool has_bias, gelu;
+    bool has_bias, gelu, dgelu;          // dgelu: aux is an input (forward pre-activation)
     unsigned int* status;
 };
 
@@ -286,6 +286,34 @@ __device__ __forceinline__ float gelu_tanh_f(float x) {
     return __fdividef(x, 1.0f + e);
 }
 
+// Derivative of the tanh-form GELU: with s = sigmoid(2u) = 0.5 (1 + tanh u)
+// and t = 1 - s, gelu'(x) = s + 2 x s t sqrt(2/pi) (1 + 3 * 0.044715 x^2).
+// t is taken as 1 - s or e s (e = exp(-2u)), whichever does not cancel.
+__device__ __forceinline__ float dgelu_tanh_f(float x) {
+    constexpr float kC0 = 0.7978845608028654f;                     // sqrt(2/pi)
+    constexpr float kTwoC0 = 2.0f * kC0;
+    constexpr float kTwoC1 = 2.0f * kC0 * 0.044715f;
+    constexpr float kThreeC1 = 3.0f * 0.044715f;
+    constexpr float kLog2e = 1.4426950408889634f;
+    const float x2 = x * x;
+    const float two_u = x * fmaf(x2, kTwoC1, kTwoC0);
+    float e;
+    asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(e) : "f"(-two_u * kLog2e));
+    const float sg = __fdividef(1.0f, 1.0f + e);
+    const float t = e > 1.0f ? 1.0f - sg : e * sg;
+    return fmaf(2.0f * x * sg * t * kC0, fmaf(kThreeC1, x2, 1.0f), sg);
+}
+
+// Multiply 8 consecutive values by gelu' of 8 bf16 pre-activations (one uint4).
+__device__ __forceinline__ void apply_dgelu8(float* v, uint4 w) {
+    const uint32_t ww[4] = {w.x, w.y, w.z, w.w};
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        v[2 * i] *= dgelu_tanh_f(__uint_as_float(ww[i] << 16));
+        v[2 * i + 1] *= dgelu_tanh_f(__uint_as_float(ww[i] & 0xFFFF0000u));
+    }
+}
+
 // 16 accumulator columns of one row -> bias / GELU -> bf16 stores.
 __device__ __forceinline__ void store_chunk(const uint32_t* acc, const GemmParams& p, const uint16_t* bias,
                                             int64_t row, int32_t n) {
@@ -304,6 +332,10 @@ __device__ __forceinline__ void store_chunk(const uint32_t* acc, const GemmParam
     }
     const int64_t off = row * p.N + n;
     uint32_t o[8];
+    if (p.dgelu) {
+        apply_dgelu8(v, __ldg(reinterpret_cast<const uint4*>(p.aux + off)));
+        apply_dgelu8(v + 8, __ldg(reinterpret_cast<const uint4*>(p.aux + off + 8)));
+    }
     if (p.gelu) {
 #pragma unroll
         for (int i = 0; i < 8; ++i) o[i] = pack_bf16x2(v[2 * i], v[2 * i + 1]);
@@ -341,6 +373,23 @@ __device__ __forceinline__ void store_64_staged(uint32_t* acc, const GemmParams&
             }
         }
     }
+    if (p.dgelu) {
+        // the forward pre-activation rows come in as whole lines through the
+        // staging tile, then each lane takes its own row
+        const int c = lane & 7;
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+            const int r = 4 * i + (lane >> 3);
+            uint4 w = make_uint4(0, 0, 0, 0);
+            if (row0 + r < row_end && n + 8 * c < p.N)
+                w = __ldg(reinterpret_cast<const uint4*>(p.aux + (row0 + r) * p.N + n + 8 * c));
+            sts128(stage + r * 128 + ((c ^ (r & 7)) << 4), w.x, w.y, w.z, w.w);
+        }
+        __syncwarp();
+#pragma unroll
+        for (int cc = 0; cc < 8; ++cc) apply_dgelu8(v + 8 * cc, lds128(stage + lane * 128 + ((cc ^ (lane & 7)) << 4)));
+        __syncwarp();
+    }
     const int passes = p.gelu ? 2 : 1;
     for (int pass = 0; pass < passes; ++pass) {
         const bool is_aux = p.gelu && pass == 0;
@@ -369,7 +418,7 @@ __device__ __forceinline__ void store_64_staged(uint32_t* acc, const GemmParams&
 }
 
 template <int kPair>
-__global__ void __launch_bounds__(kThreads, 1)
+__global__ void __maxnreg__(184)   // 11 warps x 184 registers fill the register file
 gemm_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_constant__ CUtensorMap map_b,
             const __grid_constant__ CUtensorMap map_sfa, const __grid_constant__ CUtensorMap map_sfb,
             const GemmParams p) {
@@ -688,6 +737,7 @@ te_mx_status launch_gemm(const GemmArgs& a, int sms, unsigned int* status, cudaS
     p.aux = static_cast<uint16_t*>(a.aux);
     p.has_bias = a.has_bias;
     p.gelu = a.gelu;
+    p.dgelu = a.dgelu;
     p.status = status;
 
     const int64_t slots = sms / kPair;                     // CTAs (pairs) resident at once

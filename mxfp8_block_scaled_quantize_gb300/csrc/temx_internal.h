@@ -29,7 +29,7 @@ struct GemmArgs {
     int64_t ld_sB;
     int64_t M, N, K;         // grouped: M = total_m
     const void* bias;        // bf16 [N] (grouped: [G x N]) or null
-    bool has_bias, gelu;
+    bool has_bias, gelu, dgelu;
     void* D;
     void* aux;
     int32_t groups;          // 0: dense GEMM

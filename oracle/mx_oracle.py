@@ -262,11 +262,21 @@ def gelu_tanh(x) -> np.ndarray:
 
 def dgelu_tanh(x) -> np.ndarray:
     """d/dx of gelu_tanh: 0.5 (1 + tanh u) + 0.5 x (1 - tanh^2 u) u',
-    u = sqrt(2/pi) (x + 0.044715 x^3), u' = sqrt(2/pi) (1 + 3 * 0.044715 x^2)."""
+    u = sqrt(2/pi) (x + 0.044715 x^3), u' = sqrt(2/pi) (1 + 3 * 0.044715 x^2).
+
+    Evaluated through the exact identities 0.5 (1 + tanh u) = 1 / (1 + E) and
+    1 - tanh^2 u = 4 E / (1 + E)^2 with E = exp(-2u): the same function, but
+    1 + tanh u does not cancel for u << 0 (where the derivative is ~1e-15 and
+    the tanh form loses every digit in fp64)."""
     x = np.asarray(x, dtype=np.float64)
     c = np.sqrt(2.0 / np.pi)
-    t = np.tanh(c * (x + 0.044715 * x ** 3))
-    return 0.5 * (1.0 + t) + 0.5 * x * (1.0 - t * t) * c * (1.0 + 3.0 * 0.044715 * x ** 2)
+    u = c * (x + 0.044715 * x ** 3)
+    with np.errstate(over="ignore"):
+        big = np.exp(-2.0 * u)                       # E (inf for u << 0)
+    s = 1.0 / (1.0 + big)                            # 0.5 (1 + tanh u)
+    with np.errstate(invalid="ignore"):
+        one_minus_t2 = np.where(np.isinf(big), 0.0, 4.0 * big * s * s)   # 1 - tanh^2 u
+    return s + 0.5 * x * one_minus_t2 * c * (1.0 + 3.0 * 0.044715 * x ** 2)
 
 
 def mx_gemm_dgelu(qa, sa, qb, sb, aux_bits):

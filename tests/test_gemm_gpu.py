@@ -322,3 +322,57 @@ def test_full_size_moe_grouped():
         qa, sa = O.quantize_rowwise(U.bf16_bits(d["X"][torch.from_numpy(rows)]))
         qb, sb = O.quantize_rowwise(U.bf16_bits(d["W"][g]))
         check_sampled(out, aux, rows, qa, sa, qb, sb, None, True, f"moe group {g} (m={counts[g]})")
+
+
+# ---------------------------------------------------------------- backward: dGELU epilogue, dgrad
+
+@pytest.mark.parametrize("M,N,K", [(200, 96, 384), (333, 528, 640), (2048, 2560, 256)])
+def test_dgelu_epilogue_vs_oracle(M, N, K):
+    qa, sa = O.quantize_rowwise(rand_bits((M, K), M + 5))
+    qb, sb = O.quantize_rowwise(rand_bits((N, K), N + 6, std=0.05))
+    aux_bits = rand_bits((M, N), K + 7, std=2.0)
+    aux_bits[:, :3] = O.f64_to_bf16_bits(np.array([-30.0, 0.0, 30.0]))       # saturated ends and 0
+    aux = U.from_bits(aux_bits).cuda()
+    d, dbuf = U.guarded_bf16(M, N)
+    ga, gsa = upload(qa, sa)
+    gb, gsb = upload(qb, sb)
+    binding.gemm(ga, gsa, gb, gsb, out=(d, None), dgelu_aux=aux)
+    binding.te_mx_device_status()
+    U.check_guard(dbuf, M * N)
+    ref = O.mx_gemm_dgelu(qa, sa, qb, sb, aux_bits)
+    assert_within_bound(to_f64(d), ref["d"], ref["sigma"], "dGELU D")
+
+
+def test_grouped_dgelu_vs_oracle():
+    group_m, N, K = [0, 130, 1, 256, 77], 160, 256
+    total = sum(group_m)
+    G = len(group_m)
+    qx, sx = O.quantize_rowwise(rand_bits((total, K), 61))
+    qw, sw = O.quantize_rowwise(rand_bits((G * N, K), 62, std=0.05))
+    aux_bits = rand_bits((total, N), 63, std=2.0)
+    dqx, dsx = upload(qx, sx)
+    dqw, dsw = upload(qw, sw)
+    gm = torch.tensor(group_m, dtype=torch.int32, device="cuda")
+    d, _ = binding.grouped_gemm(gm, dqx, dsx, dqw.view(G, N, K), dsw, dgelu_aux=U.from_bits(aux_bits).cuda())
+    binding.te_mx_device_status()
+    row = 0
+    for g, m in enumerate(group_m):
+        if m:
+            ref = O.mx_gemm_dgelu(qx[row:row + m], sx[row:row + m], qw[g * N:(g + 1) * N], sw[g * N:(g + 1) * N],
+                                  aux_bits[row:row + m])
+            assert_within_bound(to_f64(d)[row:row + m], ref["d"], ref["sigma"], f"group {g}")
+        row += m
+
+
+def test_full_size_fc1_dgrad_on_colwise_weight():
+    # dX[T x H] = dY[T x F] . W1[F x H]: A = row-wise dY (K = F), B = column-wise W1 = W1^T quantised along F
+    d = workloads.make_fc1()
+    dy, w = d["dY"].cuda(), d["W"].cuda()
+    qdy = binding.quantize(dy, rowwise=True)
+    qw = binding.quantize(w, rowwise=False, colwise=True)
+    dx, _ = binding.gemm(qdy["q_row"], qdy["s_row"], qw["q_col"], qw["s_col"])
+    binding.te_mx_device_status()
+    rows = sample_rows(d["dY"].shape[0], 16, 8)
+    qa, sa = O.quantize_rowwise(U.bf16_bits(d["dY"][torch.from_numpy(rows)]))
+    qb, sb = O.quantize_colwise(U.bf16_bits(d["W"]))
+    check_sampled(dx, None, rows, qa, sa, qb, sb, None, False, "fc1 dgrad")

@@ -56,3 +56,24 @@ def test_column_sums_exact():
     for c in (0, 7, 31):
         assert Fraction(s[c]) == sum(Fraction(v) for v in xv[:, c])
         assert Fraction(a[c]) == sum(abs(Fraction(v)) for v in xv[:, c])
+
+
+def _dgelu_decimal(x: float):
+    """The tanh-form derivative evaluated with 160-digit decimal arithmetic."""
+    from decimal import Decimal, getcontext
+    getcontext().prec = 160
+    X = Decimal(x)
+    pi = Decimal("3.14159265358979323846264338327950288419716939937510582097494")
+    c = (Decimal(2) / pi).sqrt()
+    u = c * (X + Decimal("0.044715") * X ** 3)
+    e2 = (2 * u).exp()
+    t = (e2 - 1) / (e2 + 1)
+    return float(Decimal("0.5") * (1 + t) + Decimal("0.5") * X * (1 - t * t) * c *
+                 (1 + 3 * Decimal("0.044715") * X ** 2))
+
+
+@pytest.mark.parametrize("x", [-12.0, -9.5, -7.21875, -5.0, -2.0, -0.75, 0.0, 0.5, 3.0, 8.0])
+def test_dgelu_relative_accuracy_in_the_tails(x):
+    ref = _dgelu_decimal(x)
+    got = float(O.dgelu_tanh(x))
+    assert abs(got - ref) <= 1e-13 * abs(ref) + 1e-300
