@@ -418,7 +418,7 @@ __device__ __forceinline__ void store_64_staged(uint32_t* acc, const GemmParams&
 }
 
 template <int kPair>
-__global__ void __maxnreg__(184)   // 11 warps x 184 registers fill the register file
+__global__ void __launch_bounds__(kThreads, 1)   // 168 registers: 3 warps share a 16K-register sub-partition
 gemm_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_constant__ CUtensorMap map_b,
             const __grid_constant__ CUtensorMap map_sfa, const __grid_constant__ CUtensorMap map_sfb,
             const GemmParams p) {
