@@ -104,6 +104,27 @@ TEMX_API te_mx_status te_mx_quantize(const void* x, int64_t rows, int64_t cols, 
                             uint8_t* q_col, uint8_t* s_col, int64_t ld_s_col,
                             void* stream);
 
+/* te_mx_quantize_dbias — te_mx_quantize plus the bias gradient of the same
+ * matrix (the fused cast/transpose/bias-grad of the gradient, cf. the
+ * cast_transpose_bgrad kernels of ROCm/TransformerEngine README, "Experimental
+ * Triton Kernels on ROCm"):
+ *   dbias[c] = bf16(sum_r x[r][c])                         (dbias: bf16 [cols])
+ * Sums are taken in fp32 in a fixed order (each 64-row band of a column, then
+ * the bands), so the result is deterministic; accuracy |dbias - exact| <=
+ * 2^-7 |exact| + 1e-5 sum_r |x[r][c]|.
+ *   workspace: device scratch of te_mx_quantize_dbias_workspace_size(rows, cols)
+ *              bytes owned by the caller (fp32 band partial sums); its contents
+ *              on entry do not matter and it is clobbered.
+ * Quantisation outputs and rules as te_mx_quantize (either orientation may be
+ * NULL, or both: then only dbias is produced); dbias must be 16-byte aligned.
+ * Returns TE_MX_ERR_WORKSPACE_TOO_SMALL if workspace_bytes is short. */
+TEMX_API size_t te_mx_quantize_dbias_workspace_size(int64_t rows, int64_t cols);
+TEMX_API te_mx_status te_mx_quantize_dbias(const void* x, int64_t rows, int64_t cols, int64_t ld_x,
+                                  uint8_t* q_row, uint8_t* s_row, int64_t ld_s_row,
+                                  uint8_t* q_col, uint8_t* s_col, int64_t ld_s_col,
+                                  void* dbias, void* workspace, size_t workspace_bytes,
+                                  void* stream);
+
 /* te_mx_gemm — MXFP8 TN GEMM with fused epilogue (HipKittens MXFP8 GEMM
  * Support, PR description: MXFP8 GEMM with BIAS and GELU AUX epilogues; the
  * review thread's TN layout and its K % 128 rule for MXFP8 scaling):

@@ -26,6 +26,8 @@ _I64, _I32, _P, _SZ = ctypes.c_int64, ctypes.c_int32, ctypes.c_void_p, ctypes.c_
 SIGNATURES = {
     "te_mx_scale_pitch": (_SZ, [_I64]),
     "te_mx_quantize": (ctypes.c_int, [_P, _I64, _I64, _I64, _P, _P, _I64, _P, _P, _I64, _P]),
+    "te_mx_quantize_dbias_workspace_size": (_SZ, [_I64, _I64]),
+    "te_mx_quantize_dbias": (ctypes.c_int, [_P, _I64, _I64, _I64, _P, _P, _I64, _P, _P, _I64, _P, _P, _SZ, _P]),
     "te_mx_gemm": (ctypes.c_int, [_P, _P, _I64, _P, _P, _I64, _I64, _I64, _I64, _P, _I32, _P, _P, _P, _SZ, _P]),
     "te_mx_grouped_gemm": (ctypes.c_int, [_I32, _P, _I64, _P, _P, _I64, _P, _P, _I64, _I64, _I64, _P, _I32,
                                           _P, _P, _P, _SZ, _P]),
@@ -76,6 +78,16 @@ def te_mx_quantize(x, rows, cols, ld_x, q_row, s_row, ld_s_row, q_col, s_col, ld
     _check(lib().te_mx_quantize(x, rows, cols, ld_x, q_row, s_row, ld_s_row, q_col, s_col, ld_s_col, stream))
 
 
+def te_mx_quantize_dbias_workspace_size(rows, cols) -> int:
+    return lib().te_mx_quantize_dbias_workspace_size(rows, cols)
+
+
+def te_mx_quantize_dbias(x, rows, cols, ld_x, q_row, s_row, ld_s_row, q_col, s_col, ld_s_col, dbias, workspace,
+                         workspace_bytes, stream) -> None:
+    _check(lib().te_mx_quantize_dbias(x, rows, cols, ld_x, q_row, s_row, ld_s_row, q_col, s_col, ld_s_col, dbias,
+                                      workspace, workspace_bytes, stream))
+
+
 def te_mx_gemm(A, sA, ld_sA, B, sB, ld_sB, M, N, K, bias, epilogue, D, aux, workspace, workspace_bytes,
                stream) -> None:
     _check(lib().te_mx_gemm(A, sA, ld_sA, B, sB, ld_sB, M, N, K, bias, epilogue, D, aux, workspace,
@@ -116,9 +128,12 @@ def _ptr(t) -> int:
     return 0 if t is None else t.data_ptr()
 
 
-def quantize(x, rowwise: bool = True, colwise: bool = False, stream=None, out=None):
+def quantize(x, rowwise: bool = True, colwise: bool = False, stream=None, out=None, dbias: bool = False,
+             workspace=None):
     """MXFP8-quantise a 2-D bf16 CUDA tensor.  Returns a dict with q_row
-    [R,C], s_row [R, pitch(C)] and/or q_col [C,R], s_col [C, pitch(R)] (uint8)."""
+    [R,C], s_row [R, pitch(C)] and/or q_col [C,R], s_col [C, pitch(R)] (uint8),
+    and with ``dbias`` also "dbias" (bf16 [C], the column sums); the bias
+    gradient's scratch is ``workspace`` (uint8 CUDA tensor) or allocated here."""
     import torch
     assert x.dtype == torch.bfloat16 and x.dim() == 2 and x.is_cuda
     rows, cols = x.shape
@@ -130,10 +145,18 @@ def quantize(x, rowwise: bool = True, colwise: bool = False, stream=None, out=No
     if colwise and "q_col" not in o:
         o["q_col"] = torch.empty(cols, rows, dtype=torch.uint8, device=x.device)
         o["s_col"] = torch.empty(cols, te_mx_scale_pitch(rows), dtype=torch.uint8, device=x.device)
-    te_mx_quantize(x.data_ptr(), rows, cols, x.stride(0),
-                   _ptr(o.get("q_row")), _ptr(o.get("s_row")), o["s_row"].stride(0) if "s_row" in o else 0,
-                   _ptr(o.get("q_col")), _ptr(o.get("s_col")), o["s_col"].stride(0) if "s_col" in o else 0,
-                   _stream_ptr(stream))
+    args = (x.data_ptr(), rows, cols, x.stride(0),
+            _ptr(o.get("q_row")), _ptr(o.get("s_row")), o["s_row"].stride(0) if "s_row" in o else 0,
+            _ptr(o.get("q_col")), _ptr(o.get("s_col")), o["s_col"].stride(0) if "s_col" in o else 0)
+    if not dbias:
+        te_mx_quantize(*args, _stream_ptr(stream))
+        return o
+    if "dbias" not in o:
+        o["dbias"] = torch.empty(cols, dtype=torch.bfloat16, device=x.device)
+    if workspace is None:
+        workspace = torch.empty(max(1, te_mx_quantize_dbias_workspace_size(rows, cols)), dtype=torch.uint8,
+                                device=x.device)
+    te_mx_quantize_dbias(*args, o["dbias"].data_ptr(), workspace.data_ptr(), workspace.numel(), _stream_ptr(stream))
     return o
 
 

@@ -177,16 +177,15 @@ const char* te_mx_last_error(void) { return t_last_error; }
 
 const char* te_mx_version(void) { return "temx 0.1 (sm_103a)"; }
 
-te_mx_status te_mx_quantize(const void* x, int64_t rows, int64_t cols, int64_t ld_x,
-                            uint8_t* q_row, uint8_t* s_row, int64_t ld_s_row,
-                            uint8_t* q_col, uint8_t* s_col, int64_t ld_s_col, void* stream) {
-    t_last_error[0] = '\0';
+static te_mx_status validate_quantize(const void* x, int64_t rows, int64_t cols, int64_t ld_x,
+                                      uint8_t* q_row, uint8_t* s_row, int64_t ld_s_row,
+                                      uint8_t* q_col, uint8_t* s_col, int64_t ld_s_col, bool dbias) {
     if (rows < 0 || cols < 0) return set_error(TE_MX_ERR_INVALID_ARG, "negative size %lld x %lld", (long long)rows, (long long)cols);
     if ((q_row == nullptr) != (s_row == nullptr))
         return set_error(TE_MX_ERR_INVALID_ARG, "q_row and s_row must both be given or both be NULL");
     if ((q_col == nullptr) != (s_col == nullptr))
         return set_error(TE_MX_ERR_INVALID_ARG, "q_col and s_col must both be given or both be NULL");
-    if (rows == 0 || cols == 0 || (!q_row && !q_col)) return TE_MX_OK;
+    if (rows == 0 || cols == 0 || (!q_row && !q_col && !dbias)) return TE_MX_OK;
     if (!x) return set_error(TE_MX_ERR_INVALID_ARG, "x is NULL");
     if (cols % 32) return set_error(TE_MX_ERR_UNSUPPORTED_SHAPE, "cols=%lld is not a multiple of 32", (long long)cols);
     if (q_col && rows % 32)
@@ -205,9 +204,39 @@ te_mx_status te_mx_quantize(const void* x, int64_t rows, int64_t cols, int64_t l
         if (ld_s_col % 16 || ld_s_col < rows / 32)
             return set_error(TE_MX_ERR_MISALIGNED, "ld_s_col=%lld must be a multiple of 16 and >= rows/32", (long long)ld_s_col);
     }
-    te_mx_status st = check_device(nullptr);
-    if (st != TE_MX_OK) return st;
-    QuantizeArgs a{x, rows, cols, ld_x, q_row, s_row, ld_s_row, q_col, s_col, ld_s_col};
+    return check_device(nullptr);
+}
+
+te_mx_status te_mx_quantize(const void* x, int64_t rows, int64_t cols, int64_t ld_x,
+                            uint8_t* q_row, uint8_t* s_row, int64_t ld_s_row,
+                            uint8_t* q_col, uint8_t* s_col, int64_t ld_s_col, void* stream) {
+    t_last_error[0] = '\0';
+    te_mx_status st = validate_quantize(x, rows, cols, ld_x, q_row, s_row, ld_s_row, q_col, s_col, ld_s_col, false);
+    if (st != TE_MX_OK || rows == 0 || cols == 0 || (!q_row && !q_col)) return st;
+    QuantizeArgs a{x, rows, cols, ld_x, q_row, s_row, ld_s_row, q_col, s_col, ld_s_col, nullptr, nullptr};
+    return quantize_launch(a, static_cast<cudaStream_t>(stream));
+}
+
+size_t te_mx_quantize_dbias_workspace_size(int64_t rows, int64_t cols) {
+    if (rows <= 0 || cols <= 0) return 0;
+    return size_t((rows + kDbiasBandRows - 1) / kDbiasBandRows) * size_t(cols) * sizeof(float);
+}
+
+te_mx_status te_mx_quantize_dbias(const void* x, int64_t rows, int64_t cols, int64_t ld_x,
+                                  uint8_t* q_row, uint8_t* s_row, int64_t ld_s_row,
+                                  uint8_t* q_col, uint8_t* s_col, int64_t ld_s_col,
+                                  void* dbias, void* workspace, size_t workspace_bytes, void* stream) {
+    t_last_error[0] = '\0';
+    if (!dbias) return set_error(TE_MX_ERR_INVALID_ARG, "dbias is NULL");
+    te_mx_status st = validate_quantize(x, rows, cols, ld_x, q_row, s_row, ld_s_row, q_col, s_col, ld_s_col, true);
+    if (st != TE_MX_OK || rows == 0 || cols == 0) return st;
+    if (!aligned(dbias, 16)) return set_error(TE_MX_ERR_MISALIGNED, "dbias is not 16-byte aligned");
+    const size_t need = te_mx_quantize_dbias_workspace_size(rows, cols);
+    if (!workspace || workspace_bytes < need)
+        return set_error(TE_MX_ERR_WORKSPACE_TOO_SMALL, "workspace of %zu bytes needed, %zu given", need, workspace_bytes);
+    if (!aligned(workspace, 16)) return set_error(TE_MX_ERR_MISALIGNED, "workspace is not 16-byte aligned");
+    QuantizeArgs a{x, rows, cols, ld_x, q_row, s_row, ld_s_row, q_col, s_col, ld_s_col,
+                   static_cast<uint16_t*>(dbias), static_cast<float*>(workspace)};
     return quantize_launch(a, static_cast<cudaStream_t>(stream));
 }
 

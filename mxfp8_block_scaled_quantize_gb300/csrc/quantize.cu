@@ -19,6 +19,7 @@
 // leave with two TMA tensor stores, so global writes are whole lines instead
 // of 32 scattered sectors per instruction.  Scale bytes (2 per row or column
 // per unit) are stored directly.  Warps never wait on each other.
+#include <cuda_bf16.h>
 #include <cuda_runtime.h>
 
 #include "ptx.cuh"
@@ -34,6 +35,7 @@ constexpr int kUnitBytes = kRows * kCols * 2;
 constexpr int kWarps = 12;
 constexpr int kStages = 2;
 constexpr int kSmemBytes = kWarps * kStages * kUnitBytes + 1024;
+static_assert(kRows == kDbiasBandRows, "bias-gradient bands are the unit rows");
 
 struct QuantizeParams {
     int64_t rows, cols;
@@ -43,6 +45,7 @@ struct QuantizeParams {
     int64_t ld_s_col;
     int64_t col_units;     // ceil(cols / 64)
     int64_t units;         // ceil(rows / 64) * col_units
+    float* partial;        // bias gradient: fp32 [ceil(rows/64) x cols] band sums
     unsigned int* status;  // device status word
 };
 
@@ -122,12 +125,17 @@ __device__ __forceinline__ void row_blocks(uint32_t row_addr, int sw, uint32_t (
 // Columns 2l and 2l+1 over the 32 rows from `row0` (a multiple of 8):
 // codes lo[8] / hi[8] (32 bytes each, rows in order) and their scale bytes.
 __device__ __forceinline__ void col_blocks(uint32_t tile, int row0, int lane, uint32_t (&lo)[8], uint32_t (&hi)[8],
-                                           uint32_t& s_lo, uint32_t& s_hi) {
+                                           uint32_t& s_lo, uint32_t& s_hi, float& sum_lo, float& sum_hi) {
     uint32_t w[32];
     const uint32_t base = tile + row0 * 128 + ((lane & 3) << 2);
     const int chunk = lane >> 2;
 #pragma unroll
     for (int r = 0; r < 32; ++r) w[r] = lds32(base + r * 128 + ((chunk ^ (r & 7)) << 4));
+#pragma unroll
+    for (int r = 0; r < 32; ++r) {                  // column sums for the bias gradient (row order)
+        sum_lo += bf16_lo(w[r]);
+        sum_hi += bf16_hi(w[r]);
+    }
     const uint32_t m2 = amax_words<32>(w);
     s_lo = scale_byte(m2 & 0xFFFFu);
     s_hi = scale_byte(m2 >> 16);
@@ -150,10 +158,23 @@ __device__ __forceinline__ void col_blocks(uint32_t tile, int row0, int lane, ui
     }
 }
 
+// Column sums (columns 2l, 2l+1, all 64 rows of the unit, row order) without
+// quantising, for a bias gradient without a column-wise copy.
+__device__ __forceinline__ void col_sums(uint32_t tile, int lane, float& sum_lo, float& sum_hi) {
+    const uint32_t base = tile + ((lane & 3) << 2);
+    const int chunk = lane >> 2;
+#pragma unroll 8
+    for (int r = 0; r < 64; ++r) {
+        const uint32_t w = lds32(base + r * 128 + ((chunk ^ (r & 7)) << 4));
+        sum_lo += bf16_lo(w);
+        sum_hi += bf16_hi(w);
+    }
+}
+
 // Byte offset of 16-byte chunk c of 64-byte row r in a 64-byte-swizzled tile.
 __device__ __forceinline__ uint32_t sw64(int r, int c) { return uint32_t(r * 64 + ((c ^ ((r >> 1) & 3)) << 4)); }
 
-template <bool kRowwise, bool kColwise>
+template <bool kRowwise, bool kColwise, bool kDbias>
 __global__ void __launch_bounds__(kWarps * 32, 1)
 quantize_kernel(const __grid_constant__ CUtensorMap x_map, const __grid_constant__ CUtensorMap qrow_map,
                 const __grid_constant__ CUtensorMap qcol_map, const QuantizeParams p) {
@@ -195,11 +216,12 @@ quantize_kernel(const __grid_constant__ CUtensorMap x_map, const __grid_constant
 
         uint32_t cc[2][2][8];             // column codes [half][column 2l / 2l+1][words]
         uint32_t rc[2][2][8];             // row codes [row l / l+32][block][words]
+        float sum_lo = 0.0f, sum_hi = 0.0f;               // bias-gradient band sums
         if (kColwise) {
             const bool second = r0 + 32 < p.rows;          // rows % 32 == 0 here
             uint32_t s_lo[2] = {0, 0}, s_hi[2] = {0, 0};
-            col_blocks(tile, 0, lane, cc[0][0], cc[0][1], s_lo[0], s_hi[0]);
-            col_blocks(tile, 32, lane, cc[1][0], cc[1][1], s_lo[1], s_hi[1]);
+            col_blocks(tile, 0, lane, cc[0][0], cc[0][1], s_lo[0], s_hi[0], sum_lo, sum_hi);
+            col_blocks(tile, 32, lane, cc[1][0], cc[1][1], s_lo[1], s_hi[1], sum_lo, sum_hi);
             const int64_t c = c0 + 2 * lane;
             if (c < p.cols) {                              // cols % 32 == 0: c + 1 valid too
                 uint8_t* sp = p.s_col + c * p.ld_s_col + (r0 >> 5);
@@ -211,6 +233,13 @@ quantize_kernel(const __grid_constant__ CUtensorMap x_map, const __grid_constant
                     st_global_u8(sp + p.ld_s_col, s_hi[0]);
                 }
             }
+        }
+        if (kDbias) {
+            if (!kColwise) col_sums(tile, lane, sum_lo, sum_hi);
+            const int64_t c = c0 + 2 * lane;
+            if (c < p.cols)                                // rows past the end were loaded as 0
+                *reinterpret_cast<float2*>(p.partial + (r0 / kDbiasBandRows) * p.cols + c) =
+                    make_float2(sum_lo, sum_hi);
         }
         if (kRowwise) {
 #pragma unroll
@@ -255,7 +284,7 @@ quantize_kernel(const __grid_constant__ CUtensorMap x_map, const __grid_constant
         if (lane == 0) {
             if (kRowwise) tma_store_2d(&qrow_map, tile, int32_t(c0), int32_t(r0));
             if (kColwise) tma_store_2d(&qcol_map, tile + 4096, int32_t(r0), int32_t(c0));
-            bulk_commit();
+            bulk_commit();             // (an empty group when only the bias gradient is produced)
             if (i + kStages < n_mine) {
                 bulk_wait_read_all();     // the stores have read the tile: refill it
                 const int64_t un = gwarp + (i + kStages) * nwarps;
@@ -269,10 +298,22 @@ quantize_kernel(const __grid_constant__ CUtensorMap x_map, const __grid_constant
     if (lane == 0) bulk_wait_all();
 }
 
-template <bool R, bool C>
+// Bias gradient, second pass: dbias[c] = bf16(sum over the bands of partial[b][c]),
+// bands in order (deterministic).
+__global__ void dbias_reduce_kernel(const float* __restrict__ partial, int64_t bands, int64_t cols,
+                                    uint16_t* __restrict__ dbias) {
+    const int64_t c = int64_t(blockIdx.x) * blockDim.x + threadIdx.x;
+    if (c >= cols) return;
+    float acc = 0.0f;
+    for (int64_t b = 0; b < bands; ++b) acc += partial[b * cols + c];
+    const __nv_bfloat16 h = __float2bfloat16_rn(acc);
+    dbias[c] = *reinterpret_cast<const uint16_t*>(&h);
+}
+
+template <bool R, bool C, bool D>
 cudaError_t launch(const CUtensorMap& xm, const CUtensorMap& qr, const CUtensorMap& qc, const QuantizeParams& p,
                    int sms, cudaStream_t stream) {
-    auto k = quantize_kernel<R, C>;
+    auto k = quantize_kernel<R, C, D>;
     cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
     if (e != cudaSuccess) return e;
     const int64_t want = (p.units + kWarps - 1) / kWarps;
@@ -284,8 +325,8 @@ cudaError_t launch(const CUtensorMap& xm, const CUtensorMap& qr, const CUtensorM
 }  // namespace
 
 te_mx_status quantize_launch(const QuantizeArgs& a, cudaStream_t stream) {
-    const bool rowwise = a.q_row != nullptr, colwise = a.q_col != nullptr;
-    if (a.rows == 0 || a.cols == 0 || (!rowwise && !colwise)) return TE_MX_OK;
+    const bool rowwise = a.q_row != nullptr, colwise = a.q_col != nullptr, dbias = a.dbias != nullptr;
+    if (a.rows == 0 || a.cols == 0 || (!rowwise && !colwise && !dbias)) return TE_MX_OK;
 
     CUtensorMap xm, qr, qc;
     te_mx_status st = encode_tensor_map_2d(&xm, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, a.x,
@@ -307,6 +348,7 @@ te_mx_status quantize_launch(const QuantizeArgs& a, cudaStream_t stream) {
     p.s_col = a.s_col; p.ld_s_col = a.ld_s_col;
     p.col_units = (a.cols + kCols - 1) / kCols;
     p.units = ((a.rows + kRows - 1) / kRows) * p.col_units;
+    p.partial = a.partial;
     st = device_status_ptr(&p.status);
     if (st != TE_MX_OK) return st;
 
@@ -314,9 +356,21 @@ te_mx_status quantize_launch(const QuantizeArgs& a, cudaStream_t stream) {
     st = device_sm_count(&sms);
     if (st != TE_MX_OK) return st;
     cudaError_t e;
-    if (rowwise && colwise) e = launch<true, true>(xm, qr, qc, p, sms, stream);
-    else if (rowwise) e = launch<true, false>(xm, qr, qc, p, sms, stream);
-    else e = launch<false, true>(xm, qr, qc, p, sms, stream);
+    if (!dbias) {
+        if (rowwise && colwise) e = launch<true, true, false>(xm, qr, qc, p, sms, stream);
+        else if (rowwise) e = launch<true, false, false>(xm, qr, qc, p, sms, stream);
+        else e = launch<false, true, false>(xm, qr, qc, p, sms, stream);
+    } else {
+        if (rowwise && colwise) e = launch<true, true, true>(xm, qr, qc, p, sms, stream);
+        else if (rowwise) e = launch<true, false, true>(xm, qr, qc, p, sms, stream);
+        else if (colwise) e = launch<false, true, true>(xm, qr, qc, p, sms, stream);
+        else e = launch<false, false, true>(xm, qr, qc, p, sms, stream);
+        if (e == cudaSuccess) {
+            const int64_t bands = (a.rows + kDbiasBandRows - 1) / kDbiasBandRows;
+            dbias_reduce_kernel<<<unsigned((a.cols + 255) / 256), 256, 0, stream>>>(a.partial, bands, a.cols, a.dbias);
+            e = cudaGetLastError();
+        }
+    }
     return cuda_status(e, "quantize kernel launch");
 }
 

@@ -18,7 +18,11 @@ struct QuantizeArgs {
     uint8_t* q_col;
     uint8_t* s_col;
     int64_t ld_s_col;
+    uint16_t* dbias;         // bf16 [cols] or null (no bias gradient)
+    float* partial;          // fp32 [ceil(rows/64) x cols] band sums (with dbias)
 };
+
+constexpr int64_t kDbiasBandRows = 64;     // rows per partial column sum
 
 struct GemmArgs {
     const uint8_t* A;        // dense: [M x K]; grouped: X [total_m x K]
