@@ -125,6 +125,28 @@ TEMX_API te_mx_status te_mx_quantize_dbias(const void* x, int64_t rows, int64_t 
                                   void* dbias, void* workspace, size_t workspace_bytes,
                                   void* stream);
 
+/* te_mx_quantize_dbias_noalloc — te_mx_quantize_dbias for callers that cannot
+ * allocate device memory.  The sources describe no such entry point; it exists
+ * for host code that has no device allocator of its own or runs under a fixed,
+ * pre-planned memory budget in which allocating after start-up is not allowed
+ * (and where a cudaMalloc, which may synchronise the device, is unwelcome).
+ * Instead of a caller workspace, the band sums go to a scratch array built
+ * into the library: 32 MiB per GPU (TE_MX_NOALLOC_SCRATCH_BYTES), held by every
+ * GPU that loads the library until the process exits.  Sizes whose scratch
+ * (te_mx_quantize_dbias_workspace_size) exceeds it are rejected with
+ * TE_MX_ERR_WORKSPACE_TOO_SMALL and a message.  The first call on a device
+ * looks up the scratch address for that device (so make that first call
+ * before recording work into a stream capture).  All calls share the one
+ * array: calls whose kernels overlap on the GPU (different streams without
+ * ordering) race on it and give wrong results.  Nothing in it needs clearing
+ * between calls (every value is written before it is read).  Arguments,
+ * outputs and results are those of te_mx_quantize_dbias.  Allocates nothing. */
+#define TE_MX_NOALLOC_SCRATCH_BYTES ((size_t)32 << 20)
+TEMX_API te_mx_status te_mx_quantize_dbias_noalloc(const void* x, int64_t rows, int64_t cols, int64_t ld_x,
+                                          uint8_t* q_row, uint8_t* s_row, int64_t ld_s_row,
+                                          uint8_t* q_col, uint8_t* s_col, int64_t ld_s_col,
+                                          void* dbias, void* stream);
+
 /* te_mx_gemm — MXFP8 TN GEMM with fused epilogue (HipKittens MXFP8 GEMM
  * Support, PR description: MXFP8 GEMM with BIAS and GELU AUX epilogues; the
  * review thread's TN layout and its K % 128 rule for MXFP8 scaling):

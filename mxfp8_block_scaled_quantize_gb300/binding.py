@@ -28,6 +28,7 @@ SIGNATURES = {
     "te_mx_quantize": (ctypes.c_int, [_P, _I64, _I64, _I64, _P, _P, _I64, _P, _P, _I64, _P]),
     "te_mx_quantize_dbias_workspace_size": (_SZ, [_I64, _I64]),
     "te_mx_quantize_dbias": (ctypes.c_int, [_P, _I64, _I64, _I64, _P, _P, _I64, _P, _P, _I64, _P, _P, _SZ, _P]),
+    "te_mx_quantize_dbias_noalloc": (ctypes.c_int, [_P, _I64, _I64, _I64, _P, _P, _I64, _P, _P, _I64, _P, _P]),
     "te_mx_gemm": (ctypes.c_int, [_P, _P, _I64, _P, _P, _I64, _I64, _I64, _I64, _P, _I32, _P, _P, _P, _SZ, _P]),
     "te_mx_grouped_gemm": (ctypes.c_int, [_I32, _P, _I64, _P, _P, _I64, _P, _P, _I64, _I64, _I64, _P, _I32,
                                           _P, _P, _P, _SZ, _P]),
@@ -86,6 +87,14 @@ def te_mx_quantize_dbias(x, rows, cols, ld_x, q_row, s_row, ld_s_row, q_col, s_c
                          workspace_bytes, stream) -> None:
     _check(lib().te_mx_quantize_dbias(x, rows, cols, ld_x, q_row, s_row, ld_s_row, q_col, s_col, ld_s_col, dbias,
                                       workspace, workspace_bytes, stream))
+
+
+def te_mx_quantize_dbias_noalloc(x, rows, cols, ld_x, q_row, s_row, ld_s_row, q_col, s_col, ld_s_col, dbias,
+                                 stream) -> None:
+    """Same as te_mx_quantize_dbias, for callers that cannot allocate device
+    memory: the scratch is built into the library (TE_MX_NOALLOC_SCRATCH_BYTES)."""
+    _check(lib().te_mx_quantize_dbias_noalloc(x, rows, cols, ld_x, q_row, s_row, ld_s_row, q_col, s_col, ld_s_col,
+                                              dbias, stream))
 
 
 def te_mx_gemm(A, sA, ld_sA, B, sB, ld_sB, M, N, K, bias, epilogue, D, aux, workspace, workspace_bytes,

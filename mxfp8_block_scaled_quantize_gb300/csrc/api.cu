@@ -98,6 +98,8 @@ te_mx_status set_error(te_mx_status st, const char* fmt, ...) {
     return st;
 }
 
+void clear_error() { t_last_error[0] = '\0'; }
+
 te_mx_status cuda_status(cudaError_t e, const char* what) {
     if (e == cudaSuccess) return TE_MX_OK;
     if (e == cudaErrorNoKernelImageForDevice)
@@ -161,25 +163,9 @@ te_mx_status encode_tensor_map_3d(CUtensorMap* map, CUtensorMapDataType dtype, c
     return TE_MX_OK;
 }
 
-}  // namespace temx
-
-using namespace temx;
-
-extern "C" {
-
-size_t te_mx_scale_pitch(int64_t k) {
-    if (k <= 0) return 0;
-    const int64_t blocks = (k + 31) / 32;
-    return size_t((blocks + 15) / 16 * 16);
-}
-
-const char* te_mx_last_error(void) { return t_last_error; }
-
-const char* te_mx_version(void) { return "temx 0.1 (sm_103a)"; }
-
-static te_mx_status validate_quantize(const void* x, int64_t rows, int64_t cols, int64_t ld_x,
-                                      uint8_t* q_row, uint8_t* s_row, int64_t ld_s_row,
-                                      uint8_t* q_col, uint8_t* s_col, int64_t ld_s_col, bool dbias) {
+te_mx_status validate_quantize(const void* x, int64_t rows, int64_t cols, int64_t ld_x,
+                                     uint8_t* q_row, uint8_t* s_row, int64_t ld_s_row,
+                                     uint8_t* q_col, uint8_t* s_col, int64_t ld_s_col, bool dbias) {
     if (rows < 0 || cols < 0) return set_error(TE_MX_ERR_INVALID_ARG, "negative size %lld x %lld", (long long)rows, (long long)cols);
     if ((q_row == nullptr) != (s_row == nullptr))
         return set_error(TE_MX_ERR_INVALID_ARG, "q_row and s_row must both be given or both be NULL");
@@ -207,6 +193,22 @@ static te_mx_status validate_quantize(const void* x, int64_t rows, int64_t cols,
     return check_device(nullptr);
 }
 
+}  // namespace temx
+
+using namespace temx;
+
+extern "C" {
+
+size_t te_mx_scale_pitch(int64_t k) {
+    if (k <= 0) return 0;
+    const int64_t blocks = (k + 31) / 32;
+    return size_t((blocks + 15) / 16 * 16);
+}
+
+const char* te_mx_last_error(void) { return t_last_error; }
+
+const char* te_mx_version(void) { return "temx 0.1 (sm_103a)"; }
+
 te_mx_status te_mx_quantize(const void* x, int64_t rows, int64_t cols, int64_t ld_x,
                             uint8_t* q_row, uint8_t* s_row, int64_t ld_s_row,
                             uint8_t* q_col, uint8_t* s_col, int64_t ld_s_col, void* stream) {
@@ -226,7 +228,7 @@ te_mx_status te_mx_quantize_dbias(const void* x, int64_t rows, int64_t cols, int
                                   uint8_t* q_row, uint8_t* s_row, int64_t ld_s_row,
                                   uint8_t* q_col, uint8_t* s_col, int64_t ld_s_col,
                                   void* dbias, void* workspace, size_t workspace_bytes, void* stream) {
-    t_last_error[0] = '\0';
+    clear_error();
     if (!dbias) return set_error(TE_MX_ERR_INVALID_ARG, "dbias is NULL");
     te_mx_status st = validate_quantize(x, rows, cols, ld_x, q_row, s_row, ld_s_row, q_col, s_col, ld_s_col, true);
     if (st != TE_MX_OK || rows == 0 || cols == 0) return st;

@@ -20,6 +20,7 @@
 // of 32 scattered sectors per instruction.  Scale bytes (2 per row or column
 // per unit) are stored directly.  Warps never wait on each other.
 #include <cuda_bf16.h>
+#include <mutex>
 #include <cuda_runtime.h>
 
 #include "ptx.cuh"
@@ -375,3 +376,62 @@ te_mx_status quantize_launch(const QuantizeArgs& a, cudaStream_t stream) {
 }
 
 }  // namespace temx
+
+// ---------------------------------------------------------------------------
+// Allocation-free bias-gradient quantisation (te_mx_quantize_dbias_noalloc).
+// The band sums live in this file-scope device array instead of a caller
+// workspace.  Host code must not hand `g_noalloc_scratch` itself to a kernel
+// (in host code that name is only a stand-in for the device symbol); its
+// device address is looked up once per device with cudaGetSymbolAddress.
+// ---------------------------------------------------------------------------
+namespace {
+
+constexpr size_t kNoAllocScratchBytes = TE_MX_NOALLOC_SCRATCH_BYTES;
+static __device__ __align__(256) float g_noalloc_scratch[kNoAllocScratchBytes / sizeof(float)];
+
+constexpr int kNoAllocMaxDevices = 64;
+float* g_noalloc_ptr[kNoAllocMaxDevices];     // per-device address, null until looked up
+std::mutex g_noalloc_mutex;
+
+// The scratch address on the current device (looked up on first use).
+te_mx_status noalloc_scratch(float** out) {
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return temx::cuda_status(e, "cudaGetDevice");
+    if (dev < 0 || dev >= kNoAllocMaxDevices)
+        return temx::set_error(TE_MX_ERR_CUDA, "device index %d out of range", dev);
+    std::lock_guard<std::mutex> lock(g_noalloc_mutex);
+    if (!g_noalloc_ptr[dev]) {
+        void* p = nullptr;
+        e = cudaGetSymbolAddress(&p, g_noalloc_scratch);
+        if (e != cudaSuccess) return temx::cuda_status(e, "cudaGetSymbolAddress(no-alloc scratch)");
+        g_noalloc_ptr[dev] = static_cast<float*>(p);
+    }
+    *out = g_noalloc_ptr[dev];
+    return TE_MX_OK;
+}
+
+}  // namespace
+
+extern "C" te_mx_status te_mx_quantize_dbias_noalloc(const void* x, int64_t rows, int64_t cols, int64_t ld_x,
+                                                     uint8_t* q_row, uint8_t* s_row, int64_t ld_s_row,
+                                                     uint8_t* q_col, uint8_t* s_col, int64_t ld_s_col,
+                                                     void* dbias, void* stream) {
+    using namespace temx;
+    clear_error();
+    if (!dbias) return set_error(TE_MX_ERR_INVALID_ARG, "dbias is NULL");
+    te_mx_status st = validate_quantize(x, rows, cols, ld_x, q_row, s_row, ld_s_row, q_col, s_col, ld_s_col, true);
+    if (st != TE_MX_OK || rows == 0 || cols == 0) return st;
+    if (reinterpret_cast<uintptr_t>(dbias) % 16) return set_error(TE_MX_ERR_MISALIGNED, "dbias is not 16-byte aligned");
+    const size_t need = te_mx_quantize_dbias_workspace_size(rows, cols);
+    if (need > kNoAllocScratchBytes)
+        return set_error(TE_MX_ERR_WORKSPACE_TOO_SMALL,
+                         "%lld x %lld needs %zu bytes of bias-gradient scratch; the built-in scratch holds %zu "
+                         "(use te_mx_quantize_dbias with a workspace)",
+                         (long long)rows, (long long)cols, need, kNoAllocScratchBytes);
+    float* scratch = nullptr;
+    if ((st = noalloc_scratch(&scratch)) != TE_MX_OK) return st;
+    QuantizeArgs a{x, rows, cols, ld_x, q_row, s_row, ld_s_row, q_col, s_col, ld_s_col,
+                   static_cast<uint16_t*>(dbias), scratch};
+    return quantize_launch(a, static_cast<cudaStream_t>(stream));
+}

@@ -45,6 +45,11 @@ te_mx_status gemm_launch(const GemmArgs& a, cudaStream_t stream);
 
 // Helpers implemented in api.cu.
 te_mx_status set_error(te_mx_status st, const char* fmt, ...);
+void clear_error();
+// Host-side argument checks of te_mx_quantize (+ the current device's arch).
+te_mx_status validate_quantize(const void* x, int64_t rows, int64_t cols, int64_t ld_x,
+                               uint8_t* q_row, uint8_t* s_row, int64_t ld_s_row,
+                               uint8_t* q_col, uint8_t* s_col, int64_t ld_s_col, bool dbias);
 te_mx_status cuda_status(cudaError_t e, const char* what);
 te_mx_status device_sm_count(int* sms);
 te_mx_status device_status_ptr(unsigned int** ptr);   // this device's status word
