@@ -180,6 +180,28 @@ class Step:
                                                        gelu=True, out=o["moe"])),
         ]
         self.outputs = [o["fprop"][0], o["fprop"][1], o["wgrad"][0], o["moe"][0], o["moe"][1]]
+        # Backward kernels outside the step (reported under "next_rows"):
+        #   dgrad  dX = dY W (M=8192, N=7168, K=18432) on the column-wise weight;
+        #   dgelu  the GELU-backward GEMM at fprop shape (8192x18432x7168) reading
+        #          the fprop's AUX (operands reused from the step: timing only);
+        #   quant_dbias  dY row+col quantisation fused with its bias gradient.
+        o["w_col"] = {"q_col": e(H, F), "s_col": e(H, pitch(F))}
+        o["dx"] = (e(T, H, dt=torch.bfloat16), None)
+        o["dgelu"] = (e(T, F, dt=torch.bfloat16), None)
+        o["dy_b"] = {"q_row": e(T, F), "s_row": e(T, pitch(F)), "q_col": e(F, T), "s_col": e(F, pitch(T)),
+                     "dbias": e(F, dt=torch.bfloat16)}
+        o["ws"] = e(max(1, temx.binding.te_mx_quantize_dbias_workspace_size(T, F)))
+        self.next_flops = {"gemm_dgrad": 2.0 * T * H * F, "gemm_dgelu": 2.0 * T * F * H}
+        self.next_bytes = {"quant_dbias_ffn_dy": qb(T, F, True) + 2.0 * F}
+        self.next_kernels = [
+            ("gemm_dgrad", lambda: temx.gemm(o["dy"]["q_row"], o["dy"]["s_row"], o["w_col"]["q_col"],
+                                             o["w_col"]["s_col"], out=o["dx"])),
+            ("gemm_dgelu", lambda: temx.gemm(o["x_row"]["q_row"], o["x_row"]["s_row"], o["w_row"]["q_row"],
+                                             o["w_row"]["s_row"], out=o["dgelu"], dgelu_aux=o["fprop"][1])),
+            ("quant_dbias_ffn_dy", lambda: temx.quantize(d["ffn_dY"], True, True, out=o["dy_b"], dbias=True,
+                                                         workspace=o["ws"])),
+        ]
+        temx.quantize(d["ffn_W"], False, True, out=o["w_col"])
 
     def run(self, events=None):
         for i, (_, fn) in enumerate(self.kernels):
@@ -215,6 +237,31 @@ def time_device(step, steps, warmup, sampler):
     for i, (name, _) in enumerate(step.kernels):
         per_kernel[name] = sum(evs[s][i][0].elapsed_time(evs[s][i][1]) for s in range(steps)) / steps
     return total_ms, per_kernel, clocks
+
+
+def time_next(step, reps, fp8_peak, hbm_gbs):
+    """CUDA-event time of each backward kernel (after the step ran once)."""
+    step.run()
+    torch.cuda.synchronize()
+    res = {}
+    for name, fn in step.next_kernels:
+        fn()
+        torch.cuda.synchronize()
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record()
+        for _ in range(reps):
+            fn()
+        b.record()
+        torch.cuda.synchronize()
+        ms = a.elapsed_time(b) / reps
+        if name in step.next_flops:
+            ach = step.next_flops[name] / (ms * 1e-3) / 1e12
+            res[name] = {"us": ms * 1e3, "achieved": ach, "unit": "TFLOP/s", "frac": ach / fp8_peak}
+        else:
+            ach = step.next_bytes[name] / (ms * 1e-3) / 1e9
+            res[name] = {"us": ms * 1e3, "achieved": ach, "unit": "GB/s", "frac": ach / hbm_gbs}
+    step.temx.te_mx_device_status()
+    return res
 
 
 def time_e2e(step, host, steps, warmup):
@@ -452,6 +499,7 @@ def main():
     qms = sum(per_kernel[n] for n in step.bytes)
     gms = sum(per_kernel[n] for n in step.flops)
 
+    next_rows = time_next(step, 20, fp8_peak, peaks["hbm_gbs"])
     e2e_ms, h2d, d2h = time_e2e(step, host, max(3, args.steps // 4), args.warmup)
     e2e_ms = dist_max(e2e_ms)
     out = {
@@ -463,7 +511,7 @@ def main():
                    "l2": "inputs larger than L2 (every operand > 126 MB except bias/group sizes)"},
         "gemm_tflops": gemm_flops / (gms * 1e-3) / 1e12, "gemm_frac": gemm_flops / (gms * 1e-3) / 1e12 / fp8_peak,
         "quantize_gbs": qbytes / (qms * 1e-3) / 1e9, "quantize_frac": qbytes / (qms * 1e-3) / 1e9 / peaks["hbm_gbs"],
-        "kernels": kern, "roofline": roofline, "clocks": clocks,
+        "kernels": kern, "roofline": roofline, "clocks": clocks, "next_rows": next_rows,
         "gpu_launches": len(step.kernels) * args.steps,
         "e2e": {"value": whole_job_tflops(gemm_flops, world, e2e_ms), "unit": UNIT,
                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},

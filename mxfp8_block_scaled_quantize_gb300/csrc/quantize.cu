@@ -299,16 +299,28 @@ quantize_kernel(const __grid_constant__ CUtensorMap x_map, const __grid_constant
     if (lane == 0) bulk_wait_all();
 }
 
-// Bias gradient, second pass: dbias[c] = bf16(sum over the bands of partial[b][c]),
-// bands in order (deterministic).
-__global__ void dbias_reduce_kernel(const float* __restrict__ partial, int64_t bands, int64_t cols,
-                                    uint16_t* __restrict__ dbias) {
-    const int64_t c = int64_t(blockIdx.x) * blockDim.x + threadIdx.x;
-    if (c >= cols) return;
+// Bias gradient, second pass: dbias[c] = bf16(sum over the bands of
+// partial[b][c]).  A block owns 32 columns (lane = column, coalesced loads);
+// warp w sums bands w, w + 8, w + 16, ... in order, then the 8 warp sums are
+// added in warp order: a fixed order, so the result is deterministic.
+constexpr int kReduceWarps = 8;
+__global__ void __launch_bounds__(kReduceWarps * 32)
+dbias_reduce_kernel(const float* __restrict__ partial, int64_t bands, int64_t cols, uint16_t* __restrict__ dbias) {
+    __shared__ float part[kReduceWarps][32];
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int64_t c = int64_t(blockIdx.x) * 32 + lane;
     float acc = 0.0f;
-    for (int64_t b = 0; b < bands; ++b) acc += partial[b * cols + c];
-    const __nv_bfloat16 h = __float2bfloat16_rn(acc);
-    dbias[c] = *reinterpret_cast<const uint16_t*>(&h);
+    if (c < cols)
+        for (int64_t b = warp; b < bands; b += kReduceWarps) acc += partial[b * cols + c];
+    part[warp][lane] = acc;
+    __syncthreads();
+    if (warp == 0 && c < cols) {
+        float sum = part[0][lane];
+#pragma unroll
+        for (int w = 1; w < kReduceWarps; ++w) sum += part[w][lane];
+        const __nv_bfloat16 h = __float2bfloat16_rn(sum);
+        dbias[c] = *reinterpret_cast<const uint16_t*>(&h);
+    }
 }
 
 template <bool R, bool C, bool D>
@@ -368,7 +380,8 @@ te_mx_status quantize_launch(const QuantizeArgs& a, cudaStream_t stream) {
         else e = launch<false, false, true>(xm, qr, qc, p, sms, stream);
         if (e == cudaSuccess) {
             const int64_t bands = (a.rows + kDbiasBandRows - 1) / kDbiasBandRows;
-            dbias_reduce_kernel<<<unsigned((a.cols + 255) / 256), 256, 0, stream>>>(a.partial, bands, a.cols, a.dbias);
+            dbias_reduce_kernel<<<unsigned((a.cols + 31) / 32), kReduceWarps * 32, 0, stream>>>(a.partial, bands,
+                                                                                                a.cols, a.dbias);
             e = cudaGetLastError();
         }
     }
