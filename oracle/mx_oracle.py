@@ -32,6 +32,11 @@ Sources of the definitions
   0.044715 x^3))); its derivative (dGELU) for the backward epilogue named in
   ROCm/TransformerEngine README, "Blockwise FP8 GEMM support on ROCm"
   (bias/beta/DGELU epilogues).
+* Float8BlockScaling (ROCm/TransformerEngine README, "Blockwise FP8 GEMM support
+  on ROCm"): 1x128 blocks for activations/gradients, 128x128 blocks for
+  weights, each with an FP32 scale amax / 448 that is cast to E8M0 (the
+  default there).  Reading of the cast: the smallest power of two >= amax/448,
+  i.e. 2^ceil(log2(amax / 448)), so that no element exceeds 448 after scaling.
 * Bias gradient: the column sums of the output gradient (the cast_transpose_bgrad
   kernels of ROCm/TransformerEngine README, "Experimental Triton Kernels on ROCm").
 
@@ -237,6 +242,45 @@ def quantize_colwise(x_bits):
     operand).
     """
     return quantize_mx(x_bits, axis=0)
+
+
+def block_scale_exponent(amax) -> np.ndarray:
+    """Float8BlockScaling scale cast to E8M0: e = ceil(log2(amax / 448)), found
+    exactly as the smallest integer e with amax <= 448 * 2^e; clamped to
+    [-127, 127]; amax == 0 gives -127."""
+    amax = np.asarray(amax, dtype=np.float64)
+    e = floor_log2(amax) - E4M3_EMAX                 # first guess: 448 * 2^e may be below amax
+    e = np.where(amax > E4M3_MAX * pow2(np.clip(e, -1000, 1000)), e + 1, e)
+    e = np.clip(e, -E8M0_BIAS, E8M0_BIAS)
+    return np.where(amax == 0.0, -E8M0_BIAS, e).astype(np.int64)
+
+
+def quantize_block(x_bits, block_2d: bool):
+    """Float8BlockScaling quantisation, E8M0-cast scales, in the MX layout.
+
+    ``block_2d`` False: 1x128 blocks along each row (row-wise copy) and 128x1
+    blocks down each column (column-wise copy).  True: 128x128 blocks; both
+    copies share each block's scale.  Rows and columns must be multiples of 128.
+    Returns (q_row [R,C], s_row [R,C/32], q_col [C,R], s_col [C,R/32]): the
+    scale of a 128-block is repeated for each of its four 32-element groups, so
+    the MX GEMM of these operands is the block-scaled GEMM.
+    """
+    x = bf16_bits_to_f64(np.asarray(x_bits, dtype=np.uint16))
+    rows, cols = x.shape
+    if rows % 128 or cols % 128:
+        raise ValueError("rows and cols must be multiples of 128")
+    ax = np.abs(x)
+    with np.errstate(invalid="ignore"):
+        if block_2d:
+            amax = ax.reshape(rows // 128, 128, cols // 128, 128).max(axis=(1, 3))   # [R/128, C/128]
+            e_row = np.repeat(np.repeat(block_scale_exponent(amax), 128, axis=0), 4, axis=1)   # [R, C/32]
+            e_col = np.repeat(np.repeat(block_scale_exponent(amax).T, 128, axis=0), 4, axis=1)  # [C, R/32]
+        else:
+            e_row = np.repeat(block_scale_exponent(ax.reshape(rows, cols // 128, 128).max(axis=2)), 4, axis=1)
+            e_col = np.repeat(block_scale_exponent(ax.T.reshape(cols, rows // 128, 128).max(axis=2)), 4, axis=1)
+    q_row = e4m3_encode(x * pow2(-np.repeat(e_row, 32, axis=1))).astype(np.uint8)
+    q_col = e4m3_encode(x.T * pow2(-np.repeat(e_col, 32, axis=1))).astype(np.uint8)
+    return q_row, (e_row + E8M0_BIAS).astype(np.uint8), q_col, (e_col + E8M0_BIAS).astype(np.uint8)
 
 
 def dequantize(q, s) -> np.ndarray:
