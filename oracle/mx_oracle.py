@@ -260,27 +260,39 @@ def quantize_block(x_bits, block_2d: bool):
 
     ``block_2d`` False: 1x128 blocks along each row (row-wise copy) and 128x1
     blocks down each column (column-wise copy).  True: 128x128 blocks; both
-    copies share each block's scale.  Rows and columns must be multiples of 128.
-    Returns (q_row [R,C], s_row [R,C/32], q_col [C,R], s_col [C,R/32]): the
-    scale of a 128-block is repeated for each of its four 32-element groups, so
-    the MX GEMM of these operands is the block-scaled GEMM.
+    copies share each block's scale.  Blocks at the right and bottom edges may
+    be partial: their amax is taken over the elements present.  A block holding
+    NaN or inf gets scale byte 0xFF and every code 0x7F (the MX convention).
+    Returns (q_row [R,C], s_row [R,ceil(C/32)], q_col [C,R], s_col
+    [C,ceil(R/32)]): the scale of a 128-block is repeated for each of its
+    32-element groups, so the MX GEMM of these operands is the block-scaled GEMM.
     """
     x = bf16_bits_to_f64(np.asarray(x_bits, dtype=np.uint16))
     rows, cols = x.shape
-    if rows % 128 or cols % 128:
-        raise ValueError("rows and cols must be multiples of 128")
-    ax = np.abs(x)
+    pr, pc = -(-rows // 128) * 128, -(-cols // 128) * 128
+    xp = np.zeros((pr, pc))                  # zero padding leaves every amax unchanged
+    xp[:rows, :cols] = x
+    ax = np.abs(xp)
     with np.errstate(invalid="ignore"):
         if block_2d:
-            amax = ax.reshape(rows // 128, 128, cols // 128, 128).max(axis=(1, 3))   # [R/128, C/128]
-            e_row = np.repeat(np.repeat(block_scale_exponent(amax), 128, axis=0), 4, axis=1)   # [R, C/32]
-            e_col = np.repeat(np.repeat(block_scale_exponent(amax).T, 128, axis=0), 4, axis=1)  # [C, R/32]
+            amax = ax.reshape(pr // 128, 128, pc // 128, 128).max(axis=(1, 3))   # [R/128, C/128]
+            a_row = np.repeat(np.repeat(amax, 128, axis=0), 4, axis=1)           # [R, C/32]
+            a_col = np.repeat(np.repeat(amax.T, 128, axis=0), 4, axis=1)         # [C, R/32]
         else:
-            e_row = np.repeat(block_scale_exponent(ax.reshape(rows, cols // 128, 128).max(axis=2)), 4, axis=1)
-            e_col = np.repeat(block_scale_exponent(ax.T.reshape(cols, rows // 128, 128).max(axis=2)), 4, axis=1)
-    q_row = e4m3_encode(x * pow2(-np.repeat(e_row, 32, axis=1))).astype(np.uint8)
-    q_col = e4m3_encode(x.T * pow2(-np.repeat(e_col, 32, axis=1))).astype(np.uint8)
-    return q_row, (e_row + E8M0_BIAS).astype(np.uint8), q_col, (e_col + E8M0_BIAS).astype(np.uint8)
+            a_row = np.repeat(ax.reshape(pr, pc // 128, 128).max(axis=2), 4, axis=1)
+            a_col = np.repeat(ax.T.reshape(pc, pr // 128, 128).max(axis=2), 4, axis=1)
+    out = []
+    for v, a in ((xp, a_row), (xp.T, a_col)):
+        bad = ~np.isfinite(a)
+        e = block_scale_exponent(np.where(bad, 0.0, a))
+        with np.errstate(invalid="ignore", over="ignore"):
+            q = e4m3_encode(v * pow2(-np.repeat(e, 32, axis=1))).astype(np.uint8)
+        q[np.repeat(bad, 32, axis=1)] = 0x7F
+        s = np.where(bad, 0xFF, e + E8M0_BIAS).astype(np.uint8)
+        out.append((q, s))
+    (q_row, s_row), (q_col, s_col) = out
+    gr, gc = -(-rows // 32), -(-cols // 32)
+    return q_row[:rows, :cols], s_row[:rows, :gc], q_col[:cols, :rows], s_col[:cols, :gr]
 
 
 def dequantize(q, s) -> np.ndarray:

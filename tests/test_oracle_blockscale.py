@@ -94,3 +94,44 @@ def test_block_scaled_gemm_equals_direct_definition():
     da = O.e4m3_decode(O.e4m3_encode(av * np.repeat(2.0 ** -ea, 128, axis=1))) * np.repeat(2.0 ** ea, 128, axis=1)
     db = O.e4m3_decode(O.e4m3_encode(bv * np.repeat(2.0 ** -eb, 128, axis=1))) * np.repeat(2.0 ** eb, 128, axis=1)
     assert np.array_equal(got, da @ db.T)
+
+
+@pytest.mark.parametrize("two_d", [False, True])
+def test_partial_edge_blocks_by_loops(two_d):
+    """Ragged 96 x 160 input: per-block loops over the elements present."""
+    rows, cols = 96, 160
+    x = rand_bits((rows, cols), 8, std=3.0)
+    v = O.bf16_bits_to_f64(x)
+    q_row, s_row, q_col, s_col = O.quantize_block(x, two_d)
+    assert s_row.shape == (rows, cols // 32) and s_col.shape == (cols, rows // 32)
+    for r in range(rows):
+        for c in range(cols):
+            if two_d:
+                rb, cb = r // 128 * 128, c // 128 * 128
+                a_r = a_c = max(abs(v[i, j]) for i in range(rb, min(rb + 128, rows))
+                                for j in range(cb, min(cb + 128, cols)))
+            else:
+                cb, rb = c // 128 * 128, r // 128 * 128
+                a_r = max(abs(v[r, j]) for j in range(cb, min(cb + 128, cols)))
+                a_c = max(abs(v[i, c]) for i in range(rb, min(rb + 128, rows)))
+            e_r = next(e for e in range(-127, 128) if a_r <= 448.0 * 2.0 ** e)
+            e_c = next(e for e in range(-127, 128) if a_c <= 448.0 * 2.0 ** e)
+            assert s_row[r, c // 32] == e_r + 127
+            assert s_col[c, r // 32] == e_c + 127
+            assert q_row[r, c] == O.e4m3_encode(v[r, c] * 2.0 ** -e_r)
+            assert q_col[c, r] == O.e4m3_encode(v[r, c] * 2.0 ** -e_c)
+        if two_d:
+            break                                     # every row of a 2D block is alike: one row suffices
+
+
+def test_non_finite_block():
+    x = O.f64_to_bf16_bits(np.ones((128, 256)))
+    x[3, 200] = 0x7FC0                                # NaN in row 3, second 128-block
+    x[70, 10] = 0x7F80                                # +inf in row 70, first block
+    q_row, s_row, q_col, s_col = O.quantize_block(x, False)
+    assert np.all(s_row[3, 4:] == 0xFF) and np.all(q_row[3, 128:] == 0x7F)
+    assert np.all(s_row[3, :4] == 127 - 8) and np.all(q_row[3, :128] == 0x78)    # 1 * 2^8 = 256
+    assert np.all(s_row[70, :4] == 0xFF) and np.all(q_row[70, :128] == 0x7F)
+    assert np.all(s_col[200] == 0xFF) and np.all(q_col[200] == 0x7F) and np.all(s_col[201] == 119)
+    q_row, s_row, q_col, s_col = O.quantize_block(x, True)
+    assert np.all(s_row == 0xFF) and np.all(q_col == 0x7F)
