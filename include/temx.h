@@ -147,6 +147,30 @@ TEMX_API te_mx_status te_mx_quantize_dbias_noalloc(const void* x, int64_t rows, 
                                           uint8_t* q_col, uint8_t* s_col, int64_t ld_s_col,
                                           void* dbias, void* stream);
 
+/* te_mx_block_quantize — Float8BlockScaling quantisation with E8M0-cast scales
+ * ("Blockwise FP8 GEMM support on ROCm", ROCm/TransformerEngine README: 1Dx1D
+ * and 1Dx2D block scaling; the recipe's FP32 scale amax/448 cast to a power of
+ * two, the default there).  Blocks: block_2d == 0 gives 1x128 blocks along a
+ * row for q_row and 128x1 blocks down a column for q_col (activations and
+ * gradients); block_2d == 1 gives 128x128 blocks shared by both copies
+ * (weights).  Per block, with amax the largest |x| of the elements present
+ * (edge blocks may be partial):
+ *   e = ceil(log2(amax / 448)) clamped to [-127, 127] (-127 for amax 0),
+ *   q = E4M3_rn_satfinite(x 2^-e)   (no element saturates),
+ * and a block holding NaN/inf gets scale byte 0xFF and codes 0x7F.
+ * Outputs use the te_mx_quantize layout exactly: s_row[r][j] = e + 127 of the
+ * block holding q_row[r][32j], i.e. each block scale is repeated over its
+ * 32-element groups, so te_mx_gemm / te_mx_grouped_gemm on these operands
+ * compute the block-scaled GEMM (1Dx1D: both operands block_2d == 0; 1Dx2D:
+ * the weight with block_2d == 1).
+ * Arguments, rules and errors as te_mx_quantize, plus: block_2d is 0 or 1
+ * (else TE_MX_ERR_INVALID_ARG).  Output is bit-exact to the definition above. */
+TEMX_API te_mx_status te_mx_block_quantize(const void* x, int64_t rows, int64_t cols, int64_t ld_x,
+                                           int32_t block_2d,
+                                           uint8_t* q_row, uint8_t* s_row, int64_t ld_s_row,
+                                           uint8_t* q_col, uint8_t* s_col, int64_t ld_s_col,
+                                           void* stream);
+
 /* te_mx_gemm — MXFP8 TN GEMM with fused epilogue (HipKittens MXFP8 GEMM
  * Support, PR description: MXFP8 GEMM with BIAS and GELU AUX epilogues; the
  * review thread's TN layout and its K % 128 rule for MXFP8 scaling):

@@ -26,6 +26,7 @@ _I64, _I32, _P, _SZ = ctypes.c_int64, ctypes.c_int32, ctypes.c_void_p, ctypes.c_
 SIGNATURES = {
     "te_mx_scale_pitch": (_SZ, [_I64]),
     "te_mx_quantize": (ctypes.c_int, [_P, _I64, _I64, _I64, _P, _P, _I64, _P, _P, _I64, _P]),
+    "te_mx_block_quantize": (ctypes.c_int, [_P, _I64, _I64, _I64, _I32, _P, _P, _I64, _P, _P, _I64, _P]),
     "te_mx_quantize_dbias_workspace_size": (_SZ, [_I64, _I64]),
     "te_mx_quantize_dbias": (ctypes.c_int, [_P, _I64, _I64, _I64, _P, _P, _I64, _P, _P, _I64, _P, _P, _SZ, _P]),
     "te_mx_quantize_dbias_noalloc": (ctypes.c_int, [_P, _I64, _I64, _I64, _P, _P, _I64, _P, _P, _I64, _P, _P]),
@@ -77,6 +78,12 @@ def te_mx_scale_pitch(k: int) -> int:
 
 def te_mx_quantize(x, rows, cols, ld_x, q_row, s_row, ld_s_row, q_col, s_col, ld_s_col, stream) -> None:
     _check(lib().te_mx_quantize(x, rows, cols, ld_x, q_row, s_row, ld_s_row, q_col, s_col, ld_s_col, stream))
+
+
+def te_mx_block_quantize(x, rows, cols, ld_x, block_2d, q_row, s_row, ld_s_row, q_col, s_col, ld_s_col,
+                         stream) -> None:
+    _check(lib().te_mx_block_quantize(x, rows, cols, ld_x, block_2d, q_row, s_row, ld_s_row, q_col, s_col,
+                                      ld_s_col, stream))
 
 
 def te_mx_quantize_dbias_workspace_size(rows, cols) -> int:
@@ -166,6 +173,29 @@ def quantize(x, rowwise: bool = True, colwise: bool = False, stream=None, out=No
         workspace = torch.empty(max(1, te_mx_quantize_dbias_workspace_size(rows, cols)), dtype=torch.uint8,
                                 device=x.device)
     te_mx_quantize_dbias(*args, o["dbias"].data_ptr(), workspace.data_ptr(), workspace.numel(), _stream_ptr(stream))
+    return o
+
+
+def block_quantize(x, block_2d: bool = False, rowwise: bool = True, colwise: bool = False, stream=None, out=None):
+    """Float8BlockScaling-quantise a 2-D bf16 CUDA tensor with E8M0-cast
+    scales: 1x128 / 128x1 blocks, or 128x128 blocks with ``block_2d``.  The
+    outputs have the layout of ``quantize`` (block scales repeated per 32
+    elements), so ``gemm`` consumes them as they are."""
+    import torch
+    assert x.dtype == torch.bfloat16 and x.dim() == 2 and x.is_cuda
+    rows, cols = x.shape
+    assert x.stride(1) == 1
+    o = dict(out or {})
+    if rowwise and "q_row" not in o:
+        o["q_row"] = torch.empty(rows, cols, dtype=torch.uint8, device=x.device)
+        o["s_row"] = torch.empty(rows, te_mx_scale_pitch(cols), dtype=torch.uint8, device=x.device)
+    if colwise and "q_col" not in o:
+        o["q_col"] = torch.empty(cols, rows, dtype=torch.uint8, device=x.device)
+        o["s_col"] = torch.empty(cols, te_mx_scale_pitch(rows), dtype=torch.uint8, device=x.device)
+    te_mx_block_quantize(x.data_ptr(), rows, cols, x.stride(0), int(bool(block_2d)),
+                         _ptr(o.get("q_row")), _ptr(o.get("s_row")), o["s_row"].stride(0) if "s_row" in o else 0,
+                         _ptr(o.get("q_col")), _ptr(o.get("s_col")), o["s_col"].stride(0) if "s_col" in o else 0,
+                         _stream_ptr(stream))
     return o
 
 

@@ -219,6 +219,17 @@ te_mx_status te_mx_quantize(const void* x, int64_t rows, int64_t cols, int64_t l
     return quantize_launch(a, static_cast<cudaStream_t>(stream));
 }
 
+te_mx_status te_mx_block_quantize(const void* x, int64_t rows, int64_t cols, int64_t ld_x, int32_t block_2d,
+                                  uint8_t* q_row, uint8_t* s_row, int64_t ld_s_row,
+                                  uint8_t* q_col, uint8_t* s_col, int64_t ld_s_col, void* stream) {
+    t_last_error[0] = '\0';
+    if (block_2d != 0 && block_2d != 1) return set_error(TE_MX_ERR_INVALID_ARG, "block_2d=%d must be 0 or 1", int(block_2d));
+    te_mx_status st = validate_quantize(x, rows, cols, ld_x, q_row, s_row, ld_s_row, q_col, s_col, ld_s_col, false);
+    if (st != TE_MX_OK || rows == 0 || cols == 0 || (!q_row && !q_col)) return st;
+    QuantizeArgs a{x, rows, cols, ld_x, q_row, s_row, ld_s_row, q_col, s_col, ld_s_col, nullptr, nullptr};
+    return block_quantize_launch(a, block_2d == 1, static_cast<cudaStream_t>(stream));
+}
+
 size_t te_mx_quantize_dbias_workspace_size(int64_t rows, int64_t cols) {
     if (rows <= 0 || cols <= 0) return 0;
     return size_t((rows + kDbiasBandRows - 1) / kDbiasBandRows) * size_t(cols) * sizeof(float);

@@ -41,6 +41,8 @@ struct GemmArgs {
 };
 
 te_mx_status quantize_launch(const QuantizeArgs& a, cudaStream_t stream);
+// Float8BlockScaling quantisation (E8M0-cast scales); `partial`/`dbias` unused.
+te_mx_status block_quantize_launch(const QuantizeArgs& a, bool block_2d, cudaStream_t stream);
 te_mx_status gemm_launch(const GemmArgs& a, cudaStream_t stream);
 
 // Helpers implemented in api.cu.

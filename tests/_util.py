@@ -36,9 +36,10 @@ def check_guard(buf, n_used):
     assert np.all(tail == CANARY), "write past the end of an output buffer"
 
 
-def gpu_quantize(x: torch.Tensor, rowwise=True, colwise=True):
-    """Run te_mx_quantize with canary-guarded outputs; returns numpy arrays and
-    asserts no byte outside the documented output region changed."""
+def gpu_quantize(x: torch.Tensor, rowwise=True, colwise=True, block_2d=None):
+    """Run te_mx_quantize (or, with ``block_2d`` given, te_mx_block_quantize)
+    with canary-guarded outputs; returns numpy arrays and asserts no byte
+    outside the documented output region changed."""
     rows, cols = x.shape
     out, bufs = {}, {}
     pr, pc = binding.te_mx_scale_pitch(cols), binding.te_mx_scale_pitch(rows)
@@ -48,7 +49,10 @@ def gpu_quantize(x: torch.Tensor, rowwise=True, colwise=True):
     if colwise:
         out["q_col"], bufs["q_col"] = guarded_u8(cols, rows)
         out["s_col"], bufs["s_col"] = guarded_u8(cols, pc)
-    binding.quantize(x, rowwise=rowwise, colwise=colwise, out=out)
+    if block_2d is None:
+        binding.quantize(x, rowwise=rowwise, colwise=colwise, out=out)
+    else:
+        binding.block_quantize(x, block_2d=block_2d, rowwise=rowwise, colwise=colwise, out=out)
     binding.te_mx_device_status()
     res = {}
     if rowwise:

@@ -67,6 +67,11 @@ def test_host_validation_rejects_bad_arguments_before_any_launch(lib):
         binding.te_mx_gemm(16, 16, 16, 16, 16, 16, 128, 128, 128, 0, 2, 16, 0, 0, 0, 0)  # aux missing
     with pytest.raises(binding.TemxError, match="INVALID_ARG"):
         binding.te_mx_grouped_gemm(0, 16, 128, 16, 16, 16, 16, 16, 16, 128, 128, 0, 0, 16, 0, 0, 0, 0)
+    with pytest.raises(binding.TemxError, match="INVALID_ARG"):
+        binding.te_mx_block_quantize(16, 128, 128, 128, 2, 16, 16, 16, 0, 0, 0, 0)   # block_2d not 0/1
+    with pytest.raises(binding.TemxError, match="UNSUPPORTED_SHAPE"):
+        binding.te_mx_block_quantize(16, 128, 48, 48, 0, 16, 16, 16, 0, 0, 0, 0)     # cols % 32
     # zero-sized problems are no-ops
+    binding.te_mx_block_quantize(0, 0, 128, 128, 1, 0, 0, 0, 0, 0, 0, 0)
     binding.te_mx_quantize(0, 0, 64, 64, 0, 0, 0, 0, 0, 0, 0)
     binding.te_mx_gemm(16, 16, 16, 16, 16, 16, 0, 128, 128, 0, 0, 16, 0, 0, 0, 0)
