@@ -47,7 +47,8 @@ def load_peaks():
         return {"hbm_gbs": 6800.0, "bf16": 1900.0, "bf16_sustained": 1700.0, "source": "fallback"}
 
 
-KERNEL_SOURCES = {"gemm": ["gemm.cu", "ptx.cuh"], "quant": ["quantize.cu", "ptx.cuh"]}
+KERNEL_SOURCES = {"gemm": ["gemm.cu", "ptx.cuh"], "quant": ["quantize.cu", "e4m3.cuh", "ptx.cuh"],
+                  "block": ["block_quantize.cu", "e4m3.cuh", "ptx.cuh"]}
 
 
 def source_sha256(kernel_name: str) -> str:
@@ -192,7 +193,13 @@ class Step:
                      "dbias": e(F, dt=torch.bfloat16)}
         o["ws"] = e(max(1, temx.binding.te_mx_quantize_dbias_workspace_size(T, F)))
         self.next_flops = {"gemm_dgrad": 2.0 * T * H * F, "gemm_dgelu": 2.0 * T * F * H}
-        self.next_bytes = {"quant_dbias_ffn_dy": qb(T, F, True) + 2.0 * F}
+        self.next_bytes = {"quant_dbias_ffn_dy": qb(T, F, True) + 2.0 * F,
+                           "block_quant_ffn_x": qb(T, H, True), "block_quant_ffn_w": qb(F, H, True),
+                           "block_quant_ffn_dy": qb(T, F, True)}
+        # Float8BlockScaling (E8M0-cast scales) quantisation of the same tensors:
+        # 1x128 / 128x1 blocks for X and dY, 128x128 blocks for W (both copies).
+        o["w_both"] = {"q_row": o["w_row"]["q_row"], "s_row": o["w_row"]["s_row"],
+                       "q_col": o["w_col"]["q_col"], "s_col": o["w_col"]["s_col"]}
         self.next_kernels = [
             ("gemm_dgrad", lambda: temx.gemm(o["dy"]["q_row"], o["dy"]["s_row"], o["w_col"]["q_col"],
                                              o["w_col"]["s_col"], out=o["dx"])),
@@ -200,6 +207,9 @@ class Step:
                                              o["w_row"]["s_row"], out=o["dgelu"], dgelu_aux=o["fprop"][1])),
             ("quant_dbias_ffn_dy", lambda: temx.quantize(d["ffn_dY"], True, True, out=o["dy_b"], dbias=True,
                                                          workspace=o["ws"])),
+            ("block_quant_ffn_x", lambda: temx.block_quantize(d["ffn_X"], False, True, True, out=o["x_row"])),
+            ("block_quant_ffn_w", lambda: temx.block_quantize(d["ffn_W"], True, True, True, out=o["w_both"])),
+            ("block_quant_ffn_dy", lambda: temx.block_quantize(d["ffn_dY"], False, True, True, out=o["dy_b"])),
         ]
         temx.quantize(d["ffn_W"], False, True, out=o["w_col"])
 
@@ -260,6 +270,7 @@ def time_next(step, reps, fp8_peak, hbm_gbs):
         else:
             ach = step.next_bytes[name] / (ms * 1e-3) / 1e9
             res[name] = {"us": ms * 1e3, "achieved": ach, "unit": "GB/s", "frac": ach / hbm_gbs}
+        res[name]["traffic"] = measured_traffic(name)
     step.temx.te_mx_device_status()
     return res
 
@@ -371,6 +382,8 @@ def whole_job_tflops(flops_per_rank: float, world: int, ms_step_max: float) -> f
 CASES = {
     "quant_both": "ffn X [8192x7168] row- and column-wise",
     "quant_row": "ffn W [18432x7168] row-wise",
+    "block_quant_x": "Float8BlockScaling ffn X [8192x7168], 1x128 and 128x1 blocks, both orientations",
+    "block_quant_w": "Float8BlockScaling ffn W [18432x7168], 128x128 blocks, both orientations",
     "gemm_fc1": "fc1 fprop 4096x4096x1024, bias + GELU + AUX",
     "gemm_ffn": "ffn fprop 8192x18432x7168, bias + GELU + AUX",
     "gemm_wgrad": "ffn wgrad 18432x7168x8192 on column-wise operands",
@@ -383,7 +396,7 @@ def run_case(case: str, reps: int):
     import mxfp8_block_scaled_quantize_gb300 as temx
     from mxfp8_block_scaled_quantize_gb300 import workloads
     dev = torch.device("cuda", 0)
-    if case in ("quant_both", "quant_row", "gemm_ffn", "gemm_wgrad"):
+    if case in ("quant_both", "quant_row", "block_quant_x", "block_quant_w", "gemm_ffn", "gemm_wgrad"):
         w = workloads.make_ffn()
     elif case == "gemm_fc1":
         w = workloads.make_fc1()
@@ -395,6 +408,12 @@ def run_case(case: str, reps: int):
     elif case == "quant_row":
         x = w["W"].to(dev)
         fn = lambda: temx.quantize(x, True, False)
+    elif case == "block_quant_x":
+        x = w["X"].to(dev)
+        fn = lambda: temx.block_quantize(x, False, True, True)
+    elif case == "block_quant_w":
+        x = w["W"].to(dev)
+        fn = lambda: temx.block_quantize(x, True, True, True)
     elif case in ("gemm_fc1", "gemm_ffn"):
         qx = temx.quantize(w["X"].to(dev), True, False)
         qw = temx.quantize(w["W"].to(dev), True, False)
@@ -487,6 +506,7 @@ def main():
             ach = step.bytes[name] / (ms * 1e-3) / 1e9
             kern[name] = {"us": ms * 1e3, "achieved": ach, "unit": "GB/s", "frac": ach / peaks["hbm_gbs"],
                           "bytes": step.bytes[name]}
+        kern[name]["traffic"] = measured_traffic(name)
     dom = max(per_kernel, key=per_kernel.get)
     dk = kern[dom]
     traffic = measured_traffic(dom)
