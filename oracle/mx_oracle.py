@@ -37,6 +37,8 @@ Sources of the definitions
   weights, each with an FP32 scale amax / 448 that is cast to E8M0 (the
   default there).  Reading of the cast: the smallest power of two >= amax/448,
   i.e. 2^ceil(log2(amax / 448)), so that no element exceeds 448 after scaling.
+* LayerNorm -> MXFP8 (LayerNormLinear / LayerNormMLP input): see the section
+  of that name below.
 * Bias gradient: the column sums of the output gradient (the cast_transpose_bgrad
   kernels of ROCm/TransformerEngine README, "Experimental Triton Kernels on ROCm").
 
@@ -210,7 +212,12 @@ def quantize_mx(x_bits, axis: int):
       axis=0: q uint8 [C, R],  s uint8 [C, R/32]   (the transposed copy)
     where s is the E8M0 byte (exponent + 127) and q the E4M3 byte.
     """
-    x = bf16_bits_to_f64(np.asarray(x_bits, dtype=np.uint16))
+    return quantize_mx_values(bf16_bits_to_f64(np.asarray(x_bits, dtype=np.uint16)), axis)
+
+
+def quantize_mx_values(x, axis: int):
+    """``quantize_mx`` of real (float64) values instead of bf16 patterns."""
+    x = np.asarray(x, dtype=np.float64)
     if axis == 0:
         x = x.T                                   # put the blocked axis last
     rows, n = x.shape
@@ -222,8 +229,9 @@ def quantize_mx(x_bits, axis: int):
     bad = ~np.isfinite(amax)                      # block holds NaN or inf
     amax_f = np.where(bad, 1.0, amax)
     e = mx_scale_exponent(amax_f)
-    v = blocks * pow2(-e)[:, :, None]             # exact: scaling by a power of two
-    q = e4m3_encode(v)
+    with np.errstate(invalid="ignore", over="ignore"):
+        v = blocks * pow2(-e)[:, :, None]         # exact: scaling by a power of two
+        q = e4m3_encode(v)
     q = np.where(bad[:, :, None], np.uint8(0x7F), q)
     s = np.where(bad, 0xFF, e + E8M0_BIAS).astype(np.uint8)
     return q.reshape(rows, n).astype(np.uint8), s
@@ -418,3 +426,107 @@ SIGMA_TOL = 1e-5
 def gemm_error_bound(ref, sigma) -> np.ndarray:
     """Per-element bound |gpu - ref| <= 2^-7 |ref| + 1e-5 sum_k |a_k b_k|."""
     return REL_TOL * np.abs(ref) + SIGMA_TOL * np.asarray(sigma)
+
+
+# --------------------------------------------------------------------------
+# LayerNorm -> MXFP8 (the input quantisation of LayerNormLinear / LayerNormMLP)
+# --------------------------------------------------------------------------
+#
+# LayerNorm as named on the TE pages: te.LayerNorm is a drop-in replacement of
+# torch.nn.LayerNorm (leeroopedia "FP8 Training Quickstart", step on module
+# replacement), with parameters 'scale' (gamma) and 'bias' (beta) and epsilon
+# 1e-5 (TE "Getting Started" JAX page, layer configuration); LayerNormLinear /
+# LayerNormDenseGeneral / LayerNormMLP fuse it with the Linear that consumes
+# its output.  Over each row (the hidden axis):
+#   mu = mean(x),  var = mean((x - mu)^2)  (biased),  rsigma = 1/sqrt(var + eps)
+#   y  = (x - mu) * rsigma * gamma + beta.
+# Reading: the fused quantiser takes y itself (no bf16 rounding between the
+# norm and the quantiser) and MXFP8-quantises it with the rule above.
+
+LAYERNORM_EPS = 1e-5
+
+
+def layernorm(x_bits, gamma_bits, beta_bits, eps: float = LAYERNORM_EPS):
+    """fp64 LayerNorm of a bf16 matrix [R, H] over each row.
+    Returns (y [R, H], mu [R], rsigma [R])."""
+    x = bf16_bits_to_f64(np.asarray(x_bits, dtype=np.uint16))
+    g = bf16_bits_to_f64(np.asarray(gamma_bits, dtype=np.uint16))
+    b = bf16_bits_to_f64(np.asarray(beta_bits, dtype=np.uint16))
+    with np.errstate(invalid="ignore", over="ignore"):
+        mu = x.mean(axis=1)
+        var = ((x - mu[:, None]) ** 2).mean(axis=1)
+        rsigma = 1.0 / np.sqrt(var + eps)
+        y = (x - mu[:, None]) * rsigma[:, None] * g[None, :] + b[None, :]
+    return y, mu, rsigma
+
+
+FP32_U = 2.0 ** -24        # unit roundoff of fp32
+LN_SUM_DEPTH = 64          # longest chain of fp32 additions in any row sum of the GPU
+
+
+def layernorm_error_bound(x_bits, gamma_bits, eps: float = LAYERNORM_EPS, depth: int = LN_SUM_DEPTH):
+    """Per-element bound E on |y_fp32 - y| for a LayerNorm evaluated in fp32 as:
+    mu = fl(S / H), S = sum of x with at most ``depth`` additions on any path;
+    var = fl(S2 / H), S2 = sum of fl(fl(x - mu)^2), same depth; rsigma =
+    fl(1 / fl(sqrt(fl(var + eps)))); y = fl(fl(fl(x - mu) * rsigma) * gamma +
+    beta) with one rounding (fused multiply-add).  Standard forward error
+    analysis (each fl() a relative error of at most u = 2^-24, a sum of depth d
+    at most d u sum|terms|), first-order terms times 1.05 for the rest."""
+    x = bf16_bits_to_f64(np.asarray(x_bits, dtype=np.uint16))
+    g = np.abs(bf16_bits_to_f64(np.asarray(gamma_bits, dtype=np.uint16)))
+    u = FP32_U
+    with np.errstate(invalid="ignore", over="ignore"):
+        mean_abs = np.abs(x).mean(axis=1)
+        mu = x.mean(axis=1)
+        var = ((x - mu[:, None]) ** 2).mean(axis=1)
+        r = 1.0 / np.sqrt(var + eps)
+        dmu = (depth + 1) * u * mean_abs                                  # |mu_fp32 - mu|
+        rho = 0.5 * ((depth + 5) * u + dmu ** 2 / (var + eps)) + 2 * u    # relative error of rsigma
+        y_abs = np.abs((x - mu[:, None]) * r[:, None]) * g[None, :]
+        e = (g[None, :] * r[:, None] * (dmu[:, None] * (1 + rho[:, None] + 2 * u)
+                                        + np.abs(x - mu[:, None]) * (rho[:, None] + 2 * u)))
+        return 1.05 * (e + u * (y_abs + np.abs(e)))
+
+
+def mx_admissible(y, err, q, s, axis: int):
+    """Is (q, s) the MX quantisation (``quantize_mx_values``) of some y' with
+    |y' - y| <= err element-wise?  The test for a quantiser whose input is
+    computed in a lower precision than the oracle's.
+
+    ``y``, ``err``: float64 [R, C]; (q, s) laid out as ``quantize_mx_values``
+    returns them for ``axis``.  Returns (ok, ambiguous), boolean arrays shaped
+    like q: ``ok`` that the code and its block's scale are admissible,
+    ``ambiguous`` that more than one (scale, code) is admissible there (outside
+    these, ``ok`` means the answer equals the unique one).
+    """
+    y = np.asarray(y, dtype=np.float64)
+    err = np.broadcast_to(np.asarray(err, dtype=np.float64), y.shape)
+    if axis == 0:
+        y, err = y.T, err.T
+    rows, n = y.shape
+    nb = n // MX_BLOCK
+    yb = y.reshape(rows, nb, MX_BLOCK)
+    eb = err.reshape(rows, nb, MX_BLOCK)
+    q = np.asarray(q, dtype=np.uint8).reshape(rows, nb, MX_BLOCK)
+    s = np.asarray(s, dtype=np.uint8)[:, :nb].astype(np.int64)
+    with np.errstate(invalid="ignore", over="ignore"):
+        bad = ~np.isfinite(np.max(np.abs(yb) + eb, axis=2))
+        a_lo = np.max(np.maximum(np.abs(yb) - eb, 0.0), axis=2)
+        a_hi = np.max(np.abs(yb) + eb, axis=2)
+        e_lo = mx_scale_exponent(np.where(bad, 1.0, a_lo))
+        e_hi = mx_scale_exponent(np.where(bad, 1.0, a_hi))
+        e = s - E8M0_BIAS
+        scale_ok = np.where(bad, s == 0xFF, (e >= e_lo) & (e <= e_hi))
+        e_use = np.where(bad | ~scale_ok, 0, e)[:, :, None]
+        v_lo = (yb - eb) * pow2(-e_use)
+        v_hi = (yb + eb) * pow2(-e_use)
+        c_lo = e4m3_decode(e4m3_encode(np.where(bad[:, :, None], 0.0, v_lo)))
+        c_hi = e4m3_decode(e4m3_encode(np.where(bad[:, :, None], 0.0, v_hi)))
+        got = e4m3_decode(q)
+        sign_ok = np.where(v_lo > 0, (q & 0x80) == 0, np.where(v_hi < 0, (q & 0x80) != 0, True))
+        code_ok = (got >= c_lo) & (got <= c_hi) & sign_ok
+    code_ok = np.where(bad[:, :, None], q == 0x7F, code_ok)
+    ok = code_ok & np.broadcast_to(scale_ok[:, :, None], code_ok.shape)
+    amb = (c_lo != c_hi) | np.broadcast_to((e_lo != e_hi)[:, :, None], code_ok.shape)
+    amb = amb & ~bad[:, :, None]
+    return ok.reshape(rows, n), amb.reshape(rows, n)
