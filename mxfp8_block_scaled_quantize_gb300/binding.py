@@ -27,6 +27,8 @@ SIGNATURES = {
     "te_mx_scale_pitch": (_SZ, [_I64]),
     "te_mx_quantize": (ctypes.c_int, [_P, _I64, _I64, _I64, _P, _P, _I64, _P, _P, _I64, _P]),
     "te_mx_block_quantize": (ctypes.c_int, [_P, _I64, _I64, _I64, _I32, _P, _P, _I64, _P, _P, _I64, _P]),
+    "te_mx_layernorm_quantize": (ctypes.c_int, [_P, _I64, _I64, _I64, _P, _P, ctypes.c_float, _P, _P, _I64, _P,
+                                                _P, _I64, _P, _P, _P]),
     "te_mx_quantize_dbias_workspace_size": (_SZ, [_I64, _I64]),
     "te_mx_quantize_dbias": (ctypes.c_int, [_P, _I64, _I64, _I64, _P, _P, _I64, _P, _P, _I64, _P, _P, _SZ, _P]),
     "te_mx_quantize_dbias_noalloc": (ctypes.c_int, [_P, _I64, _I64, _I64, _P, _P, _I64, _P, _P, _I64, _P, _P]),
@@ -84,6 +86,12 @@ def te_mx_block_quantize(x, rows, cols, ld_x, block_2d, q_row, s_row, ld_s_row, 
                          stream) -> None:
     _check(lib().te_mx_block_quantize(x, rows, cols, ld_x, block_2d, q_row, s_row, ld_s_row, q_col, s_col,
                                       ld_s_col, stream))
+
+
+def te_mx_layernorm_quantize(x, rows, hidden, ld_x, gamma, beta, eps, q_row, s_row, ld_s_row, q_col, s_col,
+                             ld_s_col, mu, rsigma, stream) -> None:
+    _check(lib().te_mx_layernorm_quantize(x, rows, hidden, ld_x, gamma, beta, eps, q_row, s_row, ld_s_row, q_col,
+                                          s_col, ld_s_col, mu, rsigma, stream))
 
 
 def te_mx_quantize_dbias_workspace_size(rows, cols) -> int:
@@ -196,6 +204,32 @@ def block_quantize(x, block_2d: bool = False, rowwise: bool = True, colwise: boo
                          _ptr(o.get("q_row")), _ptr(o.get("s_row")), o["s_row"].stride(0) if "s_row" in o else 0,
                          _ptr(o.get("q_col")), _ptr(o.get("s_col")), o["s_col"].stride(0) if "s_col" in o else 0,
                          _stream_ptr(stream))
+    return o
+
+
+def layernorm_quantize(x, gamma, beta, eps: float = 1e-5, rowwise: bool = True, colwise: bool = False,
+                       stats: bool = True, stream=None, out=None):
+    """LayerNorm over the last axis of a 2-D bf16 CUDA tensor fused with its
+    MXFP8 quantisation.  Returns a dict with q_row/s_row and/or q_col/s_col
+    (as ``quantize``) and, with ``stats``, "mu" and "rsigma" (fp32 [rows])."""
+    import torch
+    assert x.dtype == torch.bfloat16 and x.dim() == 2 and x.is_cuda and x.stride(1) == 1
+    assert gamma.dtype == torch.bfloat16 and beta.dtype == torch.bfloat16
+    rows, hidden = x.shape
+    o = dict(out or {})
+    if rowwise and "q_row" not in o:
+        o["q_row"] = torch.empty(rows, hidden, dtype=torch.uint8, device=x.device)
+        o["s_row"] = torch.empty(rows, te_mx_scale_pitch(hidden), dtype=torch.uint8, device=x.device)
+    if colwise and "q_col" not in o:
+        o["q_col"] = torch.empty(hidden, rows, dtype=torch.uint8, device=x.device)
+        o["s_col"] = torch.empty(hidden, te_mx_scale_pitch(rows), dtype=torch.uint8, device=x.device)
+    if stats and "mu" not in o:
+        o["mu"] = torch.empty(rows, dtype=torch.float32, device=x.device)
+        o["rsigma"] = torch.empty(rows, dtype=torch.float32, device=x.device)
+    te_mx_layernorm_quantize(x.data_ptr(), rows, hidden, x.stride(0), gamma.data_ptr(), beta.data_ptr(), float(eps),
+                             _ptr(o.get("q_row")), _ptr(o.get("s_row")), o["s_row"].stride(0) if "s_row" in o else 0,
+                             _ptr(o.get("q_col")), _ptr(o.get("s_col")), o["s_col"].stride(0) if "s_col" in o else 0,
+                             _ptr(o.get("mu")), _ptr(o.get("rsigma")), _stream_ptr(stream))
     return o
 
 

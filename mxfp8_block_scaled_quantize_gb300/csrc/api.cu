@@ -3,6 +3,7 @@
 #include <cuda.h>
 #include <cuda_runtime.h>
 
+#include <cmath>
 #include <cstdarg>
 #include <cstdio>
 #include <mutex>
@@ -228,6 +229,32 @@ te_mx_status te_mx_block_quantize(const void* x, int64_t rows, int64_t cols, int
     if (st != TE_MX_OK || rows == 0 || cols == 0 || (!q_row && !q_col)) return st;
     QuantizeArgs a{x, rows, cols, ld_x, q_row, s_row, ld_s_row, q_col, s_col, ld_s_col, nullptr, nullptr};
     return block_quantize_launch(a, block_2d == 1, static_cast<cudaStream_t>(stream));
+}
+
+te_mx_status te_mx_layernorm_quantize(const void* x, int64_t rows, int64_t hidden, int64_t ld_x,
+                                      const void* gamma, const void* beta, float eps,
+                                      uint8_t* q_row, uint8_t* s_row, int64_t ld_s_row,
+                                      uint8_t* q_col, uint8_t* s_col, int64_t ld_s_col,
+                                      float* mu, float* rsigma, void* stream) {
+    t_last_error[0] = '\0';
+    const bool work = rows > 0 && hidden > 0 && (q_row || q_col || mu || rsigma);
+    if (work) {
+        if (!gamma || !beta) return set_error(TE_MX_ERR_INVALID_ARG, "gamma and beta are required");
+        if (!(eps > 0.0f) || !std::isfinite(eps))
+            return set_error(TE_MX_ERR_INVALID_ARG, "eps must be positive and finite");
+        if (hidden > ln_quantize_max_hidden())
+            return set_error(TE_MX_ERR_UNSUPPORTED_SHAPE, "hidden=%lld exceeds %lld", (long long)hidden,
+                             (long long)ln_quantize_max_hidden());
+        if (!aligned(gamma, 2) || !aligned(beta, 2))
+            return set_error(TE_MX_ERR_MISALIGNED, "gamma/beta not 2-byte aligned");
+        if (!aligned(mu, 4) || !aligned(rsigma, 4)) return set_error(TE_MX_ERR_MISALIGNED, "mu/rsigma not 4-byte aligned");
+    }
+    te_mx_status st = validate_quantize(x, rows, hidden, ld_x, q_row, s_row, ld_s_row, q_col, s_col, ld_s_col,
+                                        mu != nullptr || rsigma != nullptr);
+    if (st != TE_MX_OK || !work) return st;
+    LnQuantizeArgs a{x, rows, hidden, ld_x, gamma, beta, eps, q_row, s_row, ld_s_row, q_col, s_col, ld_s_col,
+                     mu, rsigma};
+    return ln_quantize_launch(a, static_cast<cudaStream_t>(stream));
 }
 
 size_t te_mx_quantize_dbias_workspace_size(int64_t rows, int64_t cols) {

@@ -41,6 +41,20 @@ struct GemmArgs {
 };
 
 te_mx_status quantize_launch(const QuantizeArgs& a, cudaStream_t stream);
+
+struct LnQuantizeArgs {
+    const void* x;           // bf16 [rows x hidden], pitch ld_x
+    int64_t rows, hidden, ld_x;
+    const void* gamma;       // bf16 [hidden]
+    const void* beta;        // bf16 [hidden]
+    float eps;
+    uint8_t* q_row; uint8_t* s_row; int64_t ld_s_row;
+    uint8_t* q_col; uint8_t* s_col; int64_t ld_s_col;
+    float* mu;               // fp32 [rows] or null
+    float* rsigma;           // fp32 [rows] or null
+};
+te_mx_status ln_quantize_launch(const LnQuantizeArgs& a, cudaStream_t stream);
+int64_t ln_quantize_max_hidden();
 // Float8BlockScaling quantisation (E8M0-cast scales); `partial`/`dbias` unused.
 te_mx_status block_quantize_launch(const QuantizeArgs& a, bool block_2d, cudaStream_t stream);
 te_mx_status gemm_launch(const GemmArgs& a, cudaStream_t stream);

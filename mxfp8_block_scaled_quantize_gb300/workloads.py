@@ -35,14 +35,14 @@ import torch
 _CHUNK_ELEMS = 1 << 24
 
 
-def normal_bf16(shape, std: float, seed: int) -> torch.Tensor:
-    """N(0, std^2) drawn in fp32 from ``seed`` (in 16M-element chunks), rounded to bf16."""
+def normal_bf16(shape, std: float, seed: int, mean: float = 0.0) -> torch.Tensor:
+    """N(mean, std^2) drawn in fp32 from ``seed`` (in 16M-element chunks), rounded to bf16."""
     g = torch.Generator().manual_seed(seed)
     numel = math.prod(shape)
     out = torch.empty(numel, dtype=torch.bfloat16)
     for start in range(0, numel, _CHUNK_ELEMS):
         n = min(_CHUNK_ELEMS, numel - start)
-        out[start:start + n] = (torch.randn(n, generator=g) * std).to(torch.bfloat16)
+        out[start:start + n] = (torch.randn(n, generator=g) * std + mean).to(torch.bfloat16)
     return out.view(*shape)
 
 
@@ -97,6 +97,12 @@ WORKLOADS = {
     "ffn": dict(M=8192, N=18432, K=7168, tokens=8192),
     "moe": dict(tokens=16384, experts=128, top_k=8, N=1536, K=4096),
 }
+
+
+def layernorm_params(hidden: int, seed: int):
+    """LayerNorm scale (gamma) and bias (beta), bf16 [hidden]: N(1, 0.1^2) and
+    N(0, 0.1^2) (trained-looking values instead of the 1 / 0 initialisation)."""
+    return normal_bf16((hidden,), 0.1, seed, mean=1.0), normal_bf16((hidden,), 0.1, seed + 1)
 
 
 def make_tiny():

@@ -464,6 +464,21 @@ FP32_U = 2.0 ** -24        # unit roundoff of fp32
 LN_SUM_DEPTH = 64          # longest chain of fp32 additions in any row sum of the GPU
 
 
+def layernorm_stat_bounds(x_bits, eps: float = LAYERNORM_EPS, depth: int = LN_SUM_DEPTH):
+    """Bounds on the fp32 statistics of a row (the evaluation described under
+    ``layernorm_error_bound``): |mu_fp32 - mu| <= dmu and
+    |rsigma_fp32 - rsigma| <= rho * rsigma.  Returns (dmu [R], rho [R])."""
+    x = bf16_bits_to_f64(np.asarray(x_bits, dtype=np.uint16))
+    u = FP32_U
+    with np.errstate(invalid="ignore", over="ignore"):
+        mean_abs = np.abs(x).mean(axis=1)
+        mu = x.mean(axis=1)
+        var = ((x - mu[:, None]) ** 2).mean(axis=1)
+        dmu = (depth + 1) * u * mean_abs                                  # sum error + the division
+        rho = 0.5 * ((depth + 5) * u + dmu ** 2 / (var + eps)) + 2 * u    # var, +eps, sqrt, reciprocal
+    return dmu, rho
+
+
 def layernorm_error_bound(x_bits, gamma_bits, eps: float = LAYERNORM_EPS, depth: int = LN_SUM_DEPTH):
     """Per-element bound E on |y_fp32 - y| for a LayerNorm evaluated in fp32 as:
     mu = fl(S / H), S = sum of x with at most ``depth`` additions on any path;
@@ -475,13 +490,11 @@ def layernorm_error_bound(x_bits, gamma_bits, eps: float = LAYERNORM_EPS, depth:
     x = bf16_bits_to_f64(np.asarray(x_bits, dtype=np.uint16))
     g = np.abs(bf16_bits_to_f64(np.asarray(gamma_bits, dtype=np.uint16)))
     u = FP32_U
+    dmu, rho = layernorm_stat_bounds(x_bits, eps, depth)
     with np.errstate(invalid="ignore", over="ignore"):
-        mean_abs = np.abs(x).mean(axis=1)
         mu = x.mean(axis=1)
         var = ((x - mu[:, None]) ** 2).mean(axis=1)
         r = 1.0 / np.sqrt(var + eps)
-        dmu = (depth + 1) * u * mean_abs                                  # |mu_fp32 - mu|
-        rho = 0.5 * ((depth + 5) * u + dmu ** 2 / (var + eps)) + 2 * u    # relative error of rsigma
         y_abs = np.abs((x - mu[:, None]) * r[:, None]) * g[None, :]
         e = (g[None, :] * r[:, None] * (dmu[:, None] * (1 + rho[:, None] + 2 * u)
                                         + np.abs(x - mu[:, None]) * (rho[:, None] + 2 * u)))
