@@ -48,7 +48,8 @@ def load_peaks():
 
 
 KERNEL_SOURCES = {"gemm": ["gemm.cu", "ptx.cuh"], "quant": ["quantize.cu", "e4m3.cuh", "ptx.cuh"],
-                  "block": ["block_quantize.cu", "e4m3.cuh", "ptx.cuh"]}
+                  "block": ["block_quantize.cu", "e4m3.cuh", "ptx.cuh"],
+                  "ln": ["layernorm_quantize.cu", "e4m3.cuh", "ptx.cuh"]}
 
 
 def source_sha256(kernel_name: str) -> str:
@@ -146,6 +147,8 @@ class Step:
         self.temx = temx
         self.d = {k: v.to(dev) for k, v in host.items()}
         d = self.d
+        from mxfp8_block_scaled_quantize_gb300 import workloads
+        d["ln_g"], d["ln_b"] = (t.to(dev) for t in workloads.layernorm_params(host["ffn_X"].shape[1], 410))
         e = lambda *s, dt=torch.uint8: torch.empty(*s, dtype=dt, device=dev)
         pitch = temx.te_mx_scale_pitch
         T, H, F = 8192, 7168, 18432
@@ -195,9 +198,14 @@ class Step:
         self.next_flops = {"gemm_dgrad": 2.0 * T * H * F, "gemm_dgelu": 2.0 * T * F * H}
         self.next_bytes = {"quant_dbias_ffn_dy": qb(T, F, True) + 2.0 * F,
                            "block_quant_ffn_x": qb(T, H, True), "block_quant_ffn_w": qb(F, H, True),
-                           "block_quant_ffn_dy": qb(T, F, True)}
+                           "block_quant_ffn_dy": qb(T, F, True),
+                           "ln_quant_ffn_x": qb(T, H, True) + 8.0 * T + 4.0 * H}
         # Float8BlockScaling (E8M0-cast scales) quantisation of the same tensors:
         # 1x128 / 128x1 blocks for X and dY, 128x128 blocks for W (both copies).
+        # LayerNorm -> MXFP8 of the ffn input (both orientations + mu / rsigma);
+        # X stands in for the residual stream that the LayerNorm normalises.
+        o["ln"] = {"q_row": o["x_row"]["q_row"], "s_row": o["x_row"]["s_row"], "q_col": o["x_row"]["q_col"],
+                   "s_col": o["x_row"]["s_col"], "mu": e(T, dt=torch.float32), "rsigma": e(T, dt=torch.float32)}
         o["w_both"] = {"q_row": o["w_row"]["q_row"], "s_row": o["w_row"]["s_row"],
                        "q_col": o["w_col"]["q_col"], "s_col": o["w_col"]["s_col"]}
         self.next_kernels = [
@@ -210,6 +218,8 @@ class Step:
             ("block_quant_ffn_x", lambda: temx.block_quantize(d["ffn_X"], False, True, True, out=o["x_row"])),
             ("block_quant_ffn_w", lambda: temx.block_quantize(d["ffn_W"], True, True, True, out=o["w_both"])),
             ("block_quant_ffn_dy", lambda: temx.block_quantize(d["ffn_dY"], False, True, True, out=o["dy_b"])),
+            ("ln_quant_ffn_x", lambda: temx.layernorm_quantize(d["ffn_X"], d["ln_g"], d["ln_b"], 1e-5, True, True,
+                                                               out=o["ln"])),
         ]
         temx.quantize(d["ffn_W"], False, True, out=o["w_col"])
 
@@ -384,6 +394,7 @@ CASES = {
     "quant_row": "ffn W [18432x7168] row-wise",
     "block_quant_x": "Float8BlockScaling ffn X [8192x7168], 1x128 and 128x1 blocks, both orientations",
     "block_quant_w": "Float8BlockScaling ffn W [18432x7168], 128x128 blocks, both orientations",
+    "ln_quant_x": "LayerNorm -> MXFP8 of ffn X [8192x7168], both orientations + mu/rsigma",
     "gemm_fc1": "fc1 fprop 4096x4096x1024, bias + GELU + AUX",
     "gemm_ffn": "ffn fprop 8192x18432x7168, bias + GELU + AUX",
     "gemm_wgrad": "ffn wgrad 18432x7168x8192 on column-wise operands",
@@ -396,7 +407,7 @@ def run_case(case: str, reps: int):
     import mxfp8_block_scaled_quantize_gb300 as temx
     from mxfp8_block_scaled_quantize_gb300 import workloads
     dev = torch.device("cuda", 0)
-    if case in ("quant_both", "quant_row", "block_quant_x", "block_quant_w", "gemm_ffn", "gemm_wgrad"):
+    if case in ("quant_both", "quant_row", "block_quant_x", "block_quant_w", "ln_quant_x", "gemm_ffn", "gemm_wgrad"):
         w = workloads.make_ffn()
     elif case == "gemm_fc1":
         w = workloads.make_fc1()
@@ -414,6 +425,10 @@ def run_case(case: str, reps: int):
     elif case == "block_quant_w":
         x = w["W"].to(dev)
         fn = lambda: temx.block_quantize(x, True, True, True)
+    elif case == "ln_quant_x":
+        x = w["X"].to(dev)
+        g, b = (t.to(dev) for t in workloads.layernorm_params(x.shape[1], 410))
+        fn = lambda: temx.layernorm_quantize(x, g, b, 1e-5, True, True)
     elif case in ("gemm_fc1", "gemm_ffn"):
         qx = temx.quantize(w["X"].to(dev), True, False)
         qw = temx.quantize(w["W"].to(dev), True, False)

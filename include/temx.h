@@ -180,18 +180,21 @@ TEMX_API te_mx_status te_mx_block_quantize(const void* x, int64_t rows, int64_t 
  *   rsigma[r] = 1/sqrt(var + eps),  y = (x - mu) rsigma gamma + beta,
  * and y, unrounded, is MXFP8-quantised exactly as te_mx_quantize quantises
  * its input (q_row/s_row: blocks of 32 along the row; q_col/s_col: blocks of
- * 32 rows of a column, stored transposed).  Arithmetic is fp32:
- * mu = fl(S/H) with S a sum of the row in fp32 whose longest chain of additions
- * is at most 64; var likewise from fl(fl(x - mu)^2); rsigma =
- * fl(1/fl(sqrt(fl(var + eps)))); y = fma(fl(fl(x - mu) rsigma), gamma, beta)
- * with one rounding.  Codes and scales are the exact MXFP8 quantisation of
- * that fp32 y, and the sums are taken in a fixed order (deterministic).
+ * 32 rows of a column, stored transposed).  The normalised tensor is never
+ * written.  Arithmetic is fp32: mu = fl(S/H) with S a sum of the row in fp32
+ * whose longest chain of additions is at most 64; var likewise from
+ * fl(fl(x - mu)^2); rsigma = fl(1/fl(sqrt(fl(var + eps)))); y =
+ * fma(fl(fl(x - mu) rsigma), gamma, beta) with one rounding.  Codes and scales
+ * are the exact MXFP8 quantisation of that fp32 y; the sums are taken in a
+ * fixed order (deterministic).  Two kernels run on `stream`: the statistics,
+ * then normalisation + quantisation (reading mu / rsigma back).
  *
  *   x       bf16 [rows x hidden], pitch ld_x (device, 16-byte aligned, ld_x % 8 == 0);
- *   gamma, beta  bf16 [hidden] (device);  eps > 0 and finite;
- *   q_row/s_row, q_col/s_col: as te_mx_quantize (either pair may be NULL);
- *   mu, rsigma   fp32 [rows] (device) or NULL: the statistics, for the backward pass.
- * Rules: hidden % 32 == 0 and hidden <= 24576; rows % 32 == 0 when q_col is
+ *   gamma, beta  bf16 [hidden] (device, 4-byte aligned);  eps > 0 and finite;
+ *   q_row/s_row, q_col/s_col: as te_mx_quantize (either pair may be NULL:
+ *           then only the statistics are computed);
+ *   mu, rsigma   fp32 [rows] (device, required): the statistics, for the backward pass.
+ * Rules: hidden % 32 == 0 and hidden <= 32768; rows % 32 == 0 when q_col is
  * given; rows == 0 or hidden == 0 is a no-op. */
 TEMX_API te_mx_status te_mx_layernorm_quantize(const void* x, int64_t rows, int64_t hidden, int64_t ld_x,
                                                const void* gamma, const void* beta, float eps,

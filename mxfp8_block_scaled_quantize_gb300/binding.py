@@ -208,10 +208,10 @@ def block_quantize(x, block_2d: bool = False, rowwise: bool = True, colwise: boo
 
 
 def layernorm_quantize(x, gamma, beta, eps: float = 1e-5, rowwise: bool = True, colwise: bool = False,
-                       stats: bool = True, stream=None, out=None):
+                       stream=None, out=None):
     """LayerNorm over the last axis of a 2-D bf16 CUDA tensor fused with its
     MXFP8 quantisation.  Returns a dict with q_row/s_row and/or q_col/s_col
-    (as ``quantize``) and, with ``stats``, "mu" and "rsigma" (fp32 [rows])."""
+    (as ``quantize``) and "mu" and "rsigma" (fp32 [rows])."""
     import torch
     assert x.dtype == torch.bfloat16 and x.dim() == 2 and x.is_cuda and x.stride(1) == 1
     assert gamma.dtype == torch.bfloat16 and beta.dtype == torch.bfloat16
@@ -223,7 +223,7 @@ def layernorm_quantize(x, gamma, beta, eps: float = 1e-5, rowwise: bool = True, 
     if colwise and "q_col" not in o:
         o["q_col"] = torch.empty(hidden, rows, dtype=torch.uint8, device=x.device)
         o["s_col"] = torch.empty(hidden, te_mx_scale_pitch(rows), dtype=torch.uint8, device=x.device)
-    if stats and "mu" not in o:
+    if "mu" not in o:
         o["mu"] = torch.empty(rows, dtype=torch.float32, device=x.device)
         o["rsigma"] = torch.empty(rows, dtype=torch.float32, device=x.device)
     te_mx_layernorm_quantize(x.data_ptr(), rows, hidden, x.stride(0), gamma.data_ptr(), beta.data_ptr(), float(eps),

@@ -164,6 +164,22 @@ te_mx_status encode_tensor_map_3d(CUtensorMap* map, CUtensorMapDataType dtype, c
     return TE_MX_OK;
 }
 
+cudaError_t set_smem_attribute_once(const void* kernel, int bytes) {
+    struct Entry { const void* fn; int dev; int bytes; };
+    static Entry done[128];
+    static int n_done = 0;
+    static std::mutex mu;
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    std::lock_guard<std::mutex> lock(mu);
+    for (int i = 0; i < n_done; ++i)
+        if (done[i].fn == kernel && done[i].dev == dev && done[i].bytes >= bytes) return cudaSuccess;
+    e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+    if (e == cudaSuccess && n_done < 128) done[n_done++] = Entry{kernel, dev, bytes};
+    return e;
+}
+
 te_mx_status validate_quantize(const void* x, int64_t rows, int64_t cols, int64_t ld_x,
                                      uint8_t* q_row, uint8_t* s_row, int64_t ld_s_row,
                                      uint8_t* q_col, uint8_t* s_col, int64_t ld_s_col, bool dbias) {
@@ -237,20 +253,20 @@ te_mx_status te_mx_layernorm_quantize(const void* x, int64_t rows, int64_t hidde
                                       uint8_t* q_col, uint8_t* s_col, int64_t ld_s_col,
                                       float* mu, float* rsigma, void* stream) {
     t_last_error[0] = '\0';
-    const bool work = rows > 0 && hidden > 0 && (q_row || q_col || mu || rsigma);
+    const bool work = rows > 0 && hidden > 0;
     if (work) {
         if (!gamma || !beta) return set_error(TE_MX_ERR_INVALID_ARG, "gamma and beta are required");
+        if (!mu || !rsigma) return set_error(TE_MX_ERR_INVALID_ARG, "mu and rsigma are required");
         if (!(eps > 0.0f) || !std::isfinite(eps))
             return set_error(TE_MX_ERR_INVALID_ARG, "eps must be positive and finite");
         if (hidden > ln_quantize_max_hidden())
             return set_error(TE_MX_ERR_UNSUPPORTED_SHAPE, "hidden=%lld exceeds %lld", (long long)hidden,
                              (long long)ln_quantize_max_hidden());
-        if (!aligned(gamma, 2) || !aligned(beta, 2))
-            return set_error(TE_MX_ERR_MISALIGNED, "gamma/beta not 2-byte aligned");
+        if (!aligned(gamma, 4) || !aligned(beta, 4))
+            return set_error(TE_MX_ERR_MISALIGNED, "gamma/beta not 4-byte aligned");
         if (!aligned(mu, 4) || !aligned(rsigma, 4)) return set_error(TE_MX_ERR_MISALIGNED, "mu/rsigma not 4-byte aligned");
     }
-    te_mx_status st = validate_quantize(x, rows, hidden, ld_x, q_row, s_row, ld_s_row, q_col, s_col, ld_s_col,
-                                        mu != nullptr || rsigma != nullptr);
+    te_mx_status st = validate_quantize(x, rows, hidden, ld_x, q_row, s_row, ld_s_row, q_col, s_col, ld_s_col, true);
     if (st != TE_MX_OK || !work) return st;
     LnQuantizeArgs a{x, rows, hidden, ld_x, gamma, beta, eps, q_row, s_row, ld_s_row, q_col, s_col, ld_s_col,
                      mu, rsigma};

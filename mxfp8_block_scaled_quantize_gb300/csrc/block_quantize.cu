@@ -280,7 +280,7 @@ template <bool R, bool C, bool D2>
 cudaError_t launch(const CUtensorMap& xm, const CUtensorMap& qr, const CUtensorMap& qc, const BlockParams& p,
                    int sms, cudaStream_t stream) {
     auto k = block_quantize_kernel<R, C, D2>;
-    cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
+    cudaError_t e = set_smem_attribute_once(reinterpret_cast<const void*>(k), kSmemBytes);
     if (e != cudaSuccess) return e;
     const int64_t cap = int64_t(kCtasPerSm) * sms;
     const int grid = int(p.tiles < cap ? p.tiles : cap);

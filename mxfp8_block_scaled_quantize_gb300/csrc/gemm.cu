@@ -744,7 +744,7 @@ te_mx_status launch_gemm(const GemmArgs& a, int sms, unsigned int* status, cudaS
     int64_t units = grouped ? slots : (p.total_tiles < slots ? p.total_tiles : slots);
     if (units < 1) units = 1;
     auto kern = gemm_kernel<kPair>;
-    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemDyn);
+    cudaError_t e = set_smem_attribute_once(reinterpret_cast<const void*>(kern), C::kSmemDyn);
     if (e != cudaSuccess) return cuda_status(e, "cudaFuncSetAttribute(gemm)");
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(unsigned(units * kPair));

@@ -1,7 +1,6 @@
 // LayerNorm fused with MXFP8 quantisation: the input of LayerNormLinear /
 // LayerNormMLP goes from bf16 x to E4M3 codes + E8M0 scales (row-wise and
-// column-wise) in one pass over HBM, without writing the normalised bf16
-// tensor.
+// column-wise) without writing the normalised bf16 tensor.
 //
 // Definition (te.LayerNorm as the drop-in of torch.nn.LayerNorm, leeroopedia
 // "FP8 Training Quickstart"; parameters 'scale' and 'bias' and epsilon 1e-5,
@@ -17,17 +16,15 @@
 //   rsigma = fl(1 / fl(sqrt(fl(var + eps)))),
 //   y      = fma(fl(fl(x - mu) * rsigma), gamma, beta).
 //
-// Work decomposition.  A cluster of k CTAs (k = 1, 2, 4 or 8) owns a band of
-// 32 rows; CTA rank q holds chunks [q cpc, (q+1) cpc) of 64 columns in shared
-// memory (TMA, 128-byte swizzle, one mbarrier per chunk), and warp w works on
-// its chunks w, w + 8, ...  Pass 1: lane l sums row l of each chunk (a
-// 6-level tree per chunk), warps and then CTAs are combined in a fixed order
-// (CTA partials are read over distributed shared memory), so every CTA of the
-// cluster derives the same mu.  Pass 2 does the same for the squared
-// deviations.  Pass 3 quantises each chunk both ways from the shared-memory
-// copy (row-wise: lane = row; column-wise: lane = 2 columns x 32 rows, so one
-// column block per lane), stages the codes in the chunk's own buffer and
-// writes them with TMA stores.
+// Two launches.  ln_stats_kernel: one warp per row reads the row twice (the
+// second time from L1/L2) and writes mu and rsigma.  ln_apply_kernel: every
+// warp runs its own TMA pipeline over units of 32 rows x 64 columns (like the
+// MXFP8 quantiser), normalises each unit with the row statistics and gamma /
+// beta, quantises it both ways (row-wise: lane = row; column-wise: lane = 2
+// columns x 32 rows, one column block per lane, the column pair a natural
+// f32x2 operand), stages the codes in the unit's own buffer and writes them
+// with TMA stores.  No CTA-wide barrier, no cluster.  For activations up to
+// the L2 size the apply kernel reads x mostly from L2.
 #include <cuda_runtime.h>
 
 #include "e4m3.cuh"
@@ -38,73 +35,96 @@ namespace temx {
 
 namespace {
 
-constexpr int kBand = 32;                        // rows per cluster (one column-wise block)
-constexpr int kChunkCols = 64;                   // columns per chunk (128 bytes of bf16)
-constexpr int kChunkBytes = kBand * kChunkCols * 2;
-constexpr int kWarps = 8;
-constexpr int kThreads = kWarps * 32;
-constexpr int kMaxChunks = 48;                   // per CTA: 192 KB of shared memory
-constexpr int kMaxCluster = 8;
+constexpr int kUnitRows = 32;                    // rows per unit (one column-wise block)
+constexpr int kUnitCols = 64;                    // columns per unit (128 bytes of bf16)
+constexpr int kUnitBytes = kUnitRows * kUnitCols * 2;
+constexpr int kApplyWarps = 16;
+constexpr int kApplyStages = 3;
+// Per warp: the unit ring and two side areas (this unit's and the next one's)
+// with the row statistics (mu, mu, rsigma, rsigma per row) and gamma / beta
+// of the unit's columns in fp32.
+constexpr int kSideBytes = kUnitRows * 16 + 2 * kUnitCols * 4;
+constexpr int kWarpBytes = kApplyStages * kUnitBytes + 2 * kSideBytes;
+constexpr int kApplySmem = kApplyWarps * kWarpBytes + 1024;
+constexpr int kStatsWarps = 8;                   // rows per statistics CTA
+constexpr int kStatsAcc = 4;                     // independent accumulators per lane
 
-struct LnParams {
+struct ApplyParams {
     int64_t rows, hidden;
-    float eps;
+    const float* mu;
+    const float* rsigma;
     const uint16_t* gamma;
     const uint16_t* beta;
     uint8_t* s_row;
     int64_t ld_s_row;
     uint8_t* s_col;
     int64_t ld_s_col;
-    float* mu;
-    float* rsigma;
-    int nch;               // chunks per row: ceil(hidden / 64)
-    int cpc;               // chunks per CTA
+    int64_t col_units;     // ceil(hidden / 64)
+    int64_t units;         // ceil(rows / 32) * col_units
     unsigned int* status;
 };
 
-__device__ __forceinline__ uint32_t cluster_nctarank() {
-    uint32_t r;
-    asm volatile("mov.u32 %0, %%cluster_nctarank;" : "=r"(r));
+// Packed fp32 pairs (Blackwell f32x2 arithmetic; each half rounds as the
+// scalar operation would).
+__device__ __forceinline__ uint64_t pack2(float lo, float hi) {
+    uint64_t r;
+    asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(lo), "f"(hi));
     return r;
 }
-__device__ __forceinline__ void cluster_arrive_release() {
-    asm volatile("barrier.cluster.arrive.release.aligned;" ::: "memory");
+__device__ __forceinline__ float lo2(uint64_t v) { return __uint_as_float(uint32_t(v)); }
+__device__ __forceinline__ float hi2(uint64_t v) { return __uint_as_float(uint32_t(v >> 32)); }
+__device__ __forceinline__ uint64_t add2(uint64_t a, uint64_t b) {
+    uint64_t d;
+    asm("add.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+    return d;
 }
-__device__ __forceinline__ void cluster_wait_acquire() {
-    asm volatile("barrier.cluster.wait.acquire.aligned;" ::: "memory");
+__device__ __forceinline__ uint64_t sub2(uint64_t a, uint64_t b) {
+    uint64_t d;
+    asm("sub.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+    return d;
 }
-__device__ __forceinline__ float ld_cluster_f32(uint32_t cluster_addr) {
-    float v;
-    asm volatile("ld.shared::cluster.f32 %0, [%1];" : "=f"(v) : "r"(cluster_addr) : "memory");
+__device__ __forceinline__ uint64_t mul2(uint64_t a, uint64_t b) {
+    uint64_t d;
+    asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+    return d;
+}
+__device__ __forceinline__ uint64_t fma2(uint64_t a, uint64_t b, uint64_t c) {
+    uint64_t d;
+    asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(d) : "l"(a), "l"(b), "l"(c));
+    return d;
+}
+// A bf16 pair (one 32-bit word) as an fp32 pair (exact).
+__device__ __forceinline__ uint64_t bf2(uint32_t w) { return pack2(bf16_lo(w), bf16_hi(w)); }
+// max(|a|, |b|) in magnitude (the sign bit is meaningless); NaN if either is NaN.
+__device__ __forceinline__ float maxabs(float a, float b) {
+    float d;
+    asm("max.NaN.xorsign.abs.f32 %0, %1, %2;" : "=f"(d) : "f"(a), "f"(b));
+    return d;
+}
+__device__ __forceinline__ uint64_t lds64(uint32_t addr) {
+    uint64_t v;
+    asm volatile("ld.shared.b64 %0, [%1];" : "=l"(v) : "r"(addr));
     return v;
 }
-
-// Pairwise sum of 64 floats (six levels of additions).
-__device__ __forceinline__ float tree64(float (&v)[64]) {
-#pragma unroll
-    for (int s = 32; s >= 1; s >>= 1)
-#pragma unroll
-        for (int i = 0; i < s; ++i) v[i] = __fadd_rn(v[i], v[i + s]);
-    return v[0];
+__device__ __forceinline__ void lds128x2(uint32_t addr, uint64_t& a, uint64_t& b) {
+    asm volatile("ld.shared.v2.b64 {%0, %1}, [%2];" : "=l"(a), "=l"(b) : "r"(addr));
 }
 
-// The 64 bf16 of row `r` of a chunk (128-byte swizzle) as 32 words.
-__device__ __forceinline__ void load_row(uint32_t chunk, int r, uint32_t (&w)[32]) {
+// Pairwise sum of n fp32 pairs (log2 n levels), then the two halves: a tree of
+// depth log2(n) + 1 over 2n values.
+template <int kN>
+__device__ __forceinline__ float tree2(uint64_t (&v)[kN]) {
 #pragma unroll
-    for (int j = 0; j < 8; ++j) {
-        const uint4 v = lds128(chunk + r * 128 + ((j ^ (r & 7)) << 4));
-        w[4 * j + 0] = v.x; w[4 * j + 1] = v.y; w[4 * j + 2] = v.z; w[4 * j + 3] = v.w;
-    }
-}
-
-__device__ __forceinline__ float ln_y(float x, float mu, float rs, float g, float b) {
-    return __fmaf_rn(__fmul_rn(__fsub_rn(x, mu), rs), g, b);
+    for (int s = kN / 2; s >= 1; s >>= 1)
+#pragma unroll
+        for (int i = 0; i < s; ++i) v[i] = add2(v[i], v[i + s]);
+    return __fadd_rn(lo2(v[0]), hi2(v[0]));
 }
 
 // E8M0 byte of an MX block from |amax| as fp32 bits (exponent field - 8,
 // floored at 0; 0xFF for NaN/inf).
-__device__ __forceinline__ uint32_t mx_scale_byte_f32(uint32_t amax_bits) {
-    const uint32_t ef = amax_bits >> 23;
+__device__ __forceinline__ uint32_t mx_scale_byte_f32(float amax) {
+    const uint32_t ef = (__float_as_uint(amax) & 0x7FFFFFFFu) >> 23;
     if (ef == 0xFFu) return 0xFFu;
     return ef > 8u ? ef - 8u : 0u;
 }
@@ -112,323 +132,388 @@ __device__ __forceinline__ uint32_t mx_scale_byte_f32(uint32_t amax_bits) {
 // Byte offset of 16-byte chunk c of 64-byte row r in a 64-byte-swizzled tile.
 __device__ __forceinline__ uint32_t sw64(int r, int c) { return uint32_t(r * 64 + ((c ^ ((r >> 1) & 3)) << 4)); }
 
+
+// ---------------------------------------------------------------- statistics
+
+// Sum of 8 bf16 (one 16-byte vector) as a tree of depth 3.
+__device__ __forceinline__ float sum8(const uint4& v) {
+    const uint64_t a = add2(bf2(v.x), bf2(v.y)), b = add2(bf2(v.z), bf2(v.w));
+    const uint64_t c = add2(a, b);
+    return __fadd_rn(lo2(c), hi2(c));
+}
+// Sum of the squared deviations of 8 bf16 from mu (tree of depth 3).
+__device__ __forceinline__ float sqdev8(const uint4& v, uint64_t mm) {
+    const uint64_t d0 = sub2(bf2(v.x), mm), d1 = sub2(bf2(v.y), mm), d2 = sub2(bf2(v.z), mm), d3 = sub2(bf2(v.w), mm);
+    const uint64_t a = add2(mul2(d0, d0), mul2(d1, d1)), b = add2(mul2(d2, d2), mul2(d3, d3));
+    const uint64_t c = add2(a, b);
+    return __fadd_rn(lo2(c), hi2(c));
+}
+// Warp sum in a fixed butterfly order (every lane gets the same value).
+__device__ __forceinline__ float warp_sum(float v) {
+#pragma unroll
+    for (int o = 16; o >= 1; o >>= 1) v = __fadd_rn(v, __shfl_xor_sync(0xFFFFFFFFu, v, o));
+    return v;
+}
+
+// One warp per row.  The row is copied into shared memory with one bulk
+// asynchronous copy, so both passes read it there and x is read from HBM once.
+// A lane reads vectors lane, lane + 32, ... of the row (8 elements each, a
+// tree of depth 3) into kStatsAcc accumulators in turn (four vectors per step),
+// the accumulators are added pairwise and the lanes by a butterfly: for rows
+// of at most 32768 elements the longest chain is 3 + 32 + 2 + 5 = 42
+// additions.
+__device__ __forceinline__ void bulk_load(uint32_t dst, const void* src, uint32_t bytes, uint32_t bar) {
+    asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];"
+                 :: "r"(dst), "l"(src), "r"(bytes), "r"(bar) : "memory");
+}
+
+template <bool kSquares>
+__device__ __forceinline__ float row_pass(uint32_t row, int nvec, int lane, uint64_t mm) {
+    float acc[kStatsAcc] = {0.0f, 0.0f, 0.0f, 0.0f};
+    for (int v = lane; v < nvec; v += 32 * kStatsAcc) {
+#pragma unroll
+        for (int a = 0; a < kStatsAcc; ++a)
+            if (v + 32 * a < nvec) {
+                const uint4 x = lds128(row + (v + 32 * a) * 16);
+                acc[a] = __fadd_rn(acc[a], kSquares ? sqdev8(x, mm) : sum8(x));
+            }
+    }
+    return warp_sum(__fadd_rn(__fadd_rn(acc[0], acc[1]), __fadd_rn(acc[2], acc[3])));
+}
+
+__global__ void __launch_bounds__(kStatsWarps * 32)
+ln_stats_kernel(const uint16_t* __restrict__ x, int64_t rows, int64_t hidden, int64_t ld_x, float eps,
+                float* __restrict__ mu_out, float* __restrict__ rs_out, int rows_per_cta, unsigned int* status) {
+    extern __shared__ __align__(16) uint8_t rowbuf[];
+    __shared__ __align__(8) uint64_t bars[kStatsWarps];
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int64_t r = int64_t(blockIdx.x) * rows_per_cta + warp;
+    if (warp >= rows_per_cta || r >= rows) return;
+    const uint32_t bytes = uint32_t(hidden) * 2;
+    const uint32_t row = smem_u32(rowbuf) + warp * bytes;
+    const uint32_t bar = smem_u32(&bars[warp]);
+    if (lane == 0) {
+        mbar_init(bar, 1);
+        fence_mbarrier_init();
+        mbar_arrive_expect_tx(bar, bytes);
+        bulk_load(row, x + r * ld_x, bytes, bar);
+    }
+    __syncwarp();
+    if (!__all_sync(0xFFFFFFFFu, mbar_wait(bar, 0, status))) {
+        if (lane == 0) mbar_wait(bar, 0, status);        // gave up: wait once more for the copy in flight
+        return;
+    }
+    const int nvec = int(hidden / 8);
+    const float h = float(hidden);
+    const float mu = __fdiv_rn(row_pass<false>(row, nvec, lane, 0), h);
+    const float var = __fdiv_rn(row_pass<true>(row, nvec, lane, pack2(mu, mu)), h);
+    const float rs = __frcp_rn(__fsqrt_rn(__fadd_rn(var, eps)));
+    if (lane == 0) {
+        mu_out[r] = mu;
+        rs_out[r] = rs;
+    }
+}
+
+// ---------------------------------------------------------------- normalise + quantise
+
+// One unit (32 rows x 64 columns at shared address `unit`, 128-byte swizzle):
+// normalise with the row statistics at `stat` and gamma / beta at `gf` /
+// `bf`, quantise row- and/or column-wise, stage the codes in the unit buffer
+// (row codes: 64-byte swizzle over its first 2 KB; column codes: 64 columns x
+// 32 bytes over the second 2 KB) and write scale bytes.
 template <bool kRowwise, bool kColwise>
-__global__ void __launch_bounds__(kThreads, 2)
-ln_quantize_kernel(const __grid_constant__ CUtensorMap x_map, const __grid_constant__ CUtensorMap qrow_map,
-                   const __grid_constant__ CUtensorMap qcol_map, const LnParams p) {
+__device__ __forceinline__ void quantize_unit(const ApplyParams& p, uint32_t unit, int64_t r0, int64_t c0, int lane,
+                                              uint32_t stat, uint32_t gaddr, uint32_t baddr) {
+    const int valid = p.hidden - c0 < kUnitCols ? int(p.hidden - c0) : kUnitCols;
+    uint32_t rc[2][8];                           // row codes: row `lane`, two 32-column blocks
+    uint32_t sr[2] = {0, 0};
+    if (kRowwise) {
+        uint64_t mm, rr;
+        lds128x2(stat + lane * 16, mm, rr);
+#pragma unroll
+        for (int blk = 0; blk < 2; ++blk) {
+            uint64_t y[16];
+#pragma unroll
+            for (int t = 0; t < 4; ++t) {
+                const int q = blk * 4 + t;                         // 16-byte chunk of the row (8 columns)
+                const uint4 x = lds128(unit + lane * 128 + ((q ^ (lane & 7)) << 4));
+                uint64_t g0, g1, g2, g3, b0, b1, b2, b3;
+                lds128x2(gaddr + q * 32, g0, g1);
+                lds128x2(gaddr + q * 32 + 16, g2, g3);
+                lds128x2(baddr + q * 32, b0, b1);
+                lds128x2(baddr + q * 32 + 16, b2, b3);
+                y[4 * t + 0] = fma2(mul2(sub2(bf2(x.x), mm), rr), g0, b0);
+                y[4 * t + 1] = fma2(mul2(sub2(bf2(x.y), mm), rr), g1, b1);
+                y[4 * t + 2] = fma2(mul2(sub2(bf2(x.z), mm), rr), g2, b2);
+                y[4 * t + 3] = fma2(mul2(sub2(bf2(x.w), mm), rr), g3, b3);
+            }
+            float mx[16];
+#pragma unroll
+            for (int i = 0; i < 16; ++i) mx[i] = maxabs(lo2(y[i]), hi2(y[i]));
+#pragma unroll
+            for (int s2 = 8; s2 >= 1; s2 >>= 1)
+#pragma unroll
+                for (int i = 0; i < s2; ++i) mx[i] = maxabs(mx[i], mx[i + s2]);
+            sr[blk] = mx_scale_byte_f32(mx[0]);
+            const float m = inv_scale(sr[blk]);
+            const uint64_t m2 = pack2(m, m);
+#pragma unroll
+            for (int i = 0; i < 8; ++i) {
+                const uint64_t a = mul2(y[2 * i], m2), b = mul2(y[2 * i + 1], m2);
+                rc[blk][i] = cvt_e4m3x2(lo2(a), hi2(a)) | (cvt_e4m3x2(lo2(b), hi2(b)) << 16);
+            }
+            if (sr[blk] == 0xFFu) {
+#pragma unroll
+                for (int i = 0; i < 8; ++i) rc[blk][i] = 0x7F7F7F7Fu;
+            }
+        }
+    }
+    uint32_t cc_lo[8], cc_hi[8];                 // column codes: columns 2 lane, 2 lane + 1, rows 0..31
+    uint32_t s_lo = 0, s_hi = 0;
+    if (kColwise) {
+        const uint64_t g2 = lds64(gaddr + lane * 8), b2 = lds64(baddr + lane * 8);
+        const uint32_t cbase = unit + ((lane & 3) << 2);
+        const int ch = lane >> 2;
+        uint64_t y[32];
+#pragma unroll
+        for (int r = 0; r < 32; ++r) {
+            const uint32_t x = lds32(cbase + r * 128 + ((ch ^ (r & 7)) << 4));
+            uint64_t mu2, rs2;
+            lds128x2(stat + r * 16, mu2, rs2);
+            y[r] = fma2(mul2(sub2(bf2(x), mu2), rs2), g2, b2);
+        }
+        float ml[16], mh[16];
+#pragma unroll
+        for (int i = 0; i < 16; ++i) {
+            ml[i] = maxabs(lo2(y[2 * i]), lo2(y[2 * i + 1]));
+            mh[i] = maxabs(hi2(y[2 * i]), hi2(y[2 * i + 1]));
+        }
+#pragma unroll
+        for (int s2 = 8; s2 >= 1; s2 >>= 1)
+#pragma unroll
+            for (int i = 0; i < s2; ++i) {
+                ml[i] = maxabs(ml[i], ml[i + s2]);
+                mh[i] = maxabs(mh[i], mh[i + s2]);
+            }
+        s_lo = mx_scale_byte_f32(ml[0]);
+        s_hi = mx_scale_byte_f32(mh[0]);
+        const uint64_t m2 = pack2(inv_scale(s_lo), inv_scale(s_hi));
+#pragma unroll
+        for (int r = 0; r < 32; ++r) y[r] = mul2(y[r], m2);
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+            cc_lo[i] = cvt_e4m3x2(lo2(y[4 * i]), lo2(y[4 * i + 1])) |
+                       (cvt_e4m3x2(lo2(y[4 * i + 2]), lo2(y[4 * i + 3])) << 16);
+            cc_hi[i] = cvt_e4m3x2(hi2(y[4 * i]), hi2(y[4 * i + 1])) |
+                       (cvt_e4m3x2(hi2(y[4 * i + 2]), hi2(y[4 * i + 3])) << 16);
+        }
+        if (s_lo == 0xFFu) {
+#pragma unroll
+            for (int i = 0; i < 8; ++i) cc_lo[i] = 0x7F7F7F7Fu;
+        }
+        if (s_hi == 0xFFu) {
+#pragma unroll
+            for (int i = 0; i < 8; ++i) cc_hi[i] = 0x7F7F7F7Fu;
+        }
+    }
+    __syncwarp();                                // every lane has read the unit: reuse it for the codes
+    if (kRowwise) {
+#pragma unroll
+        for (int c = 0; c < 4; ++c) {
+            const uint32_t* w = rc[c >> 1] + 4 * (c & 1);
+            sts128(unit + sw64(lane, c), w[0], w[1], w[2], w[3]);
+        }
+        const int64_t r = r0 + lane;
+        if (r < p.rows) {
+            uint8_t* sp = p.s_row + r * p.ld_s_row + (c0 >> 5);
+            if (valid > 32) st_global_u16(sp, sr[0] | (sr[1] << 8));
+            else st_global_u8(sp, sr[0]);
+        }
+    }
+    if (kColwise) {
+        // Column 2 lane, then 2 lane + 1: 32 bytes each, as four 16-byte pieces.
+        // Lane l writes piece (t + l / 2) % 4 at step t, so the 8 lanes of a
+        // store phase hit 8 different 16-byte bank groups.
+        const uint32_t cb = unit + 2048 + lane * 64;
+        const int rot = (lane >> 1) & 3;
+#pragma unroll
+        for (int t = 0; t < 4; ++t) {
+            const int q = (t + rot) & 3;
+            uint32_t w[4];
+#pragma unroll
+            for (int i = 0; i < 4; ++i)
+                w[i] = q == 0 ? cc_lo[i] : q == 1 ? cc_lo[4 + i] : q == 2 ? cc_hi[i] : cc_hi[4 + i];
+            sts128(cb + 16 * q, w[0], w[1], w[2], w[3]);
+        }
+        if (2 * lane < valid) {                               // valid is a multiple of 32
+            uint8_t* sp = p.s_col + (c0 + 2 * lane) * p.ld_s_col + (r0 >> 5);
+            st_global_u8(sp, s_lo);
+            st_global_u8(sp + p.ld_s_col, s_hi);
+        }
+    }
+}
+
+template <bool kRowwise, bool kColwise>
+__global__ void __launch_bounds__(kApplyWarps * 32, 1)
+ln_apply_kernel(const __grid_constant__ CUtensorMap x_map, const __grid_constant__ CUtensorMap qrow_map,
+                const __grid_constant__ CUtensorMap qcol_map, const ApplyParams p) {
     extern __shared__ uint8_t smem_raw[];
-    __shared__ __align__(8) uint64_t bars[kMaxChunks];
-    __shared__ float wsum[kWarps][kBand];
-    __shared__ float part[2][kBand];             // this CTA's partial sums, read by the whole cluster
-    __shared__ float mu_s[kBand], rs_s[kBand];
-    __shared__ int abort_flag;
+    __shared__ __align__(8) uint64_t bars[kApplyWarps][kApplyStages];
 
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-    const uint32_t base = smem_u32(smem);
-    uint16_t* g_s = reinterpret_cast<uint16_t*>(smem + p.cpc * kChunkBytes);   // gamma of this CTA's columns
-    uint16_t* b_s = g_s + p.cpc * kChunkCols;                                    // beta
-    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-    const uint32_t rank = cluster_ctarank(), k = cluster_nctarank();
-    const int64_t r0 = int64_t(blockIdx.x / k) * kBand;
-    const int chunk0 = int(rank) * p.cpc;
-    const int my_n = max(0, min(p.cpc, p.nch - chunk0));
-    const float h = float(p.hidden);
-    volatile int* abort_v = &abort_flag;
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int64_t gwarp = int64_t(blockIdx.x) * kApplyWarps + warp;
+    const int64_t nwarps = int64_t(gridDim.x) * kApplyWarps;
+    if (gwarp >= p.units) return;
+    const int64_t n_mine = (p.units - gwarp + nwarps - 1) / nwarps;
+    const uint32_t ring = smem_u32(smem + warp * (kApplyStages * kUnitBytes));
+    // two side areas per warp (this unit's, the next unit's): stat [32][4], gamma [64], beta [64]
+    uint8_t* side = smem + kApplyWarps * kApplyStages * kUnitBytes + warp * (2 * kSideBytes);
+    auto origin = [&](int64_t i, int64_t& r0, int64_t& c0) {
+        const int64_t u = gwarp + i * nwarps;
+        r0 = (u / p.col_units) * kUnitRows;
+        c0 = (u % p.col_units) * kUnitCols;
+    };
+    auto load_side = [&](int64_t i, float& m, float& rs, uint32_t& g2, uint32_t& b2) {
+        int64_t r0, c0;
+        origin(i, r0, c0);
+        const int64_t r = r0 + lane, c = c0 + 2 * lane;
+        m = r < p.rows ? p.mu[r] : 0.0f;
+        rs = r < p.rows ? p.rsigma[r] : 0.0f;
+        g2 = c < p.hidden ? *reinterpret_cast<const uint32_t*>(p.gamma + c) : 0u;
+        b2 = c < p.hidden ? *reinterpret_cast<const uint32_t*>(p.beta + c) : 0u;
+    };
+    auto store_side = [&](uint8_t* area, float m, float rs, uint32_t g2, uint32_t b2) {
+        reinterpret_cast<float4*>(area)[lane] = make_float4(m, m, rs, rs);
+        reinterpret_cast<float2*>(area + kUnitRows * 16)[lane] = make_float2(bf16_lo(g2), bf16_hi(g2));
+        reinterpret_cast<float2*>(area + kUnitRows * 16 + kUnitCols * 4)[lane] = make_float2(bf16_lo(b2), bf16_hi(b2));
+    };
 
-    if (tid == 0) {
-        for (int j = 0; j < my_n; ++j) mbar_init(smem_u32(&bars[j]), 1);
-        abort_flag = 0;
-        fence_mbarrier_init();
-    }
-    __syncthreads();
-    if (tid == 0) {
+    if (lane == 0) {
         tma_prefetch_desc(&x_map);
-        for (int j = 0; j < my_n; ++j) {
-            const uint32_t bar = smem_u32(&bars[j]);
-            mbar_arrive_expect_tx(bar, kChunkBytes);
-            tma_load_2d(base + j * kChunkBytes, &x_map, bar, (chunk0 + j) * kChunkCols, int32_t(r0));
+        if (kRowwise) tma_prefetch_desc(&qrow_map);
+        if (kColwise) tma_prefetch_desc(&qcol_map);
+        for (int s = 0; s < kApplyStages; ++s) mbar_init(smem_u32(&bars[warp][s]), 1);
+        fence_mbarrier_init();
+        for (int s = 0; s < kApplyStages && s < n_mine; ++s) {
+            int64_t r0, c0;
+            origin(s, r0, c0);
+            const uint32_t bar = smem_u32(&bars[warp][s]);
+            mbar_arrive_expect_tx(bar, kUnitBytes);
+            tma_load_2d(ring + s * kUnitBytes, &x_map, bar, int32_t(c0), int32_t(r0));
         }
     }
-    for (int i = tid; i < my_n * kChunkCols; i += kThreads) {
-        const int64_t c = int64_t(chunk0) * kChunkCols + i;
-        g_s[i] = c < p.hidden ? p.gamma[c] : uint16_t(0);
-        b_s[i] = c < p.hidden ? p.beta[c] : uint16_t(0);
+    {
+        float m, rs;
+        uint32_t g2, b2;
+        load_side(0, m, rs, g2, b2);
+        store_side(side, m, rs, g2, b2);
     }
+    __syncwarp();
 
-    // ---------------------------------------------------------------- pass 1: row sums
-    float acc = 0.0f;
-    for (int j = warp; j < my_n; j += kWarps) {
-        if (!mbar_wait(smem_u32(&bars[j]), 0, p.status)) {
-            *abort_v = 1;
+    for (int64_t i = 0; i < n_mine; ++i) {
+        const int s = int(i % kApplyStages);
+        const uint32_t bar = smem_u32(&bars[warp][s]);
+        int64_t r0, c0;
+        origin(i, r0, c0);
+        // the next unit's statistics and gamma / beta, loaded now, stored after this unit
+        float nm = 0.0f, nrs = 0.0f;
+        uint32_t ng = 0, nb = 0;
+        if (i + 1 < n_mine) load_side(i + 1, nm, nrs, ng, nb);
+        if (!__all_sync(0xFFFFFFFFu, mbar_wait(bar, uint32_t((i / kApplyStages) & 1), p.status))) {
+            // Gave up: let this warp's loads still in flight land before leaving.
+            if (lane == 0)
+                for (int64_t j = i; j < i + kApplyStages && j < n_mine; ++j)
+                    mbar_wait(smem_u32(&bars[warp][j % kApplyStages]), uint32_t((j / kApplyStages) & 1), p.status);
             break;
         }
-        uint32_t w[32];
-        load_row(base + j * kChunkBytes, lane, w);
-        float v[64];
-#pragma unroll
-        for (int i = 0; i < 32; ++i) { v[2 * i] = bf16_lo(w[i]); v[2 * i + 1] = bf16_hi(w[i]); }
-        acc = __fadd_rn(acc, tree64(v));         // columns past the row end were loaded as 0
-    }
-    wsum[warp][lane] = acc;
-    __syncthreads();                             // also publishes gamma/beta
-    if (warp == 0) {
-        float s = wsum[0][lane];
-#pragma unroll
-        for (int w = 1; w < kWarps; ++w) s = __fadd_rn(s, wsum[w][lane]);
-        part[0][lane] = s;
-    }
-    cluster_sync();
-    if (warp == 0) {
-        float s = 0.0f;
-        for (uint32_t q = 0; q < k; ++q) s = __fadd_rn(s, ld_cluster_f32(mapa_shared(smem_u32(&part[0][lane]), q)));
-        mu_s[lane] = __fdiv_rn(s, h);
-    }
-    __syncthreads();
-
-    // ---------------------------------------------------------------- pass 2: squared deviations
-    const float mu_l = mu_s[lane];
-    acc = 0.0f;
-    if (!*abort_v) {
-        for (int j = warp; j < my_n; j += kWarps) {
-            uint32_t w[32];
-            load_row(base + j * kChunkBytes, lane, w);
-            const int64_t left = p.hidden - int64_t(chunk0 + j) * kChunkCols;
-            const int valid = left < kChunkCols ? int(left) : kChunkCols;
-            float v[64];
-#pragma unroll
-            for (int i = 0; i < 32; ++i) {
-                const float d0 = __fsub_rn(bf16_lo(w[i]), mu_l), d1 = __fsub_rn(bf16_hi(w[i]), mu_l);
-                v[2 * i] = 2 * i < valid ? __fmul_rn(d0, d0) : 0.0f;
-                v[2 * i + 1] = 2 * i + 1 < valid ? __fmul_rn(d1, d1) : 0.0f;
-            }
-            acc = __fadd_rn(acc, tree64(v));
-        }
-    }
-    wsum[warp][lane] = acc;
-    __syncthreads();
-    if (warp == 0) {
-        float s = wsum[0][lane];
-#pragma unroll
-        for (int w = 1; w < kWarps; ++w) s = __fadd_rn(s, wsum[w][lane]);
-        part[1][lane] = s;
-    }
-    cluster_sync();
-    if (warp == 0) {
-        float s = 0.0f;
-        for (uint32_t q = 0; q < k; ++q) s = __fadd_rn(s, ld_cluster_f32(mapa_shared(smem_u32(&part[1][lane]), q)));
-        const float var = __fdiv_rn(s, h);
-        const float rs = __frcp_rn(__fsqrt_rn(__fadd_rn(var, p.eps)));
-        rs_s[lane] = rs;
-        const int64_t r = r0 + lane;
-        if (rank == 0 && r < p.rows) {
-            if (p.mu) p.mu[r] = mu_l;
-            if (p.rsigma) p.rsigma[r] = rs;
-        }
-    }
-    cluster_arrive_release();                    // done reading the other CTAs' shared memory
-    __syncthreads();
-
-    // ---------------------------------------------------------------- pass 3: normalise + quantise
-    if (!*abort_v) {
-        const float rs_l = rs_s[lane];
-        for (int j = warp; j < my_n; j += kWarps) {
-            const uint32_t chunk = base + j * kChunkBytes;
-            const int64_t c0 = int64_t(chunk0 + j) * kChunkCols;
-            const int valid = p.hidden - c0 < kChunkCols ? int(p.hidden - c0) : kChunkCols;
-            const uint32_t gb = smem_u32(g_s + j * kChunkCols), bb = smem_u32(b_s + j * kChunkCols);
-            uint32_t rc[2][8];                   // row codes: row `lane`, two 32-column blocks
-            uint32_t sr[2];
-            if (kRowwise) {
-#pragma unroll
-                for (int blk = 0; blk < 2; ++blk) {
-                    float y[32];
-#pragma unroll
-                    for (int t = 0; t < 4; ++t) {
-                        const int cc = blk * 4 + t;                  // 16-byte chunk of the row (8 columns)
-                        const uint4 xv = lds128(chunk + lane * 128 + ((cc ^ (lane & 7)) << 4));
-                        const uint4 gv = lds128(gb + cc * 16), bv = lds128(bb + cc * 16);
-                        const uint32_t xw[4] = {xv.x, xv.y, xv.z, xv.w};
-                        const uint32_t gw[4] = {gv.x, gv.y, gv.z, gv.w};
-                        const uint32_t bw[4] = {bv.x, bv.y, bv.z, bv.w};
-#pragma unroll
-                        for (int i = 0; i < 4; ++i) {
-                            y[8 * t + 2 * i] = ln_y(bf16_lo(xw[i]), mu_l, rs_l, bf16_lo(gw[i]), bf16_lo(bw[i]));
-                            y[8 * t + 2 * i + 1] = ln_y(bf16_hi(xw[i]), mu_l, rs_l, bf16_hi(gw[i]), bf16_hi(bw[i]));
-                        }
-                    }
-                    uint32_t am = 0;
-#pragma unroll
-                    for (int i = 0; i < 32; ++i) am = max(am, __float_as_uint(y[i]) & 0x7FFFFFFFu);
-                    sr[blk] = mx_scale_byte_f32(am);
-                    const float m = inv_scale(sr[blk]);
-#pragma unroll
-                    for (int i = 0; i < 8; ++i)
-                        rc[blk][i] = cvt_e4m3x2(__fmul_rn(y[4 * i], m), __fmul_rn(y[4 * i + 1], m)) |
-                                     (cvt_e4m3x2(__fmul_rn(y[4 * i + 2], m), __fmul_rn(y[4 * i + 3], m)) << 16);
-                    if (sr[blk] == 0xFFu) {
-#pragma unroll
-                        for (int i = 0; i < 8; ++i) rc[blk][i] = 0x7F7F7F7Fu;
-                    }
-                }
-            }
-            uint32_t cc_lo[8], cc_hi[8];         // column codes: columns 2 lane, 2 lane + 1, rows 0..31
-            uint32_t s_lo = 0, s_hi = 0;
-            if (kColwise) {
-                const uint32_t g2 = lds32(gb + lane * 4), b2 = lds32(bb + lane * 4);
-                const float g_lo = bf16_lo(g2), g_hi = bf16_hi(g2), b_lo = bf16_lo(b2), b_hi = bf16_hi(b2);
-                const uint32_t cbase = chunk + ((lane & 3) << 2);
-                const int ch = lane >> 2;
-                uint32_t xw[32];
-#pragma unroll
-                for (int r = 0; r < 32; ++r) xw[r] = lds32(cbase + r * 128 + ((ch ^ (r & 7)) << 4));
-                uint32_t am_lo = 0, am_hi = 0;
-#pragma unroll
-                for (int r = 0; r < 32; ++r) {
-                    const float mu_r = mu_s[r], rs_r = rs_s[r];
-                    am_lo = max(am_lo, __float_as_uint(ln_y(bf16_lo(xw[r]), mu_r, rs_r, g_lo, b_lo)) & 0x7FFFFFFFu);
-                    am_hi = max(am_hi, __float_as_uint(ln_y(bf16_hi(xw[r]), mu_r, rs_r, g_hi, b_hi)) & 0x7FFFFFFFu);
-                }
-                s_lo = mx_scale_byte_f32(am_lo);
-                s_hi = mx_scale_byte_f32(am_hi);
-                const float m_lo = inv_scale(s_lo), m_hi = inv_scale(s_hi);
-#pragma unroll
-                for (int i = 0; i < 8; ++i) {
-                    float ylo[4], yhi[4];
-#pragma unroll
-                    for (int t = 0; t < 4; ++t) {
-                        const int r = 4 * i + t;
-                        const float mu_r = mu_s[r], rs_r = rs_s[r];
-                        ylo[t] = __fmul_rn(ln_y(bf16_lo(xw[r]), mu_r, rs_r, g_lo, b_lo), m_lo);
-                        yhi[t] = __fmul_rn(ln_y(bf16_hi(xw[r]), mu_r, rs_r, g_hi, b_hi), m_hi);
-                    }
-                    cc_lo[i] = cvt_e4m3x2(ylo[0], ylo[1]) | (cvt_e4m3x2(ylo[2], ylo[3]) << 16);
-                    cc_hi[i] = cvt_e4m3x2(yhi[0], yhi[1]) | (cvt_e4m3x2(yhi[2], yhi[3]) << 16);
-                }
-                if (s_lo == 0xFFu) {
-#pragma unroll
-                    for (int i = 0; i < 8; ++i) cc_lo[i] = 0x7F7F7F7Fu;
-                }
-                if (s_hi == 0xFFu) {
-#pragma unroll
-                    for (int i = 0; i < 8; ++i) cc_hi[i] = 0x7F7F7F7Fu;
-                }
-            }
-            __syncwarp();                        // every lane has read the chunk: reuse it for the codes
-            if (kRowwise) {
-#pragma unroll
-                for (int c = 0; c < 4; ++c) {
-                    const uint32_t* w = rc[c >> 1] + 4 * (c & 1);
-                    sts128(chunk + sw64(lane, c), w[0], w[1], w[2], w[3]);
-                }
-                const int64_t r = r0 + lane;
-                if (r < p.rows) {
-                    uint8_t* sp = p.s_row + r * p.ld_s_row + (c0 >> 5);
-                    if (valid > 32) st_global_u16(sp, sr[0] | (sr[1] << 8));
-                    else st_global_u8(sp, sr[0]);
-                }
-            }
-            if (kColwise) {
-                const uint32_t cb = chunk + 2048 + lane * 64;   // column 2 lane, then 2 lane + 1: 32 bytes each
-                sts128(cb, cc_lo[0], cc_lo[1], cc_lo[2], cc_lo[3]);
-                sts128(cb + 16, cc_lo[4], cc_lo[5], cc_lo[6], cc_lo[7]);
-                sts128(cb + 32, cc_hi[0], cc_hi[1], cc_hi[2], cc_hi[3]);
-                sts128(cb + 48, cc_hi[4], cc_hi[5], cc_hi[6], cc_hi[7]);
-                if (2 * lane < valid) {                           // valid is a multiple of 32
-                    uint8_t* sp = p.s_col + (c0 + 2 * lane) * p.ld_s_col + (r0 >> 5);
-                    st_global_u8(sp, s_lo);
-                    st_global_u8(sp + p.ld_s_col, s_hi);
-                }
-            }
-            fence_proxy_async_smem();
-            __syncwarp();
-            if (lane == 0) {
-                if (kRowwise) tma_store_2d(&qrow_map, chunk, int32_t(c0), int32_t(r0));
-                if (kColwise) tma_store_2d(&qcol_map, chunk + 2048, int32_t(r0), int32_t(c0));
-                bulk_commit();
+        const uint32_t unit = ring + s * kUnitBytes;
+        const uint32_t sb = smem_u32(side) + uint32_t(i & 1) * kSideBytes;
+        quantize_unit<kRowwise, kColwise>(p, unit, r0, c0, lane, sb, sb + kUnitRows * 16, sb + kUnitRows * 16 + kUnitCols * 4);
+        if (i + 1 < n_mine) store_side(side + ((i + 1) & 1) * kSideBytes, nm, nrs, ng, nb);
+        fence_proxy_async_smem();                // make the staged codes visible to the TMA engine
+        __syncwarp();
+        if (lane == 0) {
+            if (kRowwise) tma_store_2d(&qrow_map, unit, int32_t(c0), int32_t(r0));
+            if (kColwise) tma_store_2d(&qcol_map, unit + 2048, int32_t(r0), int32_t(c0));
+            bulk_commit();
+            if (i + kApplyStages < n_mine) {
+                bulk_wait_read_all();            // the stores have read the unit: refill it
+                int64_t rn, cn;
+                origin(i + kApplyStages, rn, cn);
+                mbar_arrive_expect_tx(bar, kUnitBytes);
+                tma_load_2d(unit, &x_map, bar, int32_t(cn), int32_t(rn));
             }
         }
-        if (lane == 0) bulk_wait_all();
-    } else if (tid == 0) {
-        // Gave up: let the loads still in flight land before the CTA exits.
-        for (int j = 0; j < my_n; ++j) mbar_wait(smem_u32(&bars[j]), 0, p.status);
+        __syncwarp();
     }
-    cluster_wait_acquire();                      // no CTA leaves while another may read its partials
+    if (lane == 0) bulk_wait_all();
 }
 
 template <bool R, bool C>
-cudaError_t launch(const CUtensorMap& xm, const CUtensorMap& qr, const CUtensorMap& qc, const LnParams& p,
-                   int k, int64_t bands, size_t smem, cudaStream_t stream) {
-    auto kern = ln_quantize_kernel<R, C>;
-    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, int(smem));
+cudaError_t launch_apply(const CUtensorMap& xm, const CUtensorMap& qr, const CUtensorMap& qc, const ApplyParams& p,
+                         int sms, cudaStream_t stream) {
+    auto kern = ln_apply_kernel<R, C>;
+    cudaError_t e = set_smem_attribute_once(reinterpret_cast<const void*>(kern), kApplySmem);
     if (e != cudaSuccess) return e;
-    cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3(unsigned(bands * k), 1, 1);
-    cfg.blockDim = dim3(kThreads, 1, 1);
-    cfg.dynamicSmemBytes = smem;
-    cfg.stream = stream;
-    cudaLaunchAttribute attr[1];
-    attr[0].id = cudaLaunchAttributeClusterDimension;
-    attr[0].val.clusterDim.x = unsigned(k);
-    attr[0].val.clusterDim.y = 1;
-    attr[0].val.clusterDim.z = 1;
-    cfg.attrs = attr;
-    cfg.numAttrs = 1;
-    return cudaLaunchKernelEx(&cfg, kern, xm, qr, qc, p);
+    const int64_t want = (p.units + kApplyWarps - 1) / kApplyWarps;
+    const int grid = int(want < sms ? want : sms);
+    kern<<<grid, kApplyWarps * 32, kApplySmem, stream>>>(xm, qr, qc, p);
+    return cudaGetLastError();
 }
 
 }  // namespace
 
-int64_t ln_quantize_max_hidden() { return int64_t(kMaxCluster) * kMaxChunks * kChunkCols; }
+int64_t ln_quantize_max_hidden() { return 32768; }   // keeps the longest chain of additions at 42
 
 te_mx_status ln_quantize_launch(const LnQuantizeArgs& a, cudaStream_t stream) {
     const bool rowwise = a.q_row != nullptr, colwise = a.q_col != nullptr;
-    if (a.rows == 0 || a.hidden == 0 || (!rowwise && !colwise && !a.mu && !a.rsigma)) return TE_MX_OK;
+    if (a.rows == 0 || a.hidden == 0) return TE_MX_OK;
+
+    unsigned int* status = nullptr;
+    te_mx_status st = device_status_ptr(&status);
+    if (st != TE_MX_OK) return st;
+    // rows per statistics CTA: as many as fit in ~110 KB (two CTAs per SM), at most 8
+    const int64_t row_bytes = a.hidden * 2;
+    const int rpc = int(row_bytes * kStatsWarps <= 110 * 1024 ? kStatsWarps
+                        : (110 * 1024 / row_bytes > 1 ? 110 * 1024 / row_bytes : 1));
+    const size_t stats_smem = size_t(rpc) * size_t(row_bytes);
+    cudaError_t e = set_smem_attribute_once(reinterpret_cast<const void*>(ln_stats_kernel), 110 * 1024);
+    if (e != cudaSuccess) return cuda_status(e, "layernorm statistics kernel attributes");
+    const int64_t blocks = (a.rows + rpc - 1) / rpc;
+    ln_stats_kernel<<<unsigned(blocks), kStatsWarps * 32, stats_smem, stream>>>(
+        static_cast<const uint16_t*>(a.x), a.rows, a.hidden, a.ld_x, a.eps, a.mu, a.rsigma, rpc, status);
+    e = cudaGetLastError();
+    if (e != cudaSuccess) return cuda_status(e, "layernorm statistics kernel launch");
+    if (!rowwise && !colwise) return TE_MX_OK;
 
     int sms = 0;
-    te_mx_status st = device_sm_count(&sms);
-    if (st != TE_MX_OK) return st;
-    const int64_t bands = (a.rows + kBand - 1) / kBand;
-    const int nch = int((a.hidden + kChunkCols - 1) / kChunkCols);
-    // Cluster size: at most 16 chunks (64 KB) per CTA when possible, and at
-    // least two CTAs per SM when the band count allows it.
-    int k = 1;
-    while (k < kMaxCluster && 2 * k <= nch &&
-           ((nch + k - 1) / k > 16 || bands * k < 2 * int64_t(sms)))
-        k *= 2;
-    const int cpc = (nch + k - 1) / k;
-    if (cpc > kMaxChunks)
-        return set_error(TE_MX_ERR_UNSUPPORTED_SHAPE, "hidden=%lld exceeds the largest supported %lld",
-                         (long long)a.hidden, (long long)ln_quantize_max_hidden());
-
+    if ((st = device_sm_count(&sms)) != TE_MX_OK) return st;
     CUtensorMap xm, qr, qc;
     if ((st = encode_tensor_map_2d(&xm, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, a.x, uint64_t(a.hidden),
-                                   uint64_t(a.rows), uint64_t(a.ld_x) * 2, kChunkCols, kBand,
+                                   uint64_t(a.rows), uint64_t(a.ld_x) * 2, kUnitCols, kUnitRows,
                                    CU_TENSOR_MAP_SWIZZLE_128B)) != TE_MX_OK) return st;
     qr = xm;
     qc = xm;
     if (rowwise && (st = encode_tensor_map_2d(&qr, CU_TENSOR_MAP_DATA_TYPE_UINT8, a.q_row, uint64_t(a.hidden),
-                                              uint64_t(a.rows), uint64_t(a.hidden), kChunkCols, kBand,
+                                              uint64_t(a.rows), uint64_t(a.hidden), kUnitCols, kUnitRows,
                                               CU_TENSOR_MAP_SWIZZLE_64B)) != TE_MX_OK) return st;
     if (colwise && (st = encode_tensor_map_2d(&qc, CU_TENSOR_MAP_DATA_TYPE_UINT8, a.q_col, uint64_t(a.rows),
-                                              uint64_t(a.hidden), uint64_t(a.rows), kBand, kChunkCols,
+                                              uint64_t(a.hidden), uint64_t(a.rows), kUnitRows, kUnitCols,
                                               CU_TENSOR_MAP_SWIZZLE_NONE)) != TE_MX_OK) return st;
-
-    LnParams p;
-    p.rows = a.rows; p.hidden = a.hidden; p.eps = a.eps;
+    ApplyParams p;
+    p.rows = a.rows; p.hidden = a.hidden;
+    p.mu = a.mu; p.rsigma = a.rsigma;
     p.gamma = static_cast<const uint16_t*>(a.gamma);
     p.beta = static_cast<const uint16_t*>(a.beta);
     p.s_row = a.s_row; p.ld_s_row = a.ld_s_row;
     p.s_col = a.s_col; p.ld_s_col = a.ld_s_col;
-    p.mu = a.mu; p.rsigma = a.rsigma;
-    p.nch = nch; p.cpc = cpc;
-    if ((st = device_status_ptr(&p.status)) != TE_MX_OK) return st;
-    const size_t smem = size_t(cpc) * (kChunkBytes + 2 * kChunkCols * 2) + 1024;
-
-    cudaError_t e;
-    if (rowwise && colwise) e = launch<true, true>(xm, qr, qc, p, k, bands, smem, stream);
-    else if (colwise) e = launch<false, true>(xm, qr, qc, p, k, bands, smem, stream);
-    else if (rowwise) e = launch<true, false>(xm, qr, qc, p, k, bands, smem, stream);
-    else e = launch<false, false>(xm, qr, qc, p, k, bands, smem, stream);    // statistics only
+    p.col_units = (a.hidden + kUnitCols - 1) / kUnitCols;
+    p.units = ((a.rows + kUnitRows - 1) / kUnitRows) * p.col_units;
+    p.status = status;
+    if (rowwise && colwise) e = launch_apply<true, true>(xm, qr, qc, p, sms, stream);
+    else if (colwise) e = launch_apply<false, true>(xm, qr, qc, p, sms, stream);
+    else e = launch_apply<true, false>(xm, qr, qc, p, sms, stream);
     return cuda_status(e, "layernorm quantize kernel launch");
 }
 

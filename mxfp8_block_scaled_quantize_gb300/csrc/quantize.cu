@@ -169,7 +169,12 @@ quantize_kernel(const __grid_constant__ CUtensorMap x_map, const __grid_constant
         const int s = int(i % kStages);
         const uint32_t parity = uint32_t((i / kStages) & 1);
         const uint32_t bar = smem_u32(&bars[warp][s]);
-        if (!mbar_wait(bar, parity, p.status)) break;
+        if (!__all_sync(0xFFFFFFFFu, mbar_wait(bar, parity, p.status))) {
+            if (lane == 0)                       // gave up: let this warp's loads still in flight land
+                for (int64_t j = i; j < i + kStages && j < n_mine; ++j)
+                    mbar_wait(smem_u32(&bars[warp][j % kStages]), uint32_t((j / kStages) & 1), p.status);
+            break;
+        }
         const uint32_t tile = ring + s * kUnitBytes;
         const int64_t u = gwarp + i * nwarps;
         const int64_t r0 = (u / p.col_units) * kRows, c0 = (u % p.col_units) * kCols;
@@ -286,7 +291,7 @@ template <bool R, bool C, bool D>
 cudaError_t launch(const CUtensorMap& xm, const CUtensorMap& qr, const CUtensorMap& qc, const QuantizeParams& p,
                    int sms, cudaStream_t stream) {
     auto k = quantize_kernel<R, C, D>;
-    cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
+    cudaError_t e = set_smem_attribute_once(reinterpret_cast<const void*>(k), kSmemBytes);
     if (e != cudaSuccess) return e;
     const int64_t want = (p.units + kWarps - 1) / kWarps;
     const int grid = int(want < sms ? want : sms);

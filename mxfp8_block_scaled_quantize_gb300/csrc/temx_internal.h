@@ -60,6 +60,9 @@ te_mx_status block_quantize_launch(const QuantizeArgs& a, bool block_2d, cudaStr
 te_mx_status gemm_launch(const GemmArgs& a, cudaStream_t stream);
 
 // Helpers implemented in api.cu.
+// Raise a kernel's dynamic shared memory limit to `bytes` on the current
+// device, once per (kernel, device); later calls return at once.
+cudaError_t set_smem_attribute_once(const void* kernel, int bytes);
 te_mx_status set_error(te_mx_status st, const char* fmt, ...);
 void clear_error();
 // Host-side argument checks of te_mx_quantize (+ the current device's arch).

@@ -72,13 +72,15 @@ def test_host_validation_rejects_bad_arguments_before_any_launch(lib):
     with pytest.raises(binding.TemxError, match="UNSUPPORTED_SHAPE"):
         binding.te_mx_block_quantize(16, 128, 48, 48, 0, 16, 16, 16, 0, 0, 0, 0)     # cols % 32
     with pytest.raises(binding.TemxError, match="INVALID_ARG"):      # gamma missing
-        binding.te_mx_layernorm_quantize(16, 32, 64, 64, 0, 16, 1e-5, 16, 16, 16, 0, 0, 0, 0, 0, 0)
+        binding.te_mx_layernorm_quantize(16, 32, 64, 64, 0, 16, 1e-5, 16, 16, 16, 0, 0, 0, 16, 16, 0)
     with pytest.raises(binding.TemxError, match="INVALID_ARG"):      # eps <= 0
-        binding.te_mx_layernorm_quantize(16, 32, 64, 64, 16, 16, 0.0, 16, 16, 16, 0, 0, 0, 0, 0, 0)
+        binding.te_mx_layernorm_quantize(16, 32, 64, 64, 16, 16, 0.0, 16, 16, 16, 0, 0, 0, 16, 16, 0)
     with pytest.raises(binding.TemxError, match="UNSUPPORTED_SHAPE"):   # hidden % 32
-        binding.te_mx_layernorm_quantize(16, 32, 48, 48, 16, 16, 1e-5, 16, 16, 16, 0, 0, 0, 0, 0, 0)
+        binding.te_mx_layernorm_quantize(16, 32, 48, 48, 16, 16, 1e-5, 16, 16, 16, 0, 0, 0, 16, 16, 0)
+    with pytest.raises(binding.TemxError, match="INVALID_ARG"):      # mu / rsigma missing
+        binding.te_mx_layernorm_quantize(16, 32, 64, 64, 16, 16, 1e-5, 16, 16, 16, 0, 0, 0, 0, 0, 0)
     with pytest.raises(binding.TemxError, match="UNSUPPORTED_SHAPE"):   # hidden too large
-        binding.te_mx_layernorm_quantize(16, 32, 32768, 32768, 16, 16, 1e-5, 16, 16, 2048, 0, 0, 0, 0, 0, 0)
+        binding.te_mx_layernorm_quantize(16, 32, 32800, 32800, 16, 16, 1e-5, 16, 16, 2064, 0, 0, 0, 16, 16, 0)
     # zero-sized problems are no-ops
     binding.te_mx_layernorm_quantize(16, 0, 64, 64, 16, 16, 1e-5, 16, 16, 16, 0, 0, 0, 0, 0, 0)
     binding.te_mx_block_quantize(0, 0, 128, 128, 1, 0, 0, 0, 0, 0, 0, 0)

@@ -6,8 +6,7 @@ rsigma (``layernorm_stat_bounds``).  Codes and scales: every one must be the
 MXFP8 quantisation of some y' within ``layernorm_error_bound`` of the exact y
 (``mx_admissible``); where only one answer is admissible (all but a small
 fraction of the elements, asserted) that is bit-exactness.  Covers chunk and
-cluster edge cases (hidden not a multiple of 64, CTAs with no columns, the
-largest hidden), ragged rows, each orientation alone, statistics only,
+unit edge cases (hidden not a multiple of 64, the largest hidden), ragged rows, each orientation alone, statistics only,
 constant and non-finite rows, large row means, determinism, canary-guarded
 outputs, and the full-size ffn input (sampled rows and 32-row bands).
 """
@@ -35,7 +34,7 @@ def make(rows, hidden, seed, mean=0.0, std=1.0, row_spread=True):
     return x.to(torch.bfloat16), ga.to(torch.bfloat16), be.to(torch.bfloat16)
 
 
-def run(x, ga, be, rowwise=True, colwise=True, stats=True):
+def run(x, ga, be, rowwise=True, colwise=True):
     rows, hidden = x.shape
     out, bufs = {}, {}
     pr, pc = binding.te_mx_scale_pitch(hidden), binding.te_mx_scale_pitch(rows)
@@ -45,12 +44,10 @@ def run(x, ga, be, rowwise=True, colwise=True, stats=True):
     if colwise:
         out["q_col"], bufs["q_col"] = U.guarded_u8(hidden, rows)
         out["s_col"], bufs["s_col"] = U.guarded_u8(hidden, pc)
-    if stats:
-        for key in ("mu", "rsigma"):
-            buf = torch.full((rows + 64,), float("nan"), dtype=torch.float32, device="cuda")
-            out[key], bufs[key] = buf[:rows], buf
-    binding.layernorm_quantize(x.cuda(), ga.cuda(), be.cuda(), rowwise=rowwise, colwise=colwise, stats=stats,
-                               out=out)
+    for key in ("mu", "rsigma"):
+        buf = torch.full((rows + 64,), float("nan"), dtype=torch.float32, device="cuda")
+        out[key], bufs[key] = buf[:rows], buf
+    binding.layernorm_quantize(x.cuda(), ga.cuda(), be.cuda(), rowwise=rowwise, colwise=colwise, out=out)
     binding.te_mx_device_status()
     res = {}
     if rowwise:
@@ -65,10 +62,9 @@ def run(x, ga, be, rowwise=True, colwise=True, stats=True):
         s = out["s_col"].cpu().numpy()
         assert np.all(s[:, rows // 32:] == U.CANARY)
         res["q_col"], res["s_col"] = out["q_col"].cpu().numpy(), s
-    if stats:
-        for key in ("mu", "rsigma"):
-            assert torch.isnan(bufs[key][rows:]).all(), "write past the end of " + key
-            res[key] = out[key].double().cpu().numpy()
+    for key in ("mu", "rsigma"):
+        assert torch.isnan(bufs[key][rows:]).all(), "write past the end of " + key
+        res[key] = out[key].double().cpu().numpy()
     return res
 
 
@@ -112,7 +108,7 @@ def check(x, ga, be, got, rows_idx=None, max_ambiguous=MAX_AMBIGUOUS):
 
 
 @pytest.mark.parametrize("rows,hidden", [(32, 64), (64, 96), (256, 1024), (96, 4128), (128, 7168),
-                                         (64, 2080), (32, 24576)])
+                                         (64, 2080), (32, 32768)])
 def test_both_orientations(rows, hidden):
     x, ga, be = make(rows, hidden, rows * 3 + hidden)
     check(x, ga, be, run(x, ga, be))
@@ -127,8 +123,7 @@ def test_rowwise_ragged_rows(rows, hidden):
 def test_one_orientation_and_stats_only():
     x, ga, be = make(160, 1536, 5)
     check(x, ga, be, run(x, ga, be, rowwise=False, colwise=True))
-    check(x, ga, be, run(x, ga, be, rowwise=False, colwise=False, stats=True))
-    check(x, ga, be, run(x, ga, be, rowwise=True, colwise=True, stats=False))
+    check(x, ga, be, run(x, ga, be, rowwise=False, colwise=False))
 
 
 def test_large_row_means_and_tiny_variance():
