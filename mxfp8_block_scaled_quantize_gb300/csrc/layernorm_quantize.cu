@@ -162,9 +162,31 @@ __device__ __forceinline__ float warp_sum(float v) {
 // the accumulators are added pairwise and the lanes by a butterfly: for rows
 // of at most 32768 elements the longest chain is 3 + 32 + 2 + 5 = 42
 // additions.
-__device__ __forceinline__ void bulk_load(uint32_t dst, const void* src, uint32_t bytes, uint32_t bar) {
-    asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];"
-                 :: "r"(dst), "l"(src), "r"(bytes), "r"(bar) : "memory");
+// L2 cache policies: keep x in L2 for the apply kernel (evict last), which
+// then reads it for the last time (evict first).
+__device__ __forceinline__ uint64_t l2_policy_evict_last() {
+    uint64_t p;
+    asm volatile("createpolicy.fractional.L2::evict_last.b64 %0, 1.0;" : "=l"(p));
+    return p;
+}
+__device__ __forceinline__ uint64_t l2_policy_evict_first() {
+    uint64_t p;
+    asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(p));
+    return p;
+}
+__device__ __forceinline__ void bulk_load(uint32_t dst, const void* src, uint32_t bytes, uint32_t bar,
+                                          uint64_t policy) {
+    asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint"
+                 " [%0], [%1], %2, [%3], %4;"
+                 :: "r"(dst), "l"(src), "r"(bytes), "r"(bar), "l"(policy) : "memory");
+}
+__device__ __forceinline__ void tma_load_2d_hint(uint32_t dst, const CUtensorMap* desc, uint32_t bar, int32_t x,
+                                                 int32_t y, uint64_t policy) {
+    asm volatile(
+        "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint"
+        " [%0], [%1, {%2, %3}], [%4], %5;"
+        :: "r"(dst), "l"(reinterpret_cast<uint64_t>(desc)), "r"(x), "r"(y), "r"(bar), "l"(policy)
+        : "memory");
 }
 
 template <bool kSquares>
@@ -196,7 +218,7 @@ ln_stats_kernel(const uint16_t* __restrict__ x, int64_t rows, int64_t hidden, in
         mbar_init(bar, 1);
         fence_mbarrier_init();
         mbar_arrive_expect_tx(bar, bytes);
-        bulk_load(row, x + r * ld_x, bytes, bar);
+        bulk_load(row, x + r * ld_x, bytes, bar, l2_policy_evict_last());
     }
     __syncwarp();
     if (!__all_sync(0xFFFFFFFFu, mbar_wait(bar, 0, status))) {
@@ -331,20 +353,11 @@ __device__ __forceinline__ void quantize_unit(const ApplyParams& p, uint32_t uni
         }
     }
     if (kColwise) {
-        // Column 2 lane, then 2 lane + 1: 32 bytes each, as four 16-byte pieces.
-        // Lane l writes piece (t + l / 2) % 4 at step t, so the 8 lanes of a
-        // store phase hit 8 different 16-byte bank groups.
-        const uint32_t cb = unit + 2048 + lane * 64;
-        const int rot = (lane >> 1) & 3;
-#pragma unroll
-        for (int t = 0; t < 4; ++t) {
-            const int q = (t + rot) & 3;
-            uint32_t w[4];
-#pragma unroll
-            for (int i = 0; i < 4; ++i)
-                w[i] = q == 0 ? cc_lo[i] : q == 1 ? cc_lo[4 + i] : q == 2 ? cc_hi[i] : cc_hi[4 + i];
-            sts128(cb + 16 * q, w[0], w[1], w[2], w[3]);
-        }
+        const uint32_t cb = unit + 2048 + lane * 64;        // column 2 lane, then 2 lane + 1: 32 bytes each
+        sts128(cb, cc_lo[0], cc_lo[1], cc_lo[2], cc_lo[3]);
+        sts128(cb + 16, cc_lo[4], cc_lo[5], cc_lo[6], cc_lo[7]);
+        sts128(cb + 32, cc_hi[0], cc_hi[1], cc_hi[2], cc_hi[3]);
+        sts128(cb + 48, cc_hi[4], cc_hi[5], cc_hi[6], cc_hi[7]);
         if (2 * lane < valid) {                               // valid is a multiple of 32
             uint8_t* sp = p.s_col + (c0 + 2 * lane) * p.ld_s_col + (r0 >> 5);
             st_global_u8(sp, s_lo);
@@ -389,6 +402,7 @@ ln_apply_kernel(const __grid_constant__ CUtensorMap x_map, const __grid_constant
         reinterpret_cast<float2*>(area + kUnitRows * 16 + kUnitCols * 4)[lane] = make_float2(bf16_lo(b2), bf16_hi(b2));
     };
 
+    const uint64_t policy = l2_policy_evict_first();
     if (lane == 0) {
         tma_prefetch_desc(&x_map);
         if (kRowwise) tma_prefetch_desc(&qrow_map);
@@ -400,7 +414,7 @@ ln_apply_kernel(const __grid_constant__ CUtensorMap x_map, const __grid_constant
             origin(s, r0, c0);
             const uint32_t bar = smem_u32(&bars[warp][s]);
             mbar_arrive_expect_tx(bar, kUnitBytes);
-            tma_load_2d(ring + s * kUnitBytes, &x_map, bar, int32_t(c0), int32_t(r0));
+            tma_load_2d_hint(ring + s * kUnitBytes, &x_map, bar, int32_t(c0), int32_t(r0), policy);
         }
     }
     {
@@ -442,7 +456,7 @@ ln_apply_kernel(const __grid_constant__ CUtensorMap x_map, const __grid_constant
                 int64_t rn, cn;
                 origin(i + kApplyStages, rn, cn);
                 mbar_arrive_expect_tx(bar, kUnitBytes);
-                tma_load_2d(unit, &x_map, bar, int32_t(cn), int32_t(rn));
+                tma_load_2d_hint(unit, &x_map, bar, int32_t(cn), int32_t(rn), policy);
             }
         }
         __syncwarp();
