@@ -543,3 +543,75 @@ def mx_admissible(y, err, q, s, axis: int):
     amb = (c_lo != c_hi) | np.broadcast_to((e_lo != e_hi)[:, :, None], code_ok.shape)
     amb = amb & ~bad[:, :, None]
     return ok.reshape(rows, n), amb.reshape(rows, n)
+
+
+# --------------------------------------------------------------------------
+# Grouped wgrad for MoE experts (the second expert GEMM of training)
+# --------------------------------------------------------------------------
+#
+# Expert e owns rows [R_e, R_e + m_e) of the token-major activations X and of
+# the output gradient dY (ROCm/TransformerEngine README, "Single-Launch Grouped
+# GEMM Backends on ROCm": one launch over the experts of a MoE layer).  Its weight gradient
+# is dW_e = dY_e^T X_e, a TN GEMM whose reduction axis is the expert's tokens,
+# so both operands are column-wise MXFP8 copies of dY_e and X_e, blocked
+# along tokens.  Blocks must not cross an expert boundary, so each expert's
+# tokens are zero-padded to Kp_e = round_up(m_e, 128) (128 tokens = one K-step
+# of the GEMM).  Layout (reading: any layout that keeps experts apart works;
+# this one keeps each expert's operand a strided slice of one array):
+#   codes : q[c][P_e + t],  P_e = sum_{e' < e} Kp_e'          (t < Kp_e)
+#   scales: s[c][Q_e + b],  Q_e = sum_{e' < e} round_up(Kp_e' / 32, 16)   (b < Kp_e / 32)
+# (scale rows start on 16-byte boundaries, the alignment of a tensor copy).
+# Padding tokens are zeros: their blocks get scale 0x00 and code 0.
+
+WGRAD_PAD = 128
+
+
+def grouped_layout(group_m, pad: int = WGRAD_PAD):
+    """(Kp [G], P [G], Q [G], total codes width, total scale width)."""
+    m = np.asarray(group_m, dtype=np.int64)
+    kp = -(-m // pad) * pad
+    P = np.concatenate([[0], np.cumsum(kp)[:-1]]) if len(m) else np.zeros(0, np.int64)
+    sw = -(-(kp // MX_BLOCK) // 16) * 16
+    Q = np.concatenate([[0], np.cumsum(sw)[:-1]]) if len(m) else np.zeros(0, np.int64)
+    return kp, P.astype(np.int64), Q.astype(np.int64), int(kp.sum()), int(sw.sum())
+
+
+def quantize_colwise_grouped(x_bits, group_m, pad: int = WGRAD_PAD):
+    """Per-expert column-wise MXFP8 of the token-major matrix x [T, C] (bf16
+    bits), each expert zero-padded to Kp_e tokens.  Returns (q [C, TP], s [C,
+    TS]) in the layout above; scale bytes between Kp_e / 32 and the next
+    16-byte boundary are 0 here (they are never read)."""
+    x = np.asarray(x_bits, dtype=np.uint16)
+    cols = x.shape[1]
+    kp, P, Q, tp, ts = grouped_layout(group_m, pad)
+    q = np.zeros((cols, tp), np.uint8)
+    s = np.zeros((cols, ts), np.uint8)
+    r = 0
+    for e, m in enumerate(int(v) for v in group_m):
+        if kp[e] == 0:
+            continue
+        xe = np.zeros((kp[e], cols), np.uint16)               # bf16 +0 padding
+        xe[:m] = x[r:r + m]
+        qe, se = quantize_colwise(xe)
+        q[:, P[e]:P[e] + kp[e]] = qe
+        s[:, Q[e]:Q[e] + kp[e] // MX_BLOCK] = se
+        r += m
+    return q, s
+
+
+def mx_grouped_wgrad(qa, sa, qb, sb, group_m, pad: int = WGRAD_PAD) -> dict:
+    """dW_e = deq(A_e) deq(B_e)^T for every expert, A = the grouped column-wise
+    copy of dY ([N, TP]), B that of X ([K, TP]).  Returns {"d": [G, N, K]
+    (bf16-rounded), "pre": fp64, "sigma": [G, N, K]}; an expert without tokens
+    gets zeros."""
+    kp, P, Q, _, _ = grouped_layout(group_m, pad)
+    G, n, k = len(kp), qa.shape[0], qb.shape[0]
+    pre = np.zeros((G, n, k))
+    sigma = np.zeros((G, n, k))
+    for e in range(G):
+        if kp[e] == 0:
+            continue
+        nb = kp[e] // MX_BLOCK
+        r = mx_gemm(qa[:, P[e]:P[e] + kp[e]], sa[:, Q[e]:Q[e] + nb], qb[:, P[e]:P[e] + kp[e]], sb[:, Q[e]:Q[e] + nb])
+        pre[e], sigma[e] = r["pre"], r["sigma"]
+    return {"pre": pre, "d": bf16_round(pre), "sigma": sigma}
