@@ -48,6 +48,7 @@ def load_peaks():
 
 
 KERNEL_SOURCES = {"gemm": ["gemm.cu", "ptx.cuh"], "quant": ["quantize.cu", "e4m3.cuh", "ptx.cuh"],
+                  "grouped": ["grouped_quantize.cu", "e4m3.cuh", "ptx.cuh"],
                   "block": ["block_quantize.cu", "e4m3.cuh", "ptx.cuh"],
                   "ln": ["layernorm_quantize.cu", "e4m3.cuh", "ptx.cuh"]}
 
@@ -149,6 +150,9 @@ class Step:
         d = self.d
         from mxfp8_block_scaled_quantize_gb300 import workloads
         d["ln_g"], d["ln_b"] = (t.to(dev) for t in workloads.layernorm_params(host["ffn_X"].shape[1], 410))
+        # the MoE output gradient for the expert wgrad row (made on the device side
+        # only: it is not an input of the timed step)
+        d["moe_dY"] = workloads.normal_bf16((int(host["moe_m"].sum()), 1536), 1e-3, 503).to(dev)
         e = lambda *s, dt=torch.uint8: torch.empty(*s, dtype=dt, device=dev)
         pitch = temx.te_mx_scale_pitch
         T, H, F = 8192, 7168, 18432
@@ -199,7 +203,14 @@ class Step:
         self.next_bytes = {"quant_dbias_ffn_dy": qb(T, F, True) + 2.0 * F,
                            "block_quant_ffn_x": qb(T, H, True), "block_quant_ffn_w": qb(F, H, True),
                            "block_quant_ffn_dy": qb(T, F, True),
-                           "ln_quant_ffn_x": qb(T, H, True) + 8.0 * T + 4.0 * H}
+                           "ln_quant_ffn_x": qb(T, H, True) + 8.0 * T + 4.0 * H,
+                           "grouped_quant_moe_x": qb(MT, K, False), "grouped_quant_moe_dy": qb(MT, N, False)}
+        self.next_flops["gemm_moe_wgrad"] = 2.0 * float(counts.sum()) * N * K
+        # MoE expert wgrad: per-expert column-wise copies of X and dY, then dW_e = dY_e^T X_e
+        gdev = d["moe_m"].to(torch.int32)
+        o["gx"] = temx.quantize_colwise_grouped(d["moe_X"], gdev)
+        o["gdy"] = temx.quantize_colwise_grouped(d["moe_dY"], gdev)
+        o["dw"] = e(G, N, K, dt=torch.bfloat16)
         # Float8BlockScaling (E8M0-cast scales) quantisation of the same tensors:
         # 1x128 / 128x1 blocks for X and dY, 128x128 blocks for W (both copies).
         # LayerNorm -> MXFP8 of the ffn input (both orientations + mu / rsigma);
@@ -220,6 +231,9 @@ class Step:
             ("block_quant_ffn_dy", lambda: temx.block_quantize(d["ffn_dY"], False, True, True, out=o["dy_b"])),
             ("ln_quant_ffn_x", lambda: temx.layernorm_quantize(d["ffn_X"], d["ln_g"], d["ln_b"], 1e-5, True, True,
                                                                out=o["ln"])),
+            ("grouped_quant_moe_x", lambda: temx.quantize_colwise_grouped(d["moe_X"], gdev, out=o["gx"])),
+            ("grouped_quant_moe_dy", lambda: temx.quantize_colwise_grouped(d["moe_dY"], gdev, out=o["gdy"])),
+            ("gemm_moe_wgrad", lambda: temx.grouped_gemm_wgrad(gdev, MT, o["gdy"], o["gx"], out=o["dw"])),
         ]
         temx.quantize(d["ffn_W"], False, True, out=o["w_col"])
 
@@ -395,6 +409,7 @@ CASES = {
     "block_quant_x": "Float8BlockScaling ffn X [8192x7168], 1x128 and 128x1 blocks, both orientations",
     "block_quant_w": "Float8BlockScaling ffn W [18432x7168], 128x128 blocks, both orientations",
     "ln_quant_x": "LayerNorm -> MXFP8 of ffn X [8192x7168], both orientations + mu/rsigma",
+    "gemm_moe_wgrad": "moe expert wgrad dW_e = dY_e^T X_e, 128 experts, 1536 x 4096, per-expert column-wise operands",
     "gemm_fc1": "fc1 fprop 4096x4096x1024, bias + GELU + AUX",
     "gemm_ffn": "ffn fprop 8192x18432x7168, bias + GELU + AUX",
     "gemm_wgrad": "ffn wgrad 18432x7168x8192 on column-wise operands",
@@ -411,6 +426,8 @@ def run_case(case: str, reps: int):
         w = workloads.make_ffn()
     elif case == "gemm_fc1":
         w = workloads.make_fc1()
+    elif case == "gemm_moe_wgrad":
+        w = None
     else:
         w = workloads.make_moe()
     if case == "quant_both":
@@ -438,6 +455,13 @@ def run_case(case: str, reps: int):
         qd = temx.quantize(w["dY"].to(dev), False, True)
         qx = temx.quantize(w["X"].to(dev), False, True)
         fn = lambda: temx.gemm(qd["q_col"], qd["s_col"], qx["q_col"], qx["s_col"])
+    elif case == "gemm_moe_wgrad":
+        g = workloads.make_moe_wgrad()
+        gm = g["group_m"].to(torch.int32).to(dev)
+        gx = temx.quantize_colwise_grouped(g["X"].to(dev), gm)
+        gdy = temx.quantize_colwise_grouped(g["dY"].to(dev), gm)
+        total = int(g["group_m"].sum())
+        fn = lambda: temx.grouped_gemm_wgrad(gm, total, gdy, gx)
     else:
         qx = temx.quantize(w["X"].to(dev), True, False)
         qw = temx.quantize(w["W"].view(128 * 1536, 4096).to(dev), True, False)

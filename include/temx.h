@@ -250,6 +250,56 @@ TEMX_API te_mx_status te_mx_grouped_gemm(int32_t num_groups, const int32_t* grou
                                 void* workspace, size_t workspace_bytes,
                                 void* stream);
 
+/* Grouped wgrad for MoE experts (the single-launch grouped GEMM of
+ * "Single-Launch Grouped GEMM Backends on ROCm", ROCm/TransformerEngine
+ * README, applied to the weight gradient dW_e = dY_e^T X_e).
+ *
+ * Layout of a per-expert column-wise operand.  Expert e owns rows
+ * [R_e, R_e + m_e) of a token-major matrix x [total x cols]; its copy is
+ * blocked along tokens (32 per E8M0 scale) and zero-padded to
+ * Kp_e = round_up(m_e, 128) tokens, so no block crosses an expert boundary:
+ *   q[c][P_e + t], t < Kp_e     P_e = sum_{e'<e} Kp_e'
+ *   s[c][Q_e + b], b < Kp_e/32  Q_e = sum_{e'<e} round_up(Kp_e'/32, 16)
+ * (codes of padding tokens are 0, their block scales 0x00).  Expert sizes
+ * live on the device, so the widths are bounded on the host:
+ * te_mx_grouped_code_width / te_mx_grouped_scale_width give pitches (row
+ * lengths in bytes) that always suffice for total_m tokens in num_groups
+ * experts. */
+TEMX_API int64_t te_mx_grouped_code_width(int64_t total_m, int32_t num_groups);
+TEMX_API int64_t te_mx_grouped_scale_width(int64_t total_m, int32_t num_groups);
+
+/* te_mx_quantize_colwise_grouped — the per-expert column-wise MXFP8 copy
+ * above of x (bf16 [total_m x cols], pitch ld_x; rows grouped by expert in
+ * order; group_m: device int32 [num_groups] token counts, sum <= total_m).
+ *   q  uint8 [cols x ld_q]: codes;  s  uint8 [cols x ld_s]: scales.
+ * Rules: 1 <= num_groups <= 1024; cols % 32 == 0; x, q 16-byte aligned;
+ * ld_x % 8 == 0; ld_q, ld_s multiples of 16.  Bytes of q / s past the layout's
+ * width, and scale bytes between Kp_e/32 and Q_{e+1}, are not written.
+ * A negative count, counts summing above total_m or a layout wider than
+ * ld_q / ld_s write nothing and make te_mx_device_status() report
+ * TE_MX_ERR_INVALID_ARG.  Output is bit-exact to the definition above. */
+TEMX_API te_mx_status te_mx_quantize_colwise_grouped(const void* x, int64_t total_m, int64_t cols, int64_t ld_x,
+                                                     int32_t num_groups, const int32_t* group_m,
+                                                     uint8_t* q, int64_t ld_q, uint8_t* s, int64_t ld_s,
+                                                     void* stream);
+
+/* te_mx_grouped_gemm_wgrad — dW_e = deq(dY_e)^T deq(X_e) for every expert in
+ * one launch (fp32 accumulation on the tensor cores, bf16 output):
+ *   dY, s_dY   per-expert column-wise copy of dY [total_m x M]: [M x ld_q], [M x ld_s];
+ *   X,  s_X    per-expert column-wise copy of X  [total_m x N]: [N x ld_q], [N x ld_s];
+ *   D          bf16 [num_groups x M x N] (device): D[e] = dW_e; an expert
+ *              without tokens gets zeros.
+ * group_m and total_m as for te_mx_quantize_colwise_grouped (the same device
+ * array that laid the operands out).  Rules: 1 <= num_groups <= 1024;
+ * N % 16 == 0; ld_q, ld_s multiples of 16 (ld_s >= 16); num_groups * M <
+ * 2^31; dY, X, D 16-byte aligned.  Device-side errors as above (nothing is
+ * written).  Accuracy as te_mx_gemm. */
+TEMX_API te_mx_status te_mx_grouped_gemm_wgrad(int32_t num_groups, const int32_t* group_m, int64_t total_m,
+                                               const uint8_t* dY, const uint8_t* s_dY,
+                                               const uint8_t* X, const uint8_t* s_X,
+                                               int64_t M, int64_t N, int64_t ld_q, int64_t ld_s,
+                                               void* D, void* stream);
+
 /* Workspace bytes te_mx_gemm / te_mx_grouped_gemm need: 0 for every shape
  * (scale re-layout happens in shared memory; kept so a future layout change
  * does not break the ABI). */

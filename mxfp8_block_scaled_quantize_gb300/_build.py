@@ -12,7 +12,7 @@ ROOT = os.path.dirname(PKG)
 CSRC = os.path.join(PKG, "csrc")
 BUILD = os.path.join(PKG, "_build")
 LIB = os.path.join(PKG, "libtemx.so")
-SOURCES = ["api.cu", "quantize.cu", "block_quantize.cu", "layernorm_quantize.cu", "gemm.cu"]
+SOURCES = ["api.cu", "quantize.cu", "block_quantize.cu", "layernorm_quantize.cu", "grouped_quantize.cu", "gemm.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ["-O3", "-std=c++17", "-lineinfo", "-Xcompiler", "-fPIC", "-Xcompiler", "-fvisibility=hidden",
          "-I", os.path.join(ROOT, "include"), "--expt-relaxed-constexpr"]

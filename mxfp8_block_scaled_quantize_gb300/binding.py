@@ -29,6 +29,10 @@ SIGNATURES = {
     "te_mx_block_quantize": (ctypes.c_int, [_P, _I64, _I64, _I64, _I32, _P, _P, _I64, _P, _P, _I64, _P]),
     "te_mx_layernorm_quantize": (ctypes.c_int, [_P, _I64, _I64, _I64, _P, _P, ctypes.c_float, _P, _P, _I64, _P,
                                                 _P, _I64, _P, _P, _P]),
+    "te_mx_grouped_code_width": (_I64, [_I64, _I32]),
+    "te_mx_grouped_scale_width": (_I64, [_I64, _I32]),
+    "te_mx_quantize_colwise_grouped": (ctypes.c_int, [_P, _I64, _I64, _I64, _I32, _P, _P, _I64, _P, _I64, _P]),
+    "te_mx_grouped_gemm_wgrad": (ctypes.c_int, [_I32, _P, _I64, _P, _P, _P, _P, _I64, _I64, _I64, _I64, _P, _P]),
     "te_mx_quantize_dbias_workspace_size": (_SZ, [_I64, _I64]),
     "te_mx_quantize_dbias": (ctypes.c_int, [_P, _I64, _I64, _I64, _P, _P, _I64, _P, _P, _I64, _P, _P, _SZ, _P]),
     "te_mx_quantize_dbias_noalloc": (ctypes.c_int, [_P, _I64, _I64, _I64, _P, _P, _I64, _P, _P, _I64, _P, _P]),
@@ -92,6 +96,24 @@ def te_mx_layernorm_quantize(x, rows, hidden, ld_x, gamma, beta, eps, q_row, s_r
                              ld_s_col, mu, rsigma, stream) -> None:
     _check(lib().te_mx_layernorm_quantize(x, rows, hidden, ld_x, gamma, beta, eps, q_row, s_row, ld_s_row, q_col,
                                           s_col, ld_s_col, mu, rsigma, stream))
+
+
+def te_mx_grouped_code_width(total_m, num_groups) -> int:
+    return lib().te_mx_grouped_code_width(total_m, num_groups)
+
+
+def te_mx_grouped_scale_width(total_m, num_groups) -> int:
+    return lib().te_mx_grouped_scale_width(total_m, num_groups)
+
+
+def te_mx_quantize_colwise_grouped(x, total_m, cols, ld_x, num_groups, group_m, q, ld_q, s, ld_s, stream) -> None:
+    _check(lib().te_mx_quantize_colwise_grouped(x, total_m, cols, ld_x, num_groups, group_m, q, ld_q, s, ld_s,
+                                                stream))
+
+
+def te_mx_grouped_gemm_wgrad(num_groups, group_m, total_m, dY, s_dY, X, s_X, M, N, ld_q, ld_s, D, stream) -> None:
+    _check(lib().te_mx_grouped_gemm_wgrad(num_groups, group_m, total_m, dY, s_dY, X, s_X, M, N, ld_q, ld_s, D,
+                                          stream))
 
 
 def te_mx_quantize_dbias_workspace_size(rows, cols) -> int:
@@ -231,6 +253,40 @@ def layernorm_quantize(x, gamma, beta, eps: float = 1e-5, rowwise: bool = True, 
                              _ptr(o.get("q_col")), _ptr(o.get("s_col")), o["s_col"].stride(0) if "s_col" in o else 0,
                              _ptr(o.get("mu")), _ptr(o.get("rsigma")), _stream_ptr(stream))
     return o
+
+
+def quantize_colwise_grouped(x, group_m, stream=None, out=None):
+    """Per-expert column-wise MXFP8 copy of the token-major bf16 CUDA tensor x
+    [total_m, cols] (experts' rows in order, ``group_m``: int32 CUDA tensor of
+    token counts).  Returns {"q": uint8 [cols, ld_q], "s": uint8 [cols, ld_s]}
+    in the padded per-expert layout (widths from te_mx_grouped_*_width)."""
+    import torch
+    assert x.dtype == torch.bfloat16 and x.dim() == 2 and x.is_cuda and x.stride(1) == 1
+    assert group_m.dtype == torch.int32 and group_m.is_cuda
+    total_m, cols = x.shape
+    G = group_m.numel()
+    o = dict(out or {})
+    if "q" not in o:
+        o["q"] = torch.empty(cols, te_mx_grouped_code_width(total_m, G), dtype=torch.uint8, device=x.device)
+        o["s"] = torch.empty(cols, te_mx_grouped_scale_width(total_m, G), dtype=torch.uint8, device=x.device)
+    te_mx_quantize_colwise_grouped(x.data_ptr(), total_m, cols, x.stride(0), G, group_m.data_ptr(), o["q"].data_ptr(),
+                                   o["q"].stride(0), o["s"].data_ptr(), o["s"].stride(0), _stream_ptr(stream))
+    return o
+
+
+def grouped_gemm_wgrad(group_m, total_m, dy, x, stream=None, out=None):
+    """dW_e = dY_e^T X_e for every expert: ``dy`` and ``x`` are the dicts of
+    quantize_colwise_grouped of dY [total_m, M] and X [total_m, N] (same
+    group_m).  Returns bf16 [G, M, N] (``out`` if given)."""
+    import torch
+    G = group_m.numel()
+    M, N = dy["q"].shape[0], x["q"].shape[0]
+    assert dy["q"].stride(0) == x["q"].stride(0) and dy["s"].stride(0) == x["s"].stride(0)
+    d = out if out is not None else torch.empty(G, M, N, dtype=torch.bfloat16, device=dy["q"].device)
+    te_mx_grouped_gemm_wgrad(G, group_m.data_ptr(), total_m, dy["q"].data_ptr(), dy["s"].data_ptr(), x["q"].data_ptr(),
+                             x["s"].data_ptr(), M, N, dy["q"].stride(0), dy["s"].stride(0), d.data_ptr(),
+                             _stream_ptr(stream))
+    return d
 
 
 def gemm(qa, sa, qb, sb, bias=None, gelu: bool = False, stream=None, out=None, dgelu_aux=None):

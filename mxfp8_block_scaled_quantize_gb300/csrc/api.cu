@@ -273,6 +273,73 @@ te_mx_status te_mx_layernorm_quantize(const void* x, int64_t rows, int64_t hidde
     return ln_quantize_launch(a, static_cast<cudaStream_t>(stream));
 }
 
+int64_t te_mx_grouped_code_width(int64_t total_m, int32_t num_groups) {
+    if (total_m < 0 || num_groups < 0) return 0;
+    return grouped_code_width(total_m, num_groups);
+}
+
+int64_t te_mx_grouped_scale_width(int64_t total_m, int32_t num_groups) {
+    if (total_m < 0 || num_groups < 0) return 0;
+    const int64_t w = grouped_scale_width(total_m, num_groups);
+    return w < 16 ? 16 : w;
+}
+
+te_mx_status te_mx_quantize_colwise_grouped(const void* x, int64_t total_m, int64_t cols, int64_t ld_x,
+                                            int32_t num_groups, const int32_t* group_m,
+                                            uint8_t* q, int64_t ld_q, uint8_t* s, int64_t ld_s, void* stream) {
+    t_last_error[0] = '\0';
+    if (num_groups < 1 || num_groups > 1024)
+        return set_error(TE_MX_ERR_INVALID_ARG, "num_groups=%d must be in [1, 1024]", int(num_groups));
+    if (!group_m || !q || !s) return set_error(TE_MX_ERR_INVALID_ARG, "group_m, q and s are required");
+    if (total_m < 0 || cols < 0) return set_error(TE_MX_ERR_INVALID_ARG, "negative size");
+    if (cols % 32) return set_error(TE_MX_ERR_UNSUPPORTED_SHAPE, "cols=%lld is not a multiple of 32", (long long)cols);
+    if (total_m > (int64_t(1) << 31) - 1024 || cols > (int64_t(1) << 31) - 64)
+        return set_error(TE_MX_ERR_UNSUPPORTED_SHAPE, "a dimension exceeds 2^31");
+    if (ld_q % 16 || ld_q <= 0 || ld_s % 16 || ld_s <= 0)
+        return set_error(TE_MX_ERR_MISALIGNED, "ld_q=%lld and ld_s=%lld must be positive multiples of 16",
+                         (long long)ld_q, (long long)ld_s);
+    if (cols == 0) return check_device(nullptr);
+    if (total_m > 0 && (!x || ld_x < cols || ld_x % 8 || !aligned(x, 16)))
+        return set_error(TE_MX_ERR_MISALIGNED, "x must be 16-byte aligned with ld_x >= cols, ld_x %% 8 == 0");
+    if (!aligned(q, 16)) return set_error(TE_MX_ERR_MISALIGNED, "q is not 16-byte aligned");
+    te_mx_status st = check_device(nullptr);
+    if (st != TE_MX_OK) return st;
+    GroupedColwiseArgs a{x, total_m, cols, ld_x > 0 ? ld_x : cols, num_groups, group_m, q, ld_q, s, ld_s};
+    return grouped_colwise_launch(a, static_cast<cudaStream_t>(stream));
+}
+
+te_mx_status te_mx_grouped_gemm_wgrad(int32_t num_groups, const int32_t* group_m, int64_t total_m,
+                                      const uint8_t* dY, const uint8_t* s_dY, const uint8_t* X, const uint8_t* s_X,
+                                      int64_t M, int64_t N, int64_t ld_q, int64_t ld_s, void* D, void* stream) {
+    t_last_error[0] = '\0';
+    if (num_groups < 1 || num_groups > 1024)
+        return set_error(TE_MX_ERR_INVALID_ARG, "num_groups=%d must be in [1, 1024]", int(num_groups));
+    if (!group_m || !dY || !s_dY || !X || !s_X || !D)
+        return set_error(TE_MX_ERR_INVALID_ARG, "group_m, dY, s_dY, X, s_X and D are required");
+    if (total_m < 0 || M < 0 || N < 0) return set_error(TE_MX_ERR_INVALID_ARG, "negative size");
+    if (N % 16) return set_error(TE_MX_ERR_UNSUPPORTED_SHAPE, "N=%lld is not a multiple of 16", (long long)N);
+    if (int64_t(num_groups) * M >= (int64_t(1) << 31) || N > (int64_t(1) << 31) - 256)
+        return set_error(TE_MX_ERR_UNSUPPORTED_SHAPE, "num_groups * M or N exceeds 2^31");
+    if (ld_q % 16 || ld_q <= 0 || ld_s % 16 || ld_s < 16)
+        return set_error(TE_MX_ERR_MISALIGNED, "ld_q=%lld must be a positive multiple of 16 and ld_s=%lld a "
+                         "multiple of 16 >= 16", (long long)ld_q, (long long)ld_s);
+    if (!aligned(dY, 16) || !aligned(X, 16) || !aligned(D, 16))
+        return set_error(TE_MX_ERR_MISALIGNED, "dY, X and D must be 16-byte aligned");
+    te_mx_status st = check_device(nullptr);
+    if (st != TE_MX_OK || M == 0 || N == 0) return st;
+    GemmArgs a{};
+    a.A = dY; a.sA = s_dY; a.ld_sA = ld_s;
+    a.B = X; a.sB = s_X; a.ld_sB = ld_s;
+    a.M = M; a.N = N; a.K = 0;
+    a.D = D;
+    a.groups = num_groups;
+    a.group_m = group_m;
+    a.wgrad = true;
+    a.ld_code = ld_q;
+    a.total_m = total_m;
+    return gemm_launch(a, static_cast<cudaStream_t>(stream));
+}
+
 size_t te_mx_quantize_dbias_workspace_size(int64_t rows, int64_t cols) {
     if (rows <= 0 || cols <= 0) return 0;
     return size_t((rows + kDbiasBandRows - 1) / kDbiasBandRows) * size_t(cols) * sizeof(float);

@@ -107,17 +107,23 @@ struct GemmParams {
     uint16_t* D;
     uint16_t* aux;
     bool has_bias, gelu, dgelu;          // dgelu: aux is an input (forward pre-activation)
+    bool wgrad;                          // grouped wgrad: per-group K range, D = [groups x M x N]
+    int64_t total_m;                     // wgrad: bound on the token counts' sum
+    int64_t ld_code, ld_sfa, ld_sfb;     // wgrad: operand pitches (capacities)
     unsigned int* status;
 };
 
 __device__ __forceinline__ int64_t imin64(int64_t a, int64_t b) { return a < b ? a : b; }
 
 struct Tile {
-    int32_t a_row;           // first row of the (pair) tile
-    int32_t row_end;         // rows >= row_end are not stored
+    int32_t a_row;           // first A row of the (pair) tile
+    int32_t d_row;           // first output row (= a_row except for wgrad)
+    int32_t row_end;         // output rows >= row_end are not stored
     int32_t n0;              // first output column
     int32_t b_row;           // first B row of the tile
     int32_t group;           // bias / B group
+    int32_t k0, nk;          // K-steps [k0, k0 + nk) of 128
+    int32_t sf0;             // first scale column (bytes, a multiple of 16)
 };
 
 // Shared state besides the stage ring.
@@ -142,11 +148,29 @@ struct __align__(16) SharedState {
 // Linear tile index -> tile.  Dense: bands of kGroupM m-tiles, n-major inside
 // a band, so the CTAs running at one time share a few A row-bands and B
 // column-bands in L2.  Grouped: group-major, then n-major over the group's
-// m-tiles.  `hint` carries the group found last time (tiles increase).
+// m-tiles.  Wgrad: group-major, every group the full M x N output over its
+// own K range.  `hint` carries the group found last time (tiles increase).
 template <int kTileM, typename SH>
 __device__ __forceinline__ Tile map_tile(const GemmParams& p, const SH& sh, int64_t t, int32_t& hint) {
     Tile tl;
-    if (p.groups == 0) {
+    tl.k0 = 0;
+    tl.nk = p.k_iters;
+    tl.sf0 = 0;
+    if (p.wgrad) {
+        const int64_t per = int64_t(p.m_tiles) * p.n_tiles;
+        const int32_t g = int32_t(t / per);
+        const int32_t local = int32_t(t - int64_t(g) * per);
+        const int32_t mt = local % p.m_tiles, nt = local / p.m_tiles;
+        tl.a_row = mt * kTileM;
+        tl.d_row = int32_t(int64_t(g) * p.M + tl.a_row);
+        tl.row_end = int32_t(int64_t(g) * p.M + imin64(p.M, int64_t(tl.a_row) + kTileM));
+        tl.n0 = nt * kBN;
+        tl.b_row = tl.n0;
+        tl.group = g;
+        tl.k0 = sh.row_start[g];
+        tl.nk = sh.row_start[g + 1] - sh.row_start[g];
+        tl.sf0 = sh.tile_start[g];
+    } else if (p.groups == 0) {
         const int64_t per_band = int64_t(kGroupM) * p.n_tiles;
         const int64_t band = t / per_band;
         const int32_t first_m = int32_t(band * kGroupM);
@@ -155,6 +179,7 @@ __device__ __forceinline__ Tile map_tile(const GemmParams& p, const SH& sh, int6
         const int32_t mt = first_m + int32_t(local % gm);
         const int32_t nt = int32_t(local / gm);
         tl.a_row = mt * kTileM;
+        tl.d_row = tl.a_row;
         tl.row_end = int32_t(imin64(p.M, int64_t(tl.a_row) + kTileM));
         tl.n0 = nt * kBN;
         tl.b_row = tl.n0;
@@ -168,6 +193,7 @@ __device__ __forceinline__ Tile map_tile(const GemmParams& p, const SH& sh, int6
         const int32_t mtg = (rows + kTileM - 1) / kTileM;
         const int32_t mt = local % mtg, nt = local / mtg;
         tl.a_row = sh.row_start[g] + mt * kTileM;
+        tl.d_row = tl.a_row;
         tl.row_end = min(sh.row_start[g + 1], tl.a_row + kTileM);
         tl.n0 = nt * kBN;
         tl.b_row = g * p.N + tl.n0;
@@ -226,6 +252,52 @@ __device__ void group_prefix(const GemmParams& p, SH& sh, int lane) {
         sh.grouped_tiles = tincl;
     }
     if (__any_sync(0xFFFFFFFFu, bad) && lane == 0) set_device_status(p.status, kStatusBadArg);
+}
+
+// Wgrad launch (one warp): expert g's padded tokens are K-steps
+// [row_start[g], row_start[g+1]) of 128, its scales start at byte
+// tile_start[g] (16-byte aligned): Kp_g = round_up(m_g, 128), scale width
+// round_up(Kp_g / 32, 16).  A negative size, a sum above total_m or a layout
+// wider than the operand pitches sets the status word and leaves no tiles.
+template <typename SH>
+__device__ void wgrad_prefix(const GemmParams& p, SH& sh, int lane) {
+    const int G = p.groups;
+    const int per = (G + 31) / 32;
+    const int lo = min(G, lane * per), hi = min(G, lo + per);
+    bool bad = false;
+    int64_t toks = 0, steps = 0, sfw = 0;
+    for (int g = lo; g < hi; ++g) {
+        const int64_t m = p.group_m[g];
+        bad |= m < 0;
+        const int64_t ks = (m < 0 ? 0 : m + 127) / 128;
+        toks += m < 0 ? 0 : m;
+        steps += ks;
+        sfw += (4 * ks + 15) / 16 * 16;
+    }
+    int64_t t_in = toks, k_in = steps, s_in = sfw;
+    for (int o = 1; o < 32; o <<= 1) {
+        const int64_t a = __shfl_up_sync(0xFFFFFFFFu, t_in, o), b = __shfl_up_sync(0xFFFFFFFFu, k_in, o),
+                      c = __shfl_up_sync(0xFFFFFFFFu, s_in, o);
+        if (lane >= o) { t_in += a; k_in += b; s_in += c; }
+    }
+    int64_t k0 = k_in - steps, s0 = s_in - sfw;
+    for (int g = lo; g < hi; ++g) {
+        const int64_t m = p.group_m[g];
+        const int64_t ks = (m < 0 ? 0 : m + 127) / 128;
+        sh.row_start[g] = int32_t(k0);
+        sh.tile_start[g] = int32_t(s0);
+        k0 += ks;
+        s0 += (4 * ks + 15) / 16 * 16;
+    }
+    const int64_t tt = __shfl_sync(0xFFFFFFFFu, t_in, 31), kt = __shfl_sync(0xFFFFFFFFu, k_in, 31),
+                  st = __shfl_sync(0xFFFFFFFFu, s_in, 31);
+    bad = __any_sync(0xFFFFFFFFu, bad) || tt > p.total_m || kt * kBK > p.ld_code || st > p.ld_sfa || st > p.ld_sfb;
+    if (lane == 0) {
+        sh.row_start[G] = int32_t(kt);
+        sh.tile_start[G] = int32_t(st);
+        sh.grouped_tiles = bad ? 0 : int64_t(G) * p.m_tiles * p.n_tiles;
+        if (bad) set_device_status(p.status, kStatusBadArg);
+    }
 }
 
 // Bounded mbarrier wait that also returns false once another role aborted.
@@ -468,7 +540,10 @@ gemm_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_constant__ C
         }
         tc_fence_before();
     }
-    if (p.groups > 0 && warp == 2) group_prefix<C::kTileM>(p, sh, lane);
+    if (p.groups > 0 && warp == 2) {
+        if (p.wgrad) wgrad_prefix(p, sh, lane);
+        else group_prefix<C::kTileM>(p, sh, lane);
+    }
     __syncthreads();
     if constexpr (kPair == 2) cluster_sync();      // peer barriers initialised before any remote use
     tc_fence_after();
@@ -485,19 +560,20 @@ gemm_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_constant__ C
                 const Tile tl = map_tile<C::kTileM>(p, sh, t, hint);
                 const int32_t a_row = tl.a_row + int32_t(rank) * kBM;
                 const int32_t b_row = tl.b_row + int32_t(rank) * C::kBRows;
-                for (int32_t k = 0; k < p.k_iters; ++k) {
+                for (int32_t k = 0; k < tl.nk; ++k) {
+                    const int32_t kx = (tl.k0 + k) * kBK;
                     if (!wait_or_abort(smem_u32(&sh.empty[stage]), phase ^ 1u, sh, p.status)) { ok = false; break; }
                     uint8_t* st = smem + stage * C::kStageBytes;
                     const uint32_t full = leader(sh.full[stage]);
                     if constexpr (kPair == 2) {
                         if (rank == 0) mbar_arrive_expect_tx(smem_u32(&sh.full[stage]), C::kABytes + C::kBBytes);
                         else mbar_arrive_expect_tx_cluster_relaxed(full, C::kABytes + C::kBBytes);
-                        tma_load_2d_pair(smem_u32(st), &map_a, full, k * kBK, a_row);
-                        tma_load_2d_pair(smem_u32(st + C::kABytes), &map_b, full, k * kBK, b_row);
+                        tma_load_2d_pair(smem_u32(st), &map_a, full, kx, a_row);
+                        tma_load_2d_pair(smem_u32(st + C::kABytes), &map_b, full, kx, b_row);
                     } else {
                         mbar_arrive_expect_tx(full, C::kABytes + C::kBBytes);
-                        tma_load_2d(smem_u32(st), &map_a, full, k * kBK, a_row);
-                        tma_load_2d(smem_u32(st + C::kABytes), &map_b, full, k * kBK, b_row);
+                        tma_load_2d(smem_u32(st), &map_a, full, kx, a_row);
+                        tma_load_2d(smem_u32(st + C::kABytes), &map_b, full, kx, b_row);
                     }
                     if (++stage == C::kStages) { stage = 0; phase ^= 1u; }
                 }
@@ -507,14 +583,16 @@ gemm_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_constant__ C
         // ------------------------------------------------ MMA issuer (one lane of the MMA CTA)
         if (lane == 0 && rank == 0) {
             uint32_t stage = 0, phase = 0, grp = 0;   // grp: global index of the current scale group
-            int32_t local = 0;
+            int32_t local = 0, hint = 0;
             bool ok = true;
             for (int64_t t = unit; t < total && ok; t += units, ++local) {
+                // K-steps of this tile (wgrad: the expert's own; 0 for an expert without tokens)
+                const int32_t nk = p.wgrad ? map_tile<C::kTileM>(p, sh, t, hint).nk : p.k_iters;
                 if (local > 0) {
                     if (!wait_or_abort(smem_u32(&sh.tmem_empty), uint32_t(local - 1) & 1u, sh, p.status)) break;
                     tc_fence_after();
                 }
-                for (int32_t k = 0; k < p.k_iters; ++k) {
+                for (int32_t k = 0; k < nk; ++k) {
                     if (!wait_or_abort(smem_u32(&sh.full[stage]), phase, sh, p.status)) { ok = false; break; }
                     uint8_t* st = smem + stage * C::kStageBytes;
                     if ((k & 3) == 0) {
@@ -540,7 +618,7 @@ gemm_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_constant__ C
                     }
                     if constexpr (kPair == 2) tc_commit_pair_mc(smem_u32(&sh.empty[stage]), 0x3);
                     else tc_commit(smem_u32(&sh.empty[stage]));
-                    if ((k & 3) == 3 || k == p.k_iters - 1) {      // last K-step of the scale group
+                    if ((k & 3) == 3 || k == nk - 1) {             // last K-step of the scale group
                         if constexpr (kPair == 2) tc_commit_pair_mc(smem_u32(&sh.grp_done[grp % kSfTmemGroups]), 0x1);
                         else tc_commit(smem_u32(&sh.grp_done[grp % kSfTmemGroups]));
                         ++grp;
@@ -564,12 +642,18 @@ gemm_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_constant__ C
         // (sf_ready).  So every barrier phase here is observed by its waiter
         // before the barrier can complete again.
         uint8_t* ring = smem + C::kStages * C::kStageBytes;
-        const int32_t ngroups = (p.k_iters + 3) / 4;
+        auto tile_groups = [](const Tile& t) { return (t.nk + 3) / 4; };
         int64_t lt = unit;                // next group to load: tile lt, group lg
         int32_t lg = 0, lhint = 0;
         uint32_t jl = 0;                  // its global index
         Tile ltl{};
-        if (lt < total) ltl = map_tile<C::kTileM>(p, sh, lt, lhint);
+        auto seek = [&]() {               // the first tile from lt on that has scale groups
+            for (; lt < total; lt += units) {
+                ltl = map_tile<C::kTileM>(p, sh, lt, lhint);
+                if (tile_groups(ltl) > 0) break;
+            }
+        };
+        seek();
         bool ok = true;
         auto load_next = [&]() -> bool {  // lane 0
             if (lt >= total) return true;
@@ -580,13 +664,13 @@ gemm_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_constant__ C
             const uint32_t bar = smem_u32(&sh.sf_full[slot]);
             const uint32_t dst = smem_u32(ring + slot * kSfGroupBytes);
             mbar_arrive_expect_tx(bar, kSfGroupBytes);
-            tma_load_2d(dst, &map_sfa, bar, lg * 16, ltl.a_row + int32_t(rank) * kBM);
-            tma_load_2d(dst + kSFABytes, &map_sfb, bar, lg * 16, ltl.b_row);
+            tma_load_2d(dst, &map_sfa, bar, ltl.sf0 + lg * 16, ltl.a_row + int32_t(rank) * kBM);
+            tma_load_2d(dst + kSFABytes, &map_sfb, bar, ltl.sf0 + lg * 16, ltl.b_row);
             ++jl;
-            if (++lg == ngroups) {
+            if (++lg == tile_groups(ltl)) {
                 lg = 0;
                 lt += units;
-                if (lt < total) ltl = map_tile<C::kTileM>(p, sh, lt, lhint);
+                seek();
             }
             return true;
         };
@@ -594,7 +678,10 @@ gemm_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_constant__ C
             for (int i = 0; i < kSfAhead && ok; ++i) ok = load_next();
         ok = __shfl_sync(0xFFFFFFFFu, ok, 0);
         uint32_t j = 0;
+        int32_t chint = 0;
         for (int64_t t = unit; t < total && ok; t += units) {
+            const Tile ct = map_tile<C::kTileM>(p, sh, t, chint);
+            const int32_t ngroups = tile_groups(ct);
             for (int32_t g = 0; g < ngroups && ok; ++g, ++j) {
                 const uint32_t slot = j % kSfRing, bit = (j / kSfRing) & 1u;
                 if (!wait_or_abort(smem_u32(&sh.sf_full[slot]), bit, sh, p.status)) { ok = false; break; }
@@ -612,7 +699,7 @@ gemm_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_constant__ C
                                                ((j - 3) / kSfTmemGroups) & 1u, sh, p.status);
                         if (ok) {
                             tc_fence_after();
-                            const int nchunks = min(4, p.k_iters - 4 * g);
+                            const int nchunks = min(4, ct.nk - 4 * g);
                             for (int c = 0; c < nchunks; ++c) {
                                 const uint32_t col = tmem + kSfCol0 + ((j % kSfTmemGroups) * 4 + c) * kSfSlotCols;
                                 const uint64_t d0 = smem_desc(sf + c * 512, 0, 128, 0);
@@ -647,10 +734,15 @@ gemm_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_constant__ C
             if (!wait_or_abort(smem_u32(&sh.tmem_full), uint32_t(local) & 1u, sh, p.status)) break;
             tc_fence_after();
             uint32_t acc0[64], acc1[64];
-            const uint32_t taddr = tmem + (uint32_t(32 * q) << 16) + uint32_t(128 * h);
-            tmem_ld_32x32b_x64(taddr, acc0);
-            tmem_ld_32x32b_x64(taddr + 64, acc1);
-            tmem_ld_wait();
+            if (tl.nk > 0) {
+                const uint32_t taddr = tmem + (uint32_t(32 * q) << 16) + uint32_t(128 * h);
+                tmem_ld_32x32b_x64(taddr, acc0);
+                tmem_ld_32x32b_x64(taddr + 64, acc1);
+                tmem_ld_wait();
+            } else {                             // no K-steps (an expert without tokens): the product is 0
+#pragma unroll
+                for (int i = 0; i < 64; ++i) acc0[i] = acc1[i] = 0u;
+            }
             tc_fence_before();
             // Once all 8 epilogue warps hold their registers, one relaxed arrive
             // per CTA releases the accumulator (the reads retired at wait::ld;
@@ -663,7 +755,7 @@ gemm_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_constant__ C
                     else mbar_arrive(smem_u32(&sh.tmem_empty));
                 }
             }
-            const int64_t row = int64_t(tl.a_row) + int64_t(rank) * kBM + 32 * q + lane;
+            const int64_t row = int64_t(tl.d_row) + int64_t(rank) * kBM + 32 * q + lane;
             if constexpr (C::kStagedStores) {
                 const int64_t row0 = row - lane;
                 if (row0 < tl.row_end) {             // warp-uniform: some row of this warp is stored
@@ -681,7 +773,7 @@ gemm_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_constant__ C
                 // a burst of D/AUX stores at the start of that tile slows its
                 // loads, so the 8 chunks are spread over about half of the
                 // tile's mainloop (~700 cycles per K-step).
-                const uint32_t gap_ns = uint32_t(p.k_iters) * 20u;
+                const uint32_t gap_ns = uint32_t(tl.nk) * 20u;
 #pragma unroll
                 for (int j = 0; j < 4; ++j) {
                     if (nb + 16 * j < p.N) store_chunk(acc0 + 16 * j, p, bias, row, nb + 16 * j);
@@ -709,24 +801,29 @@ template <int kPair>
 te_mx_status launch_gemm(const GemmArgs& a, int sms, unsigned int* status, cudaStream_t stream) {
     using C = Cfg<kPair>;
     const bool grouped = a.groups > 0;
-    const uint64_t b_rows = grouped ? uint64_t(a.groups) * uint64_t(a.N) : uint64_t(a.N);
+    const bool wg = a.wgrad;
+    // Extent and pitch of the operands along the reduction axis: K for the
+    // dense and grouped GEMMs, the token capacity of the padded layout for wgrad.
+    const uint64_t kext = wg ? uint64_t(a.ld_code) : uint64_t(a.K);
+    const uint64_t b_rows = (grouped && !wg) ? uint64_t(a.groups) * uint64_t(a.N) : uint64_t(a.N);
     const uint64_t sf_cols = uint64_t(a.K / 32) < 16 ? 16 : uint64_t(a.K / 32);
+    const uint64_t sfa_cols = wg ? uint64_t(a.ld_sA) : sf_cols, sfb_cols = wg ? uint64_t(a.ld_sB) : sf_cols;
     CUtensorMap ma, mb, msa, msb;
     te_mx_status st;
-    if ((st = encode_tensor_map_2d(&ma, CU_TENSOR_MAP_DATA_TYPE_UINT8, a.A, uint64_t(a.K), uint64_t(a.M),
-                                   uint64_t(a.K), kBK, kBM, CU_TENSOR_MAP_SWIZZLE_128B)) != TE_MX_OK) return st;
-    if ((st = encode_tensor_map_2d(&mb, CU_TENSOR_MAP_DATA_TYPE_UINT8, a.B, uint64_t(a.K), b_rows,
-                                   uint64_t(a.K), kBK, C::kBRows, CU_TENSOR_MAP_SWIZZLE_128B)) != TE_MX_OK) return st;
-    if ((st = encode_tensor_map_2d(&msa, CU_TENSOR_MAP_DATA_TYPE_UINT8, a.sA, sf_cols, uint64_t(a.M),
+    if ((st = encode_tensor_map_2d(&ma, CU_TENSOR_MAP_DATA_TYPE_UINT8, a.A, kext, uint64_t(a.M),
+                                   kext, kBK, kBM, CU_TENSOR_MAP_SWIZZLE_128B)) != TE_MX_OK) return st;
+    if ((st = encode_tensor_map_2d(&mb, CU_TENSOR_MAP_DATA_TYPE_UINT8, a.B, kext, b_rows,
+                                   kext, kBK, C::kBRows, CU_TENSOR_MAP_SWIZZLE_128B)) != TE_MX_OK) return st;
+    if ((st = encode_tensor_map_2d(&msa, CU_TENSOR_MAP_DATA_TYPE_UINT8, a.sA, sfa_cols, uint64_t(a.M),
                                    uint64_t(a.ld_sA), 16, kBM, CU_TENSOR_MAP_SWIZZLE_NONE)) != TE_MX_OK) return st;
-    if ((st = encode_tensor_map_2d(&msb, CU_TENSOR_MAP_DATA_TYPE_UINT8, a.sB, sf_cols, b_rows,
+    if ((st = encode_tensor_map_2d(&msb, CU_TENSOR_MAP_DATA_TYPE_UINT8, a.sB, sfb_cols, b_rows,
                                    uint64_t(a.ld_sB), 16, kBN, CU_TENSOR_MAP_SWIZZLE_NONE)) != TE_MX_OK) return st;
 
     GemmParams p{};
     p.M = a.M;
     p.N = int32_t(a.N);
     p.K = int32_t(a.K);
-    p.k_iters = int32_t(a.K / kBK);
+    p.k_iters = wg ? 0 : int32_t(a.K / kBK);
     p.n_tiles = int32_t((a.N + kBN - 1) / kBN);
     p.m_tiles = int32_t((a.M + C::kTileM - 1) / C::kTileM);
     p.total_tiles = grouped ? 0 : int64_t(p.m_tiles) * p.n_tiles;
@@ -738,6 +835,11 @@ te_mx_status launch_gemm(const GemmArgs& a, int sms, unsigned int* status, cudaS
     p.has_bias = a.has_bias;
     p.gelu = a.gelu;
     p.dgelu = a.dgelu;
+    p.wgrad = wg;
+    p.total_m = a.total_m;
+    p.ld_code = a.ld_code;
+    p.ld_sfa = a.ld_sA;
+    p.ld_sfb = a.ld_sB;
     p.status = status;
 
     const int64_t slots = sms / kPair;                     // CTAs (pairs) resident at once
@@ -759,11 +861,18 @@ te_mx_status launch_gemm(const GemmArgs& a, int sms, unsigned int* status, cudaS
     cfg.attrs = attr;
     cfg.numAttrs = 1;
     if constexpr (kPair == 2) {
-        // persistent grid: never more pairs than can be resident together
-        int max_clusters = 0;
-        e = cudaOccupancyMaxActiveClusters(&max_clusters, kern, &cfg);
-        if (e != cudaSuccess) return cuda_status(e, "cudaOccupancyMaxActiveClusters(gemm)");
-        if (max_clusters < 1) return set_error(TE_MX_ERR_CUDA, "no CTA pair of the GEMM fits on this device");
+        // persistent grid: never more pairs than can be resident together (the
+        // occupancy query is slow, so its answer is kept per device)
+        static int max_clusters_of[64];
+        int dev = 0;
+        if ((e = cudaGetDevice(&dev)) != cudaSuccess) return cuda_status(e, "cudaGetDevice");
+        int max_clusters = dev < 64 ? __atomic_load_n(&max_clusters_of[dev], __ATOMIC_RELAXED) : 0;
+        if (max_clusters == 0) {
+            e = cudaOccupancyMaxActiveClusters(&max_clusters, kern, &cfg);
+            if (e != cudaSuccess) return cuda_status(e, "cudaOccupancyMaxActiveClusters(gemm)");
+            if (max_clusters < 1) return set_error(TE_MX_ERR_CUDA, "no CTA pair of the GEMM fits on this device");
+            if (dev < 64) __atomic_store_n(&max_clusters_of[dev], max_clusters, __ATOMIC_RELAXED);
+        }
         if (units > max_clusters) units = max_clusters;
         cfg.gridDim = dim3(unsigned(units * kPair));
     }
@@ -782,7 +891,7 @@ te_mx_status gemm_launch(const GemmArgs& a, cudaStream_t stream) {
     // CTA pairs once there are enough 256-row tiles to fill the GPU; single
     // CTAs for small problems (finer tiles, more of them).
     const int64_t pair_tiles = ((a.M + 255) / 256) * ((a.N + kBN - 1) / kBN);
-    const bool pair = a.groups > 0 ? a.M >= 256 * 8 : pair_tiles >= sms / 2;
+    const bool pair = a.wgrad ? a.M >= 256 : (a.groups > 0 ? a.M >= 256 * 8 : pair_tiles >= sms / 2);
     return pair ? launch_gemm<2>(a, sms, status, stream) : launch_gemm<1>(a, sms, status, stream);
 }
 

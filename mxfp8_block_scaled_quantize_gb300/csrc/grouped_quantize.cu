@@ -1,0 +1,263 @@
+// Per-expert column-wise MXFP8 quantisation: the operands of the grouped
+// wgrad GEMM dW_e = dY_e^T X_e of a MoE layer (one launch over the experts,
+// "Single-Launch Grouped GEMM Backends on ROCm", ROCm/TransformerEngine
+// README).
+//
+// Expert e owns rows [R_e, R_e + m_e) of the token-major input x [T x C].  Its
+// column-wise copy is blocked along tokens (32 per E8M0 scale, the MXFP8 rule
+// of te_mx_quantize) and zero-padded to Kp_e = round_up(m_e, 128) tokens, so
+// no block crosses an expert boundary and the GEMM's 128-token K-steps stay
+// inside one expert:
+//   q[c][P_e + t] = E4M3 code of x[R_e + t][c]   (t < m_e; 0 for m_e <= t < Kp_e)
+//   s[c][Q_e + b] = E8M0 scale of tokens 32b .. 32b + 31 of expert e
+//   P_e = sum_{e' < e} Kp_e',  Q_e = sum_{e' < e} round_up(Kp_e' / 32, 16)
+// Expert sizes are read on the device.
+//
+// Work decomposition.  A unit is one padded 32-token block of one expert
+// times 64 columns.  Every warp runs its own TMA pipeline over units (like
+// the MXFP8 quantiser): 32 x 64 bf16 in, lane l quantises columns 2l, 2l+1 of
+// the block (tokens past the expert's end masked to 0), the codes are staged
+// in the consumed buffer (64 columns x 32 bytes) and leave with one TMA store.
+#include <cuda_runtime.h>
+
+#include "e4m3.cuh"
+#include "ptx.cuh"
+#include "temx_internal.h"
+
+namespace temx {
+
+namespace {
+
+constexpr int kRows = 32;                        // tokens per block (one scale)
+constexpr int kCols = 64;                        // columns per unit (128 bytes of bf16)
+constexpr int kUnitBytes = kRows * kCols * 2;
+constexpr int kWarps = 16;
+constexpr int kStages = 3;
+constexpr int kMaxGroups = 1024;
+constexpr int kSmem = kWarps * kStages * kUnitBytes + 1024;
+
+struct GroupedParams {
+    int64_t total_m, cols;
+    int32_t groups;
+    const int32_t* group_m;  // device
+    uint8_t* s;
+    int64_t ld_q, ld_s;      // code / scale row pitch = capacities
+    int64_t col_units;       // ceil(cols / 64)
+    unsigned int* status;
+};
+
+struct GroupTable {
+    int32_t blk[kMaxGroups + 1];     // padded 32-token blocks before expert g (= P_g / 32)
+    int32_t row[kMaxGroups + 1];     // input rows before expert g (= R_g)
+    int32_t sc[kMaxGroups + 1];      // scale columns before expert g (= Q_g)
+    int32_t bad;
+};
+
+// Prefix sums of the expert sizes (one warp).  A negative size, a sum above
+// total_m or a layout wider than the given pitches sets the status word and
+// the kernel writes nothing.
+__device__ void build_table(const GroupedParams& p, GroupTable& t, int lane) {
+    const int G = p.groups;
+    const int per = (G + 31) / 32;
+    const int lo = min(G, lane * per), hi = min(G, lo + per);
+    bool bad = false;
+    int64_t rows = 0, blks = 0, scs = 0;
+    for (int g = lo; g < hi; ++g) {
+        const int64_t m = p.group_m[g];
+        bad |= m < 0;
+        const int64_t mm = m < 0 ? 0 : m;
+        const int64_t kb = (mm + 127) / 128 * 4;                       // Kp / 32
+        rows += mm;
+        blks += kb;
+        scs += (kb + 15) / 16 * 16;
+    }
+    int64_t r_in = rows, b_in = blks, s_in = scs;
+    for (int o = 1; o < 32; o <<= 1) {
+        const int64_t r = __shfl_up_sync(0xFFFFFFFFu, r_in, o), b = __shfl_up_sync(0xFFFFFFFFu, b_in, o),
+                      s = __shfl_up_sync(0xFFFFFFFFu, s_in, o);
+        if (lane >= o) { r_in += r; b_in += b; s_in += s; }
+    }
+    int64_t r0 = r_in - rows, b0 = b_in - blks, s0 = s_in - scs;
+    for (int g = lo; g < hi; ++g) {
+        t.row[g] = int32_t(r0);
+        t.blk[g] = int32_t(b0);
+        t.sc[g] = int32_t(s0);
+        const int64_t m = p.group_m[g] < 0 ? 0 : p.group_m[g];
+        const int64_t kb = (m + 127) / 128 * 4;
+        r0 += m;
+        b0 += kb;
+        s0 += (kb + 15) / 16 * 16;
+    }
+    const int64_t rt = __shfl_sync(0xFFFFFFFFu, r_in, 31), bt = __shfl_sync(0xFFFFFFFFu, b_in, 31),
+                  st = __shfl_sync(0xFFFFFFFFu, s_in, 31);
+    bad = __any_sync(0xFFFFFFFFu, bad);
+    if (lane == 0) {
+        t.row[G] = int32_t(rt);
+        t.blk[G] = int32_t(bt);
+        t.sc[G] = int32_t(st);
+        bad |= rt > p.total_m || bt * kRows > p.ld_q || st > p.ld_s;
+        t.bad = bad ? 1 : 0;
+        if (bad && blockIdx.x == 0) set_device_status(p.status, kStatusBadArg);
+    }
+}
+
+__global__ void __launch_bounds__(kWarps * 32, 1)
+grouped_colwise_kernel(const __grid_constant__ CUtensorMap x_map, const __grid_constant__ CUtensorMap q_map,
+                       const GroupedParams p) {
+    extern __shared__ uint8_t smem_raw[];
+    __shared__ __align__(8) uint64_t bars[kWarps][kStages];
+    __shared__ GroupTable tab;
+
+    uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    if (warp == 0) build_table(p, tab, lane);
+    __syncthreads();
+    if (tab.bad) return;
+
+    const int64_t units = int64_t(tab.blk[p.groups]) * p.col_units;
+    const int64_t gwarp = int64_t(blockIdx.x) * kWarps + warp;
+    const int64_t nwarps = int64_t(gridDim.x) * kWarps;
+    if (gwarp >= units) return;
+    const int64_t n_mine = (units - gwarp + nwarps - 1) / nwarps;
+    const uint32_t ring = smem_u32(smem + warp * (kStages * kUnitBytes));
+
+    // unit i of this warp -> expert g, block, columns.  `h` is a lower bound on
+    // the expert, moved forward only (a warp's units only move forward).
+    auto locate = [&](int64_t i, int32_t& h, int32_t& blk, int64_t& c0) {
+        const int64_t u = gwarp + i * nwarps;
+        blk = int32_t(u / p.col_units);
+        c0 = (u % p.col_units) * kCols;
+        while (tab.blk[h + 1] <= blk) ++h;       // blk < tab.blk[groups]: stops at an expert
+    };
+    int32_t load_hint = 0;                       // lane 0: the loads run kStages units ahead
+    auto load = [&](int64_t i, uint32_t dst, uint32_t bar) {
+        int32_t blk;
+        int64_t c0;
+        locate(i, load_hint, blk, c0);
+        const int32_t g = load_hint;
+        const int32_t r = tab.row[g] + (blk - tab.blk[g]) * kRows;    // rows past the expert are masked later
+        mbar_arrive_expect_tx(bar, kUnitBytes);
+        tma_load_2d(dst, &x_map, bar, int32_t(c0), r);
+    };
+
+    if (lane == 0) {
+        tma_prefetch_desc(&x_map);
+        tma_prefetch_desc(&q_map);
+        for (int s = 0; s < kStages; ++s) mbar_init(smem_u32(&bars[warp][s]), 1);
+        fence_mbarrier_init();
+        for (int s = 0; s < kStages && s < n_mine; ++s) load(s, ring + s * kUnitBytes, smem_u32(&bars[warp][s]));
+    }
+    __syncwarp();
+
+    int32_t g = 0;
+    for (int64_t i = 0; i < n_mine; ++i) {
+        const int s = int(i % kStages);
+        const uint32_t bar = smem_u32(&bars[warp][s]);
+        int32_t blk;
+        int64_t c0;
+        locate(i, g, blk, c0);
+        const int32_t m = tab.row[g + 1] - tab.row[g];
+        const int32_t valid = m - (blk - tab.blk[g]) * kRows;          // tokens of the expert in this block
+        if (!__all_sync(0xFFFFFFFFu, mbar_wait(bar, uint32_t((i / kStages) & 1), p.status))) {
+            if (lane == 0)                       // gave up: let this warp's loads still in flight land
+                for (int64_t j = i; j < i + kStages && j < n_mine; ++j)
+                    mbar_wait(smem_u32(&bars[warp][j % kStages]), uint32_t((j / kStages) & 1), p.status);
+            break;
+        }
+        const uint32_t unit = ring + s * kUnitBytes;
+        // columns 2 lane, 2 lane + 1 over the block's 32 tokens (128-byte swizzle)
+        uint32_t w[32];
+        const uint32_t base = unit + ((lane & 3) << 2);
+        const int ch = lane >> 2;
+#pragma unroll
+        for (int r = 0; r < 32; ++r) {
+            const uint32_t v = lds32(base + r * 128 + ((ch ^ (r & 7)) << 4));
+            w[r] = r < valid ? v : 0u;
+        }
+        const uint32_t m2 = amax_words<32>(w);
+        const uint32_t ef_lo = (m2 & 0xFFFFu) >> 7, ef_hi = m2 >> 23;
+        const uint32_t s_lo = ef_lo == 0xFFu ? 0xFFu : (ef_lo > 8u ? ef_lo - 8u : 0u);
+        const uint32_t s_hi = ef_hi == 0xFFu ? 0xFFu : (ef_hi > 8u ? ef_hi - 8u : 0u);
+        const float k_lo = inv_scale(s_lo), k_hi = inv_scale(s_hi);
+        uint32_t lo[8], hi[8];
+#pragma unroll
+        for (int q = 0; q < 8; ++q) {
+            const uint32_t a0 = w[4 * q], a1 = w[4 * q + 1], a2 = w[4 * q + 2], a3 = w[4 * q + 3];
+            lo[q] = cvt_e4m3x2(__fmul_rn(bf16_lo(a0), k_lo), __fmul_rn(bf16_lo(a1), k_lo)) |
+                    (cvt_e4m3x2(__fmul_rn(bf16_lo(a2), k_lo), __fmul_rn(bf16_lo(a3), k_lo)) << 16);
+            hi[q] = cvt_e4m3x2(__fmul_rn(bf16_hi(a0), k_hi), __fmul_rn(bf16_hi(a1), k_hi)) |
+                    (cvt_e4m3x2(__fmul_rn(bf16_hi(a2), k_hi), __fmul_rn(bf16_hi(a3), k_hi)) << 16);
+        }
+        if (s_lo == 0xFFu) {
+#pragma unroll
+            for (int q = 0; q < 8; ++q) lo[q] = 0x7F7F7F7Fu;
+        }
+        if (s_hi == 0xFFu) {
+#pragma unroll
+            for (int q = 0; q < 8; ++q) hi[q] = 0x7F7F7F7Fu;
+        }
+        __syncwarp();                            // every lane has read the unit: reuse it for the codes
+        const uint32_t cb = unit + lane * 64;    // column 2 lane, then 2 lane + 1: 32 bytes each
+        sts128(cb, lo[0], lo[1], lo[2], lo[3]);
+        sts128(cb + 16, lo[4], lo[5], lo[6], lo[7]);
+        sts128(cb + 32, hi[0], hi[1], hi[2], hi[3]);
+        sts128(cb + 48, hi[4], hi[5], hi[6], hi[7]);
+        const int64_t c = c0 + 2 * lane;
+        if (c < p.cols) {                        // cols % 32 == 0: c + 1 < cols too
+            uint8_t* sp = p.s + c * p.ld_s + tab.sc[g] + (blk - tab.blk[g]);
+            st_global_u8(sp, s_lo);
+            st_global_u8(sp + p.ld_s, s_hi);
+        }
+        fence_proxy_async_smem();                // make the staged codes visible to the TMA engine
+        __syncwarp();
+        if (lane == 0) {
+            tma_store_2d(&q_map, unit, blk * kRows, int32_t(c0));
+            bulk_commit();
+            if (i + kStages < n_mine) {
+                bulk_wait_read_all();            // the store has read the unit: refill it
+                load(i + kStages, unit, bar);
+            }
+        }
+        __syncwarp();
+    }
+    if (lane == 0) bulk_wait_all();
+}
+
+}  // namespace
+
+int64_t grouped_code_width(int64_t total_m, int32_t groups) {
+    return (total_m + 127 * int64_t(groups) + 15) / 16 * 16;
+}
+int64_t grouped_scale_width(int64_t total_m, int32_t groups) {
+    return ((total_m + 127 * int64_t(groups)) / 32 + 12 * int64_t(groups) + 15) / 16 * 16;
+}
+
+te_mx_status grouped_colwise_launch(const GroupedColwiseArgs& a, cudaStream_t stream) {
+    CUtensorMap xm, qm;
+    te_mx_status st = encode_tensor_map_2d(&xm, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, a.x, uint64_t(a.cols),
+                                           uint64_t(a.total_m), uint64_t(a.ld_x) * 2, kCols, kRows,
+                                           CU_TENSOR_MAP_SWIZZLE_128B);
+    if (st != TE_MX_OK) return st;
+    if ((st = encode_tensor_map_2d(&qm, CU_TENSOR_MAP_DATA_TYPE_UINT8, a.q, uint64_t(a.ld_q), uint64_t(a.cols),
+                                   uint64_t(a.ld_q), kRows, kCols, CU_TENSOR_MAP_SWIZZLE_NONE)) != TE_MX_OK)
+        return st;
+    GroupedParams p;
+    p.total_m = a.total_m; p.cols = a.cols;
+    p.groups = a.groups; p.group_m = a.group_m;
+    p.s = a.s; p.ld_q = a.ld_q; p.ld_s = a.ld_s;
+    p.col_units = (a.cols + kCols - 1) / kCols;
+    if ((st = device_status_ptr(&p.status)) != TE_MX_OK) return st;
+    int sms = 0;
+    if ((st = device_sm_count(&sms)) != TE_MX_OK) return st;
+    cudaError_t e = set_smem_attribute_once(reinterpret_cast<const void*>(grouped_colwise_kernel), kSmem);
+    if (e == cudaSuccess) {
+        const int64_t bound = grouped_code_width(a.total_m, a.groups) / kRows * p.col_units;
+        const int64_t want = (bound + kWarps - 1) / kWarps;
+        const int grid = int(want < sms ? (want > 0 ? want : 1) : sms);
+        grouped_colwise_kernel<<<grid, kWarps * 32, kSmem, stream>>>(xm, qm, p);
+        e = cudaGetLastError();
+    }
+    return cuda_status(e, "grouped column-wise quantize kernel launch");
+}
+
+}  // namespace temx

@@ -38,6 +38,12 @@ struct GemmArgs {
     void* aux;
     int32_t groups;          // 0: dense GEMM
     const int32_t* group_m;  // device int32 [groups] (grouped only)
+    // Grouped wgrad (dW_e = dY_e^T X_e): A = column-wise dY [M x ld_code], B =
+    // column-wise X [N x ld_code] in the per-expert padded layout, group_m the
+    // experts' token counts, D = [groups x M x N]; K is unused.
+    bool wgrad;
+    int64_t ld_code;         // code row pitch (token capacity)
+    int64_t total_m;         // bound on the sum of the token counts
 };
 
 te_mx_status quantize_launch(const QuantizeArgs& a, cudaStream_t stream);
@@ -54,6 +60,20 @@ struct LnQuantizeArgs {
     float* rsigma;           // fp32 [rows] or null
 };
 te_mx_status ln_quantize_launch(const LnQuantizeArgs& a, cudaStream_t stream);
+
+struct GroupedColwiseArgs {
+    const void* x;           // bf16 [total_m x cols], pitch ld_x (token-major)
+    int64_t total_m, cols, ld_x;
+    int32_t groups;
+    const int32_t* group_m;  // device int32 [groups]
+    uint8_t* q;              // [cols x ld_q]
+    int64_t ld_q;
+    uint8_t* s;              // [cols x ld_s]
+    int64_t ld_s;
+};
+te_mx_status grouped_colwise_launch(const GroupedColwiseArgs& a, cudaStream_t stream);
+int64_t grouped_code_width(int64_t total_m, int32_t groups);    // an upper bound of sum round_up(m_e, 128)
+int64_t grouped_scale_width(int64_t total_m, int32_t groups);   // an upper bound of sum round_up(Kp_e / 32, 16)
 int64_t ln_quantize_max_hidden();
 // Float8BlockScaling quantisation (E8M0-cast scales); `partial`/`dbias` unused.
 te_mx_status block_quantize_launch(const QuantizeArgs& a, bool block_2d, cudaStream_t stream);

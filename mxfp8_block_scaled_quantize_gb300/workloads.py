@@ -99,6 +99,15 @@ WORKLOADS = {
 }
 
 
+def make_moe_wgrad():
+    """Expert wgrad of the MoE layer: the routing and X of ``make_moe`` and an
+    output gradient dY [sum m_e x 1536] N(0, 1e-3^2) (the gradient scale of the
+    fc1 workload; the MoE workload names none)."""
+    d = make_moe()
+    total = int(d["group_m"].sum())
+    return {"group_m": d["group_m"], "X": d["X"], "dY": normal_bf16((total, 1536), 1e-3, 503)}
+
+
 def layernorm_params(hidden: int, seed: int):
     """LayerNorm scale (gamma) and bias (beta), bf16 [hidden]: N(1, 0.1^2) and
     N(0, 0.1^2) (trained-looking values instead of the 1 / 0 initialisation)."""
