@@ -13,11 +13,12 @@
 //   P_e = sum_{e' < e} Kp_e',  Q_e = sum_{e' < e} round_up(Kp_e' / 32, 16)
 // Expert sizes are read on the device.
 //
-// Work decomposition.  A unit is one padded 32-token block of one expert
-// times 64 columns.  Every warp runs its own TMA pipeline over units (like
-// the MXFP8 quantiser): 32 x 64 bf16 in, lane l quantises columns 2l, 2l+1 of
-// the block (tokens past the expert's end masked to 0), the codes are staged
-// in the consumed buffer (64 columns x 32 bytes) and leave with one TMA store.
+// Work decomposition.  A unit is 64 padded tokens (two blocks; Kp_e is a
+// multiple of 128, so a unit never crosses an expert) times 64 columns.
+// Every warp runs its own TMA pipeline over units (like the MXFP8 quantiser):
+// 64 x 64 bf16 in, lane l quantises columns 2l, 2l+1 over both blocks (tokens
+// past the expert's end masked to 0), the codes are staged in the consumed
+// buffer (64 columns x 64 bytes, 64-byte swizzle) and leave with one TMA store.
 #include <cuda_runtime.h>
 
 #include "e4m3.cuh"
@@ -28,11 +29,11 @@ namespace temx {
 
 namespace {
 
-constexpr int kRows = 32;                        // tokens per block (one scale)
+constexpr int kRows = 64;                        // tokens per unit (two blocks)
 constexpr int kCols = 64;                        // columns per unit (128 bytes of bf16)
 constexpr int kUnitBytes = kRows * kCols * 2;
-constexpr int kWarps = 16;
-constexpr int kStages = 3;
+constexpr int kWarps = 12;
+constexpr int kStages = 2;
 constexpr int kMaxGroups = 1024;
 constexpr int kSmem = kWarps * kStages * kUnitBytes + 1024;
 
@@ -47,7 +48,7 @@ struct GroupedParams {
 };
 
 struct GroupTable {
-    int32_t blk[kMaxGroups + 1];     // padded 32-token blocks before expert g (= P_g / 32)
+    int32_t blk[kMaxGroups + 1];     // padded 64-token units before expert g (= P_g / 64)
     int32_t row[kMaxGroups + 1];     // input rows before expert g (= R_g)
     int32_t sc[kMaxGroups + 1];      // scale columns before expert g (= Q_g)
     int32_t bad;
@@ -68,7 +69,7 @@ __device__ void build_table(const GroupedParams& p, GroupTable& t, int lane) {
         const int64_t mm = m < 0 ? 0 : m;
         const int64_t kb = (mm + 127) / 128 * 4;                       // Kp / 32
         rows += mm;
-        blks += kb;
+        blks += kb / 2;
         scs += (kb + 15) / 16 * 16;
     }
     int64_t r_in = rows, b_in = blks, s_in = scs;
@@ -85,7 +86,7 @@ __device__ void build_table(const GroupedParams& p, GroupTable& t, int lane) {
         const int64_t m = p.group_m[g] < 0 ? 0 : p.group_m[g];
         const int64_t kb = (m + 127) / 128 * 4;
         r0 += m;
-        b0 += kb;
+        b0 += kb / 2;
         s0 += (kb + 15) / 16 * 16;
     }
     const int64_t rt = __shfl_sync(0xFFFFFFFFu, r_in, 31), bt = __shfl_sync(0xFFFFFFFFu, b_in, 31),
@@ -157,7 +158,7 @@ grouped_colwise_kernel(const __grid_constant__ CUtensorMap x_map, const __grid_c
         int64_t c0;
         locate(i, g, blk, c0);
         const int32_t m = tab.row[g + 1] - tab.row[g];
-        const int32_t valid = m - (blk - tab.blk[g]) * kRows;          // tokens of the expert in this block
+        const int32_t valid = m - (blk - tab.blk[g]) * kRows;          // tokens of the expert in this unit
         if (!__all_sync(0xFFFFFFFFu, mbar_wait(bar, uint32_t((i / kStages) & 1), p.status))) {
             if (lane == 0)                       // gave up: let this warp's loads still in flight land
                 for (int64_t j = i; j < i + kStages && j < n_mine; ++j)
@@ -165,48 +166,60 @@ grouped_colwise_kernel(const __grid_constant__ CUtensorMap x_map, const __grid_c
             break;
         }
         const uint32_t unit = ring + s * kUnitBytes;
-        // columns 2 lane, 2 lane + 1 over the block's 32 tokens (128-byte swizzle)
-        uint32_t w[32];
+        // columns 2 lane, 2 lane + 1 over the unit's two 32-token blocks
+        // (128-byte swizzle on the way in, 64-byte swizzle for the codes)
+        uint32_t lo[2][8], hi[2][8], s_lo[2], s_hi[2];
         const uint32_t base = unit + ((lane & 3) << 2);
         const int ch = lane >> 2;
 #pragma unroll
-        for (int r = 0; r < 32; ++r) {
-            const uint32_t v = lds32(base + r * 128 + ((ch ^ (r & 7)) << 4));
-            w[r] = r < valid ? v : 0u;
-        }
-        const uint32_t m2 = amax_words<32>(w);
-        const uint32_t ef_lo = (m2 & 0xFFFFu) >> 7, ef_hi = m2 >> 23;
-        const uint32_t s_lo = ef_lo == 0xFFu ? 0xFFu : (ef_lo > 8u ? ef_lo - 8u : 0u);
-        const uint32_t s_hi = ef_hi == 0xFFu ? 0xFFu : (ef_hi > 8u ? ef_hi - 8u : 0u);
-        const float k_lo = inv_scale(s_lo), k_hi = inv_scale(s_hi);
-        uint32_t lo[8], hi[8];
+        for (int h = 0; h < 2; ++h) {
+            uint32_t w[32];
 #pragma unroll
-        for (int q = 0; q < 8; ++q) {
-            const uint32_t a0 = w[4 * q], a1 = w[4 * q + 1], a2 = w[4 * q + 2], a3 = w[4 * q + 3];
-            lo[q] = cvt_e4m3x2(__fmul_rn(bf16_lo(a0), k_lo), __fmul_rn(bf16_lo(a1), k_lo)) |
-                    (cvt_e4m3x2(__fmul_rn(bf16_lo(a2), k_lo), __fmul_rn(bf16_lo(a3), k_lo)) << 16);
-            hi[q] = cvt_e4m3x2(__fmul_rn(bf16_hi(a0), k_hi), __fmul_rn(bf16_hi(a1), k_hi)) |
-                    (cvt_e4m3x2(__fmul_rn(bf16_hi(a2), k_hi), __fmul_rn(bf16_hi(a3), k_hi)) << 16);
-        }
-        if (s_lo == 0xFFu) {
+            for (int r = 0; r < 32; ++r) {
+                const uint32_t v = lds32(base + (32 * h + r) * 128 + ((ch ^ (r & 7)) << 4));
+                w[r] = 32 * h + r < valid ? v : 0u;
+            }
+            const uint32_t m2 = amax_words<32>(w);
+            const uint32_t ef_lo = (m2 & 0xFFFFu) >> 7, ef_hi = m2 >> 23;
+            s_lo[h] = ef_lo == 0xFFu ? 0xFFu : (ef_lo > 8u ? ef_lo - 8u : 0u);
+            s_hi[h] = ef_hi == 0xFFu ? 0xFFu : (ef_hi > 8u ? ef_hi - 8u : 0u);
+            const float k_lo = inv_scale(s_lo[h]), k_hi = inv_scale(s_hi[h]);
 #pragma unroll
-            for (int q = 0; q < 8; ++q) lo[q] = 0x7F7F7F7Fu;
-        }
-        if (s_hi == 0xFFu) {
+            for (int q = 0; q < 8; ++q) {
+                const uint32_t a0 = w[4 * q], a1 = w[4 * q + 1], a2 = w[4 * q + 2], a3 = w[4 * q + 3];
+                lo[h][q] = cvt_e4m3x2(__fmul_rn(bf16_lo(a0), k_lo), __fmul_rn(bf16_lo(a1), k_lo)) |
+                           (cvt_e4m3x2(__fmul_rn(bf16_lo(a2), k_lo), __fmul_rn(bf16_lo(a3), k_lo)) << 16);
+                hi[h][q] = cvt_e4m3x2(__fmul_rn(bf16_hi(a0), k_hi), __fmul_rn(bf16_hi(a1), k_hi)) |
+                           (cvt_e4m3x2(__fmul_rn(bf16_hi(a2), k_hi), __fmul_rn(bf16_hi(a3), k_hi)) << 16);
+            }
+            if (s_lo[h] == 0xFFu) {
 #pragma unroll
-            for (int q = 0; q < 8; ++q) hi[q] = 0x7F7F7F7Fu;
+                for (int q = 0; q < 8; ++q) lo[h][q] = 0x7F7F7F7Fu;
+            }
+            if (s_hi[h] == 0xFFu) {
+#pragma unroll
+                for (int q = 0; q < 8; ++q) hi[h][q] = 0x7F7F7F7Fu;
+            }
         }
         __syncwarp();                            // every lane has read the unit: reuse it for the codes
-        const uint32_t cb = unit + lane * 64;    // column 2 lane, then 2 lane + 1: 32 bytes each
-        sts128(cb, lo[0], lo[1], lo[2], lo[3]);
-        sts128(cb + 16, lo[4], lo[5], lo[6], lo[7]);
-        sts128(cb + 32, hi[0], hi[1], hi[2], hi[3]);
-        sts128(cb + 48, hi[4], hi[5], hi[6], hi[7]);
+#pragma unroll
+        for (int j = 0; j < 2; ++j) {            // column 2 lane + j: 64 bytes, chunk 2h + t of its row
+            const int cl = 2 * lane + j;
+#pragma unroll
+            for (int h = 0; h < 2; ++h)
+#pragma unroll
+                for (int t = 0; t < 2; ++t) {
+                    const uint32_t* w = (j ? hi[h] : lo[h]) + 4 * t;
+                    sts128(unit + uint32_t(cl * 64 + (((2 * h + t) ^ ((cl >> 1) & 3)) << 4)), w[0], w[1], w[2], w[3]);
+                }
+        }
         const int64_t c = c0 + 2 * lane;
         if (c < p.cols) {                        // cols % 32 == 0: c + 1 < cols too
-            uint8_t* sp = p.s + c * p.ld_s + tab.sc[g] + (blk - tab.blk[g]);
-            st_global_u8(sp, s_lo);
-            st_global_u8(sp + p.ld_s, s_hi);
+            uint8_t* sp = p.s + c * p.ld_s + tab.sc[g] + 2 * (blk - tab.blk[g]);
+            st_global_u8(sp, s_lo[0]);
+            st_global_u8(sp + 1, s_lo[1]);
+            st_global_u8(sp + p.ld_s, s_hi[0]);
+            st_global_u8(sp + p.ld_s + 1, s_hi[1]);
         }
         fence_proxy_async_smem();                // make the staged codes visible to the TMA engine
         __syncwarp();
@@ -239,7 +252,7 @@ te_mx_status grouped_colwise_launch(const GroupedColwiseArgs& a, cudaStream_t st
                                            CU_TENSOR_MAP_SWIZZLE_128B);
     if (st != TE_MX_OK) return st;
     if ((st = encode_tensor_map_2d(&qm, CU_TENSOR_MAP_DATA_TYPE_UINT8, a.q, uint64_t(a.ld_q), uint64_t(a.cols),
-                                   uint64_t(a.ld_q), kRows, kCols, CU_TENSOR_MAP_SWIZZLE_NONE)) != TE_MX_OK)
+                                   uint64_t(a.ld_q), kRows, kCols, CU_TENSOR_MAP_SWIZZLE_64B)) != TE_MX_OK)
         return st;
     GroupedParams p;
     p.total_m = a.total_m; p.cols = a.cols;
@@ -251,7 +264,7 @@ te_mx_status grouped_colwise_launch(const GroupedColwiseArgs& a, cudaStream_t st
     if ((st = device_sm_count(&sms)) != TE_MX_OK) return st;
     cudaError_t e = set_smem_attribute_once(reinterpret_cast<const void*>(grouped_colwise_kernel), kSmem);
     if (e == cudaSuccess) {
-        const int64_t bound = grouped_code_width(a.total_m, a.groups) / kRows * p.col_units;
+        const int64_t bound = (grouped_code_width(a.total_m, a.groups) + kRows - 1) / kRows * p.col_units;
         const int64_t want = (bound + kWarps - 1) / kWarps;
         const int grid = int(want < sms ? (want > 0 ? want : 1) : sms);
         grouped_colwise_kernel<<<grid, kWarps * 32, kSmem, stream>>>(xm, qm, p);
