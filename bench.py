@@ -206,6 +206,8 @@ class Step:
                            "ln_quant_ffn_x": qb(T, H, True) + 8.0 * T + 4.0 * H,
                            "grouped_quant_moe_x": qb(MT, K, False), "grouped_quant_moe_dy": qb(MT, N, False)}
         self.next_flops["gemm_moe_wgrad"] = 2.0 * float(counts.sum()) * N * K
+        self.next_flops["gemm_wgrad_accum_f32"] = 2.0 * F * H * T
+        o["main_grad"] = torch.zeros(F, H, dtype=torch.float32, device=dev)   # fp32 weight-gradient accumulator
         # MoE expert wgrad: per-expert column-wise copies of X and dY, then dW_e = dY_e^T X_e
         gdev = d["moe_m"].to(torch.int32)
         o["gx"] = temx.quantize_colwise_grouped(d["moe_X"], gdev)
@@ -234,6 +236,8 @@ class Step:
             ("grouped_quant_moe_x", lambda: temx.quantize_colwise_grouped(d["moe_X"], gdev, out=o["gx"])),
             ("grouped_quant_moe_dy", lambda: temx.quantize_colwise_grouped(d["moe_dY"], gdev, out=o["gdy"])),
             ("gemm_moe_wgrad", lambda: temx.grouped_gemm_wgrad(gdev, MT, o["gdy"], o["gx"], out=o["dw"])),
+            ("gemm_wgrad_accum_f32", lambda: temx.gemm(o["dy"]["q_col"], o["dy"]["s_col"], o["x_row"]["q_col"],
+                                                       o["x_row"]["s_col"], accumulate=o["main_grad"])),
         ]
         temx.quantize(d["ffn_W"], False, True, out=o["w_col"])
 

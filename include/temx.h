@@ -74,7 +74,14 @@ typedef enum te_mx_epilogue {
      * pre-activation saved by the forward GELU_AUX GEMM, and
      * D = bf16(acc * gelu'(aux)), gelu' the derivative of the tanh form.
      * bias must be NULL. */
-    TE_MX_EPI_DGELU = 4
+    TE_MX_EPI_DGELU = 4,
+    /* Accumulation into an fp32 output (the beta epilogue and fp32 output of
+     * "Blockwise FP8 GEMM support on ROCm", ROCm/TransformerEngine README,
+     * with beta = 1: gradient accumulation into an fp32 main gradient):
+     * D is fp32 [M x N], read and written, D = fl32(D + acc).  bias and aux
+     * must be NULL.  te_mx_gemm only (and the accumulate flag of
+     * te_mx_grouped_gemm_wgrad). */
+    TE_MX_EPI_ACCUMULATE_F32 = 5
 } te_mx_epilogue;
 
 /* Smallest legal scale pitch for k quantised elements per row:
@@ -287,8 +294,9 @@ TEMX_API te_mx_status te_mx_quantize_colwise_grouped(const void* x, int64_t tota
  * one launch (fp32 accumulation on the tensor cores, bf16 output):
  *   dY, s_dY   per-expert column-wise copy of dY [total_m x M]: [M x ld_q], [M x ld_s];
  *   X,  s_X    per-expert column-wise copy of X  [total_m x N]: [N x ld_q], [N x ld_s];
- *   D          bf16 [num_groups x M x N] (device): D[e] = dW_e; an expert
- *              without tokens gets zeros.
+ *   accumulate 0: D is bf16 [num_groups x M x N], D[e] = dW_e (zeros for an
+ *              expert without tokens);  1: D is fp32 [num_groups x M x N] and
+ *              D[e] = fl32(D[e] + dW_e) (unchanged for an expert without tokens).
  * group_m and total_m as for te_mx_quantize_colwise_grouped (the same device
  * array that laid the operands out).  Rules: 1 <= num_groups <= 1024;
  * N % 16 == 0; ld_q, ld_s multiples of 16 (ld_s >= 16); num_groups * M <
@@ -298,7 +306,7 @@ TEMX_API te_mx_status te_mx_grouped_gemm_wgrad(int32_t num_groups, const int32_t
                                                const uint8_t* dY, const uint8_t* s_dY,
                                                const uint8_t* X, const uint8_t* s_X,
                                                int64_t M, int64_t N, int64_t ld_q, int64_t ld_s,
-                                               void* D, void* stream);
+                                               int32_t accumulate, void* D, void* stream);
 
 /* Workspace bytes te_mx_gemm / te_mx_grouped_gemm need: 0 for every shape
  * (scale re-layout happens in shared memory; kept so a future layout change

@@ -19,7 +19,7 @@ TE_MX_OK = 0
 STATUS_NAMES = {0: "TE_MX_OK", 1: "TE_MX_ERR_INVALID_ARG", 2: "TE_MX_ERR_UNSUPPORTED_SHAPE",
                 3: "TE_MX_ERR_MISALIGNED", 4: "TE_MX_ERR_WORKSPACE_TOO_SMALL", 5: "TE_MX_ERR_CUDA",
                 6: "TE_MX_ERR_DEVICE_TIMEOUT", 7: "TE_MX_ERR_ARCH"}
-EPI_NONE, EPI_BIAS, EPI_GELU_AUX, EPI_BIAS_GELU_AUX, EPI_DGELU = 0, 1, 2, 3, 4
+EPI_NONE, EPI_BIAS, EPI_GELU_AUX, EPI_BIAS_GELU_AUX, EPI_DGELU, EPI_ACCUMULATE_F32 = 0, 1, 2, 3, 4, 5
 
 # (name, restype, argtypes) for every function declared in include/temx.h
 _I64, _I32, _P, _SZ = ctypes.c_int64, ctypes.c_int32, ctypes.c_void_p, ctypes.c_size_t
@@ -32,7 +32,8 @@ SIGNATURES = {
     "te_mx_grouped_code_width": (_I64, [_I64, _I32]),
     "te_mx_grouped_scale_width": (_I64, [_I64, _I32]),
     "te_mx_quantize_colwise_grouped": (ctypes.c_int, [_P, _I64, _I64, _I64, _I32, _P, _P, _I64, _P, _I64, _P]),
-    "te_mx_grouped_gemm_wgrad": (ctypes.c_int, [_I32, _P, _I64, _P, _P, _P, _P, _I64, _I64, _I64, _I64, _P, _P]),
+    "te_mx_grouped_gemm_wgrad": (ctypes.c_int, [_I32, _P, _I64, _P, _P, _P, _P, _I64, _I64, _I64, _I64, _I32, _P,
+                                                _P]),
     "te_mx_quantize_dbias_workspace_size": (_SZ, [_I64, _I64]),
     "te_mx_quantize_dbias": (ctypes.c_int, [_P, _I64, _I64, _I64, _P, _P, _I64, _P, _P, _I64, _P, _P, _SZ, _P]),
     "te_mx_quantize_dbias_noalloc": (ctypes.c_int, [_P, _I64, _I64, _I64, _P, _P, _I64, _P, _P, _I64, _P, _P]),
@@ -111,9 +112,10 @@ def te_mx_quantize_colwise_grouped(x, total_m, cols, ld_x, num_groups, group_m, 
                                                 stream))
 
 
-def te_mx_grouped_gemm_wgrad(num_groups, group_m, total_m, dY, s_dY, X, s_X, M, N, ld_q, ld_s, D, stream) -> None:
-    _check(lib().te_mx_grouped_gemm_wgrad(num_groups, group_m, total_m, dY, s_dY, X, s_X, M, N, ld_q, ld_s, D,
-                                          stream))
+def te_mx_grouped_gemm_wgrad(num_groups, group_m, total_m, dY, s_dY, X, s_X, M, N, ld_q, ld_s, accumulate, D,
+                             stream) -> None:
+    _check(lib().te_mx_grouped_gemm_wgrad(num_groups, group_m, total_m, dY, s_dY, X, s_X, M, N, ld_q, ld_s,
+                                          accumulate, D, stream))
 
 
 def te_mx_quantize_dbias_workspace_size(rows, cols) -> int:
@@ -274,28 +276,38 @@ def quantize_colwise_grouped(x, group_m, stream=None, out=None):
     return o
 
 
-def grouped_gemm_wgrad(group_m, total_m, dy, x, stream=None, out=None):
+def grouped_gemm_wgrad(group_m, total_m, dy, x, stream=None, out=None, accumulate: bool = False):
     """dW_e = dY_e^T X_e for every expert: ``dy`` and ``x`` are the dicts of
     quantize_colwise_grouped of dY [total_m, M] and X [total_m, N] (same
-    group_m).  Returns bf16 [G, M, N] (``out`` if given)."""
+    group_m).  Returns bf16 [G, M, N] (``out`` if given); with ``accumulate``,
+    ``out`` is an fp32 [G, M, N] tensor that is added to."""
     import torch
     G = group_m.numel()
     M, N = dy["q"].shape[0], x["q"].shape[0]
     assert dy["q"].stride(0) == x["q"].stride(0) and dy["s"].stride(0) == x["s"].stride(0)
+    if accumulate:
+        assert out is not None and out.dtype == torch.float32
     d = out if out is not None else torch.empty(G, M, N, dtype=torch.bfloat16, device=dy["q"].device)
     te_mx_grouped_gemm_wgrad(G, group_m.data_ptr(), total_m, dy["q"].data_ptr(), dy["s"].data_ptr(), x["q"].data_ptr(),
-                             x["s"].data_ptr(), M, N, dy["q"].stride(0), dy["s"].stride(0), d.data_ptr(),
-                             _stream_ptr(stream))
+                             x["s"].data_ptr(), M, N, dy["q"].stride(0), dy["s"].stride(0), int(bool(accumulate)),
+                             d.data_ptr(), _stream_ptr(stream))
     return d
 
 
-def gemm(qa, sa, qb, sb, bias=None, gelu: bool = False, stream=None, out=None, dgelu_aux=None):
+def gemm(qa, sa, qb, sb, bias=None, gelu: bool = False, stream=None, out=None, dgelu_aux=None,
+         accumulate=None):
     """D = epilogue(deq(qa) . deq(qb)^T (+ bias)) in bf16; returns (D, aux or None).
     With ``dgelu_aux`` (bf16 [M, N], the forward pre-activation) the epilogue is
-    D = bf16(acc * gelu'(dgelu_aux))."""
+    D = bf16(acc * gelu'(dgelu_aux)).  With ``accumulate`` (an fp32 [M, N] CUDA
+    tensor) it is accumulate += deq(qa) . deq(qb)^T in fp32."""
     import torch
     M, K = qa.shape
     N = qb.shape[0]
+    if accumulate is not None:
+        assert accumulate.dtype == torch.float32 and bias is None and not gelu and dgelu_aux is None
+        te_mx_gemm(qa.data_ptr(), sa.data_ptr(), sa.stride(0), qb.data_ptr(), sb.data_ptr(), sb.stride(0),
+                   M, N, K, 0, EPI_ACCUMULATE_F32, accumulate.data_ptr(), 0, 0, 0, _stream_ptr(stream))
+        return accumulate, None
     epi = (EPI_BIAS if bias is not None else EPI_NONE) + (EPI_GELU_AUX if gelu else 0)
     if dgelu_aux is not None:
         assert bias is None and not gelu

@@ -310,12 +310,14 @@ te_mx_status te_mx_quantize_colwise_grouped(const void* x, int64_t total_m, int6
 
 te_mx_status te_mx_grouped_gemm_wgrad(int32_t num_groups, const int32_t* group_m, int64_t total_m,
                                       const uint8_t* dY, const uint8_t* s_dY, const uint8_t* X, const uint8_t* s_X,
-                                      int64_t M, int64_t N, int64_t ld_q, int64_t ld_s, void* D, void* stream) {
+                                      int64_t M, int64_t N, int64_t ld_q, int64_t ld_s, int32_t accumulate,
+                                      void* D, void* stream) {
     t_last_error[0] = '\0';
     if (num_groups < 1 || num_groups > 1024)
         return set_error(TE_MX_ERR_INVALID_ARG, "num_groups=%d must be in [1, 1024]", int(num_groups));
     if (!group_m || !dY || !s_dY || !X || !s_X || !D)
         return set_error(TE_MX_ERR_INVALID_ARG, "group_m, dY, s_dY, X, s_X and D are required");
+    if (accumulate != 0 && accumulate != 1) return set_error(TE_MX_ERR_INVALID_ARG, "accumulate must be 0 or 1");
     if (total_m < 0 || M < 0 || N < 0) return set_error(TE_MX_ERR_INVALID_ARG, "negative size");
     if (N % 16) return set_error(TE_MX_ERR_UNSUPPORTED_SHAPE, "N=%lld is not a multiple of 16", (long long)N);
     if (int64_t(num_groups) * M >= (int64_t(1) << 31) || N > (int64_t(1) << 31) - 256)
@@ -335,6 +337,7 @@ te_mx_status te_mx_grouped_gemm_wgrad(int32_t num_groups, const int32_t* group_m
     a.groups = num_groups;
     a.group_m = group_m;
     a.wgrad = true;
+    a.acc_f32 = accumulate == 1;
     a.ld_code = ld_q;
     a.total_m = total_m;
     return gemm_launch(a, static_cast<cudaStream_t>(stream));
@@ -367,8 +370,10 @@ static te_mx_status validate_gemm_common(const uint8_t* A, const uint8_t* sA, in
                                          const uint8_t* B, const uint8_t* sB, int64_t ld_sB,
                                          int64_t N, int64_t K, const void* bias, int32_t epi,
                                          void* D, void* aux) {
-    if (epi < TE_MX_EPI_NONE || epi > TE_MX_EPI_DGELU)
+    if (epi < TE_MX_EPI_NONE || epi > TE_MX_EPI_ACCUMULATE_F32)
         return set_error(TE_MX_ERR_INVALID_ARG, "unknown epilogue %d", epi);
+    if (epi == TE_MX_EPI_ACCUMULATE_F32 && (bias || aux))
+        return set_error(TE_MX_ERR_INVALID_ARG, "the accumulating epilogue takes no bias and no aux");
     if (!A || !sA || !B || !sB || !D) return set_error(TE_MX_ERR_INVALID_ARG, "A, sA, B, sB and D are required");
     const bool has_bias = epi == TE_MX_EPI_BIAS || epi == TE_MX_EPI_BIAS_GELU_AUX;
     const bool gelu = epi == TE_MX_EPI_GELU_AUX || epi == TE_MX_EPI_BIAS_GELU_AUX || epi == TE_MX_EPI_DGELU;
@@ -404,6 +409,7 @@ te_mx_status te_mx_gemm(const uint8_t* A, const uint8_t* sA, int64_t ld_sA,
     a.has_bias = epilogue == TE_MX_EPI_BIAS || epilogue == TE_MX_EPI_BIAS_GELU_AUX;
     a.gelu = epilogue == TE_MX_EPI_GELU_AUX || epilogue == TE_MX_EPI_BIAS_GELU_AUX;
     a.dgelu = epilogue == TE_MX_EPI_DGELU;
+    a.acc_f32 = epilogue == TE_MX_EPI_ACCUMULATE_F32;
     a.D = D; a.aux = aux; a.groups = 0; a.group_m = nullptr;
     return gemm_launch(a, static_cast<cudaStream_t>(stream));
 }
@@ -422,6 +428,8 @@ te_mx_status te_mx_grouped_gemm(int32_t num_groups, const int32_t* group_m, int6
     if (total_m < 0) return set_error(TE_MX_ERR_INVALID_ARG, "negative total_m");
     if (total_m == 0) return TE_MX_OK;
     if (total_m > (int64_t(1) << 31) - 256) return set_error(TE_MX_ERR_UNSUPPORTED_SHAPE, "total_m too large");
+    if (epilogue == TE_MX_EPI_ACCUMULATE_F32)
+        return set_error(TE_MX_ERR_INVALID_ARG, "the accumulating epilogue is for te_mx_gemm and the wgrad GEMM");
     te_mx_status st = validate_gemm_common(X, sX, ld_sX, W, sW, ld_sW, N, K, bias, epilogue, D, aux);
     if (st != TE_MX_OK) return st;
     if (int64_t(num_groups) * N > (int64_t(1) << 31) - 256) return set_error(TE_MX_ERR_UNSUPPORTED_SHAPE, "G*N too large");

@@ -107,6 +107,7 @@ struct GemmParams {
     uint16_t* D;
     uint16_t* aux;
     bool has_bias, gelu, dgelu;          // dgelu: aux is an input (forward pre-activation)
+    bool acc_f32;                        // D is fp32 and is accumulated into: D = D + acc
     bool wgrad;                          // grouped wgrad: per-group K range, D = [groups x M x N]
     int64_t total_m;                     // wgrad: bound on the token counts' sum
     int64_t ld_code, ld_sfa, ld_sfb;     // wgrad: operand pitches (capacities)
@@ -392,6 +393,16 @@ __device__ __forceinline__ void store_chunk(const uint32_t* acc, const GemmParam
     float v[16];
 #pragma unroll
     for (int i = 0; i < 16; ++i) v[i] = __uint_as_float(acc[i]);
+    if (p.acc_f32) {                             // D (fp32) += acc, one rounding per element
+        float4* d = reinterpret_cast<float4*>(reinterpret_cast<float*>(p.D) + row * p.N + n);
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+            const float4 o = d[q];
+            d[q] = make_float4(__fadd_rn(o.x, v[4 * q]), __fadd_rn(o.y, v[4 * q + 1]), __fadd_rn(o.z, v[4 * q + 2]),
+                               __fadd_rn(o.w, v[4 * q + 3]));
+        }
+        return;
+    }
     if (p.has_bias) {
         const uint4 b0 = __ldg(reinterpret_cast<const uint4*>(bias + n));
         const uint4 b1 = __ldg(reinterpret_cast<const uint4*>(bias + n + 8));
@@ -431,6 +442,47 @@ __device__ __forceinline__ void store_64_staged(uint32_t* acc, const GemmParams&
                                                 int64_t row0, int64_t row_end, int32_t n, uint32_t stage,
                                                 int lane) {
     float* v = reinterpret_cast<float*>(acc);
+    if (p.acc_f32) {
+        // D (fp32) += acc in two halves of 32 columns (128-byte rows): the old
+        // rows come in as whole lines through the staging tile, each lane adds
+        // its row, and the sums leave as whole lines again.
+        float* d = reinterpret_cast<float*>(p.D);
+        const int c = lane & 7;
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+            const int32_t nh = n + 32 * h;
+#pragma unroll
+            for (int i = 0; i < 8; ++i) {
+                const int r = 4 * i + (lane >> 3);
+                float4 o = make_float4(0.f, 0.f, 0.f, 0.f);
+                if (row0 + r < row_end && nh + 4 * c < p.N)
+                    o = *reinterpret_cast<const float4*>(d + (row0 + r) * p.N + nh + 4 * c);
+                sts128(stage + r * 128 + ((c ^ (r & 7)) << 4), __float_as_uint(o.x), __float_as_uint(o.y),
+                       __float_as_uint(o.z), __float_as_uint(o.w));
+            }
+            __syncwarp();
+#pragma unroll
+            for (int cc = 0; cc < 8; ++cc) {
+                const uint32_t a = stage + lane * 128 + ((cc ^ (lane & 7)) << 4);
+                const uint4 o = lds128(a);
+                const float* x = v + 32 * h + 4 * cc;
+                sts128(a, __float_as_uint(__fadd_rn(__uint_as_float(o.x), x[0])),
+                       __float_as_uint(__fadd_rn(__uint_as_float(o.y), x[1])),
+                       __float_as_uint(__fadd_rn(__uint_as_float(o.z), x[2])),
+                       __float_as_uint(__fadd_rn(__uint_as_float(o.w), x[3])));
+            }
+            __syncwarp();
+#pragma unroll
+            for (int i = 0; i < 8; ++i) {
+                const int r = 4 * i + (lane >> 3);
+                const uint4 w = lds128(stage + r * 128 + ((c ^ (r & 7)) << 4));
+                if (row0 + r < row_end && nh + 4 * c < p.N)
+                    st_global_v4(d + (row0 + r) * p.N + nh + 4 * c, w.x, w.y, w.z, w.w);
+            }
+            __syncwarp();
+        }
+        return;
+    }
     if (p.has_bias) {
 #pragma unroll
         for (int c = 0; c < 8; ++c) {
@@ -835,6 +887,7 @@ te_mx_status launch_gemm(const GemmArgs& a, int sms, unsigned int* status, cudaS
     p.has_bias = a.has_bias;
     p.gelu = a.gelu;
     p.dgelu = a.dgelu;
+    p.acc_f32 = a.acc_f32;
     p.wgrad = wg;
     p.total_m = a.total_m;
     p.ld_code = a.ld_code;

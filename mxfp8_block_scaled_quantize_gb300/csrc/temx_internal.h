@@ -34,6 +34,7 @@ struct GemmArgs {
     int64_t M, N, K;         // grouped: M = total_m
     const void* bias;        // bf16 [N] (grouped: [G x N]) or null
     bool has_bias, gelu, dgelu;
+    bool acc_f32;            // D is fp32 in/out: D = D + A B^T (no bias / GELU)
     void* D;
     void* aux;
     int32_t groups;          // 0: dense GEMM
@@ -56,8 +57,8 @@ struct LnQuantizeArgs {
     float eps;
     uint8_t* q_row; uint8_t* s_row; int64_t ld_s_row;
     uint8_t* q_col; uint8_t* s_col; int64_t ld_s_col;
-    float* mu;               // fp32 [rows] or null
-    float* rsigma;           // fp32 [rows] or null
+    float* mu;               // fp32 [rows]
+    float* rsigma;           // fp32 [rows]
 };
 te_mx_status ln_quantize_launch(const LnQuantizeArgs& a, cudaStream_t stream);
 

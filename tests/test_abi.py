@@ -81,6 +81,12 @@ def test_host_validation_rejects_bad_arguments_before_any_launch(lib):
         binding.te_mx_layernorm_quantize(16, 32, 64, 64, 16, 16, 1e-5, 16, 16, 16, 0, 0, 0, 0, 0, 0)
     with pytest.raises(binding.TemxError, match="UNSUPPORTED_SHAPE"):   # hidden too large
         binding.te_mx_layernorm_quantize(16, 32, 32800, 32800, 16, 16, 1e-5, 16, 16, 2064, 0, 0, 0, 16, 16, 0)
+    with pytest.raises(binding.TemxError, match="INVALID_ARG"):      # accumulate with a bias
+        binding.te_mx_gemm(16, 16, 16, 16, 16, 16, 128, 128, 128, 16, 5, 16, 0, 0, 0, 0)
+    with pytest.raises(binding.TemxError, match="INVALID_ARG"):      # accumulate is not for the grouped GEMM
+        binding.te_mx_grouped_gemm(2, 16, 128, 16, 16, 16, 16, 16, 16, 128, 128, 0, 5, 16, 0, 0, 0, 0)
+    with pytest.raises(binding.TemxError, match="INVALID_ARG"):      # wgrad accumulate flag not 0/1
+        binding.te_mx_grouped_gemm_wgrad(2, 16, 128, 16, 16, 16, 16, 128, 128, 128, 16, 2, 16, 0)
     # zero-sized problems are no-ops
     binding.te_mx_layernorm_quantize(16, 0, 64, 64, 16, 16, 1e-5, 16, 16, 16, 0, 0, 0, 0, 0, 0)
     binding.te_mx_block_quantize(0, 0, 128, 128, 1, 0, 0, 0, 0, 0, 0, 0)
