@@ -107,7 +107,6 @@ struct GemmParams {
     uint16_t* D;
     uint16_t* aux;
     bool has_bias, gelu, dgelu;          // dgelu: aux is an input (forward pre-activation)
-    bool acc_f32;                        // D is fp32 and is accumulated into: D = D + acc
     bool wgrad;                          // grouped wgrad: per-group K range, D = [groups x M x N]
     int64_t total_m;                     // wgrad: bound on the token counts' sum
     int64_t ld_code, ld_sfa, ld_sfb;     // wgrad: operand pitches (capacities)
@@ -151,13 +150,13 @@ struct __align__(16) SharedState {
 // column-bands in L2.  Grouped: group-major, then n-major over the group's
 // m-tiles.  Wgrad: group-major, every group the full M x N output over its
 // own K range.  `hint` carries the group found last time (tiles increase).
-template <int kTileM, typename SH>
+template <int kTileM, bool kWgrad, typename SH>
 __device__ __forceinline__ Tile map_tile(const GemmParams& p, const SH& sh, int64_t t, int32_t& hint) {
     Tile tl;
     tl.k0 = 0;
     tl.nk = p.k_iters;
     tl.sf0 = 0;
-    if (p.wgrad) {
+    if constexpr (kWgrad) {
         const int64_t per = int64_t(p.m_tiles) * p.n_tiles;
         const int32_t g = int32_t(t / per);
         const int32_t local = int32_t(t - int64_t(g) * per);
@@ -388,12 +387,13 @@ __device__ __forceinline__ void apply_dgelu8(float* v, uint4 w) {
 }
 
 // 16 accumulator columns of one row -> bias / GELU -> bf16 stores.
+template <bool kAcc>
 __device__ __forceinline__ void store_chunk(const uint32_t* acc, const GemmParams& p, const uint16_t* bias,
                                             int64_t row, int32_t n) {
     float v[16];
 #pragma unroll
     for (int i = 0; i < 16; ++i) v[i] = __uint_as_float(acc[i]);
-    if (p.acc_f32) {                             // D (fp32) += acc, one rounding per element
+    if constexpr (kAcc) {                        // D (fp32) += acc, one rounding per element
         float4* d = reinterpret_cast<float4*>(reinterpret_cast<float*>(p.D) + row * p.N + n);
 #pragma unroll
         for (int q = 0; q < 4; ++q) {
@@ -438,48 +438,25 @@ __device__ __forceinline__ void store_chunk(const uint32_t* acc, const GemmParam
 // bytes into the warp's staging tile (16-byte chunks XOR-swizzled by row, so
 // neither the writes nor the reads conflict), then every store instruction
 // writes 4 complete rows.
+template <bool kAcc>
 __device__ __forceinline__ void store_64_staged(uint32_t* acc, const GemmParams& p, const uint16_t* bias,
                                                 int64_t row0, int64_t row_end, int32_t n, uint32_t stage,
                                                 int lane) {
     float* v = reinterpret_cast<float*>(acc);
-    if (p.acc_f32) {
-        // D (fp32) += acc in two halves of 32 columns (128-byte rows): the old
-        // rows come in as whole lines through the staging tile, each lane adds
-        // its row, and the sums leave as whole lines again.
-        float* d = reinterpret_cast<float*>(p.D);
-        const int c = lane & 7;
+    if constexpr (kAcc) {
+        // D (fp32) += acc: each lane reads, adds and writes its own row, 16
+        // bytes at a time (whole 32-byte sectors).
+        const int64_t row = row0 + lane;
+        if (row < row_end) {
+            float4* d = reinterpret_cast<float4*>(reinterpret_cast<float*>(p.D) + row * p.N + n);
 #pragma unroll
-        for (int h = 0; h < 2; ++h) {
-            const int32_t nh = n + 32 * h;
-#pragma unroll
-            for (int i = 0; i < 8; ++i) {
-                const int r = 4 * i + (lane >> 3);
-                float4 o = make_float4(0.f, 0.f, 0.f, 0.f);
-                if (row0 + r < row_end && nh + 4 * c < p.N)
-                    o = *reinterpret_cast<const float4*>(d + (row0 + r) * p.N + nh + 4 * c);
-                sts128(stage + r * 128 + ((c ^ (r & 7)) << 4), __float_as_uint(o.x), __float_as_uint(o.y),
-                       __float_as_uint(o.z), __float_as_uint(o.w));
+            for (int q = 0; q < 16; ++q) {
+                if (n + 4 * q < p.N) {
+                    const float4 o = d[q];
+                    d[q] = make_float4(__fadd_rn(o.x, v[4 * q]), __fadd_rn(o.y, v[4 * q + 1]),
+                                       __fadd_rn(o.z, v[4 * q + 2]), __fadd_rn(o.w, v[4 * q + 3]));
+                }
             }
-            __syncwarp();
-#pragma unroll
-            for (int cc = 0; cc < 8; ++cc) {
-                const uint32_t a = stage + lane * 128 + ((cc ^ (lane & 7)) << 4);
-                const uint4 o = lds128(a);
-                const float* x = v + 32 * h + 4 * cc;
-                sts128(a, __float_as_uint(__fadd_rn(__uint_as_float(o.x), x[0])),
-                       __float_as_uint(__fadd_rn(__uint_as_float(o.y), x[1])),
-                       __float_as_uint(__fadd_rn(__uint_as_float(o.z), x[2])),
-                       __float_as_uint(__fadd_rn(__uint_as_float(o.w), x[3])));
-            }
-            __syncwarp();
-#pragma unroll
-            for (int i = 0; i < 8; ++i) {
-                const int r = 4 * i + (lane >> 3);
-                const uint4 w = lds128(stage + r * 128 + ((c ^ (r & 7)) << 4));
-                if (row0 + r < row_end && nh + 4 * c < p.N)
-                    st_global_v4(d + (row0 + r) * p.N + nh + 4 * c, w.x, w.y, w.z, w.w);
-            }
-            __syncwarp();
         }
         return;
     }
@@ -541,7 +518,7 @@ __device__ __forceinline__ void store_64_staged(uint32_t* acc, const GemmParams&
     }
 }
 
-template <int kPair>
+template <int kPair, bool kAcc, bool kWgrad>   // kAcc: fp32 D accumulated into; kWgrad: grouped wgrad
 __global__ void __launch_bounds__(kThreads, 1)   // 168 registers: 3 warps share a 16K-register sub-partition
 gemm_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_constant__ CUtensorMap map_b,
             const __grid_constant__ CUtensorMap map_sfa, const __grid_constant__ CUtensorMap map_sfb,
@@ -593,7 +570,7 @@ gemm_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_constant__ C
         tc_fence_before();
     }
     if (p.groups > 0 && warp == 2) {
-        if (p.wgrad) wgrad_prefix(p, sh, lane);
+        if constexpr (kWgrad) wgrad_prefix(p, sh, lane);
         else group_prefix<C::kTileM>(p, sh, lane);
     }
     __syncthreads();
@@ -609,7 +586,7 @@ gemm_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_constant__ C
             uint32_t stage = 0, phase = 0;
             bool ok = true;
             for (int64_t t = unit; t < total && ok; t += units) {
-                const Tile tl = map_tile<C::kTileM>(p, sh, t, hint);
+                const Tile tl = map_tile<C::kTileM, kWgrad>(p, sh, t, hint);
                 const int32_t a_row = tl.a_row + int32_t(rank) * kBM;
                 const int32_t b_row = tl.b_row + int32_t(rank) * C::kBRows;
                 for (int32_t k = 0; k < tl.nk; ++k) {
@@ -639,7 +616,8 @@ gemm_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_constant__ C
             bool ok = true;
             for (int64_t t = unit; t < total && ok; t += units, ++local) {
                 // K-steps of this tile (wgrad: the expert's own; 0 for an expert without tokens)
-                const int32_t nk = p.wgrad ? map_tile<C::kTileM>(p, sh, t, hint).nk : p.k_iters;
+                int32_t nk = p.k_iters;
+                if constexpr (kWgrad) nk = map_tile<C::kTileM, kWgrad>(p, sh, t, hint).nk;
                 if (local > 0) {
                     if (!wait_or_abort(smem_u32(&sh.tmem_empty), uint32_t(local - 1) & 1u, sh, p.status)) break;
                     tc_fence_after();
@@ -701,7 +679,7 @@ gemm_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_constant__ C
         Tile ltl{};
         auto seek = [&]() {               // the first tile from lt on that has scale groups
             for (; lt < total; lt += units) {
-                ltl = map_tile<C::kTileM>(p, sh, lt, lhint);
+                ltl = map_tile<C::kTileM, kWgrad>(p, sh, lt, lhint);
                 if (tile_groups(ltl) > 0) break;
             }
         };
@@ -732,7 +710,7 @@ gemm_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_constant__ C
         uint32_t j = 0;
         int32_t chint = 0;
         for (int64_t t = unit; t < total && ok; t += units) {
-            const Tile ct = map_tile<C::kTileM>(p, sh, t, chint);
+            const Tile ct = map_tile<C::kTileM, kWgrad>(p, sh, t, chint);
             const int32_t ngroups = tile_groups(ct);
             for (int32_t g = 0; g < ngroups && ok; ++g, ++j) {
                 const uint32_t slot = j % kSfRing, bit = (j / kSfRing) & 1u;
@@ -782,11 +760,11 @@ gemm_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_constant__ C
         const int e = warp - 2, q = warp & 3, h = e >> 2;
         int32_t hint = 0, local = 0;
         for (int64_t t = unit; t < total; t += units, ++local) {
-            const Tile tl = map_tile<C::kTileM>(p, sh, t, hint);
+            const Tile tl = map_tile<C::kTileM, kWgrad>(p, sh, t, hint);
             if (!wait_or_abort(smem_u32(&sh.tmem_full), uint32_t(local) & 1u, sh, p.status)) break;
             tc_fence_after();
             uint32_t acc0[64], acc1[64];
-            if (tl.nk > 0) {
+            if (!kWgrad || tl.nk > 0) {
                 const uint32_t taddr = tmem + (uint32_t(32 * q) << 16) + uint32_t(128 * h);
                 tmem_ld_32x32b_x64(taddr, acc0);
                 tmem_ld_32x32b_x64(taddr + 64, acc1);
@@ -815,8 +793,8 @@ gemm_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_constant__ C
                     const int32_t nb = tl.n0 + 128 * h;
                     const uint32_t stage = smem_u32(smem + C::kStages * C::kStageBytes + kSfRing * kSfGroupBytes) +
                                            uint32_t(e) * 4096u;
-                    if (nb < p.N) store_64_staged(acc0, p, bias, row0, tl.row_end, nb, stage, lane);
-                    if (nb + 64 < p.N) store_64_staged(acc1, p, bias, row0, tl.row_end, nb + 64, stage, lane);
+                    if (nb < p.N) store_64_staged<kAcc>(acc0, p, bias, row0, tl.row_end, nb, stage, lane);
+                    if (nb + 64 < p.N) store_64_staged<kAcc>(acc1, p, bias, row0, tl.row_end, nb + 64, stage, lane);
                 }
             } else if (row < tl.row_end) {
                 const uint16_t* bias = p.has_bias ? p.bias + int64_t(tl.group) * p.N : nullptr;
@@ -828,12 +806,12 @@ gemm_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_constant__ C
                 const uint32_t gap_ns = uint32_t(tl.nk) * 20u;
 #pragma unroll
                 for (int j = 0; j < 4; ++j) {
-                    if (nb + 16 * j < p.N) store_chunk(acc0 + 16 * j, p, bias, row, nb + 16 * j);
+                    if (nb + 16 * j < p.N) store_chunk<kAcc>(acc0 + 16 * j, p, bias, row, nb + 16 * j);
                     __nanosleep(gap_ns);
                 }
 #pragma unroll
                 for (int j = 0; j < 4; ++j) {
-                    if (nb + 64 + 16 * j < p.N) store_chunk(acc1 + 16 * j, p, bias, row, nb + 64 + 16 * j);
+                    if (nb + 64 + 16 * j < p.N) store_chunk<kAcc>(acc1 + 16 * j, p, bias, row, nb + 64 + 16 * j);
                     if (j < 3) __nanosleep(gap_ns);
                 }
             }
@@ -849,7 +827,7 @@ gemm_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_constant__ C
     }
 }
 
-template <int kPair>
+template <int kPair, bool kAcc, bool kWgrad>
 te_mx_status launch_gemm(const GemmArgs& a, int sms, unsigned int* status, cudaStream_t stream) {
     using C = Cfg<kPair>;
     const bool grouped = a.groups > 0;
@@ -887,7 +865,6 @@ te_mx_status launch_gemm(const GemmArgs& a, int sms, unsigned int* status, cudaS
     p.has_bias = a.has_bias;
     p.gelu = a.gelu;
     p.dgelu = a.dgelu;
-    p.acc_f32 = a.acc_f32;
     p.wgrad = wg;
     p.total_m = a.total_m;
     p.ld_code = a.ld_code;
@@ -898,7 +875,7 @@ te_mx_status launch_gemm(const GemmArgs& a, int sms, unsigned int* status, cudaS
     const int64_t slots = sms / kPair;                     // CTAs (pairs) resident at once
     int64_t units = grouped ? slots : (p.total_tiles < slots ? p.total_tiles : slots);
     if (units < 1) units = 1;
-    auto kern = gemm_kernel<kPair>;
+    auto kern = gemm_kernel<kPair, kAcc, kWgrad>;
     cudaError_t e = set_smem_attribute_once(reinterpret_cast<const void*>(kern), C::kSmemDyn);
     if (e != cudaSuccess) return cuda_status(e, "cudaFuncSetAttribute(gemm)");
     cudaLaunchConfig_t cfg = {};
@@ -945,7 +922,16 @@ te_mx_status gemm_launch(const GemmArgs& a, cudaStream_t stream) {
     // CTAs for small problems (finer tiles, more of them).
     const int64_t pair_tiles = ((a.M + 255) / 256) * ((a.N + kBN - 1) / kBN);
     const bool pair = a.wgrad ? a.M >= 256 : (a.groups > 0 ? a.M >= 256 * 8 : pair_tiles >= sms / 2);
-    return pair ? launch_gemm<2>(a, sms, status, stream) : launch_gemm<1>(a, sms, status, stream);
+    if (a.wgrad) {
+        if (a.acc_f32) return pair ? launch_gemm<2, true, true>(a, sms, status, stream)
+                                   : launch_gemm<1, true, true>(a, sms, status, stream);
+        return pair ? launch_gemm<2, false, true>(a, sms, status, stream)
+                    : launch_gemm<1, false, true>(a, sms, status, stream);
+    }
+    if (a.acc_f32) return pair ? launch_gemm<2, true, false>(a, sms, status, stream)
+                               : launch_gemm<1, true, false>(a, sms, status, stream);
+    return pair ? launch_gemm<2, false, false>(a, sms, status, stream)
+                : launch_gemm<1, false, false>(a, sms, status, stream);
 }
 
 }  // namespace temx
