@@ -50,7 +50,7 @@ def load_peaks():
 KERNEL_SOURCES = {"gemm": ["gemm.cu", "ptx.cuh"], "quant": ["quantize.cu", "e4m3.cuh", "ptx.cuh"],
                   "grouped": ["grouped_quantize.cu", "e4m3.cuh", "ptx.cuh"],
                   "block": ["block_quantize.cu", "e4m3.cuh", "ptx.cuh"],
-                  "ln": ["layernorm_quantize.cu", "e4m3.cuh", "ptx.cuh"]}
+                  "ln": ["layernorm_quantize.cu", "e4m3.cuh", "ptx.cuh", "units.cuh"]}
 
 
 def source_sha256(kernel_name: str) -> str:

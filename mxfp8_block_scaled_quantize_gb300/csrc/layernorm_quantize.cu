@@ -16,20 +16,24 @@
 //   rsigma = fl(1 / fl(sqrt(fl(var + eps)))),
 //   y      = fma(fl(fl(x - mu) * rsigma), gamma, beta).
 //
-// Two launches.  ln_stats_kernel: one warp per row reads the row twice (the
-// second time from L1/L2) and writes mu and rsigma.  ln_apply_kernel: every
-// warp runs its own TMA pipeline over units of 32 rows x 64 columns (like the
-// MXFP8 quantiser), normalises each unit with the row statistics and gamma /
-// beta, quantises it both ways (row-wise: lane = row; column-wise: lane = 2
-// columns x 32 rows, one column block per lane, the column pair a natural
-// f32x2 operand), stages the codes in the unit's own buffer and writes them
-// with TMA stores.  No CTA-wide barrier, no cluster.  For activations up to
-// the L2 size the apply kernel reads x mostly from L2.
+// Two launches.  ln_stats_kernel: persistent; one warp per row at a time,
+// each row copied into shared memory (two buffers per warp, so the next copy
+// overlaps this row's sums) and read there twice; writes mu and rsigma.
+// ln_apply_kernel: every warp runs its own TMA pipeline over units of 32 rows
+// x 64 columns (like the MXFP8 quantiser), normalises each unit with the row
+// statistics and gamma / beta, quantises it, stages the codes in the unit's
+// own buffer and writes them with TMA stores.  Both orientations evaluate y
+// once per element (lane = 2 columns x 32 rows: column blocks are lane-local,
+// row blocks are reduced through a transposed scratch); one orientation alone
+// uses its natural layout (row-wise: lane = row).  No CTA-wide barrier, no
+// cluster.  For activations up to the L2 size the apply kernel reads x mostly
+// from L2.
 #include <cuda_runtime.h>
 
 #include "e4m3.cuh"
 #include "ptx.cuh"
 #include "temx_internal.h"
+#include "units.cuh"
 
 namespace temx {
 
@@ -46,8 +50,9 @@ constexpr int kApplyStages = 3;
 constexpr int kSideBytes = kUnitRows * 16 + 2 * kUnitCols * 4;
 constexpr int kWarpBytes = kApplyStages * kUnitBytes + 2 * kSideBytes;
 constexpr int kApplySmem = kApplyWarps * kWarpBytes + 1024;
-constexpr int kStatsWarps = 8;                   // rows per statistics CTA
-constexpr int kStatsAcc = 4;                     // independent accumulators per lane
+constexpr int kStatsMaxWarps = 32;               // warps per statistics CTA, at most
+constexpr int kStatsSmem = 220 * 1024;           // two row buffers per warp
+constexpr int kStatsAcc = 8;                     // independent accumulators per lane
 
 struct ApplyParams {
     int64_t rows, hidden;
@@ -109,6 +114,15 @@ __device__ __forceinline__ uint64_t lds64(uint32_t addr) {
 __device__ __forceinline__ void lds128x2(uint32_t addr, uint64_t& a, uint64_t& b) {
     asm volatile("ld.shared.v2.b64 {%0, %1}, [%2];" : "=l"(a), "=l"(b) : "r"(addr));
 }
+__device__ __forceinline__ void sts32(uint32_t addr, uint32_t v) {
+    asm volatile("st.shared.b32 [%0], %1;" :: "r"(addr), "r"(v) : "memory");
+}
+__device__ __forceinline__ void sts64(uint32_t addr, uint64_t v) {
+    asm volatile("st.shared.b64 [%0], %1;" :: "r"(addr), "l"(v) : "memory");
+}
+__device__ __forceinline__ void sts16(uint32_t addr, uint32_t v) {
+    asm volatile("st.shared.b16 [%0], %1;" :: "r"(addr), "h"(static_cast<uint16_t>(v)) : "memory");
+}
 
 // Pairwise sum of n fp32 pairs (log2 n levels), then the two halves: a tree of
 // depth log2(n) + 1 over 2n values.
@@ -158,9 +172,9 @@ __device__ __forceinline__ float warp_sum(float v) {
 // One warp per row.  The row is copied into shared memory with one bulk
 // asynchronous copy, so both passes read it there and x is read from HBM once.
 // A lane reads vectors lane, lane + 32, ... of the row (8 elements each, a
-// tree of depth 3) into kStatsAcc accumulators in turn (four vectors per step),
-// the accumulators are added pairwise and the lanes by a butterfly: for rows
-// of at most 32768 elements the longest chain is 3 + 32 + 2 + 5 = 42
+// tree of depth 3) into kStatsAcc accumulators in turn (eight vectors per
+// step), the accumulators are added pairwise and the lanes by a butterfly: for
+// rows of at most 32768 elements the longest chain is 3 + 16 + 3 + 5 = 27
 // additions.
 // L2 cache policies: keep x in L2 for the apply kernel (evict last), which
 // then reads it for the last time (evict first).
@@ -191,7 +205,9 @@ __device__ __forceinline__ void tma_load_2d_hint(uint32_t dst, const CUtensorMap
 
 template <bool kSquares>
 __device__ __forceinline__ float row_pass(uint32_t row, int nvec, int lane, uint64_t mm) {
-    float acc[kStatsAcc] = {0.0f, 0.0f, 0.0f, 0.0f};
+    float acc[kStatsAcc];
+#pragma unroll
+    for (int a = 0; a < kStatsAcc; ++a) acc[a] = 0.0f;
     for (int v = lane; v < nvec; v += 32 * kStatsAcc) {
 #pragma unroll
         for (int a = 0; a < kStatsAcc; ++a)
@@ -200,39 +216,102 @@ __device__ __forceinline__ float row_pass(uint32_t row, int nvec, int lane, uint
                 acc[a] = __fadd_rn(acc[a], kSquares ? sqdev8(x, mm) : sum8(x));
             }
     }
-    return warp_sum(__fadd_rn(__fadd_rn(acc[0], acc[1]), __fadd_rn(acc[2], acc[3])));
+#pragma unroll
+    for (int w = kStatsAcc / 2; w >= 1; w >>= 1)
+#pragma unroll
+        for (int a = 0; a < w; ++a) acc[a] = __fadd_rn(acc[a], acc[a + w]);
+    return warp_sum(acc[0]);
 }
 
-__global__ void __launch_bounds__(kStatsWarps * 32)
+// Barrier over the `n` threads of one row group (named barrier `id`) that
+// also returns the AND of `ok` over them.
+__device__ __forceinline__ bool group_and(bool ok, int id, int n) {
+    uint32_t r;
+    asm volatile(
+        "{\n\t.reg .pred p, q;\n\t"
+        "setp.ne.u32 p, %1, 0;\n\t"
+        "bar.red.and.pred q, %2, %3, p;\n\t"
+        "selp.u32 %0, 1, 0, q;\n\t}"
+        : "=r"(r) : "r"(uint32_t(ok)), "r"(id), "r"(n) : "memory");
+    return r != 0;
+}
+
+// Persistent.  A row is shared by a group of P warps (P = 1, 2 or 4), warp p
+// of the group taking the p-th contiguous part of it; group g of the grid
+// takes rows g, g + G, g + 2G, ... (G groups in the grid).  Each warp copies
+// its part through two buffers, so the next row's copy is in flight while
+// this row is summed.  The parts' sums meet in shared memory behind the
+// group's named barrier and are added in a fixed order (depth + 2 at most).
+// The copies keep x in L2 for the apply kernel (evict last).
+__global__ void __launch_bounds__(kStatsMaxWarps * 32)
 ln_stats_kernel(const uint16_t* __restrict__ x, int64_t rows, int64_t hidden, int64_t ld_x, float eps,
-                float* __restrict__ mu_out, float* __restrict__ rs_out, int rows_per_cta, unsigned int* status) {
+                float* __restrict__ mu_out, float* __restrict__ rs_out, int parts, unsigned int* status) {
     extern __shared__ __align__(16) uint8_t rowbuf[];
-    __shared__ __align__(8) uint64_t bars[kStatsWarps];
+    __shared__ __align__(8) uint64_t bars[kStatsMaxWarps][2];
+    __shared__ float part_sum[kStatsMaxWarps][2];          // [group * parts + part][S, S2]
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int64_t r = int64_t(blockIdx.x) * rows_per_cta + warp;
-    if (warp >= rows_per_cta || r >= rows) return;
-    const uint32_t bytes = uint32_t(hidden) * 2;
-    const uint32_t row = smem_u32(rowbuf) + warp * bytes;
-    const uint32_t bar = smem_u32(&bars[warp]);
+    const int groups = int(blockDim.x >> 5) / parts;
+    const int g = warp / parts, part = warp % parts;
+    const int64_t gg = int64_t(blockIdx.x) * groups + g, ngroups = int64_t(gridDim.x) * groups;
+    if (gg >= rows) return;                                // the whole group leaves
+    const int64_t n_mine = (rows - gg + ngroups - 1) / ngroups;
+    const int64_t part_elems = hidden / parts;             // a multiple of 8
+    const uint32_t bytes = uint32_t(part_elems) * 2;
+    const uint32_t buf = smem_u32(rowbuf) + uint32_t(warp) * 2 * bytes;
+    const uint16_t* src = x + part * part_elems;
+    const uint64_t policy = l2_policy_evict_last();
     if (lane == 0) {
-        mbar_init(bar, 1);
+        mbar_init(smem_u32(&bars[warp][0]), 1);
+        mbar_init(smem_u32(&bars[warp][1]), 1);
         fence_mbarrier_init();
-        mbar_arrive_expect_tx(bar, bytes);
-        bulk_load(row, x + r * ld_x, bytes, bar, l2_policy_evict_last());
+        for (int s = 0; s < 2 && s < n_mine; ++s) {
+            const uint32_t bar = smem_u32(&bars[warp][s]);
+            mbar_arrive_expect_tx(bar, bytes);
+            bulk_load(buf + s * bytes, src + (gg + s * ngroups) * ld_x, bytes, bar, policy);
+        }
     }
     __syncwarp();
-    if (!__all_sync(0xFFFFFFFFu, mbar_wait(bar, 0, status))) {
-        if (lane == 0) mbar_wait(bar, 0, status);        // gave up: wait once more for the copy in flight
-        return;
-    }
-    const int nvec = int(hidden / 8);
+    const int nvec = int(part_elems / 8);
     const float h = float(hidden);
-    const float mu = __fdiv_rn(row_pass<false>(row, nvec, lane, 0), h);
-    const float var = __fdiv_rn(row_pass<true>(row, nvec, lane, pack2(mu, mu)), h);
-    const float rs = __frcp_rn(__fsqrt_rn(__fadd_rn(var, eps)));
-    if (lane == 0) {
-        mu_out[r] = mu;
-        rs_out[r] = rs;
+    const int nthreads = parts * 32;
+    auto combine = [&](float v, int k) {                 // the group's sum of v, same in every warp
+        if (parts == 1) return v;
+        if (lane == 0) part_sum[warp][k] = v;
+        group_and(true, g, nthreads);
+        const int w0 = g * parts;
+        float a = __fadd_rn(part_sum[w0][k], part_sum[w0 + 1][k]);
+        if (parts == 4) a = __fadd_rn(a, __fadd_rn(part_sum[w0 + 2][k], part_sum[w0 + 3][k]));
+        return a;
+    };
+    for (int64_t i = 0; i < n_mine; ++i) {
+        const int s = int(i & 1);
+        const uint32_t bar = smem_u32(&bars[warp][s]);
+        bool ok = __all_sync(0xFFFFFFFFu, mbar_wait(bar, uint32_t((i >> 1) & 1), status));
+        if (parts > 1) ok = group_and(ok, g, nthreads);     // the group leaves together
+        if (!ok) {
+            // Gave up: let this warp's copies still in flight land before leaving.
+            if (lane == 0)
+                for (int64_t j = i; j < i + 2 && j < n_mine; ++j)
+                    mbar_wait(smem_u32(&bars[warp][j & 1]), uint32_t((j >> 1) & 1), status);
+            return;
+        }
+        const uint32_t row = buf + s * bytes;
+        const float mu = __fdiv_rn(combine(row_pass<false>(row, nvec, lane, 0), 0), h);
+        const float var = __fdiv_rn(combine(row_pass<true>(row, nvec, lane, pack2(mu, mu)), 1), h);
+        const float rs = __frcp_rn(__fsqrt_rn(__fadd_rn(var, eps)));
+        // row_pass ends in a butterfly over every lane: the buffer has been read
+        if (lane == 0) {
+            if (i + 2 < n_mine) {
+                mbar_arrive_expect_tx(bar, bytes);
+                bulk_load(row, src + (gg + (i + 2) * ngroups) * ld_x, bytes, bar, policy);
+            }
+            if (part == 0) {
+                const int64_t r = gg + i * ngroups;
+                mu_out[r] = mu;
+                rs_out[r] = rs;
+            }
+        }
+        __syncwarp();
     }
 }
 
@@ -366,6 +445,126 @@ __device__ __forceinline__ void quantize_unit(const ApplyParams& p, uint32_t uni
     }
 }
 
+// Both orientations from one evaluation of y per element.  Lane l holds
+// columns 2l, 2l + 1 of all 32 rows (the column pair is the f32x2 operand), so
+// the column blocks are lane-local.  A row block spans 16 lanes: every lane
+// writes its per-row maxima into the consumed unit (a 32 x 32 fp32 scratch at
+// the addresses the lane read x from), lane r reduces row r's two blocks, and
+// the two row scales come back through the statistics area of the side data
+// as (m, m) pairs.  Row codes are staged one 16-bit pair per lane and row,
+// column codes as in the column-wise path.
+__device__ __forceinline__ void quantize_unit_both(const ApplyParams& p, uint32_t unit, int64_t r0, int64_t c0,
+                                                   int lane, uint32_t stat, uint32_t gaddr, uint32_t baddr) {
+    const int valid = p.hidden - c0 < kUnitCols ? int(p.hidden - c0) : kUnitCols;
+    const uint64_t g2 = lds64(gaddr + lane * 8), b2 = lds64(baddr + lane * 8);
+    const uint32_t cbase = unit + ((lane & 3) << 2);
+    const int ch = lane >> 2;
+    uint64_t y[32];
+#pragma unroll
+    for (int r = 0; r < 32; ++r) {
+        const uint32_t x = lds32(cbase + r * 128 + ((ch ^ (r & 7)) << 4));
+        uint64_t mu2, rs2;
+        lds128x2(stat + r * 16, mu2, rs2);
+        y[r] = fma2(mul2(sub2(bf2(x), mu2), rs2), g2, b2);
+    }
+    __syncwarp();                                // every lane has read x and the statistics
+    // row partial maxima of this lane's column pair, where the lane read x
+#pragma unroll
+    for (int r = 0; r < 32; ++r)
+        sts32(cbase + r * 128 + ((ch ^ (r & 7)) << 4), __float_as_uint(maxabs(lo2(y[r]), hi2(y[r]))));
+    __syncwarp();
+    float t[32];                                 // row `lane` of the scratch: lanes 0..15, then 16..31
+#pragma unroll
+    for (int c = 0; c < 8; ++c) {
+        const uint4 v = lds128(unit + lane * 128 + ((c ^ (lane & 7)) << 4));
+        t[4 * c + 0] = __uint_as_float(v.x);
+        t[4 * c + 1] = __uint_as_float(v.y);
+        t[4 * c + 2] = __uint_as_float(v.z);
+        t[4 * c + 3] = __uint_as_float(v.w);
+    }
+#pragma unroll
+    for (int s2 = 8; s2 >= 1; s2 >>= 1)
+#pragma unroll
+        for (int i = 0; i < s2; ++i) {
+            t[i] = maxabs(t[i], t[i + s2]);
+            t[16 + i] = maxabs(t[16 + i], t[16 + i + s2]);
+        }
+    const uint32_t sr0 = mx_scale_byte_f32(t[0]), sr1 = mx_scale_byte_f32(t[16]);
+    {
+        const int64_t r = r0 + lane;
+        if (r < p.rows) {
+            uint8_t* sp = p.s_row + r * p.ld_s_row + (c0 >> 5);
+            if (valid > 32) st_global_u16(sp, sr0 | (sr1 << 8));
+            else st_global_u8(sp, sr0);
+        }
+        const float m0 = inv_scale(sr0), m1 = inv_scale(sr1);   // -inf for a non-finite block
+        sts64(stat + lane * 8, pack2(m0, m0));
+        sts64(stat + 256 + lane * 8, pack2(m1, m1));
+    }
+    const bool nonfinite = __any_sync(0xFFFFFFFFu, sr0 == 0xFFu || sr1 == 0xFFu);
+    __syncwarp();                                // row scales visible; the scratch is consumed
+    {
+        const uint32_t ms = stat + (lane >> 4) * 256;      // this lane's row block
+        const uint32_t rcode = unit + (lane & 7) * 2;
+        const int rch = lane >> 3;
+#pragma unroll
+        for (int r = 0; r < 32; r += 2) {
+            uint64_t m_a, m_b;
+            lds128x2(ms + r * 8, m_a, m_b);
+            const uint64_t a = mul2(y[r], m_a), b = mul2(y[r + 1], m_b);
+            uint32_t ca = cvt_e4m3x2(lo2(a), hi2(a)), cb = cvt_e4m3x2(lo2(b), hi2(b));
+            if (nonfinite) {
+                if (__float_as_uint(lo2(m_a)) == 0xFF800000u) ca = 0x7F7Fu;
+                if (__float_as_uint(lo2(m_b)) == 0xFF800000u) cb = 0x7F7Fu;
+            }
+            sts16(rcode + r * 64 + ((rch ^ ((r >> 1) & 3)) << 4), ca);
+            sts16(rcode + (r + 1) * 64 + ((rch ^ (((r + 1) >> 1) & 3)) << 4), cb);
+        }
+    }
+    // column blocks: lane-local
+    float ml[16], mh[16];
+#pragma unroll
+    for (int i = 0; i < 16; ++i) {
+        ml[i] = maxabs(lo2(y[2 * i]), lo2(y[2 * i + 1]));
+        mh[i] = maxabs(hi2(y[2 * i]), hi2(y[2 * i + 1]));
+    }
+#pragma unroll
+    for (int s2 = 8; s2 >= 1; s2 >>= 1)
+#pragma unroll
+        for (int i = 0; i < s2; ++i) {
+            ml[i] = maxabs(ml[i], ml[i + s2]);
+            mh[i] = maxabs(mh[i], mh[i + s2]);
+        }
+    const uint32_t s_lo = mx_scale_byte_f32(ml[0]), s_hi = mx_scale_byte_f32(mh[0]);
+    const uint64_t m2 = pack2(inv_scale(s_lo), inv_scale(s_hi));
+    uint32_t cc_lo[8], cc_hi[8];
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+        const uint64_t a = mul2(y[4 * i], m2), b = mul2(y[4 * i + 1], m2);
+        const uint64_t c = mul2(y[4 * i + 2], m2), d = mul2(y[4 * i + 3], m2);
+        cc_lo[i] = cvt_e4m3x2(lo2(a), lo2(b)) | (cvt_e4m3x2(lo2(c), lo2(d)) << 16);
+        cc_hi[i] = cvt_e4m3x2(hi2(a), hi2(b)) | (cvt_e4m3x2(hi2(c), hi2(d)) << 16);
+    }
+    if (s_lo == 0xFFu) {
+#pragma unroll
+        for (int i = 0; i < 8; ++i) cc_lo[i] = 0x7F7F7F7Fu;
+    }
+    if (s_hi == 0xFFu) {
+#pragma unroll
+        for (int i = 0; i < 8; ++i) cc_hi[i] = 0x7F7F7F7Fu;
+    }
+    const uint32_t cb = unit + 2048 + lane * 64;            // column 2 lane, then 2 lane + 1: 32 bytes each
+    sts128(cb, cc_lo[0], cc_lo[1], cc_lo[2], cc_lo[3]);
+    sts128(cb + 16, cc_lo[4], cc_lo[5], cc_lo[6], cc_lo[7]);
+    sts128(cb + 32, cc_hi[0], cc_hi[1], cc_hi[2], cc_hi[3]);
+    sts128(cb + 48, cc_hi[4], cc_hi[5], cc_hi[6], cc_hi[7]);
+    if (2 * lane < valid) {                                   // valid is a multiple of 32
+        uint8_t* sp = p.s_col + (c0 + 2 * lane) * p.ld_s_col + (r0 >> 5);
+        st_global_u8(sp, s_lo);
+        st_global_u8(sp + p.ld_s_col, s_hi);
+    }
+}
+
 template <bool kRowwise, bool kColwise>
 __global__ void __launch_bounds__(kApplyWarps * 32, 1)
 ln_apply_kernel(const __grid_constant__ CUtensorMap x_map, const __grid_constant__ CUtensorMap qrow_map,
@@ -382,19 +581,18 @@ ln_apply_kernel(const __grid_constant__ CUtensorMap x_map, const __grid_constant
     const uint32_t ring = smem_u32(smem + warp * (kApplyStages * kUnitBytes));
     // two side areas per warp (this unit's, the next unit's): stat [32][4], gamma [64], beta [64]
     uint8_t* side = smem + kApplyWarps * kApplyStages * kUnitBytes + warp * (2 * kSideBytes);
-    auto origin = [&](int64_t i, int64_t& r0, int64_t& c0) {
-        const int64_t u = gwarp + i * nwarps;
-        r0 = (u / p.col_units) * kUnitRows;
-        c0 = (u % p.col_units) * kUnitCols;
-    };
-    auto load_side = [&](int64_t i, float& m, float& rs, uint32_t& g2, uint32_t& b2) {
-        int64_t r0, c0;
-        origin(i, r0, c0);
-        const int64_t r = r0 + lane, c = c0 + 2 * lane;
+    // (band, column unit) of this unit, of the next one and of the next load
+    const UnitWalk walk(nwarps, p.col_units);
+    int32_t band, col;
+    walk.start(gwarp, band, col);
+    int32_t nband = band, ncol = col;
+    walk.step(nband, ncol);
+    auto load_side = [&](int32_t b, int32_t c, float& m, float& rs, uint32_t& g2, uint32_t& b2) {
+        const int64_t r = int64_t(b) * kUnitRows + lane, cc = int64_t(c) * kUnitCols + 2 * lane;
         m = r < p.rows ? p.mu[r] : 0.0f;
         rs = r < p.rows ? p.rsigma[r] : 0.0f;
-        g2 = c < p.hidden ? *reinterpret_cast<const uint32_t*>(p.gamma + c) : 0u;
-        b2 = c < p.hidden ? *reinterpret_cast<const uint32_t*>(p.beta + c) : 0u;
+        g2 = cc < p.hidden ? *reinterpret_cast<const uint32_t*>(p.gamma + cc) : 0u;
+        b2 = cc < p.hidden ? *reinterpret_cast<const uint32_t*>(p.beta + cc) : 0u;
     };
     auto store_side = [&](uint8_t* area, float m, float rs, uint32_t g2, uint32_t b2) {
         reinterpret_cast<float4*>(area)[lane] = make_float4(m, m, rs, rs);
@@ -403,6 +601,7 @@ ln_apply_kernel(const __grid_constant__ CUtensorMap x_map, const __grid_constant
     };
 
     const uint64_t policy = l2_policy_evict_first();
+    int32_t lband = band, lcol = col;                  // next unit to load (lane 0)
     if (lane == 0) {
         tma_prefetch_desc(&x_map);
         if (kRowwise) tma_prefetch_desc(&qrow_map);
@@ -410,31 +609,30 @@ ln_apply_kernel(const __grid_constant__ CUtensorMap x_map, const __grid_constant
         for (int s = 0; s < kApplyStages; ++s) mbar_init(smem_u32(&bars[warp][s]), 1);
         fence_mbarrier_init();
         for (int s = 0; s < kApplyStages && s < n_mine; ++s) {
-            int64_t r0, c0;
-            origin(s, r0, c0);
             const uint32_t bar = smem_u32(&bars[warp][s]);
             mbar_arrive_expect_tx(bar, kUnitBytes);
-            tma_load_2d_hint(ring + s * kUnitBytes, &x_map, bar, int32_t(c0), int32_t(r0), policy);
+            tma_load_2d_hint(ring + s * kUnitBytes, &x_map, bar, lcol * kUnitCols, lband * kUnitRows, policy);
+            walk.step(lband, lcol);
         }
     }
     {
         float m, rs;
         uint32_t g2, b2;
-        load_side(0, m, rs, g2, b2);
+        load_side(band, col, m, rs, g2, b2);
         store_side(side, m, rs, g2, b2);
     }
     __syncwarp();
 
+    int s = 0;
+    uint32_t phase = 0;
     for (int64_t i = 0; i < n_mine; ++i) {
-        const int s = int(i % kApplyStages);
         const uint32_t bar = smem_u32(&bars[warp][s]);
-        int64_t r0, c0;
-        origin(i, r0, c0);
+        const int64_t r0 = int64_t(band) * kUnitRows, c0 = int64_t(col) * kUnitCols;
         // the next unit's statistics and gamma / beta, loaded now, stored after this unit
         float nm = 0.0f, nrs = 0.0f;
         uint32_t ng = 0, nb = 0;
-        if (i + 1 < n_mine) load_side(i + 1, nm, nrs, ng, nb);
-        if (!__all_sync(0xFFFFFFFFu, mbar_wait(bar, uint32_t((i / kApplyStages) & 1), p.status))) {
+        if (i + 1 < n_mine) load_side(nband, ncol, nm, nrs, ng, nb);
+        if (!__all_sync(0xFFFFFFFFu, mbar_wait(bar, phase, p.status))) {
             // Gave up: let this warp's loads still in flight land before leaving.
             if (lane == 0)
                 for (int64_t j = i; j < i + kApplyStages && j < n_mine; ++j)
@@ -443,7 +641,11 @@ ln_apply_kernel(const __grid_constant__ CUtensorMap x_map, const __grid_constant
         }
         const uint32_t unit = ring + s * kUnitBytes;
         const uint32_t sb = smem_u32(side) + uint32_t(i & 1) * kSideBytes;
-        quantize_unit<kRowwise, kColwise>(p, unit, r0, c0, lane, sb, sb + kUnitRows * 16, sb + kUnitRows * 16 + kUnitCols * 4);
+        if constexpr (kRowwise && kColwise)
+            quantize_unit_both(p, unit, r0, c0, lane, sb, sb + kUnitRows * 16, sb + kUnitRows * 16 + kUnitCols * 4);
+        else
+            quantize_unit<kRowwise, kColwise>(p, unit, r0, c0, lane, sb, sb + kUnitRows * 16,
+                                              sb + kUnitRows * 16 + kUnitCols * 4);
         if (i + 1 < n_mine) store_side(side + ((i + 1) & 1) * kSideBytes, nm, nrs, ng, nb);
         fence_proxy_async_smem();                // make the staged codes visible to the TMA engine
         __syncwarp();
@@ -453,13 +655,19 @@ ln_apply_kernel(const __grid_constant__ CUtensorMap x_map, const __grid_constant
             bulk_commit();
             if (i + kApplyStages < n_mine) {
                 bulk_wait_read_all();            // the stores have read the unit: refill it
-                int64_t rn, cn;
-                origin(i + kApplyStages, rn, cn);
                 mbar_arrive_expect_tx(bar, kUnitBytes);
-                tma_load_2d_hint(unit, &x_map, bar, int32_t(cn), int32_t(rn), policy);
+                tma_load_2d_hint(unit, &x_map, bar, lcol * kUnitCols, lband * kUnitRows, policy);
+                walk.step(lband, lcol);
             }
         }
         __syncwarp();
+        band = nband;
+        col = ncol;
+        walk.step(nband, ncol);
+        if (++s == kApplyStages) {
+            s = 0;
+            phase ^= 1u;
+        }
     }
     if (lane == 0) bulk_wait_all();
 }
@@ -478,7 +686,7 @@ cudaError_t launch_apply(const CUtensorMap& xm, const CUtensorMap& qr, const CUt
 
 }  // namespace
 
-int64_t ln_quantize_max_hidden() { return 32768; }   // keeps the longest chain of additions at 42
+int64_t ln_quantize_max_hidden() { return 32768; }   // keeps the longest chain of additions at 27
 
 te_mx_status ln_quantize_launch(const LnQuantizeArgs& a, cudaStream_t stream) {
     const bool rowwise = a.q_row != nullptr, colwise = a.q_col != nullptr;
@@ -487,22 +695,25 @@ te_mx_status ln_quantize_launch(const LnQuantizeArgs& a, cudaStream_t stream) {
     unsigned int* status = nullptr;
     te_mx_status st = device_status_ptr(&status);
     if (st != TE_MX_OK) return st;
-    // rows per statistics CTA: as many as fit in ~110 KB (two CTAs per SM), at most 8
-    const int64_t row_bytes = a.hidden * 2;
-    const int rpc = int(row_bytes * kStatsWarps <= 110 * 1024 ? kStatsWarps
-                        : (110 * 1024 / row_bytes > 1 ? 110 * 1024 / row_bytes : 1));
-    const size_t stats_smem = size_t(rpc) * size_t(row_bytes);
-    cudaError_t e = set_smem_attribute_once(reinterpret_cast<const void*>(ln_stats_kernel), 110 * 1024);
+    int sms = 0;
+    if ((st = device_sm_count(&sms)) != TE_MX_OK) return st;
+    // statistics: one CTA per SM with as many row groups as two row buffers
+    // each allow (at most 32), P warps per row so that G x P <= 32
+    const int64_t buf_bytes = 2 * a.hidden * 2;
+    const int64_t fit = kStatsSmem / buf_bytes;
+    const int groups = int(fit < kStatsMaxWarps ? fit : kStatsMaxWarps);
+    const int parts = groups <= kStatsMaxWarps / 4 ? 4 : (groups <= kStatsMaxWarps / 2 ? 2 : 1);
+    const size_t stats_smem = size_t(groups) * size_t(buf_bytes);
+    cudaError_t e = set_smem_attribute_once(reinterpret_cast<const void*>(ln_stats_kernel), kStatsSmem);
     if (e != cudaSuccess) return cuda_status(e, "layernorm statistics kernel attributes");
-    const int64_t blocks = (a.rows + rpc - 1) / rpc;
-    ln_stats_kernel<<<unsigned(blocks), kStatsWarps * 32, stats_smem, stream>>>(
-        static_cast<const uint16_t*>(a.x), a.rows, a.hidden, a.ld_x, a.eps, a.mu, a.rsigma, rpc, status);
+    const int64_t want = (a.rows + groups - 1) / groups;
+    const int64_t blocks = want < int64_t(sms) ? want : int64_t(sms);
+    ln_stats_kernel<<<unsigned(blocks), groups * parts * 32, stats_smem, stream>>>(
+        static_cast<const uint16_t*>(a.x), a.rows, a.hidden, a.ld_x, a.eps, a.mu, a.rsigma, parts, status);
     e = cudaGetLastError();
     if (e != cudaSuccess) return cuda_status(e, "layernorm statistics kernel launch");
     if (!rowwise && !colwise) return TE_MX_OK;
 
-    int sms = 0;
-    if ((st = device_sm_count(&sms)) != TE_MX_OK) return st;
     CUtensorMap xm, qr, qc;
     if ((st = encode_tensor_map_2d(&xm, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, a.x, uint64_t(a.hidden),
                                    uint64_t(a.rows), uint64_t(a.ld_x) * 2, kUnitCols, kUnitRows,
