@@ -189,8 +189,9 @@ TEMX_API te_mx_status te_mx_block_quantize(const void* x, int64_t rows, int64_t 
  * its input (q_row/s_row: blocks of 32 along the row; q_col/s_col: blocks of
  * 32 rows of a column, stored transposed).  The normalised tensor is never
  * written.  Arithmetic is fp32: mu = fl(S/H) with S a sum of the row in fp32
- * whose longest chain of additions is at most 64; var likewise from
- * fl(fl(x - mu)^2); rsigma = fl(1/fl(sqrt(fl(var + eps)))); y =
+ * whose longest chain of additions is at most 64; var likewise from the
+ * squares of fl(x - mu), each rounded on its own or fused into the addition
+ * that accumulates it; rsigma = fl(1/fl(sqrt(fl(var + eps)))); y =
  * fma(fl(fl(x - mu) rsigma), gamma, beta) with one rounding.  Codes and scales
  * are the exact MXFP8 quantisation of that fp32 y; the sums are taken in a
  * fixed order (deterministic).  Two kernels run on `stream`: the statistics,

@@ -11,14 +11,18 @@
 // then y is MXFP8-quantised exactly as te_mx_quantize quantises its input
 // (blocks of 32, scale byte = max(exponent field(amax) - 8, 0), E4M3 RNE
 // satfinite, 0xFF / 0x7F for non-finite blocks).  Everything is fp32:
-//   mu     = fl(S / H), S a tree sum of the row (depth <= 64 additions),
-//   var    = fl(S2 / H), S2 a tree sum of fl(fl(x - mu)^2),
+//   mu     = fl(S / H), S a sum of the row (at most 64 additions on the
+//            path of any element),
+//   var    = fl(S2 / H), S2 a sum of the squares of fl(x - mu) (the same
+//            depth; each square rounded on its own or fused into the
+//            addition that accumulates it),
 //   rsigma = fl(1 / fl(sqrt(fl(var + eps)))),
 //   y      = fma(fl(fl(x - mu) * rsigma), gamma, beta).
 //
-// Two launches.  ln_stats_kernel: persistent; one warp per row at a time,
-// each row copied into shared memory (two buffers per warp, so the next copy
-// overlaps this row's sums) and read there twice; writes mu and rsigma.
+// Two launches.  ln_stats_kernel: persistent; four warps per row (one for
+// rows under 2048 elements), each warp's part of the row copied into shared
+// memory (two buffers per warp, so the next copy overlaps this row's sums)
+// and read there twice; writes mu and rsigma.
 // ln_apply_kernel: every warp runs its own TMA pipeline over units of 32 rows
 // x 64 columns (like the MXFP8 quantiser), normalises each unit with the row
 // statistics and gamma / beta, quantises it, stages the codes in the unit's
@@ -53,6 +57,7 @@ constexpr int kApplySmem = kApplyWarps * kWarpBytes + 1024;
 constexpr int kStatsMaxWarps = 32;               // warps per statistics CTA, at most
 constexpr int kStatsSmem = 220 * 1024;           // two row buffers per warp
 constexpr int kStatsAcc = 8;                     // independent accumulators per lane
+constexpr int kStatsParts = 4;                   // warps per row (long rows)
 
 struct ApplyParams {
     int64_t rows, hidden;
@@ -149,18 +154,25 @@ __device__ __forceinline__ uint32_t sw64(int r, int c) { return uint32_t(r * 64 
 
 // ---------------------------------------------------------------- statistics
 
-// Sum of 8 bf16 (one 16-byte vector) as a tree of depth 3.
-__device__ __forceinline__ float sum8(const uint4& v) {
-    const uint64_t a = add2(bf2(v.x), bf2(v.y)), b = add2(bf2(v.z), bf2(v.w));
-    const uint64_t c = add2(a, b);
-    return __fadd_rn(lo2(c), hi2(c));
+// fl(x + c) and fl(x - c) for the bf16 x in the low / high half of a word
+// (mixed-precision add / sub: one rounding of the exact result, as the fp32
+// operation on the exactly widened x).
+__device__ __forceinline__ float addb_lo(uint32_t w, float c) {
+    float d;
+    asm("{.reg .b16 l, h;\n\tmov.b32 {l, h}, %1;\n\tadd.rn.f32.bf16 %0, l, %2;\n\t}" : "=f"(d) : "r"(w), "f"(c));
+    return d;
 }
-// Sum of the squared deviations of 8 bf16 from mu (tree of depth 3).
-__device__ __forceinline__ float sqdev8(const uint4& v, uint64_t mm) {
-    const uint64_t d0 = sub2(bf2(v.x), mm), d1 = sub2(bf2(v.y), mm), d2 = sub2(bf2(v.z), mm), d3 = sub2(bf2(v.w), mm);
-    const uint64_t a = add2(mul2(d0, d0), mul2(d1, d1)), b = add2(mul2(d2, d2), mul2(d3, d3));
-    const uint64_t c = add2(a, b);
-    return __fadd_rn(lo2(c), hi2(c));
+__device__ __forceinline__ float addb_hi(uint32_t w, float c) {
+    float d;
+    asm("{.reg .b16 l, h;\n\tmov.b32 {l, h}, %1;\n\tadd.rn.f32.bf16 %0, h, %2;\n\t}" : "=f"(d) : "r"(w), "f"(c));
+    return d;
+}
+// (fl(lo - c), fl(hi - c)) of a bf16 pair as an fp32 pair.
+__device__ __forceinline__ uint64_t subb2(uint32_t w, float c) {
+    float a, b;
+    asm("{.reg .b16 l, h;\n\tmov.b32 {l, h}, %2;\n\tsub.rn.f32.bf16 %0, l, %3;\n\tsub.rn.f32.bf16 %1, h, %3;\n\t}"
+        : "=f"(a), "=f"(b) : "r"(w), "f"(c));
+    return pack2(a, b);
 }
 // Warp sum in a fixed butterfly order (every lane gets the same value).
 __device__ __forceinline__ float warp_sum(float v) {
@@ -169,13 +181,12 @@ __device__ __forceinline__ float warp_sum(float v) {
     return v;
 }
 
-// One warp per row.  The row is copied into shared memory with one bulk
-// asynchronous copy, so both passes read it there and x is read from HBM once.
-// A lane reads vectors lane, lane + 32, ... of the row (8 elements each, a
-// tree of depth 3) into kStatsAcc accumulators in turn (eight vectors per
-// step), the accumulators are added pairwise and the lanes by a butterfly: for
-// rows of at most 32768 elements the longest chain is 3 + 16 + 3 + 5 = 27
-// additions.
+// Each row part is copied into shared memory with one bulk asynchronous copy,
+// so both passes read it there and x is read from HBM once.  Longest chain of
+// additions for rows of at most 32768 elements (four parts of 1024 vectors, 32
+// per lane, 4 per accumulator): 8 x 4 + 3 + 5 + 2 = 42 for the sum, 4 x 4 +
+// 3 + 1 + 5 + 2 = 27 for the squares; rows under 2048 elements (one warp, at
+// most 8 vectors per lane): 8 + 3 + 5 = 16.
 // L2 cache policies: keep x in L2 for the apply kernel (evict last), which
 // then reads it for the last time (evict first).
 __device__ __forceinline__ uint64_t l2_policy_evict_last() {
@@ -203,24 +214,56 @@ __device__ __forceinline__ void tma_load_2d_hint(uint32_t dst, const CUtensorMap
         : "memory");
 }
 
+// One part of a row (nvec 16-byte vectors at shared address `row`): the sum
+// of its elements (kSquares false) or of their squared deviations from mu.
+// Lane l takes vectors l, l + 32, ... into kStatsAcc accumulators in turn.
+// Sums: every element is added to its accumulator in order (8 additions per
+// vector).  Squares: (x - mu) in pairs, each pair accumulated by a fused
+// multiply-add into a pair accumulator (4 per vector).  Then the
+// accumulators pairwise (3 levels; squares: + the two halves) and the lanes
+// by a butterfly (5).
 template <bool kSquares>
-__device__ __forceinline__ float row_pass(uint32_t row, int nvec, int lane, uint64_t mm) {
-    float acc[kStatsAcc];
+__device__ __forceinline__ float row_pass(uint32_t row, int nvec, int lane, float mu) {
+    if constexpr (!kSquares) {
+        float acc[kStatsAcc];
 #pragma unroll
-    for (int a = 0; a < kStatsAcc; ++a) acc[a] = 0.0f;
-    for (int v = lane; v < nvec; v += 32 * kStatsAcc) {
+        for (int a = 0; a < kStatsAcc; ++a) acc[a] = 0.0f;
+        for (int v = lane; v < nvec; v += 32 * kStatsAcc) {
 #pragma unroll
-        for (int a = 0; a < kStatsAcc; ++a)
-            if (v + 32 * a < nvec) {
-                const uint4 x = lds128(row + (v + 32 * a) * 16);
-                acc[a] = __fadd_rn(acc[a], kSquares ? sqdev8(x, mm) : sum8(x));
-            }
+            for (int a = 0; a < kStatsAcc; ++a)
+                if (v + 32 * a < nvec) {
+                    const uint4 x = lds128(row + (v + 32 * a) * 16);
+                    float t = acc[a];
+                    t = addb_hi(x.x, addb_lo(x.x, t));
+                    t = addb_hi(x.y, addb_lo(x.y, t));
+                    t = addb_hi(x.z, addb_lo(x.z, t));
+                    acc[a] = addb_hi(x.w, addb_lo(x.w, t));
+                }
+        }
+#pragma unroll
+        for (int w = kStatsAcc / 2; w >= 1; w >>= 1)
+#pragma unroll
+            for (int a = 0; a < w; ++a) acc[a] = __fadd_rn(acc[a], acc[a + w]);
+        return warp_sum(acc[0]);
+    } else {
+        uint64_t acc[kStatsAcc];
+#pragma unroll
+        for (int a = 0; a < kStatsAcc; ++a) acc[a] = 0;
+        for (int v = lane; v < nvec; v += 32 * kStatsAcc) {
+#pragma unroll
+            for (int a = 0; a < kStatsAcc; ++a)
+                if (v + 32 * a < nvec) {
+                    const uint4 x = lds128(row + (v + 32 * a) * 16);
+                    const uint64_t d0 = subb2(x.x, mu), d1 = subb2(x.y, mu), d2 = subb2(x.z, mu), d3 = subb2(x.w, mu);
+                    acc[a] = fma2(d3, d3, fma2(d2, d2, fma2(d1, d1, fma2(d0, d0, acc[a]))));
+                }
+        }
+#pragma unroll
+        for (int w = kStatsAcc / 2; w >= 1; w >>= 1)
+#pragma unroll
+            for (int a = 0; a < w; ++a) acc[a] = add2(acc[a], acc[a + w]);
+        return warp_sum(__fadd_rn(lo2(acc[0]), hi2(acc[0])));
     }
-#pragma unroll
-    for (int w = kStatsAcc / 2; w >= 1; w >>= 1)
-#pragma unroll
-        for (int a = 0; a < w; ++a) acc[a] = __fadd_rn(acc[a], acc[a + w]);
-    return warp_sum(acc[0]);
 }
 
 // Barrier over the `n` threads of one row group (named barrier `id`) that
@@ -235,20 +278,31 @@ __device__ __forceinline__ bool group_and(bool ok, int id, int n) {
         : "=r"(r) : "r"(uint32_t(ok)), "r"(id), "r"(n) : "memory");
     return r != 0;
 }
+__device__ __forceinline__ void group_sync(int id, int n) {
+    asm volatile("bar.sync %0, %1;" :: "r"(id), "r"(n) : "memory");
+}
+__device__ __forceinline__ void group_arrive(int id, int n) {
+    asm volatile("bar.arrive %0, %1;" :: "r"(id), "r"(n) : "memory");
+}
 
-// Persistent.  A row is shared by a group of P warps (P = 1, 2 or 4), warp p
-// of the group taking the p-th contiguous part of it; group g of the grid
-// takes rows g, g + G, g + 2G, ... (G groups in the grid).  Each warp copies
-// its part through two buffers, so the next row's copy is in flight while
-// this row is summed.  The parts' sums meet in shared memory behind the
-// group's named barrier and are added in a fixed order (depth + 2 at most).
-// The copies keep x in L2 for the apply kernel (evict last).
+// Persistent.  A row is shared by a group of kStatsParts warps (or taken by
+// one warp when rows are short), warp p of the group taking the p-th
+// contiguous part of it; group g of the grid takes rows g, g + G, g + 2G, ...
+// (G groups in the grid).  Each warp copies its part through two buffers, so
+// the next row's copy is in flight while this row is summed.  The parts' sums
+// meet in shared memory behind the group's named barriers and are added in a
+// fixed order: barrier g (every warp waits; it also ANDs the copy waits, so a
+// group gives up together) for the sum, barrier 8 + g for the squares (only
+// part 0 waits: it alone finishes the row).  The copies keep x in L2 for the
+// apply kernel (evict last).
 __global__ void __launch_bounds__(kStatsMaxWarps * 32)
 ln_stats_kernel(const uint16_t* __restrict__ x, int64_t rows, int64_t hidden, int64_t ld_x, float eps,
                 float* __restrict__ mu_out, float* __restrict__ rs_out, int parts, unsigned int* status) {
     extern __shared__ __align__(16) uint8_t rowbuf[];
     __shared__ __align__(8) uint64_t bars[kStatsMaxWarps][2];
-    __shared__ float part_sum[kStatsMaxWarps][2];          // [group * parts + part][S, S2]
+    // [group * parts + part][S of even rows, S of odd rows, S2]: part 0 may
+    // still read a row's S when the other parts write the next row's
+    __shared__ float part_sum[kStatsMaxWarps][3];
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int groups = int(blockDim.x >> 5) / parts;
     const int g = warp / parts, part = warp % parts;
@@ -260,6 +314,9 @@ ln_stats_kernel(const uint16_t* __restrict__ x, int64_t rows, int64_t hidden, in
     const uint32_t buf = smem_u32(rowbuf) + uint32_t(warp) * 2 * bytes;
     const uint16_t* src = x + part * part_elems;
     const uint64_t policy = l2_policy_evict_last();
+    // the apply kernel may be scheduled as these CTAs retire (it waits for
+    // this grid's completion before reading its results)
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
     if (lane == 0) {
         mbar_init(smem_u32(&bars[warp][0]), 1);
         mbar_init(smem_u32(&bars[warp][1]), 1);
@@ -274,42 +331,48 @@ ln_stats_kernel(const uint16_t* __restrict__ x, int64_t rows, int64_t hidden, in
     const int nvec = int(part_elems / 8);
     const float h = float(hidden);
     const int nthreads = parts * 32;
-    auto combine = [&](float v, int k) {                 // the group's sum of v, same in every warp
-        if (parts == 1) return v;
-        if (lane == 0) part_sum[warp][k] = v;
-        group_and(true, g, nthreads);
-        const int w0 = g * parts;
-        float a = __fadd_rn(part_sum[w0][k], part_sum[w0 + 1][k]);
-        if (parts == 4) a = __fadd_rn(a, __fadd_rn(part_sum[w0 + 2][k], part_sum[w0 + 3][k]));
-        return a;
-    };
+    const int w0 = g * parts;
     for (int64_t i = 0; i < n_mine; ++i) {
         const int s = int(i & 1);
         const uint32_t bar = smem_u32(&bars[warp][s]);
         bool ok = __all_sync(0xFFFFFFFFu, mbar_wait(bar, uint32_t((i >> 1) & 1), status));
-        if (parts > 1) ok = group_and(ok, g, nthreads);     // the group leaves together
+        const uint32_t row = buf + s * bytes;
+        float sum = row_pass<false>(row, nvec, lane, 0.0f);   // reads garbage (in bounds) if a copy timed out
+        if (parts > 1) {
+            if (lane == 0) part_sum[warp][s] = sum;
+            ok = group_and(ok, g, nthreads);
+            sum = __fadd_rn(__fadd_rn(part_sum[w0][s], part_sum[w0 + 1][s]),
+                            __fadd_rn(part_sum[w0 + 2][s], part_sum[w0 + 3][s]));
+        }
         if (!ok) {
-            // Gave up: let this warp's copies still in flight land before leaving.
+            // Gave up (the whole group): let this warp's copies still in flight land before leaving.
             if (lane == 0)
                 for (int64_t j = i; j < i + 2 && j < n_mine; ++j)
                     mbar_wait(smem_u32(&bars[warp][j & 1]), uint32_t((j >> 1) & 1), status);
             return;
         }
-        const uint32_t row = buf + s * bytes;
-        const float mu = __fdiv_rn(combine(row_pass<false>(row, nvec, lane, 0), 0), h);
-        const float var = __fdiv_rn(combine(row_pass<true>(row, nvec, lane, pack2(mu, mu)), 1), h);
-        const float rs = __frcp_rn(__fsqrt_rn(__fadd_rn(var, eps)));
+        const float mu = __fdiv_rn(sum, h);
+        float sq = row_pass<true>(row, nvec, lane, mu);
         // row_pass ends in a butterfly over every lane: the buffer has been read
+        if (lane == 0 && i + 2 < n_mine) {
+            mbar_arrive_expect_tx(bar, bytes);
+            bulk_load(row, src + (gg + (i + 2) * ngroups) * ld_x, bytes, bar, policy);
+        }
+        if (parts > 1) {
+            if (lane == 0) part_sum[warp][2] = sq;
+            if (part != 0) {
+                group_arrive(8 + g, nthreads);
+                continue;
+            }
+            group_sync(8 + g, nthreads);
+            sq = __fadd_rn(__fadd_rn(part_sum[w0][2], part_sum[w0 + 1][2]),
+                           __fadd_rn(part_sum[w0 + 2][2], part_sum[w0 + 3][2]));
+        }
         if (lane == 0) {
-            if (i + 2 < n_mine) {
-                mbar_arrive_expect_tx(bar, bytes);
-                bulk_load(row, src + (gg + (i + 2) * ngroups) * ld_x, bytes, bar, policy);
-            }
-            if (part == 0) {
-                const int64_t r = gg + i * ngroups;
-                mu_out[r] = mu;
-                rs_out[r] = rs;
-            }
+            const float rs = __frcp_rn(__fsqrt_rn(__fadd_rn(__fdiv_rn(sq, h), eps)));
+            const int64_t r = gg + i * ngroups;
+            mu_out[r] = mu;
+            rs_out[r] = rs;
         }
         __syncwarp();
     }
@@ -615,6 +678,10 @@ ln_apply_kernel(const __grid_constant__ CUtensorMap x_map, const __grid_constant
             walk.step(lband, lcol);
         }
     }
+    // mu / rsigma come from the statistics kernel, launched just before this
+    // one as its programmatic dependent: wait for it to complete (x itself
+    // was complete before the statistics kernel started).
+    asm volatile("griddepcontrol.wait;" ::: "memory");
     {
         float m, rs;
         uint32_t g2, b2;
@@ -680,13 +747,25 @@ cudaError_t launch_apply(const CUtensorMap& xm, const CUtensorMap& qr, const CUt
     if (e != cudaSuccess) return e;
     const int64_t want = (p.units + kApplyWarps - 1) / kApplyWarps;
     const int grid = int(want < sms ? want : sms);
-    kern<<<grid, kApplyWarps * 32, kApplySmem, stream>>>(xm, qr, qc, p);
-    return cudaGetLastError();
+    // Programmatic dependent launch: the CTAs may start (and load x) as the
+    // statistics kernel's CTAs retire; they wait for its results before
+    // reading mu / rsigma.
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(unsigned(grid));
+    cfg.blockDim = dim3(kApplyWarps * 32);
+    cfg.dynamicSmemBytes = kApplySmem;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, kern, xm, qr, qc, p);
 }
 
 }  // namespace
 
-int64_t ln_quantize_max_hidden() { return 32768; }   // keeps the longest chain of additions at 27
+int64_t ln_quantize_max_hidden() { return 32768; }   // keeps the longest chain of additions at 42
 
 te_mx_status ln_quantize_launch(const LnQuantizeArgs& a, cudaStream_t stream) {
     const bool rowwise = a.q_row != nullptr, colwise = a.q_col != nullptr;
@@ -698,11 +777,14 @@ te_mx_status ln_quantize_launch(const LnQuantizeArgs& a, cudaStream_t stream) {
     int sms = 0;
     if ((st = device_sm_count(&sms)) != TE_MX_OK) return st;
     // statistics: one CTA per SM with as many row groups as two row buffers
-    // each allow (at most 32), P warps per row so that G x P <= 32
+    // each allow; rows of 2048 elements or more are shared by four warps (at
+    // most 8 groups, barriers 0..15), shorter rows take one warp each (at
+    // most 32 groups)
     const int64_t buf_bytes = 2 * a.hidden * 2;
     const int64_t fit = kStatsSmem / buf_bytes;
-    const int groups = int(fit < kStatsMaxWarps ? fit : kStatsMaxWarps);
-    const int parts = groups <= kStatsMaxWarps / 4 ? 4 : (groups <= kStatsMaxWarps / 2 ? 2 : 1);
+    const int parts = a.hidden >= 2048 ? kStatsParts : 1;
+    const int64_t cap = kStatsMaxWarps / parts;
+    const int groups = int(fit < cap ? fit : cap);
     const size_t stats_smem = size_t(groups) * size_t(buf_bytes);
     cudaError_t e = set_smem_attribute_once(reinterpret_cast<const void*>(ln_stats_kernel), kStatsSmem);
     if (e != cudaSuccess) return cuda_status(e, "layernorm statistics kernel attributes");

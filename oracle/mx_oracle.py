@@ -482,7 +482,9 @@ def layernorm_stat_bounds(x_bits, eps: float = LAYERNORM_EPS, depth: int = LN_SU
 def layernorm_error_bound(x_bits, gamma_bits, eps: float = LAYERNORM_EPS, depth: int = LN_SUM_DEPTH):
     """Per-element bound E on |y_fp32 - y| for a LayerNorm evaluated in fp32 as:
     mu = fl(S / H), S = sum of x with at most ``depth`` additions on any path;
-    var = fl(S2 / H), S2 = sum of fl(fl(x - mu)^2), same depth; rsigma =
+    var = fl(S2 / H), S2 = sum of the squares of fl(x - mu), same depth, each
+    square rounded on its own or fused into the addition that accumulates it
+    (one rounding fewer, inside the same bound); rsigma =
     fl(1 / fl(sqrt(fl(var + eps)))); y = fl(fl(fl(x - mu) * rsigma) * gamma +
     beta) with one rounding (fused multiply-add).  Standard forward error
     analysis (each fl() a relative error of at most u = 2^-24, a sum of depth d
