@@ -509,87 +509,107 @@ __device__ __forceinline__ void quantize_unit(const ApplyParams& p, uint32_t uni
 }
 
 // Both orientations from one evaluation of y per element.  Lane l holds
-// columns 2l, 2l + 1 of all 32 rows (the column pair is the f32x2 operand), so
-// the column blocks are lane-local.  A row block spans 16 lanes: every lane
-// writes its per-row maxima into the consumed unit (a 32 x 32 fp32 scratch at
-// the addresses the lane read x from), lane r reduces row r's two blocks, and
-// the two row scales come back through the statistics area of the side data
-// as (m, m) pairs.  Row codes are staged one 16-bit pair per lane and row,
-// column codes as in the column-wise path.
+// columns 2l (lo) and 2l + 1 (hi) of all 32 rows as fp32 pairs of consecutive
+// rows, ylo[k] = (y[2k][2l], y[2k+1][2l]) and yhi[k] likewise, so the column
+// blocks are lane-local and the statistics of a row pair are one load.  A row
+// block spans 16 lanes: every lane writes its per-row-pair maxima into the
+// consumed unit (a 16 x 32 scratch of fp32 pairs, 16-byte chunks XOR-swizzled
+// by row pair), lane (p, b) = (l & 15, l >> 4) reduces rows 2p and 2p + 1 of
+// block b, and the row scales come back through the statistics area of the
+// side data, [block][row] in fp32.  Row codes are staged one 16-bit pair per
+// lane and row, column codes as in the column-wise path.  The side data's
+// statistics are (mu[2k], mu[2k+1], rsigma[2k], rsigma[2k+1]) per row pair.
 __device__ __forceinline__ void quantize_unit_both(const ApplyParams& p, uint32_t unit, int64_t r0, int64_t c0,
                                                    int lane, uint32_t stat, uint32_t gaddr, uint32_t baddr) {
     const int valid = p.hidden - c0 < kUnitCols ? int(p.hidden - c0) : kUnitCols;
-    const uint64_t g2 = lds64(gaddr + lane * 8), b2 = lds64(baddr + lane * 8);
-    const uint32_t cbase = unit + ((lane & 3) << 2);
-    const int ch = lane >> 2;
-    uint64_t y[32];
+    uint64_t ylo[16], yhi[16];
+    {
+        const uint64_t g2 = lds64(gaddr + lane * 8), b2 = lds64(baddr + lane * 8);
+        const uint64_t glo = pack2(lo2(g2), lo2(g2)), ghi = pack2(hi2(g2), hi2(g2));
+        const uint64_t blo = pack2(lo2(b2), lo2(b2)), bhi = pack2(hi2(b2), hi2(b2));
+        const uint32_t cbase = unit + ((lane & 3) << 2);
+        const int ch = lane >> 2;
 #pragma unroll
-    for (int r = 0; r < 32; ++r) {
-        const uint32_t x = lds32(cbase + r * 128 + ((ch ^ (r & 7)) << 4));
-        uint64_t mu2, rs2;
-        lds128x2(stat + r * 16, mu2, rs2);
-        y[r] = fma2(mul2(sub2(bf2(x), mu2), rs2), g2, b2);
+        for (int k = 0; k < 16; ++k) {
+            const int r = 2 * k;
+            const uint32_t w0 = lds32(cbase + r * 128 + ((ch ^ (r & 7)) << 4));
+            const uint32_t w1 = lds32(cbase + (r + 1) * 128 + ((ch ^ ((r + 1) & 7)) << 4));
+            uint64_t mu2, rs2;
+            lds128x2(stat + k * 16, mu2, rs2);
+            ylo[k] = fma2(mul2(sub2(pack2(bf16_lo(w0), bf16_lo(w1)), mu2), rs2), glo, blo);
+            yhi[k] = fma2(mul2(sub2(pack2(bf16_hi(w0), bf16_hi(w1)), mu2), rs2), ghi, bhi);
+        }
     }
     __syncwarp();                                // every lane has read x and the statistics
-    // row partial maxima of this lane's column pair, where the lane read x
+    // per-row-pair maxima of this lane's two columns: scratch [pair k][lane l]
 #pragma unroll
-    for (int r = 0; r < 32; ++r)
-        sts32(cbase + r * 128 + ((ch ^ (r & 7)) << 4), __float_as_uint(maxabs(lo2(y[r]), hi2(y[r]))));
+    for (int k = 0; k < 16; ++k) {
+        const uint64_t m = pack2(maxabs(lo2(ylo[k]), lo2(yhi[k])), maxabs(hi2(ylo[k]), hi2(yhi[k])));
+        sts64(unit + k * 256 + (lane >> 4) * 128 + ((((lane >> 1) & 7) ^ (k & 7)) << 4) + (lane & 1) * 8, m);
+    }
     __syncwarp();
-    float t[32];                                 // row `lane` of the scratch: lanes 0..15, then 16..31
+    const int pr = lane & 15, blk = lane >> 4;   // rows 2 pr, 2 pr + 1 of row block blk
+    float ta[16], tb[16];
 #pragma unroll
-    for (int c = 0; c < 8; ++c) {
-        const uint4 v = lds128(unit + lane * 128 + ((c ^ (lane & 7)) << 4));
-        t[4 * c + 0] = __uint_as_float(v.x);
-        t[4 * c + 1] = __uint_as_float(v.y);
-        t[4 * c + 2] = __uint_as_float(v.z);
-        t[4 * c + 3] = __uint_as_float(v.w);
+    for (int j = 0; j < 8; ++j) {
+        uint64_t u, v;
+        lds128x2(unit + pr * 256 + blk * 128 + ((j ^ (pr & 7)) << 4), u, v);
+        ta[2 * j] = lo2(u); tb[2 * j] = hi2(u);
+        ta[2 * j + 1] = lo2(v); tb[2 * j + 1] = hi2(v);
     }
 #pragma unroll
     for (int s2 = 8; s2 >= 1; s2 >>= 1)
 #pragma unroll
         for (int i = 0; i < s2; ++i) {
-            t[i] = maxabs(t[i], t[i + s2]);
-            t[16 + i] = maxabs(t[16 + i], t[16 + i + s2]);
+            ta[i] = maxabs(ta[i], ta[i + s2]);
+            tb[i] = maxabs(tb[i], tb[i + s2]);
         }
-    const uint32_t sr0 = mx_scale_byte_f32(t[0]), sr1 = mx_scale_byte_f32(t[16]);
+    const uint32_t sa = mx_scale_byte_f32(ta[0]), sb = mx_scale_byte_f32(tb[0]);
     {
-        const int64_t r = r0 + lane;
+        // row 2 pr (lanes of block 0) / 2 pr + 1 (block 1): both blocks' bytes
+        const uint32_t mine = sa | (sb << 8);
+        const uint32_t other = __shfl_xor_sync(0xFFFFFFFFu, mine, 16);
+        const int64_t r = r0 + 2 * pr + blk;
         if (r < p.rows) {
             uint8_t* sp = p.s_row + r * p.ld_s_row + (c0 >> 5);
-            if (valid > 32) st_global_u16(sp, sr0 | (sr1 << 8));
-            else st_global_u8(sp, sr0);
+            const uint32_t b0 = blk ? (other >> 8) : (mine & 0xFFu);      // block 0's byte of row r
+            const uint32_t b1 = blk ? (mine >> 8) : (other & 0xFFu);      // block 1's byte of row r
+            if (valid > 32) st_global_u16(sp, b0 | (b1 << 8));
+            else st_global_u8(sp, b0);
         }
-        const float m0 = inv_scale(sr0), m1 = inv_scale(sr1);   // -inf for a non-finite block
-        sts64(stat + lane * 8, pack2(m0, m0));
-        sts64(stat + 256 + lane * 8, pack2(m1, m1));
+        sts64(stat + blk * 128 + pr * 8, pack2(inv_scale(sa), inv_scale(sb)));   // -inf for a non-finite block
     }
-    const bool nonfinite = __any_sync(0xFFFFFFFFu, sr0 == 0xFFu || sr1 == 0xFFu);
+    const bool nonfinite = __any_sync(0xFFFFFFFFu, sa == 0xFFu || sb == 0xFFu);
     __syncwarp();                                // row scales visible; the scratch is consumed
     {
-        const uint32_t ms = stat + (lane >> 4) * 256;      // this lane's row block
+        const uint32_t ms = stat + (lane >> 4) * 128;      // this lane's row block
         const uint32_t rcode = unit + (lane & 7) * 2;
         const int rch = lane >> 3;
 #pragma unroll
-        for (int r = 0; r < 32; r += 2) {
-            uint64_t m_a, m_b;
-            lds128x2(ms + r * 8, m_a, m_b);
-            const uint64_t a = mul2(y[r], m_a), b = mul2(y[r + 1], m_b);
-            uint32_t ca = cvt_e4m3x2(lo2(a), hi2(a)), cb = cvt_e4m3x2(lo2(b), hi2(b));
-            if (nonfinite) {
-                if (__float_as_uint(lo2(m_a)) == 0xFF800000u) ca = 0x7F7Fu;
-                if (__float_as_uint(lo2(m_b)) == 0xFF800000u) cb = 0x7F7Fu;
+        for (int k = 0; k < 16; k += 2) {
+            uint64_t m_a, m_b;                   // (m[2k], m[2k+1]), (m[2k+2], m[2k+3])
+            lds128x2(ms + k * 8, m_a, m_b);
+#pragma unroll
+            for (int t = 0; t < 2; ++t) {
+                const uint64_t m2 = t ? m_b : m_a;
+                const int r = 2 * (k + t);
+                const uint64_t a = mul2(ylo[k + t], m2), b = mul2(yhi[k + t], m2);
+                uint32_t c_even = cvt_e4m3x2(lo2(a), lo2(b)), c_odd = cvt_e4m3x2(hi2(a), hi2(b));
+                if (nonfinite) {
+                    if (__float_as_uint(lo2(m2)) == 0xFF800000u) c_even = 0x7F7Fu;
+                    if (__float_as_uint(hi2(m2)) == 0xFF800000u) c_odd = 0x7F7Fu;
+                }
+                sts16(rcode + r * 64 + ((rch ^ ((r >> 1) & 3)) << 4), c_even);
+                sts16(rcode + (r + 1) * 64 + ((rch ^ (((r + 1) >> 1) & 3)) << 4), c_odd);
             }
-            sts16(rcode + r * 64 + ((rch ^ ((r >> 1) & 3)) << 4), ca);
-            sts16(rcode + (r + 1) * 64 + ((rch ^ (((r + 1) >> 1) & 3)) << 4), cb);
         }
     }
     // column blocks: lane-local
     float ml[16], mh[16];
 #pragma unroll
-    for (int i = 0; i < 16; ++i) {
-        ml[i] = maxabs(lo2(y[2 * i]), lo2(y[2 * i + 1]));
-        mh[i] = maxabs(hi2(y[2 * i]), hi2(y[2 * i + 1]));
+    for (int k = 0; k < 16; ++k) {
+        ml[k] = maxabs(lo2(ylo[k]), hi2(ylo[k]));
+        mh[k] = maxabs(lo2(yhi[k]), hi2(yhi[k]));
     }
 #pragma unroll
     for (int s2 = 8; s2 >= 1; s2 >>= 1)
@@ -599,14 +619,15 @@ __device__ __forceinline__ void quantize_unit_both(const ApplyParams& p, uint32_
             mh[i] = maxabs(mh[i], mh[i + s2]);
         }
     const uint32_t s_lo = mx_scale_byte_f32(ml[0]), s_hi = mx_scale_byte_f32(mh[0]);
-    const uint64_t m2 = pack2(inv_scale(s_lo), inv_scale(s_hi));
+    const float il = inv_scale(s_lo), ih = inv_scale(s_hi);
+    const uint64_t ml2 = pack2(il, il), mh2 = pack2(ih, ih);
     uint32_t cc_lo[8], cc_hi[8];
 #pragma unroll
     for (int i = 0; i < 8; ++i) {
-        const uint64_t a = mul2(y[4 * i], m2), b = mul2(y[4 * i + 1], m2);
-        const uint64_t c = mul2(y[4 * i + 2], m2), d = mul2(y[4 * i + 3], m2);
-        cc_lo[i] = cvt_e4m3x2(lo2(a), lo2(b)) | (cvt_e4m3x2(lo2(c), lo2(d)) << 16);
-        cc_hi[i] = cvt_e4m3x2(hi2(a), hi2(b)) | (cvt_e4m3x2(hi2(c), hi2(d)) << 16);
+        const uint64_t a = mul2(ylo[2 * i], ml2), b = mul2(ylo[2 * i + 1], ml2);
+        const uint64_t c = mul2(yhi[2 * i], mh2), d = mul2(yhi[2 * i + 1], mh2);
+        cc_lo[i] = cvt_e4m3x2(lo2(a), hi2(a)) | (cvt_e4m3x2(lo2(b), hi2(b)) << 16);
+        cc_hi[i] = cvt_e4m3x2(lo2(c), hi2(c)) | (cvt_e4m3x2(lo2(d), hi2(d)) << 16);
     }
     if (s_lo == 0xFFu) {
 #pragma unroll
@@ -658,7 +679,13 @@ ln_apply_kernel(const __grid_constant__ CUtensorMap x_map, const __grid_constant
         b2 = cc < p.hidden ? *reinterpret_cast<const uint32_t*>(p.beta + cc) : 0u;
     };
     auto store_side = [&](uint8_t* area, float m, float rs, uint32_t g2, uint32_t b2) {
-        reinterpret_cast<float4*>(area)[lane] = make_float4(m, m, rs, rs);
+        if constexpr (kRowwise && kColwise) {          // (mu, mu', rsigma, rsigma') per row pair
+            float* pair = reinterpret_cast<float*>(area) + (lane >> 1) * 4 + (lane & 1);
+            pair[0] = m;
+            pair[2] = rs;
+        } else {
+            reinterpret_cast<float4*>(area)[lane] = make_float4(m, m, rs, rs);
+        }
         reinterpret_cast<float2*>(area + kUnitRows * 16)[lane] = make_float2(bf16_lo(g2), bf16_hi(g2));
         reinterpret_cast<float2*>(area + kUnitRows * 16 + kUnitCols * 4)[lane] = make_float2(bf16_lo(b2), bf16_hi(b2));
     };
