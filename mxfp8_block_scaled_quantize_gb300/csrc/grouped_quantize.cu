@@ -24,6 +24,7 @@
 #include "e4m3.cuh"
 #include "ptx.cuh"
 #include "temx_internal.h"
+#include "units.cuh"
 
 namespace temx {
 
@@ -122,23 +123,20 @@ grouped_colwise_kernel(const __grid_constant__ CUtensorMap x_map, const __grid_c
     const int64_t n_mine = (units - gwarp + nwarps - 1) / nwarps;
     const uint32_t ring = smem_u32(smem + warp * (kStages * kUnitBytes));
 
-    // unit i of this warp -> expert g, block, columns.  `h` is a lower bound on
-    // the expert, moved forward only (a warp's units only move forward).
-    auto locate = [&](int64_t i, int32_t& h, int32_t& blk, int64_t& c0) {
-        const int64_t u = gwarp + i * nwarps;
-        blk = int32_t(u / p.col_units);
-        c0 = (u % p.col_units) * kCols;
-        while (tab.blk[h + 1] <= blk) ++h;       // blk < tab.blk[groups]: stops at an expert
-    };
-    int32_t load_hint = 0;                       // lane 0: the loads run kStages units ahead
-    auto load = [&](int64_t i, uint32_t dst, uint32_t bar) {
-        int32_t blk;
-        int64_t c0;
-        locate(i, load_hint, blk, c0);
+    // The units of this warp as (32-row block, column unit), walked without
+    // dividing; the expert of a block is found from a lower bound that only
+    // moves forward (a warp's units only move forward).
+    const UnitWalk walk(nwarps, p.col_units);
+    int32_t blk, col;
+    walk.start(gwarp, blk, col);
+    int32_t lblk = blk, lcol = col, load_hint = 0;     // lane 0: the loads run kStages units ahead
+    auto load = [&](uint32_t dst, uint32_t bar) {
+        while (tab.blk[load_hint + 1] <= lblk) ++load_hint;           // lblk < tab.blk[groups]
         const int32_t g = load_hint;
-        const int32_t r = tab.row[g] + (blk - tab.blk[g]) * kRows;    // rows past the expert are masked later
+        const int32_t r = tab.row[g] + (lblk - tab.blk[g]) * kRows;   // rows past the expert are masked later
         mbar_arrive_expect_tx(bar, kUnitBytes);
-        tma_load_2d(dst, &x_map, bar, int32_t(c0), r);
+        tma_load_2d(dst, &x_map, bar, lcol * kCols, r);
+        walk.step(lblk, lcol);
     };
 
     if (lane == 0) {
@@ -146,20 +144,20 @@ grouped_colwise_kernel(const __grid_constant__ CUtensorMap x_map, const __grid_c
         tma_prefetch_desc(&q_map);
         for (int s = 0; s < kStages; ++s) mbar_init(smem_u32(&bars[warp][s]), 1);
         fence_mbarrier_init();
-        for (int s = 0; s < kStages && s < n_mine; ++s) load(s, ring + s * kUnitBytes, smem_u32(&bars[warp][s]));
+        for (int s = 0; s < kStages && s < n_mine; ++s) load(ring + s * kUnitBytes, smem_u32(&bars[warp][s]));
     }
     __syncwarp();
 
     int32_t g = 0;
+    int s = 0;
+    uint32_t parity = 0;
     for (int64_t i = 0; i < n_mine; ++i) {
-        const int s = int(i % kStages);
         const uint32_t bar = smem_u32(&bars[warp][s]);
-        int32_t blk;
-        int64_t c0;
-        locate(i, g, blk, c0);
+        while (tab.blk[g + 1] <= blk) ++g;       // blk < tab.blk[groups]: stops at an expert
+        const int64_t c0 = int64_t(col) * kCols;
         const int32_t m = tab.row[g + 1] - tab.row[g];
         const int32_t valid = m - (blk - tab.blk[g]) * kRows;          // tokens of the expert in this unit
-        if (!__all_sync(0xFFFFFFFFu, mbar_wait(bar, uint32_t((i / kStages) & 1), p.status))) {
+        if (!__all_sync(0xFFFFFFFFu, mbar_wait(bar, parity, p.status))) {
             if (lane == 0)                       // gave up: let this warp's loads still in flight land
                 for (int64_t j = i; j < i + kStages && j < n_mine; ++j)
                     mbar_wait(smem_u32(&bars[warp][j % kStages]), uint32_t((j / kStages) & 1), p.status);
@@ -228,10 +226,15 @@ grouped_colwise_kernel(const __grid_constant__ CUtensorMap x_map, const __grid_c
             bulk_commit();
             if (i + kStages < n_mine) {
                 bulk_wait_read_all();            // the store has read the unit: refill it
-                load(i + kStages, unit, bar);
+                load(unit, bar);
             }
         }
         __syncwarp();
+        walk.step(blk, col);
+        if (++s == kStages) {
+            s = 0;
+            parity ^= 1u;
+        }
     }
     if (lane == 0) bulk_wait_all();
 }

@@ -26,6 +26,7 @@
 #include "e4m3.cuh"
 #include "ptx.cuh"
 #include "temx_internal.h"
+#include "units.cuh"
 
 namespace temx {
 
@@ -148,6 +149,11 @@ quantize_kernel(const __grid_constant__ CUtensorMap x_map, const __grid_constant
     if (gwarp >= p.units) return;
     const int64_t n_mine = (p.units - gwarp + nwarps - 1) / nwarps;
     const uint32_t ring = smem_u32(smem + warp * (kStages * kUnitBytes));
+    // (band, column unit) of this unit and of the next load (lane 0)
+    const UnitWalk walk(nwarps, p.col_units);
+    int32_t band, col;
+    walk.start(gwarp, band, col);
+    int32_t lband = band, lcol = col;
 
     if (lane == 0) {
         tma_prefetch_desc(&x_map);
@@ -156,18 +162,17 @@ quantize_kernel(const __grid_constant__ CUtensorMap x_map, const __grid_constant
         for (int s = 0; s < kStages; ++s) mbar_init(smem_u32(&bars[warp][s]), 1);
         fence_mbarrier_init();
         for (int s = 0; s < kStages && s < n_mine; ++s) {
-            const int64_t u = gwarp + s * nwarps;
             const uint32_t bar = smem_u32(&bars[warp][s]);
             mbar_arrive_expect_tx(bar, kUnitBytes);
-            tma_load_2d(ring + s * kUnitBytes, &x_map, bar,
-                        int32_t((u % p.col_units) * kCols), int32_t((u / p.col_units) * kRows));
+            tma_load_2d(ring + s * kUnitBytes, &x_map, bar, lcol * kCols, lband * kRows);
+            walk.step(lband, lcol);
         }
     }
     __syncwarp();
 
+    int s = 0;
+    uint32_t parity = 0;
     for (int64_t i = 0; i < n_mine; ++i) {
-        const int s = int(i % kStages);
-        const uint32_t parity = uint32_t((i / kStages) & 1);
         const uint32_t bar = smem_u32(&bars[warp][s]);
         if (!__all_sync(0xFFFFFFFFu, mbar_wait(bar, parity, p.status))) {
             if (lane == 0)                       // gave up: let this warp's loads still in flight land
@@ -176,8 +181,7 @@ quantize_kernel(const __grid_constant__ CUtensorMap x_map, const __grid_constant
             break;
         }
         const uint32_t tile = ring + s * kUnitBytes;
-        const int64_t u = gwarp + i * nwarps;
-        const int64_t r0 = (u / p.col_units) * kRows, c0 = (u % p.col_units) * kCols;
+        const int64_t r0 = int64_t(band) * kRows, c0 = int64_t(col) * kCols;
 
         uint32_t cc[2][2][8];             // column codes [half][column 2l / 2l+1][words]
         uint32_t rc[2][2][8];             // row codes [row l / l+32][block][words]
@@ -252,13 +256,17 @@ quantize_kernel(const __grid_constant__ CUtensorMap x_map, const __grid_constant
             bulk_commit();             // (an empty group when only the bias gradient is produced)
             if (i + kStages < n_mine) {
                 bulk_wait_read_all();     // the stores have read the tile: refill it
-                const int64_t un = gwarp + (i + kStages) * nwarps;
                 mbar_arrive_expect_tx(bar, kUnitBytes);
-                tma_load_2d(tile, &x_map, bar, int32_t((un % p.col_units) * kCols),
-                            int32_t((un / p.col_units) * kRows));
+                tma_load_2d(tile, &x_map, bar, lcol * kCols, lband * kRows);
+                walk.step(lband, lcol);
             }
         }
         __syncwarp();
+        walk.step(band, col);
+        if (++s == kStages) {
+            s = 0;
+            parity ^= 1u;
+        }
     }
     if (lane == 0) bulk_wait_all();
 }
