@@ -30,8 +30,9 @@
 // once per element (lane = 2 columns x 32 rows: column blocks are lane-local,
 // row blocks are reduced through a transposed scratch); one orientation alone
 // uses its natural layout (row-wise: lane = row).  No CTA-wide barrier, no
-// cluster.  For activations up to the L2 size the apply kernel reads x mostly
-// from L2.
+// cluster.  The apply kernel reads x again: from L2 when the activation is
+// well under the L2 size, from DRAM for one the size of L2 (measured: a
+// 117 MB activation is re-read from DRAM).
 #include <cuda_runtime.h>
 
 #include "e4m3.cuh"
@@ -187,8 +188,9 @@ __device__ __forceinline__ float warp_sum(float v) {
 // per lane, 4 per accumulator): 8 x 4 + 3 + 5 + 2 = 42 for the sum, 4 x 4 +
 // 3 + 1 + 5 + 2 = 27 for the squares; rows under 2048 elements (one warp, at
 // most 8 vectors per lane): 8 + 3 + 5 = 16.
-// L2 cache policies: keep x in L2 for the apply kernel (evict last), which
-// then reads it for the last time (evict first).
+// L2 cache policies: the statistics kernel's copies ask to keep x in L2 for
+// the apply kernel (evict last), which then reads it for the last time
+// (evict first).
 __device__ __forceinline__ uint64_t l2_policy_evict_last() {
     uint64_t p;
     asm volatile("createpolicy.fractional.L2::evict_last.b64 %0, 1.0;" : "=l"(p));
@@ -293,8 +295,8 @@ __device__ __forceinline__ void group_arrive(int id, int n) {
 // meet in shared memory behind the group's named barriers and are added in a
 // fixed order: barrier g (every warp waits; it also ANDs the copy waits, so a
 // group gives up together) for the sum, barrier 8 + g for the squares (only
-// part 0 waits: it alone finishes the row).  The copies keep x in L2 for the
-// apply kernel (evict last).
+// part 0 waits: it alone finishes the row).  The copies carry an evict-last
+// hint for the apply kernel's second read of x.
 __global__ void __launch_bounds__(kStatsMaxWarps * 32)
 ln_stats_kernel(const uint16_t* __restrict__ x, int64_t rows, int64_t hidden, int64_t ld_x, float eps,
                 float* __restrict__ mu_out, float* __restrict__ rs_out, int parts, unsigned int* status) {
