@@ -120,9 +120,6 @@ __device__ __forceinline__ uint64_t lds64(uint32_t addr) {
 __device__ __forceinline__ void lds128x2(uint32_t addr, uint64_t& a, uint64_t& b) {
     asm volatile("ld.shared.v2.b64 {%0, %1}, [%2];" : "=l"(a), "=l"(b) : "r"(addr));
 }
-__device__ __forceinline__ void sts32(uint32_t addr, uint32_t v) {
-    asm volatile("st.shared.b32 [%0], %1;" :: "r"(addr), "r"(v) : "memory");
-}
 __device__ __forceinline__ void sts64(uint32_t addr, uint64_t v) {
     asm volatile("st.shared.b64 [%0], %1;" :: "r"(addr), "l"(v) : "memory");
 }
