@@ -195,7 +195,9 @@ TEMX_API te_mx_status te_mx_block_quantize(const void* x, int64_t rows, int64_t 
  * fma(fl(fl(x - mu) rsigma), gamma, beta) with one rounding.  Codes and scales
  * are the exact MXFP8 quantisation of that fp32 y; the sums are taken in a
  * fixed order (deterministic).  Two kernels run on `stream`: the statistics,
- * then normalisation + quantisation (reading mu / rsigma back).
+ * then normalisation + quantisation (reading mu / rsigma back), the second as
+ * a programmatic dependent launch of the first (it waits for the first
+ * grid's results; work queued after the call waits for both, as usual).
  *
  *   x       bf16 [rows x hidden], pitch ld_x (device, 16-byte aligned, ld_x % 8 == 0);
  *   gamma, beta  bf16 [hidden] (device, 4-byte aligned);  eps > 0 and finite;
