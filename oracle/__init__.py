@@ -9,4 +9,5 @@ from .mx_oracle import (  # noqa: F401
     f64_to_bf16_bits, gelu_tanh, gemm_error_bound, grouped_layout, mx_gemm, mx_gemm_dgelu, mx_grouped_gemm,
     mx_grouped_wgrad, quantize_colwise_grouped,
     mx_scale_exponent, quantize_block, quantize_colwise, quantize_rowwise,
+    block_gemm_fp32, block_scale_fp32, dequantize_fp32, quantize_block_fp32,
 )

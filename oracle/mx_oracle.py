@@ -49,6 +49,11 @@ Readings where the sources are silent (each one is listed in the design notes):
 * A negative value that rounds to zero keeps its sign (code 0x80).
 * A block holding a NaN or an infinity: scale byte 0xFF (E8M0 NaN) and every
   element code 0x7F (E4M3 NaN).
+* Float8BlockScaling with FP32 scales (the README's second mode): the scale is
+  s = amax / 448 rounded to fp32; elements are multiplied by r = fl32(1 / s)
+  in fp32 (one multiply per element, as a quantiser does) and rounded to E4M3
+  (nearest even, saturating); r is capped at the largest finite fp32;
+  amax == 0 gives s = r = 1.
 * GELU is applied to the unrounded pre-activation; AUX is that
   pre-activation rounded to bf16.
 """
@@ -303,6 +308,80 @@ def quantize_block(x_bits, block_2d: bool):
     return q_row[:rows, :cols], s_row[:rows, :gc], q_col[:cols, :rows], s_col[:cols, :gr]
 
 
+FP32_MAX = float(np.finfo(np.float32).max)
+BLOCK_EDGE = 128           # Float8BlockScaling block: 1x128, 128x1 or 128x128 elements
+
+
+def block_scale_fp32(amax):
+    """Float8BlockScaling with the FP32 scales kept (the README's second mode,
+    "compute the GEMM with the FP32 scales directly").  Per block:
+      s = fl32(amax / 448)       the FP32 scale (the dequantisation factor),
+      r = fl32(1 / s)            the quantisation multiplier, at most the
+                                 largest finite fp32,
+    each an IEEE fp32 operation rounded to nearest even.  amax == 0 gives
+    s = r = 1; a non-finite amax gives s = r = NaN (codes 0x7F).
+    Returns (s, r) as float32 arrays."""
+    a = np.asarray(amax, dtype=np.float32)           # exact: amax is a bf16 value
+    with np.errstate(divide="ignore", over="ignore", invalid="ignore"):
+        s = a / np.float32(E4M3_MAX)
+        r = np.minimum(np.float32(1.0) / s, np.float32(FP32_MAX))
+    one = np.float32(1.0)
+    s = np.where(a == 0, one, s)
+    r = np.where(a == 0, one, r)
+    bad = ~np.isfinite(a)
+    s = np.where(bad, np.float32(np.nan), s)
+    r = np.where(bad, np.float32(np.nan), r)
+    return s.astype(np.float32), r.astype(np.float32)
+
+
+def quantize_block_fp32(x_bits, block_2d: bool):
+    """Float8BlockScaling quantisation keeping FP32 scales.
+
+    Blocks as in ``quantize_block`` (1x128 / 128x1, or 128x128 shared by both
+    copies; partial edge blocks take the amax of the elements present).  Codes:
+    q = E4M3_rn_satfinite(fl32(x * r)) with r from ``block_scale_fp32``
+    (0x7F for a block holding NaN or inf).  Scales: one fp32 s per block and
+    row of the copy, s_row [R, ceil(C/128)] and s_col [C, ceil(R/128)]; a
+    128x128 block's scale is repeated over its 128 rows in both copies.
+    Returns (q_row [R,C], s_row, q_col [C,R], s_col)."""
+    x = bf16_bits_to_f64(np.asarray(x_bits, dtype=np.uint16))
+    rows, cols = x.shape
+    e = BLOCK_EDGE
+    pr, pc = -(-rows // e) * e, -(-cols // e) * e
+    xp = np.zeros((pr, pc))                  # zero padding leaves every amax unchanged
+    xp[:rows, :cols] = x
+    ax = np.abs(xp)
+    with np.errstate(invalid="ignore"):
+        if block_2d:
+            amax = ax.reshape(pr // e, e, pc // e, e).max(axis=(1, 3))
+            a_row = np.repeat(amax, e, axis=0)               # [R, C/128]
+            a_col = np.repeat(amax.T, e, axis=0)             # [C, R/128]
+        else:
+            a_row = ax.reshape(pr, pc // e, e).max(axis=2)
+            a_col = ax.T.reshape(pc, pr // e, e).max(axis=2)
+    out = []
+    for v, a in ((xp, a_row), (xp.T, a_col)):
+        sc, r = block_scale_fp32(a)
+        bad = ~np.isfinite(a)
+        with np.errstate(invalid="ignore", over="ignore"):
+            prod = v.astype(np.float32) * np.repeat(r, e, axis=1)      # fl32(x * r)
+            q = e4m3_encode(prod.astype(np.float64)).astype(np.uint8)
+        q[np.repeat(bad, e, axis=1)] = 0x7F
+        out.append((q, sc))
+    (q_row, s_row), (q_col, s_col) = out
+    gr, gc = -(-rows // e), -(-cols // e)
+    return q_row[:rows, :cols], s_row[:rows, :gc], q_col[:cols, :rows], s_col[:cols, :gr]
+
+
+def dequantize_fp32(q, s) -> np.ndarray:
+    """E4M3 bytes [R, C] with fp32 scales [R, >= ceil(C/128)] (one per row and
+    128 columns) -> float64 [R, C], exactly (a 4-bit by 24-bit product)."""
+    q = np.asarray(q, dtype=np.uint8)
+    rows, n = q.shape
+    sc = np.asarray(s, dtype=np.float32).astype(np.float64)[:, :-(-n // BLOCK_EDGE)]
+    return e4m3_decode(q) * np.repeat(sc, BLOCK_EDGE, axis=1)[:, :n]
+
+
 def dequantize(q, s) -> np.ndarray:
     """E4M3 bytes [R, C] with E8M0 bytes [R, C/32] -> float64 [R, C] (exact)."""
     q = np.asarray(q, dtype=np.uint8)
@@ -378,6 +457,22 @@ def mx_gemm(qa, sa, qb, sb, bias_bits=None, gelu: bool = False):
     """
     a = dequantize(qa, sa)
     b = dequantize(qb, sb)
+    pre = a @ b.T
+    if bias_bits is not None:
+        pre = pre + bf16_bits_to_f64(bias_bits)[None, :]
+    sigma = np.abs(a) @ np.abs(b).T
+    if gelu:
+        return {"pre": pre, "d": bf16_round(gelu_tanh(pre)), "aux": bf16_round(pre), "sigma": sigma}
+    return {"pre": pre, "d": bf16_round(pre), "aux": None, "sigma": sigma}
+
+
+def block_gemm_fp32(qa, sa, qb, sb, bias_bits=None, gelu: bool = False):
+    """Float8BlockScaling TN GEMM with the FP32 scales applied directly:
+    pre = deq(A) . deq(B)^T (+ bias), deq = code * its block's fp32 scale
+    (``dequantize_fp32``; the K blocks are 128 long), then the epilogue as in
+    ``mx_gemm``.  Returns the same dict."""
+    a = dequantize_fp32(qa, sa)
+    b = dequantize_fp32(qb, sb)
     pre = a @ b.T
     if bias_bits is not None:
         pre = pre + bf16_bits_to_f64(bias_bits)[None, :]

@@ -100,3 +100,20 @@ def test_wrong_gelu_constant_is_caught(monkeypatch):
                         lambda x: 0.5 * x * (1 + np.tanh(np.sqrt(2 / np.pi) * (x + 0.0447 * x ** 3))))
     with pytest.raises(AssertionError):
         G.test_gelu_matches_library_and_identities()
+
+
+def test_fp32_scale_mutations_are_caught(monkeypatch):
+    from tests import test_oracle_blockscale_fp32 as F
+    orig = O.block_scale_fp32
+    # the quantisation scale used as the stored scale (448 / amax instead of amax / 448)
+    monkeypatch.setattr(O, "block_scale_fp32", lambda a: tuple(reversed(orig(a))))
+    with pytest.raises(AssertionError):
+        F.test_scale_pair_exhaustive()
+    with pytest.raises(AssertionError):
+        F.test_round_trip_accuracy()
+    monkeypatch.setattr(O, "block_scale_fp32", orig)
+    # the K blocks' scales misaligned by one block
+    orig_deq = O.dequantize_fp32
+    monkeypatch.setattr(O, "dequantize_fp32", lambda q, s: orig_deq(q, np.roll(np.asarray(s), 1, axis=1)))
+    with pytest.raises(AssertionError):
+        F.test_gemm_exact_small()
