@@ -178,6 +178,30 @@ TEMX_API te_mx_status te_mx_block_quantize(const void* x, int64_t rows, int64_t 
                                            uint8_t* q_col, uint8_t* s_col, int64_t ld_s_col,
                                            void* stream);
 
+/* te_mx_block_quantize_fp32 — Float8BlockScaling quantisation that keeps the
+ * FP32 scales (the README's second mode: "compute the GEMM with the FP32
+ * scales directly"; te_mx_gemm_fp32_scales consumes the result).  Blocks as
+ * te_mx_block_quantize.  Per block, with amax the largest |x| present:
+ *   s = fl32(amax / 448)                 the stored fp32 scale,
+ *   r = min(fl32(1 / s), FLT_MAX),       q = E4M3_rn_satfinite(fl32(x r)),
+ * every operation IEEE fp32 rounded to nearest even; amax 0 gives s = r = 1;
+ * a block holding NaN/inf gets s = NaN and codes 0x7F.
+ *   q_row, q_col      E4M3 codes as te_mx_quantize (device, 16-byte aligned).
+ *   s_row             fp32 [rows x ld_s_row]: s_row[r][j] is the scale of the
+ *                     block holding q_row[r][128 j] (2D: repeated over the
+ *                     block's 128 rows); ld_s_row >= ceil(cols / 128) and a
+ *                     multiple of 4 (te_mx_block_scale_pitch_fp32(cols)).
+ *   s_col             fp32 [cols x ld_s_col]: the scale of the block holding
+ *                     q_col[c][128 j]; ld_s_col >= ceil(rows / 128), % 4 == 0.
+ * Scale arrays 16-byte aligned.  Other rules and errors as te_mx_quantize;
+ * block_2d 0 or 1.  Output is bit-exact to the definition above. */
+TEMX_API int64_t te_mx_block_scale_pitch_fp32(int64_t n);
+TEMX_API te_mx_status te_mx_block_quantize_fp32(const void* x, int64_t rows, int64_t cols, int64_t ld_x,
+                                                int32_t block_2d,
+                                                uint8_t* q_row, float* s_row, int64_t ld_s_row,
+                                                uint8_t* q_col, float* s_col, int64_t ld_s_col,
+                                                void* stream);
+
 /* te_mx_layernorm_quantize — LayerNorm fused with MXFP8 quantisation (the
  * input of LayerNormLinear / LayerNormMLP; te.LayerNorm as the drop-in of
  * torch.nn.LayerNorm, leeroopedia "FP8 Training Quickstart"; parameters

@@ -27,6 +27,8 @@ SIGNATURES = {
     "te_mx_scale_pitch": (_SZ, [_I64]),
     "te_mx_quantize": (ctypes.c_int, [_P, _I64, _I64, _I64, _P, _P, _I64, _P, _P, _I64, _P]),
     "te_mx_block_quantize": (ctypes.c_int, [_P, _I64, _I64, _I64, _I32, _P, _P, _I64, _P, _P, _I64, _P]),
+    "te_mx_block_scale_pitch_fp32": (_I64, [_I64]),
+    "te_mx_block_quantize_fp32": (ctypes.c_int, [_P, _I64, _I64, _I64, _I32, _P, _P, _I64, _P, _P, _I64, _P]),
     "te_mx_layernorm_quantize": (ctypes.c_int, [_P, _I64, _I64, _I64, _P, _P, ctypes.c_float, _P, _P, _I64, _P,
                                                 _P, _I64, _P, _P, _P]),
     "te_mx_grouped_code_width": (_I64, [_I64, _I32]),
@@ -205,6 +207,40 @@ def quantize(x, rowwise: bool = True, colwise: bool = False, stream=None, out=No
         workspace = torch.empty(max(1, te_mx_quantize_dbias_workspace_size(rows, cols)), dtype=torch.uint8,
                                 device=x.device)
     te_mx_quantize_dbias(*args, o["dbias"].data_ptr(), workspace.data_ptr(), workspace.numel(), _stream_ptr(stream))
+    return o
+
+
+def te_mx_block_scale_pitch_fp32(n) -> int:
+    return int(lib().te_mx_block_scale_pitch_fp32(n))
+
+
+def te_mx_block_quantize_fp32(x, rows, cols, ld_x, block_2d, q_row, s_row, ld_s_row, q_col, s_col, ld_s_col,
+                              stream) -> None:
+    _check(lib().te_mx_block_quantize_fp32(x, rows, cols, ld_x, block_2d, q_row, s_row, ld_s_row, q_col, s_col,
+                                           ld_s_col, stream))
+
+
+def block_quantize_fp32(x, block_2d: bool = False, rowwise: bool = True, colwise: bool = False, stream=None,
+                        out=None):
+    """Float8BlockScaling-quantise a 2-D bf16 CUDA tensor keeping FP32 scales:
+    E4M3 codes as ``block_quantize`` and fp32 scales, one per block and row
+    (``s_row`` [rows, pitch(cols)], ``s_col`` [cols, pitch(rows)]), for
+    ``gemm_fp32_scales``."""
+    import torch
+    assert x.dtype == torch.bfloat16 and x.dim() == 2 and x.is_cuda
+    rows, cols = x.shape
+    assert x.stride(1) == 1
+    o = dict(out or {})
+    if rowwise and "q_row" not in o:
+        o["q_row"] = torch.empty(rows, cols, dtype=torch.uint8, device=x.device)
+        o["s_row"] = torch.empty(rows, te_mx_block_scale_pitch_fp32(cols), dtype=torch.float32, device=x.device)
+    if colwise and "q_col" not in o:
+        o["q_col"] = torch.empty(cols, rows, dtype=torch.uint8, device=x.device)
+        o["s_col"] = torch.empty(cols, te_mx_block_scale_pitch_fp32(rows), dtype=torch.float32, device=x.device)
+    te_mx_block_quantize_fp32(x.data_ptr(), rows, cols, x.stride(0), int(bool(block_2d)),
+                              _ptr(o.get("q_row")), _ptr(o.get("s_row")), o["s_row"].stride(0) if "s_row" in o else 0,
+                              _ptr(o.get("q_col")), _ptr(o.get("s_col")), o["s_col"].stride(0) if "s_col" in o else 0,
+                              _stream_ptr(stream))
     return o
 
 

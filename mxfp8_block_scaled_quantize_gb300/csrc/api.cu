@@ -244,7 +244,41 @@ te_mx_status te_mx_block_quantize(const void* x, int64_t rows, int64_t cols, int
     te_mx_status st = validate_quantize(x, rows, cols, ld_x, q_row, s_row, ld_s_row, q_col, s_col, ld_s_col, false);
     if (st != TE_MX_OK || rows == 0 || cols == 0 || (!q_row && !q_col)) return st;
     QuantizeArgs a{x, rows, cols, ld_x, q_row, s_row, ld_s_row, q_col, s_col, ld_s_col, nullptr, nullptr};
-    return block_quantize_launch(a, block_2d == 1, static_cast<cudaStream_t>(stream));
+    return block_quantize_launch(a, block_2d == 1, false, static_cast<cudaStream_t>(stream));
+}
+
+int64_t te_mx_block_scale_pitch_fp32(int64_t n) {
+    if (n <= 0) return 0;
+    return ((n + 127) / 128 + 3) / 4 * 4;
+}
+
+te_mx_status te_mx_block_quantize_fp32(const void* x, int64_t rows, int64_t cols, int64_t ld_x, int32_t block_2d,
+                                       uint8_t* q_row, float* s_row, int64_t ld_s_row,
+                                       uint8_t* q_col, float* s_col, int64_t ld_s_col, void* stream) {
+    t_last_error[0] = '\0';
+    if (block_2d != 0 && block_2d != 1) return set_error(TE_MX_ERR_INVALID_ARG, "block_2d=%d must be 0 or 1", int(block_2d));
+    // the code / shape / device checks of te_mx_quantize (MX scale pitches that pass stand in for the fp32 ones)
+    uint8_t* sr = reinterpret_cast<uint8_t*>(s_row);
+    uint8_t* sc = reinterpret_cast<uint8_t*>(s_col);
+    if (rows > 0 && cols > 0) {
+        if (q_row && s_row) {
+            if (!aligned(s_row, 16)) return set_error(TE_MX_ERR_MISALIGNED, "s_row is not 16-byte aligned");
+            if (ld_s_row % 4 || ld_s_row < (cols + 127) / 128)
+                return set_error(TE_MX_ERR_MISALIGNED, "ld_s_row=%lld must be a multiple of 4 and >= ceil(cols/128)",
+                                 (long long)ld_s_row);
+        }
+        if (q_col && s_col) {
+            if (!aligned(s_col, 16)) return set_error(TE_MX_ERR_MISALIGNED, "s_col is not 16-byte aligned");
+            if (ld_s_col % 4 || ld_s_col < (rows + 127) / 128)
+                return set_error(TE_MX_ERR_MISALIGNED, "ld_s_col=%lld must be a multiple of 4 and >= ceil(rows/128)",
+                                 (long long)ld_s_col);
+        }
+    }
+    te_mx_status st = validate_quantize(x, rows, cols, ld_x, q_row, sr, int64_t(te_mx_scale_pitch(cols)), q_col, sc,
+                                        int64_t(te_mx_scale_pitch(rows)), false);
+    if (st != TE_MX_OK || rows == 0 || cols == 0 || (!q_row && !q_col)) return st;
+    QuantizeArgs a{x, rows, cols, ld_x, q_row, sr, ld_s_row, q_col, sc, ld_s_col, nullptr, nullptr};
+    return block_quantize_launch(a, block_2d == 1, true, static_cast<cudaStream_t>(stream));
 }
 
 te_mx_status te_mx_layernorm_quantize(const void* x, int64_t rows, int64_t hidden, int64_t ld_x,

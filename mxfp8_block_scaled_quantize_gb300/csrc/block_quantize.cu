@@ -15,6 +15,13 @@
 // its 32-element groups.  The MXFP8 GEMM then computes the block-scaled GEMM
 // with no change.
 //
+// The README's second mode keeps the FP32 scales (kF32): per block
+//   s = fl32(amax / 448)  (stored, fp32),  r = min(fl32(1 / s), FLT_MAX),
+//   q = E4M3_rn_satfinite(fl32(x * r)),
+// s = r = 1 for amax 0, s = NaN and codes 0x7F for a non-finite block; one
+// fp32 scale per block and row of each copy ([rows][ceil(cols / 128)] and
+// [cols][ceil(rows / 128)], a 128x128 block's scale repeated over its rows).
+//
 // Work decomposition.  A CTA owns 128 x 128 tiles (two 64-column TMA boxes,
 // 128-byte swizzle) in a kStages-deep ring.  Warp 8 is the producer: it loads
 // tiles, and when the compute warps have staged a tile's codes it stores them
@@ -48,8 +55,8 @@ constexpr int kSmemBytes = kStages * kTileBytes + 1024;
 
 struct BlockParams {
     int64_t rows, cols;
-    uint8_t* s_row;
-    int64_t ld_s_row;
+    uint8_t* s_row;        // E8M0 bytes, or fp32 scales (kF32) at this address
+    int64_t ld_s_row;      // bytes, or fp32 elements (kF32)
     uint8_t* s_col;
     int64_t ld_s_col;
     int64_t col_tiles;     // ceil(cols / 128)
@@ -77,6 +84,37 @@ __device__ __forceinline__ uint32_t block_scale_byte(uint32_t amax_bits) {
     return e > 0 ? uint32_t(e) : 0u;
 }
 
+// A block's quantisation: multiplier m (x * m is rounded to E4M3), whether
+// the block is non-finite, and what is stored (E8M0 byte, or fp32 scale s).
+struct BlockScale {
+    float m;
+    bool bad;
+    uint32_t byte;
+    float s;
+};
+template <bool kF32>
+__device__ __forceinline__ BlockScale block_scale(uint32_t amax_bits) {
+    BlockScale b;
+    if constexpr (kF32) {
+        b.bad = (amax_bits >> 7) == 0xFFu;
+        b.byte = 0;
+        if (b.bad) {
+            b.s = b.m = __uint_as_float(0x7FC00000u);
+        } else if (amax_bits == 0) {
+            b.s = b.m = 1.0f;
+        } else {
+            b.s = __fdiv_rn(__uint_as_float(amax_bits << 16), 448.0f);
+            b.m = fminf(__frcp_rn(b.s), 3.40282347e38f);
+        }
+    } else {
+        b.byte = block_scale_byte(amax_bits);
+        b.bad = b.byte == 0xFFu;
+        b.m = inv_scale(b.byte);
+        b.s = 0.0f;
+    }
+    return b;
+}
+
 // The eight compute warps only (the producer warp does not take part).
 __device__ __forceinline__ void compute_sync() {
     asm volatile("bar.sync 1, %0;" ::"n"(kComputeWarps * 32) : "memory");
@@ -91,7 +129,7 @@ __device__ __forceinline__ void put_scales(uint8_t* p, uint32_t sb, int64_t n) {
     }
 }
 
-template <bool kRowwise, bool kColwise, bool k2d>
+template <bool kRowwise, bool kColwise, bool k2d, bool kF32>
 __global__ void __launch_bounds__(kThreads, kCtasPerSm)
 block_quantize_kernel(const __grid_constant__ CUtensorMap x_map, const __grid_constant__ CUtensorMap qrow_map,
                       const __grid_constant__ CUtensorMap qcol_map, const BlockParams p) {
@@ -214,19 +252,23 @@ block_quantize_kernel(const __grid_constant__ CUtensorMap x_map, const __grid_co
         }
         if (kRowwise) {
             const uint32_t a = k2d ? blk : max(sh.row_amax[buf][0][row], sh.row_amax[buf][1][row]);
-            const uint32_t sb = block_scale_byte(a);
-            const float m = inv_scale(sb);
+            const BlockScale bs = block_scale<kF32>(a);
             const int sw = row & 7;
 #pragma unroll
             for (int j = 0; j < 4; ++j) {                // 16 codes per chunk, chunks 4b .. 4b+3 of the row
                 uint32_t c[4];
 #pragma unroll
-                for (int q = 0; q < 4; ++q) c[q] = quant4(wr[8 * j + 2 * q], wr[8 * j + 2 * q + 1], m);
-                if (sb == 0xFFu) c[0] = c[1] = c[2] = c[3] = 0x7F7F7F7Fu;
+                for (int q = 0; q < 4; ++q) c[q] = quant4(wr[8 * j + 2 * q], wr[8 * j + 2 * q + 1], bs.m);
+                if (bs.bad) c[0] = c[1] = c[2] = c[3] = 0x7F7F7F7Fu;
                 sts128(tile + row * 128 + (((4 * b + j) ^ sw) << 4), c[0], c[1], c[2], c[3]);
             }
             const int64_t r = int64_t(r0) + row;
-            if (b == 0 && r < p.rows) put_scales(p.s_row + r * p.ld_s_row + (c0 >> 5), sb, (p.cols - c0) >> 5);
+            if (b == 0 && r < p.rows) {
+                if constexpr (kF32)
+                    reinterpret_cast<float*>(p.s_row)[r * p.ld_s_row + c0 / kEdge] = bs.s;
+                else
+                    put_scales(p.s_row + r * p.ld_s_row + (c0 >> 5), bs.byte, (p.cols - c0) >> 5);
+            }
         }
         if (kColwise) {
             uint32_t a2;
@@ -236,8 +278,8 @@ block_quantize_kernel(const __grid_constant__ CUtensorMap x_map, const __grid_co
                 a2 = max_u16x2(max_u16x2(sh.col_amax[buf][0][b * 32 + lane], sh.col_amax[buf][1][b * 32 + lane]),
                                max_u16x2(sh.col_amax[buf][2][b * 32 + lane], sh.col_amax[buf][3][b * 32 + lane]));
             }
-            const uint32_t s_lo = block_scale_byte(a2 & 0xFFFFu), s_hi = block_scale_byte(a2 >> 16);
-            const float m_lo = inv_scale(s_lo), m_hi = inv_scale(s_hi);
+            const BlockScale b_lo = block_scale<kF32>(a2 & 0xFFFFu), b_hi = block_scale<kF32>(a2 >> 16);
+            const float m_lo = b_lo.m, m_hi = b_hi.m;
             uint32_t lo[8], hi[8];
 #pragma unroll
             for (int k = 0; k < 8; ++k) {
@@ -247,11 +289,11 @@ block_quantize_kernel(const __grid_constant__ CUtensorMap x_map, const __grid_co
                 hi[k] = cvt_e4m3x2(__fmul_rn(bf16_hi(a0), m_hi), __fmul_rn(bf16_hi(a1), m_hi)) |
                         (cvt_e4m3x2(__fmul_rn(bf16_hi(a2w), m_hi), __fmul_rn(bf16_hi(a3), m_hi)) << 16);
             }
-            if (s_lo == 0xFFu) {
+            if (b_lo.bad) {
 #pragma unroll
                 for (int k = 0; k < 8; ++k) lo[k] = 0x7F7F7F7Fu;
             }
-            if (s_hi == 0xFFu) {
+            if (b_hi.bad) {
 #pragma unroll
                 for (int k = 0; k < 8; ++k) hi[k] = 0x7F7F7F7Fu;
             }
@@ -266,8 +308,13 @@ block_quantize_kernel(const __grid_constant__ CUtensorMap x_map, const __grid_co
                     sts128(tile + kBoxBytes + C * 128 + (((2 * g + t) ^ (C & 7)) << 4), w[4 * t], w[4 * t + 1],
                            w[4 * t + 2], w[4 * t + 3]);
                 const int64_t c = int64_t(c0) + C;
-                if (g == 0 && c < p.cols)
-                    put_scales(p.s_col + c * p.ld_s_col + (r0 >> 5), j ? s_hi : s_lo, (p.rows - r0 + 31) >> 5);
+                if (g == 0 && c < p.cols) {
+                    if constexpr (kF32)
+                        reinterpret_cast<float*>(p.s_col)[c * p.ld_s_col + r0 / kEdge] = j ? b_hi.s : b_lo.s;
+                    else
+                        put_scales(p.s_col + c * p.ld_s_col + (r0 >> 5), j ? b_hi.byte : b_lo.byte,
+                                   (p.rows - r0 + 31) >> 5);
+                }
             }
         }
         fence_proxy_async_smem();                      // the staged codes are read by the TMA engine
@@ -276,10 +323,10 @@ block_quantize_kernel(const __grid_constant__ CUtensorMap x_map, const __grid_co
     }
 }
 
-template <bool R, bool C, bool D2>
+template <bool R, bool C, bool D2, bool F32>
 cudaError_t launch(const CUtensorMap& xm, const CUtensorMap& qr, const CUtensorMap& qc, const BlockParams& p,
                    int sms, cudaStream_t stream) {
-    auto k = block_quantize_kernel<R, C, D2>;
+    auto k = block_quantize_kernel<R, C, D2, F32>;
     cudaError_t e = set_smem_attribute_once(reinterpret_cast<const void*>(k), kSmemBytes);
     if (e != cudaSuccess) return e;
     const int64_t cap = int64_t(kCtasPerSm) * sms;
@@ -288,9 +335,22 @@ cudaError_t launch(const CUtensorMap& xm, const CUtensorMap& qr, const CUtensorM
     return cudaGetLastError();
 }
 
+template <bool F32>
+cudaError_t launch_all(bool rowwise, bool colwise, bool block_2d, const CUtensorMap& xm, const CUtensorMap& qr,
+                       const CUtensorMap& qc, const BlockParams& p, int sms, cudaStream_t stream) {
+    if (block_2d) {
+        if (rowwise && colwise) return launch<true, true, true, F32>(xm, qr, qc, p, sms, stream);
+        if (rowwise) return launch<true, false, true, F32>(xm, qr, qc, p, sms, stream);
+        return launch<false, true, true, F32>(xm, qr, qc, p, sms, stream);
+    }
+    if (rowwise && colwise) return launch<true, true, false, F32>(xm, qr, qc, p, sms, stream);
+    if (rowwise) return launch<true, false, false, F32>(xm, qr, qc, p, sms, stream);
+    return launch<false, true, false, F32>(xm, qr, qc, p, sms, stream);
+}
+
 }  // namespace
 
-te_mx_status block_quantize_launch(const QuantizeArgs& a, bool block_2d, cudaStream_t stream) {
+te_mx_status block_quantize_launch(const QuantizeArgs& a, bool block_2d, bool fp32_scales, cudaStream_t stream) {
     const bool rowwise = a.q_row != nullptr, colwise = a.q_col != nullptr;
     if (a.rows == 0 || a.cols == 0 || (!rowwise && !colwise)) return TE_MX_OK;
 
@@ -318,16 +378,8 @@ te_mx_status block_quantize_launch(const QuantizeArgs& a, bool block_2d, cudaStr
     int sms = 0;
     if ((st = device_sm_count(&sms)) != TE_MX_OK) return st;
 
-    cudaError_t e;
-    if (block_2d) {
-        if (rowwise && colwise) e = launch<true, true, true>(xm, qr, qc, p, sms, stream);
-        else if (rowwise) e = launch<true, false, true>(xm, qr, qc, p, sms, stream);
-        else e = launch<false, true, true>(xm, qr, qc, p, sms, stream);
-    } else {
-        if (rowwise && colwise) e = launch<true, true, false>(xm, qr, qc, p, sms, stream);
-        else if (rowwise) e = launch<true, false, false>(xm, qr, qc, p, sms, stream);
-        else e = launch<false, true, false>(xm, qr, qc, p, sms, stream);
-    }
+    const cudaError_t e = fp32_scales ? launch_all<true>(rowwise, colwise, block_2d, xm, qr, qc, p, sms, stream)
+                                      : launch_all<false>(rowwise, colwise, block_2d, xm, qr, qc, p, sms, stream);
     return cuda_status(e, "block quantize kernel launch");
 }
 

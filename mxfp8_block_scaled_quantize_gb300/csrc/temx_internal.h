@@ -76,8 +76,9 @@ te_mx_status grouped_colwise_launch(const GroupedColwiseArgs& a, cudaStream_t st
 int64_t grouped_code_width(int64_t total_m, int32_t groups);    // an upper bound of sum round_up(m_e, 128)
 int64_t grouped_scale_width(int64_t total_m, int32_t groups);   // an upper bound of sum round_up(Kp_e / 32, 16)
 int64_t ln_quantize_max_hidden();
-// Float8BlockScaling quantisation (E8M0-cast scales); `partial`/`dbias` unused.
-te_mx_status block_quantize_launch(const QuantizeArgs& a, bool block_2d, cudaStream_t stream);
+// Float8BlockScaling quantisation; `partial`/`dbias` unused.  fp32_scales:
+// s_row / s_col hold fp32 scales (pitches in elements), else E8M0 bytes.
+te_mx_status block_quantize_launch(const QuantizeArgs& a, bool block_2d, bool fp32_scales, cudaStream_t stream);
 te_mx_status gemm_launch(const GemmArgs& a, cudaStream_t stream);
 
 // Helpers implemented in api.cu.

@@ -87,6 +87,17 @@ def test_host_validation_rejects_bad_arguments_before_any_launch(lib):
         binding.te_mx_grouped_gemm(2, 16, 128, 16, 16, 16, 16, 16, 16, 128, 128, 0, 5, 16, 0, 0, 0, 0)
     with pytest.raises(binding.TemxError, match="INVALID_ARG"):      # wgrad accumulate flag not 0/1
         binding.te_mx_grouped_gemm_wgrad(2, 16, 128, 16, 16, 16, 16, 128, 128, 128, 16, 2, 16, 0)
+    with pytest.raises(binding.TemxError, match="INVALID_ARG"):
+        binding.te_mx_block_quantize_fp32(16, 128, 128, 128, 2, 16, 16, 4, 0, 0, 0, 0)  # block_2d not 0/1
+    with pytest.raises(binding.TemxError, match="MISALIGNED"):
+        binding.te_mx_block_quantize_fp32(16, 128, 512, 512, 0, 16, 16, 2, 0, 0, 0, 0)  # ld_s_row % 4
+    with pytest.raises(binding.TemxError, match="MISALIGNED"):
+        binding.te_mx_block_quantize_fp32(16, 128, 640, 640, 0, 16, 16, 4, 0, 0, 0, 0)  # ld_s_row < 5 blocks
+    with pytest.raises(binding.TemxError, match="MISALIGNED"):
+        binding.te_mx_block_quantize_fp32(16, 128, 128, 128, 0, 0, 0, 0, 16, 8, 4, 0)   # s_col not 16-aligned
+    with pytest.raises(binding.TemxError, match="UNSUPPORTED_SHAPE"):
+        binding.te_mx_block_quantize_fp32(16, 128, 48, 48, 0, 16, 16, 4, 0, 0, 0, 0)    # cols % 32
+    assert binding.te_mx_block_scale_pitch_fp32(7168) == 56 and binding.te_mx_block_scale_pitch_fp32(130) == 4
     # zero-sized problems are no-ops
     binding.te_mx_layernorm_quantize(16, 0, 64, 64, 16, 16, 1e-5, 16, 16, 16, 0, 0, 0, 0, 0, 0)
     binding.te_mx_block_quantize(0, 0, 128, 128, 1, 0, 0, 0, 0, 0, 0, 0)
