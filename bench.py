@@ -207,6 +207,13 @@ class Step:
                            "grouped_quant_moe_x": qb(MT, K, False), "grouped_quant_moe_dy": qb(MT, N, False)}
         self.next_flops["gemm_moe_wgrad"] = 2.0 * float(counts.sum()) * N * K
         self.next_flops["gemm_wgrad_accum_f32"] = 2.0 * F * H * T
+        self.next_flops["gemm_fp32_scales_fprop"] = 2.0 * T * F * H
+        self.next_bytes["block_quant_fp32_ffn_x"] = qb(T, H, True)     # fp32 scale per 128 = 1/32 B per element
+        self.next_bytes["block_quant_fp32_ffn_w"] = qb(F, H, True)
+        p32 = temx.te_mx_block_scale_pitch_fp32
+        f32 = lambda r, c: torch.empty(r, c, dtype=torch.float32, device=dev)
+        o["x32"] = {"q_row": e(T, H), "s_row": f32(T, p32(H)), "q_col": e(H, T), "s_col": f32(H, p32(T))}
+        o["w32"] = {"q_row": e(F, H), "s_row": f32(F, p32(H)), "q_col": e(H, F), "s_col": f32(H, p32(F))}
         o["main_grad"] = torch.zeros(F, H, dtype=torch.float32, device=dev)   # fp32 weight-gradient accumulator
         # MoE expert wgrad: per-expert column-wise copies of X and dY, then dW_e = dY_e^T X_e
         gdev = d["moe_m"].to(torch.int32)
@@ -238,6 +245,13 @@ class Step:
             ("gemm_moe_wgrad", lambda: temx.grouped_gemm_wgrad(gdev, MT, o["gdy"], o["gx"], out=o["dw"])),
             ("gemm_wgrad_accum_f32", lambda: temx.gemm(o["dy"]["q_col"], o["dy"]["s_col"], o["x_row"]["q_col"],
                                                        o["x_row"]["s_col"], accumulate=o["main_grad"])),
+            # Float8BlockScaling keeping FP32 scales: X (1x128 blocks) and W (128x128),
+            # then the ffn fprop computed with those scales (bias + GELU + AUX)
+            ("block_quant_fp32_ffn_x", lambda: temx.block_quantize_fp32(d["ffn_X"], False, True, True, out=o["x32"])),
+            ("block_quant_fp32_ffn_w", lambda: temx.block_quantize_fp32(d["ffn_W"], True, True, True, out=o["w32"])),
+            ("gemm_fp32_scales_fprop", lambda: temx.gemm_fp32_scales(o["x32"]["q_row"], o["x32"]["s_row"],
+                                                                     o["w32"]["q_row"], o["w32"]["s_row"], True,
+                                                                     bias=d["ffn_b"], gelu=True, out=o["fprop"])),
         ]
         temx.quantize(d["ffn_W"], False, True, out=o["w_col"])
 
@@ -440,6 +454,7 @@ CASES = {
     "grouped_quant_x": "per-expert column-wise MXFP8 of moe X [131072x4096] (experts padded to 128 tokens)",
     "gemm_fc1": "fc1 fprop 4096x4096x1024, bias + GELU + AUX",
     "gemm_ffn": "ffn fprop 8192x18432x7168, bias + GELU + AUX",
+    "gemm_ffn_fp32": "ffn fprop 8192x18432x7168 with FP32 block scales (X 1x128, W 128x128), bias + GELU + AUX",
     "gemm_wgrad": "ffn wgrad 18432x7168x8192 on column-wise operands",
     "gemm_moe": "moe grouped 128 experts x 1536 x 4096, GELU + AUX",
 }
@@ -450,7 +465,8 @@ def run_case(case: str, reps: int):
     import mxfp8_block_scaled_quantize_gb300 as temx
     from mxfp8_block_scaled_quantize_gb300 import workloads
     dev = torch.device("cuda", 0)
-    if case in ("quant_both", "quant_row", "block_quant_x", "block_quant_w", "ln_quant_x", "gemm_ffn", "gemm_wgrad"):
+    if case in ("quant_both", "quant_row", "block_quant_x", "block_quant_w", "ln_quant_x", "gemm_ffn", "gemm_wgrad",
+                "gemm_ffn_fp32"):
         w = workloads.make_ffn()
     elif case == "gemm_fc1":
         w = workloads.make_fc1()
@@ -479,6 +495,12 @@ def run_case(case: str, reps: int):
         qw = temx.quantize(w["W"].to(dev), True, False)
         b = w["bias"].to(dev)
         fn = lambda: temx.gemm(qx["q_row"], qx["s_row"], qw["q_row"], qw["s_row"], bias=b, gelu=True)
+    elif case == "gemm_ffn_fp32":
+        qx = temx.block_quantize_fp32(w["X"].to(dev), False)
+        qw = temx.block_quantize_fp32(w["W"].to(dev), True)
+        b = w["bias"].to(dev)
+        fn = lambda: temx.gemm_fp32_scales(qx["q_row"], qx["s_row"], qw["q_row"], qw["s_row"], True, bias=b,
+                                           gelu=True)
     elif case == "gemm_wgrad":
         qd = temx.quantize(w["dY"].to(dev), False, True)
         qx = temx.quantize(w["X"].to(dev), False, True)

@@ -261,6 +261,26 @@ TEMX_API te_mx_status te_mx_gemm(const uint8_t* A, const uint8_t* sA, int64_t ld
                         void* workspace, size_t workspace_bytes,
                         void* stream);
 
+/* te_mx_gemm_fp32_scales — the Float8BlockScaling TN GEMM computed with the
+ * FP32 scales directly (ROCm/TransformerEngine README, "Blockwise FP8 GEMM
+ * support on ROCm", second mode), on te_mx_block_quantize_fp32 output:
+ *   pre[m][n] = sum_kb sA[m][kb] sB[n][kb] sum_{k in block kb} A[m][k] B[n][k]
+ *   (+ bias[n]),  D = the epilogue of pre as in te_mx_gemm,
+ * with 128-long K blocks kb.  A: E4M3 [M x K], B: E4M3 [N x K] (K-contiguous);
+ * sA fp32 [M x ld_sA], sB fp32 [N x ld_sB] (one scale per row and K block;
+ * pitches multiples of 4, >= K/128; 16-byte aligned).  b_blocks_2d = 1 tells
+ * the GEMM that sB is constant over 128-row blocks (128x128 weight blocks,
+ * 1Dx2D scaling), so it reads one scale per block; 0 for 1x128 B blocks
+ * (1Dx1D).  Epilogues: NONE, BIAS, GELU_AUX, BIAS_GELU_AUX, DGELU (not
+ * ACCUMULATE_F32).  Each K block's fp32 product (tensor cores, no block
+ * scaling) is scaled and accumulated in fp32.  Shapes, alignment, errors and
+ * the accuracy bound as te_mx_gemm; asynchronous on `stream`. */
+TEMX_API te_mx_status te_mx_gemm_fp32_scales(const uint8_t* A, const float* sA, int64_t ld_sA,
+                                             const uint8_t* B, const float* sB, int64_t ld_sB,
+                                             int32_t b_blocks_2d, int64_t M, int64_t N, int64_t K,
+                                             const void* bias, int32_t epilogue,
+                                             void* D, void* aux, void* stream);
+
 /* te_mx_grouped_gemm — one launch over G groups (MoE experts) of the same
  * GEMM ("Single-Launch Grouped GEMM Backends on ROCm", ROCm/TransformerEngine
  * README; MXFP8 grouped GEMM), with ragged and possibly empty groups:

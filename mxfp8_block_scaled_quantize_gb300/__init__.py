@@ -6,7 +6,8 @@ seeded synthetic inputs.
 """
 from .binding import (  # noqa: F401
     EPI_ACCUMULATE_F32, EPI_BIAS, EPI_BIAS_GELU_AUX, EPI_DGELU, EPI_GELU_AUX, EPI_NONE, TemxError, block_quantize,
-    block_quantize_fp32, gemm, grouped_gemm, te_mx_block_quantize_fp32, te_mx_block_scale_pitch_fp32,
+    block_quantize_fp32, gemm, gemm_fp32_scales, grouped_gemm, te_mx_block_quantize_fp32,
+    te_mx_block_scale_pitch_fp32, te_mx_gemm_fp32_scales,
     grouped_gemm_wgrad, layernorm_quantize, quantize, quantize_colwise_grouped, te_mx_block_quantize,
     te_mx_grouped_gemm_wgrad, te_mx_layernorm_quantize, te_mx_quantize_colwise_grouped,
     te_mx_device_status, te_mx_gemm, te_mx_gemm_workspace_size, te_mx_grouped_gemm, te_mx_quantize,

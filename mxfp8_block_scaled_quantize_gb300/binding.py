@@ -40,6 +40,8 @@ SIGNATURES = {
     "te_mx_quantize_dbias": (ctypes.c_int, [_P, _I64, _I64, _I64, _P, _P, _I64, _P, _P, _I64, _P, _P, _SZ, _P]),
     "te_mx_quantize_dbias_noalloc": (ctypes.c_int, [_P, _I64, _I64, _I64, _P, _P, _I64, _P, _P, _I64, _P, _P]),
     "te_mx_gemm": (ctypes.c_int, [_P, _P, _I64, _P, _P, _I64, _I64, _I64, _I64, _P, _I32, _P, _P, _P, _SZ, _P]),
+    "te_mx_gemm_fp32_scales": (ctypes.c_int, [_P, _P, _I64, _P, _P, _I64, _I32, _I64, _I64, _I64, _P, _I32, _P, _P,
+                                              _P]),
     "te_mx_grouped_gemm": (ctypes.c_int, [_I32, _P, _I64, _P, _P, _I64, _P, _P, _I64, _I64, _I64, _P, _I32,
                                           _P, _P, _P, _SZ, _P]),
     "te_mx_gemm_workspace_size": (_SZ, [_I64, _I64, _I64, _I32]),
@@ -359,6 +361,39 @@ def gemm(qa, sa, qb, sb, bias=None, gelu: bool = False, stream=None, out=None, d
     te_mx_gemm(qa.data_ptr(), sa.data_ptr(), sa.stride(0), qb.data_ptr(), sb.data_ptr(), sb.stride(0),
                M, N, K, _ptr(bias), epi, d.data_ptr(), _ptr(aux), 0, 0, _stream_ptr(stream))
     return d, aux
+
+
+def te_mx_gemm_fp32_scales(A, sA, ld_sA, B, sB, ld_sB, b_blocks_2d, M, N, K, bias, epilogue, D, aux,
+                           stream) -> None:
+    _check(lib().te_mx_gemm_fp32_scales(A, sA, ld_sA, B, sB, ld_sB, b_blocks_2d, M, N, K, bias, epilogue, D, aux,
+                                        stream))
+
+
+def gemm_fp32_scales(qa, sa, qb, sb, b_blocks_2d: bool, bias=None, gelu: bool = False, stream=None, out=None,
+                     dgelu_aux=None):
+    """Float8BlockScaling GEMM with FP32 scales (``block_quantize_fp32``
+    output; ``b_blocks_2d`` for 128x128 weight blocks): D = epilogue(sum over
+    128-long K blocks of sA sB A_kb . B_kb^T (+ bias)); returns (D, aux or None).
+    With ``dgelu_aux`` the epilogue is the GELU backward (see ``gemm``)."""
+    import torch
+    M, K = qa.shape
+    N = qb.shape[0]
+    epi = (EPI_BIAS if bias is not None else EPI_NONE) + (EPI_GELU_AUX if gelu else 0)
+    aux = None
+    if dgelu_aux is not None:
+        assert bias is None and not gelu
+        epi = EPI_DGELU
+    if out is None:
+        d = torch.empty(M, N, dtype=torch.bfloat16, device=qa.device)
+        if gelu:
+            aux = torch.empty(M, N, dtype=torch.bfloat16, device=qa.device)
+    else:
+        d, aux = out
+    aux_ptr = dgelu_aux.data_ptr() if dgelu_aux is not None else _ptr(aux)
+    te_mx_gemm_fp32_scales(qa.data_ptr(), sa.data_ptr(), sa.stride(0), qb.data_ptr(), sb.data_ptr(), sb.stride(0),
+                           int(bool(b_blocks_2d)), M, N, K, _ptr(bias), epi, d.data_ptr(), aux_ptr,
+                           _stream_ptr(stream))
+    return d, (aux if dgelu_aux is None else None)
 
 
 def grouped_gemm(group_m, qx, sx, qw, sw, bias=None, gelu: bool = False, stream=None, out=None, dgelu_aux=None):

@@ -448,6 +448,39 @@ te_mx_status te_mx_gemm(const uint8_t* A, const uint8_t* sA, int64_t ld_sA,
     return gemm_launch(a, static_cast<cudaStream_t>(stream));
 }
 
+te_mx_status te_mx_gemm_fp32_scales(const uint8_t* A, const float* sA, int64_t ld_sA,
+                                    const uint8_t* B, const float* sB, int64_t ld_sB, int32_t b_blocks_2d,
+                                    int64_t M, int64_t N, int64_t K, const void* bias, int32_t epilogue,
+                                    void* D, void* aux, void* stream) {
+    t_last_error[0] = '\0';
+    if (M < 0) return set_error(TE_MX_ERR_INVALID_ARG, "negative M");
+    if (M == 0) return TE_MX_OK;
+    if (M > (int64_t(1) << 31) - 256) return set_error(TE_MX_ERR_UNSUPPORTED_SHAPE, "M too large");
+    if (b_blocks_2d != 0 && b_blocks_2d != 1)
+        return set_error(TE_MX_ERR_INVALID_ARG, "b_blocks_2d=%d must be 0 or 1", int(b_blocks_2d));
+    if (epilogue == TE_MX_EPI_ACCUMULATE_F32)
+        return set_error(TE_MX_ERR_INVALID_ARG, "the accumulating epilogue is not offered with FP32 scales");
+    // the MX checks with stand-in scale pitches, then the FP32 scale rules
+    const int64_t mx_pitch = int64_t(te_mx_scale_pitch(K));
+    te_mx_status st = validate_gemm_common(A, reinterpret_cast<const uint8_t*>(sA), mx_pitch, B,
+                                           reinterpret_cast<const uint8_t*>(sB), mx_pitch, N, K, bias, epilogue, D, aux);
+    if (st != TE_MX_OK) return st;
+    if (ld_sA % 4 || ld_sA < K / 128 || ld_sB % 4 || ld_sB < K / 128)
+        return set_error(TE_MX_ERR_MISALIGNED, "FP32 scale pitches must be multiples of 4 and >= K/128");
+    if ((st = check_device(nullptr)) != TE_MX_OK) return st;
+    GemmArgs a{};
+    a.A = A; a.sA = reinterpret_cast<const uint8_t*>(sA); a.ld_sA = ld_sA;
+    a.B = B; a.sB = reinterpret_cast<const uint8_t*>(sB); a.ld_sB = ld_sB;
+    a.M = M; a.N = N; a.K = K; a.bias = bias;
+    a.has_bias = epilogue == TE_MX_EPI_BIAS || epilogue == TE_MX_EPI_BIAS_GELU_AUX;
+    a.gelu = epilogue == TE_MX_EPI_GELU_AUX || epilogue == TE_MX_EPI_BIAS_GELU_AUX;
+    a.dgelu = epilogue == TE_MX_EPI_DGELU;
+    a.D = D; a.aux = aux; a.groups = 0; a.group_m = nullptr;
+    a.f32_scales = true;
+    a.b_2d = b_blocks_2d == 1;
+    return gemm_launch(a, static_cast<cudaStream_t>(stream));
+}
+
 te_mx_status te_mx_grouped_gemm(int32_t num_groups, const int32_t* group_m, int64_t total_m,
                                 const uint8_t* X, const uint8_t* sX, int64_t ld_sX,
                                 const uint8_t* W, const uint8_t* sW, int64_t ld_sW,

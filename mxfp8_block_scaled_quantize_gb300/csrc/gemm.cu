@@ -77,7 +77,20 @@ struct Cfg {
     // M >> 4 at bit 24; scale-factor byte ids at bits 4..5 (B) and 29..30 (A).
     static constexpr uint32_t kIdescBase =
         (uint32_t(kBN >> 3) << 17) | (1u << 23) | (uint32_t(kTileM >> 4) << 24);
+    // FP32 scales: each K-step's product is computed as two N = 128 halves.
+    // Instruction descriptor, kind::f8f6f4 (no block scaling): fp32 D (bits
+    // 4..5 = 1), E4M3 A and B (formats 0), both K-major, N >> 3 at bit 17,
+    // M >> 4 at bit 24.  A half's B rows start kBHalfBytes into the B tile.
+    static constexpr uint32_t kIdescF32 = (1u << 4) | (uint32_t(128 >> 3) << 17) | (uint32_t(kTileM >> 4) << 24);
+    static constexpr int kBHalfBytes = (kBRows / 2) * kBK;
 };
+// FP32 scales: output column of TMEM column j (0..127) of product half h.
+// A CTA pair's N = 128 MMA takes 64 B rows from each CTA, whose B tiles hold
+// output columns 0..127 and 128..255.
+template <int kPair>
+__device__ __forceinline__ int f32_half_col(int h, int j) {
+    return kPair == 2 ? (j < 64 ? 64 * h + j : 128 + 64 * h + (j - 64)) : 128 * h + j;
+}
 static_assert(Cfg<1>::kStageBytes % 1024 == 0 && Cfg<2>::kStageBytes % 1024 == 0, "stage alignment");
 
 __device__ __forceinline__ uint32_t idesc_sf(uint32_t base, uint32_t sf_id) {
@@ -110,6 +123,7 @@ struct GemmParams {
     bool wgrad;                          // grouped wgrad: per-group K range, D = [groups x M x N]
     int64_t total_m;                     // wgrad: bound on the token counts' sum
     int64_t ld_code, ld_sfa, ld_sfb;     // wgrad: operand pitches (capacities)
+    bool b_2d;                           // FP32 scales: B's scales constant over 128-row blocks
     unsigned int* status;
 };
 
@@ -138,6 +152,11 @@ struct __align__(16) SharedState {
     uint64_t tmem_full;
     uint64_t tmem_empty;                   // (MMA CTA) accumulator drained by the epilogue of every CTA
     uint64_t epi_drained;                  // this CTA's 8 epilogue warps hold their accumulator rows
+    // FP32-scale mode: the two halves of a K-step's product in TMEM (columns
+    // 256 and 384; the scaled accumulator is columns 0..255)
+    uint64_t scr_full[2];                  // a product half landed (each CTA)
+    uint64_t scr_empty[2];                 // (MMA CTA) the epilogue warps of that half (both CTAs) read it
+    uint64_t sf_done[kSfRing];             // this CTA's epilogue warps are done with a scale group
     uint32_t tmem_base;
     int32_t abort;
     int64_t grouped_tiles;                 // total tiles of a grouped launch
@@ -518,7 +537,10 @@ __device__ __forceinline__ void store_64_staged(uint32_t* acc, const GemmParams&
     }
 }
 
-template <int kPair, bool kAcc, bool kWgrad>   // kAcc: fp32 D accumulated into; kWgrad: grouped wgrad
+// kAcc: fp32 D accumulated into; kWgrad: grouped wgrad; kF32: Float8BlockScaling
+// operands with FP32 scales (dense only): every K-step's product lands in one
+// of two TMEM buffers and the epilogue warps accumulate it, scaled, in registers.
+template <int kPair, bool kAcc, bool kWgrad, bool kF32>
 __global__ void __launch_bounds__(kThreads, 1)   // 168 registers: 3 warps share a 16K-register sub-partition
 gemm_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_constant__ CUtensorMap map_b,
             const __grid_constant__ CUtensorMap map_sfa, const __grid_constant__ CUtensorMap map_sfb,
@@ -551,6 +573,13 @@ gemm_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_constant__ C
         mbar_init(smem_u32(&sh.tmem_full), 1);
         mbar_init(smem_u32(&sh.tmem_empty), kPair);
         mbar_init(smem_u32(&sh.epi_drained), kEpiWarps);
+        if constexpr (kF32) {
+            for (int b = 0; b < 2; ++b) {
+                mbar_init(smem_u32(&sh.scr_full[b]), 1);
+                mbar_init(smem_u32(&sh.scr_empty[b]), (kEpiWarps / 2) * kPair);
+            }
+            for (int s = 0; s < kSfRing; ++s) mbar_init(smem_u32(&sh.sf_done[s]), kEpiWarps);
+        }
         sh.abort = 0;
         sh.grouped_tiles = 0;
         fence_mbarrier_init();
@@ -610,7 +639,43 @@ gemm_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_constant__ C
         }
     } else if (warp == 1) {
         // ------------------------------------------------ MMA issuer (one lane of the MMA CTA)
-        if (lane == 0 && rank == 0) {
+        if (lane == 0 && rank == 0 && kF32) {
+            // Every K-step: for each half hb, 4 MMAs (N = 128, K = 32 each)
+            // into product buffer hb, once the epilogue warps of that half
+            // (both CTAs) read its previous product.
+            uint32_t stage = 0, phase = 0, kg = 0;
+            bool ok = true;
+            for (int64_t t = unit; t < total && ok; t += units) {
+                for (int32_t k = 0; k < p.k_iters && ok; ++k, ++kg) {
+                    if (!wait_or_abort(smem_u32(&sh.full[stage]), phase, sh, p.status)) { ok = false; break; }
+                    uint8_t* st = smem + stage * C::kStageBytes;
+                    const uint64_t a_desc = smem_desc(smem_u32(st), 16, 1024, 2);
+#pragma unroll
+                    for (int hb = 0; hb < 2; ++hb) {
+                        if (kg >= 1 && !wait_or_abort(smem_u32(&sh.scr_empty[hb]), (kg - 1) & 1u, sh, p.status)) {
+                            ok = false;
+                            break;
+                        }
+                        tc_fence_after();
+                        const uint64_t b_desc = smem_desc(smem_u32(st + C::kABytes + hb * C::kBHalfBytes), 16, 1024, 2);
+                        const uint32_t d = tmem + 256u + 128u * uint32_t(hb);
+#pragma unroll
+                        for (int kk = 0; kk < 4; ++kk) {
+                            if constexpr (kPair == 2)
+                                mma_f8_pair(d, a_desc + 2 * kk, b_desc + 2 * kk, C::kIdescF32, kk != 0 ? 1u : 0u);
+                            else
+                                mma_f8(d, a_desc + 2 * kk, b_desc + 2 * kk, C::kIdescF32, kk != 0 ? 1u : 0u);
+                        }
+                        if constexpr (kPair == 2) tc_commit_pair_mc(smem_u32(&sh.scr_full[hb]), 0x3);
+                        else tc_commit(smem_u32(&sh.scr_full[hb]));
+                    }
+                    if (!ok) break;
+                    if constexpr (kPair == 2) tc_commit_pair_mc(smem_u32(&sh.empty[stage]), 0x3);
+                    else tc_commit(smem_u32(&sh.empty[stage]));
+                    if (++stage == C::kStages) { stage = 0; phase ^= 1u; }
+                }
+            }
+        } else if (lane == 0 && rank == 0) {
             uint32_t stage = 0, phase = 0, grp = 0;   // grp: global index of the current scale group
             int32_t local = 0, hint = 0;
             bool ok = true;
@@ -688,8 +753,11 @@ gemm_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_constant__ C
         auto load_next = [&]() -> bool {  // lane 0
             if (lt >= total) return true;
             const uint32_t slot = jl % kSfRing;
+            // reuse a slot once its previous group is consumed: copied into
+            // TMEM (MX), or read by this CTA's epilogue warps (FP32 scales)
             if (jl >= kSfRing &&
-                !wait_or_abort(smem_u32(&sh.sf_ready[slot]), ((jl / kSfRing) - 1) & 1u, sh, p.status))
+                !wait_or_abort(smem_u32(kF32 ? &sh.sf_done[slot] : &sh.sf_ready[slot]), ((jl / kSfRing) - 1) & 1u,
+                               sh, p.status))
                 return false;
             const uint32_t bar = smem_u32(&sh.sf_full[slot]);
             const uint32_t dst = smem_u32(ring + slot * kSfGroupBytes);
@@ -716,6 +784,32 @@ gemm_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_constant__ C
                 const uint32_t slot = j % kSfRing, bit = (j / kSfRing) & 1u;
                 if (!wait_or_abort(smem_u32(&sh.sf_full[slot]), bit, sh, p.status)) { ok = false; break; }
                 const uint32_t sf = smem_u32(ring + slot * kSfGroupBytes);
+                if constexpr (kF32) {
+                    // B's scales [256 columns][4 K-steps] -> [4 K-steps][256 columns] (fp32), so
+                    // that the epilogue reads 4 consecutive columns' scales at once; A's stay
+                    // [128 rows][4 K-steps].  The whole warp reads before anyone writes.
+                    uint4 v[8];
+#pragma unroll
+                    for (int i = 0; i < 8; ++i) v[i] = lds128(sf + kSFABytes + (8 * lane + i) * 16);
+                    __syncwarp();
+                    const uint32_t w = sf + kSFABytes + 32 * lane;
+                    sts128(w, v[0].x, v[1].x, v[2].x, v[3].x);
+                    sts128(w + 16, v[4].x, v[5].x, v[6].x, v[7].x);
+                    sts128(w + 1024, v[0].y, v[1].y, v[2].y, v[3].y);
+                    sts128(w + 1040, v[4].y, v[5].y, v[6].y, v[7].y);
+                    sts128(w + 2048, v[0].z, v[1].z, v[2].z, v[3].z);
+                    sts128(w + 2064, v[4].z, v[5].z, v[6].z, v[7].z);
+                    sts128(w + 3072, v[0].w, v[1].w, v[2].w, v[3].w);
+                    sts128(w + 3088, v[4].w, v[5].w, v[6].w, v[7].w);
+                    fence_proxy_async_smem();            // the slot is next written by TMA
+                    __syncwarp();
+                    if (lane == 0) {
+                        mbar_arrive(smem_u32(&sh.sf_ready[slot]));
+                        ok = load_next();
+                    }
+                    ok = __shfl_sync(0xFFFFFFFFu, ok, 0);
+                    continue;
+                }
                 sf_to_tmem_layout(sf, lane);
                 fence_proxy_async_smem();
                 __syncwarp();
@@ -759,11 +853,82 @@ gemm_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_constant__ C
         // ------------------------------------------------ epilogue (every CTA)
         const int e = warp - 2, q = warp & 3, h = e >> 2;
         int32_t hint = 0, local = 0;
+        uint32_t kg = 0, jg = 0;                 // FP32 scales: K-steps and scale groups consumed
         for (int64_t t = unit; t < total; t += units, ++local) {
             const Tile tl = map_tile<C::kTileM, kWgrad>(p, sh, t, hint);
-            if (!wait_or_abort(smem_u32(&sh.tmem_full), uint32_t(local) & 1u, sh, p.status)) break;
-            tc_fence_after();
             uint32_t acc0[64], acc1[64];
+            if constexpr (kF32) {
+                // acc (TMEM columns 128 h ..) += product half h * sA[row][kb] * sB[col][kb], one
+                // K-step (128) per scale block; then the accumulator comes back as usual
+                uint32_t slot = 0;
+                bool ok = true;
+                const uint32_t lanes = uint32_t(32 * q) << 16;
+                for (int32_t k = 0; k < tl.nk; ++k, ++kg) {
+                    if ((k & 3) == 0) {
+                        slot = jg % kSfRing;
+                        // (the lanes decide together: warp-collective tcgen05 operations follow)
+                        if (!__all_sync(0xFFFFFFFFu, wait_or_abort(smem_u32(&sh.sf_ready[slot]), (jg / kSfRing) & 1u,
+                                                                   sh, p.status))) {
+                            ok = false;
+                            break;
+                        }
+                    }
+                    if (!__all_sync(0xFFFFFFFFu, wait_or_abort(smem_u32(&sh.scr_full[h]), kg & 1u, sh, p.status))) {
+                        ok = false;
+                        break;
+                    }
+                    tc_fence_after();
+                    const uint32_t sf = smem_u32(smem + C::kStages * C::kStageBytes + slot * kSfGroupBytes);
+                    const float sa = __uint_as_float(lds32(sf + (32 * q + lane) * 16 + (k & 3) * 4));
+                    const uint32_t sbt = sf + kSFABytes + (k & 3) * 1024;          // B scales [kb][256 columns]
+#pragma unroll 1
+                    for (int c = 0; c < 4; ++c) {                                   // one chunk in registers at a time
+                        const int col0 = f32_half_col<kPair>(h, 32 * c);            // 32 consecutive columns
+                        uint32_t v[32], a[32];
+                        tmem_ld_32x32b_x32(tmem + lanes + 256u + 128u * uint32_t(h) + uint32_t(32 * c), v);
+                        if (k > 0) tmem_ld_32x32b_x32(tmem + lanes + uint32_t(128 * h + 32 * c), a);
+                        tmem_ld_wait();
+                        if (p.b_2d) {
+                            const float f = sa * __uint_as_float(lds32(sbt + (col0 & ~127) * 4));
+#pragma unroll
+                            for (int j = 0; j < 32; ++j)
+                                a[j] = __float_as_uint(__fmaf_rn(__uint_as_float(v[j]), f,
+                                                                 k > 0 ? __uint_as_float(a[j]) : 0.0f));
+                        } else {
+#pragma unroll
+                            for (int j4 = 0; j4 < 8; ++j4) {
+                                const uint4 w = lds128(sbt + (col0 + 4 * j4) * 4);
+                                const float sbj[4] = {__uint_as_float(w.x), __uint_as_float(w.y), __uint_as_float(w.z),
+                                                      __uint_as_float(w.w)};
+#pragma unroll
+                                for (int i = 0; i < 4; ++i) {
+                                    const int j = 4 * j4 + i;
+                                    a[j] = __float_as_uint(__fmaf_rn(__fmul_rn(__uint_as_float(v[j]), sbj[i]), sa,
+                                                                     k > 0 ? __uint_as_float(a[j]) : 0.0f));
+                                }
+                            }
+                        }
+                        tmem_st_32x32b_x32(tmem + lanes + uint32_t(128 * h + 32 * c), a);
+                    }
+                    tmem_st_wait();
+                    tc_fence_before();
+                    __syncwarp();
+                    const bool last_of_group = (k & 3) == 3 || k == tl.nk - 1;
+                    if (lane == 0) {
+                        if constexpr (kPair == 2) mbar_arrive_cluster_relaxed(leader(sh.scr_empty[h]));
+                        else mbar_arrive(smem_u32(&sh.scr_empty[h]));
+                        if (last_of_group) mbar_arrive(smem_u32(&sh.sf_done[slot]));
+                    }
+                    if (last_of_group) ++jg;
+                }
+                if (!ok) break;
+                tc_fence_after();
+                tmem_ld_32x32b_x64(tmem + lanes + uint32_t(128 * h), acc0);     // acc1: after acc0 is stored
+                tmem_ld_wait();
+            } else {
+            if (!__all_sync(0xFFFFFFFFu, wait_or_abort(smem_u32(&sh.tmem_full), uint32_t(local) & 1u, sh, p.status)))
+                break;                           // (all lanes together: tcgen05.ld is warp-collective)
+            tc_fence_after();
             if (!kWgrad || tl.nk > 0) {
                 const uint32_t taddr = tmem + (uint32_t(32 * q) << 16) + uint32_t(128 * h);
                 tmem_ld_32x32b_x64(taddr, acc0);
@@ -785,34 +950,52 @@ gemm_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_constant__ C
                     else mbar_arrive(smem_u32(&sh.tmem_empty));
                 }
             }
+            }
             const int64_t row = int64_t(tl.d_row) + int64_t(rank) * kBM + 32 * q + lane;
             if constexpr (C::kStagedStores) {
                 const int64_t row0 = row - lane;
                 if (row0 < tl.row_end) {             // warp-uniform: some row of this warp is stored
                     const uint16_t* bias = p.has_bias ? p.bias + int64_t(tl.group) * p.N : nullptr;
-                    const int32_t nb = tl.n0 + 128 * h;
+                    // output columns of acc0 / acc1 (FP32 scales: the product halves' column order)
+                    const int32_t nb0 = tl.n0 + (kF32 ? f32_half_col<kPair>(h, 0) : 128 * h);
+                    const int32_t nb1 = tl.n0 + (kF32 ? f32_half_col<kPair>(h, 64) : 128 * h + 64);
                     const uint32_t stage = smem_u32(smem + C::kStages * C::kStageBytes + kSfRing * kSfGroupBytes) +
                                            uint32_t(e) * 4096u;
-                    if (nb < p.N) store_64_staged<kAcc>(acc0, p, bias, row0, tl.row_end, nb, stage, lane);
-                    if (nb + 64 < p.N) store_64_staged<kAcc>(acc1, p, bias, row0, tl.row_end, nb + 64, stage, lane);
+                    if (nb0 < p.N) store_64_staged<kAcc>(acc0, p, bias, row0, tl.row_end, nb0, stage, lane);
+                    if constexpr (kF32) {
+                        tmem_ld_32x32b_x64(tmem + (uint32_t(32 * q) << 16) + uint32_t(128 * h + 64), acc1);
+                        tmem_ld_wait();
+                    }
+                    if (nb1 < p.N) store_64_staged<kAcc>(acc1, p, bias, row0, tl.row_end, nb1, stage, lane);
                 }
-            } else if (row < tl.row_end) {
+            } else {
+                // (tcgen05.ld is warp-collective: the lanes' row test guards the stores only)
+                const bool live = row < tl.row_end;
                 const uint16_t* bias = p.has_bias ? p.bias + int64_t(tl.group) * p.N : nullptr;
-                const int32_t nb = tl.n0 + 128 * h;
+                const int32_t nb = tl.n0 + 128 * h;    // single CTA: the halves' columns are in order
                 // The next tile's operands stream in while these stores go out;
                 // a burst of D/AUX stores at the start of that tile slows its
                 // loads, so the 8 chunks are spread over about half of the
                 // tile's mainloop (~700 cycles per K-step).
                 const uint32_t gap_ns = uint32_t(tl.nk) * 20u;
+                if (live) {
 #pragma unroll
-                for (int j = 0; j < 4; ++j) {
-                    if (nb + 16 * j < p.N) store_chunk<kAcc>(acc0 + 16 * j, p, bias, row, nb + 16 * j);
-                    __nanosleep(gap_ns);
+                    for (int j = 0; j < 4; ++j) {
+                        if (nb + 16 * j < p.N) store_chunk<kAcc>(acc0 + 16 * j, p, bias, row, nb + 16 * j);
+                        __nanosleep(gap_ns);
+                    }
                 }
+                if constexpr (kF32) {
+                    __syncwarp();
+                    tmem_ld_32x32b_x64(tmem + (uint32_t(32 * q) << 16) + uint32_t(128 * h + 64), acc1);
+                    tmem_ld_wait();
+                }
+                if (live) {
 #pragma unroll
-                for (int j = 0; j < 4; ++j) {
-                    if (nb + 64 + 16 * j < p.N) store_chunk<kAcc>(acc1 + 16 * j, p, bias, row, nb + 64 + 16 * j);
-                    if (j < 3) __nanosleep(gap_ns);
+                    for (int j = 0; j < 4; ++j) {
+                        if (nb + 64 + 16 * j < p.N) store_chunk<kAcc>(acc1 + 16 * j, p, bias, row, nb + 64 + 16 * j);
+                        if (j < 3) __nanosleep(gap_ns);
+                    }
                 }
             }
         }
@@ -827,7 +1010,7 @@ gemm_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_constant__ C
     }
 }
 
-template <int kPair, bool kAcc, bool kWgrad>
+template <int kPair, bool kAcc, bool kWgrad, bool kF32 = false>
 te_mx_status launch_gemm(const GemmArgs& a, int sms, unsigned int* status, cudaStream_t stream) {
     using C = Cfg<kPair>;
     const bool grouped = a.groups > 0;
@@ -836,8 +1019,12 @@ te_mx_status launch_gemm(const GemmArgs& a, int sms, unsigned int* status, cudaS
     // dense and grouped GEMMs, the token capacity of the padded layout for wgrad.
     const uint64_t kext = wg ? uint64_t(a.ld_code) : uint64_t(a.K);
     const uint64_t b_rows = (grouped && !wg) ? uint64_t(a.groups) * uint64_t(a.N) : uint64_t(a.N);
-    const uint64_t sf_cols = uint64_t(a.K / 32) < 16 ? 16 : uint64_t(a.K / 32);
+    // scale rows in bytes: E8M0, one per 32 K; FP32 scales, 4 bytes per 128 K
+    const uint64_t sf_bytes = kF32 ? uint64_t(a.K / 128) * 4 : uint64_t(a.K / 32);
+    const uint64_t sf_cols = sf_bytes < 16 ? 16 : sf_bytes;
     const uint64_t sfa_cols = wg ? uint64_t(a.ld_sA) : sf_cols, sfb_cols = wg ? uint64_t(a.ld_sB) : sf_cols;
+    const uint64_t sfa_pitch = kF32 ? uint64_t(a.ld_sA) * 4 : uint64_t(a.ld_sA);
+    const uint64_t sfb_pitch = kF32 ? uint64_t(a.ld_sB) * 4 : uint64_t(a.ld_sB);
     CUtensorMap ma, mb, msa, msb;
     te_mx_status st;
     if ((st = encode_tensor_map_2d(&ma, CU_TENSOR_MAP_DATA_TYPE_UINT8, a.A, kext, uint64_t(a.M),
@@ -845,9 +1032,9 @@ te_mx_status launch_gemm(const GemmArgs& a, int sms, unsigned int* status, cudaS
     if ((st = encode_tensor_map_2d(&mb, CU_TENSOR_MAP_DATA_TYPE_UINT8, a.B, kext, b_rows,
                                    kext, kBK, C::kBRows, CU_TENSOR_MAP_SWIZZLE_128B)) != TE_MX_OK) return st;
     if ((st = encode_tensor_map_2d(&msa, CU_TENSOR_MAP_DATA_TYPE_UINT8, a.sA, sfa_cols, uint64_t(a.M),
-                                   uint64_t(a.ld_sA), 16, kBM, CU_TENSOR_MAP_SWIZZLE_NONE)) != TE_MX_OK) return st;
+                                   sfa_pitch, 16, kBM, CU_TENSOR_MAP_SWIZZLE_NONE)) != TE_MX_OK) return st;
     if ((st = encode_tensor_map_2d(&msb, CU_TENSOR_MAP_DATA_TYPE_UINT8, a.sB, sfb_cols, b_rows,
-                                   uint64_t(a.ld_sB), 16, kBN, CU_TENSOR_MAP_SWIZZLE_NONE)) != TE_MX_OK) return st;
+                                   sfb_pitch, 16, kBN, CU_TENSOR_MAP_SWIZZLE_NONE)) != TE_MX_OK) return st;
 
     GemmParams p{};
     p.M = a.M;
@@ -870,12 +1057,13 @@ te_mx_status launch_gemm(const GemmArgs& a, int sms, unsigned int* status, cudaS
     p.ld_code = a.ld_code;
     p.ld_sfa = a.ld_sA;
     p.ld_sfb = a.ld_sB;
+    p.b_2d = a.b_2d;
     p.status = status;
 
     const int64_t slots = sms / kPair;                     // CTAs (pairs) resident at once
     int64_t units = grouped ? slots : (p.total_tiles < slots ? p.total_tiles : slots);
     if (units < 1) units = 1;
-    auto kern = gemm_kernel<kPair, kAcc, kWgrad>;
+    auto kern = gemm_kernel<kPair, kAcc, kWgrad, kF32>;
     cudaError_t e = set_smem_attribute_once(reinterpret_cast<const void*>(kern), C::kSmemDyn);
     if (e != cudaSuccess) return cuda_status(e, "cudaFuncSetAttribute(gemm)");
     cudaLaunchConfig_t cfg = {};
@@ -922,6 +1110,8 @@ te_mx_status gemm_launch(const GemmArgs& a, cudaStream_t stream) {
     // CTAs for small problems (finer tiles, more of them).
     const int64_t pair_tiles = ((a.M + 255) / 256) * ((a.N + kBN - 1) / kBN);
     const bool pair = a.wgrad ? a.M >= 256 : (a.groups > 0 ? a.M >= 256 * 8 : pair_tiles >= sms / 2);
+    if (a.f32_scales) return pair ? launch_gemm<2, false, false, true>(a, sms, status, stream)
+                                  : launch_gemm<1, false, false, true>(a, sms, status, stream);
     if (a.wgrad) {
         if (a.acc_f32) return pair ? launch_gemm<2, true, true>(a, sms, status, stream)
                                    : launch_gemm<1, true, true>(a, sms, status, stream);

@@ -45,6 +45,11 @@ struct GemmArgs {
     bool wgrad;
     int64_t ld_code;         // code row pitch (token capacity)
     int64_t total_m;         // bound on the sum of the token counts
+    // Float8BlockScaling with FP32 scales (dense): sA [M x ld_sA] and sB
+    // [N x ld_sB] fp32, one scale per row and 128 K (pitches in elements);
+    // b_2d: sB constant over 128-row blocks (128x128 weight blocks).
+    bool f32_scales;
+    bool b_2d;
 };
 
 te_mx_status quantize_launch(const QuantizeArgs& a, cudaStream_t stream);

@@ -98,6 +98,17 @@ def test_host_validation_rejects_bad_arguments_before_any_launch(lib):
     with pytest.raises(binding.TemxError, match="UNSUPPORTED_SHAPE"):
         binding.te_mx_block_quantize_fp32(16, 128, 48, 48, 0, 16, 16, 4, 0, 0, 0, 0)    # cols % 32
     assert binding.te_mx_block_scale_pitch_fp32(7168) == 56 and binding.te_mx_block_scale_pitch_fp32(130) == 4
+    with pytest.raises(binding.TemxError, match="INVALID_ARG"):      # b_blocks_2d not 0/1
+        binding.te_mx_gemm_fp32_scales(16, 16, 4, 16, 16, 4, 2, 128, 128, 256, 0, 0, 16, 0, 0)
+    with pytest.raises(binding.TemxError, match="INVALID_ARG"):      # no accumulating epilogue
+        binding.te_mx_gemm_fp32_scales(16, 16, 4, 16, 16, 4, 1, 128, 128, 256, 0, 5, 16, 0, 0)
+    with pytest.raises(binding.TemxError, match="MISALIGNED"):       # scale pitch % 4
+        binding.te_mx_gemm_fp32_scales(16, 16, 2, 16, 16, 4, 1, 128, 128, 256, 0, 0, 16, 0, 0)
+    with pytest.raises(binding.TemxError, match="MISALIGNED"):       # scale pitch < K/128
+        binding.te_mx_gemm_fp32_scales(16, 16, 4, 16, 16, 4, 1, 128, 128, 1024, 0, 0, 16, 0, 0)
+    with pytest.raises(binding.TemxError, match="UNSUPPORTED_SHAPE"):   # K % 128
+        binding.te_mx_gemm_fp32_scales(16, 16, 4, 16, 16, 4, 1, 128, 128, 96, 0, 0, 16, 0, 0)
+    binding.te_mx_gemm_fp32_scales(16, 16, 4, 16, 16, 4, 1, 0, 128, 256, 0, 0, 16, 0, 0)   # M == 0: no-op
     # zero-sized problems are no-ops
     binding.te_mx_layernorm_quantize(16, 0, 64, 64, 16, 16, 1e-5, 16, 16, 16, 0, 0, 0, 0, 0, 0)
     binding.te_mx_block_quantize(0, 0, 128, 128, 1, 0, 0, 0, 0, 0, 0, 0)
