@@ -53,20 +53,24 @@ constexpr int kSfWarp = 10;
 constexpr int kGroupM = 16;              // m-tiles per raster band (L2 reuse of B)
 constexpr int kMaxGroups = 1024;
 constexpr int kSFABytes = kBM * 16;      // 128 rows x 16 scale bytes (4 K-steps)
-constexpr int kSFBBytes = kBN * 16;      // every CTA holds all 256 B rows' scales
-constexpr int kSfGroupBytes = kSFABytes + kSFBBytes;   // one scale group (4 K-steps)
+constexpr int kSfGroupBytes = kSFABytes + kBN * 16;   // one scale group slot (4 K-steps; B rows of a 256 tile)
 constexpr int kSfRing = 3;               // scale-group slots in shared memory
 constexpr int kSfAhead = 2;              // scale groups loaded ahead of the one being prepared
 constexpr int kSfTmemGroups = 4;         // scale groups resident in TMEM
 
-template <int kPair>
+// kF32 (Float8BlockScaling with FP32 scales): 128-column tiles, so that an
+// epilogue thread keeps its 64 accumulator columns in registers while the
+// K-step products are double-buffered in TMEM.
+template <int kPair, bool kF32 = false>
 struct Cfg {
     static constexpr int kTileM = kBM * kPair;            // rows of one (pair) tile
+    static constexpr int kBN = kF32 ? 128 : ::temx::kBN;  // tile columns
     static constexpr int kBRows = kBN / kPair;            // B rows loaded per CTA
     static constexpr int kABytes = kBM * kBK;             // 16 KB
-    static constexpr int kBBytes = kBRows * kBK;          // 32 KB or 16 KB
-    static constexpr int kStages = kPair == 2 ? 5 : 4;
+    static constexpr int kBBytes = kBRows * kBK;          // 32, 16 or 8 KB
+    static constexpr int kStages = kF32 ? (kPair == 2 ? 6 : 5) : (kPair == 2 ? 5 : 4);
     static constexpr int kStageBytes = kABytes + kBBytes;
+    static constexpr int kSFBBytes = kBN * 16;            // every CTA holds all of the tile's B rows' scales
     // CTA pairs stage the epilogue's bf16 rows in shared memory (4 KB per
     // epilogue warp) so that global stores are written as whole lines.
     static constexpr bool kStagedStores = kPair == 2;
@@ -77,21 +81,15 @@ struct Cfg {
     // M >> 4 at bit 24; scale-factor byte ids at bits 4..5 (B) and 29..30 (A).
     static constexpr uint32_t kIdescBase =
         (uint32_t(kBN >> 3) << 17) | (1u << 23) | (uint32_t(kTileM >> 4) << 24);
-    // FP32 scales: each K-step's product is computed as two N = 128 halves.
-    // Instruction descriptor, kind::f8f6f4 (no block scaling): fp32 D (bits
-    // 4..5 = 1), E4M3 A and B (formats 0), both K-major, N >> 3 at bit 17,
-    // M >> 4 at bit 24.  A half's B rows start kBHalfBytes into the B tile.
-    static constexpr uint32_t kIdescF32 = (1u << 4) | (uint32_t(128 >> 3) << 17) | (uint32_t(kTileM >> 4) << 24);
-    static constexpr int kBHalfBytes = (kBRows / 2) * kBK;
+    // Instruction descriptor, kind::f8f6f4 (no block scaling; FP32 scales):
+    // fp32 D (bits 4..5 = 1), E4M3 A and B (formats 0), both K-major, N >> 3
+    // at bit 17, M >> 4 at bit 24.
+    static constexpr uint32_t kIdescF32 = (1u << 4) | (uint32_t(kBN >> 3) << 17) | (uint32_t(kTileM >> 4) << 24);
 };
-// FP32 scales: output column of TMEM column j (0..127) of product half h.
-// A CTA pair's N = 128 MMA takes 64 B rows from each CTA, whose B tiles hold
-// output columns 0..127 and 128..255.
-template <int kPair>
-__device__ __forceinline__ int f32_half_col(int h, int j) {
-    return kPair == 2 ? (j < 64 ? 64 * h + j : 128 + 64 * h + (j - 64)) : 128 * h + j;
-}
-static_assert(Cfg<1>::kStageBytes % 1024 == 0 && Cfg<2>::kStageBytes % 1024 == 0, "stage alignment");
+static_assert(Cfg<1>::kStageBytes % 1024 == 0 && Cfg<2>::kStageBytes % 1024 == 0 &&
+              Cfg<1, true>::kStageBytes % 1024 == 0 && Cfg<2, true>::kStageBytes % 1024 == 0, "stage alignment");
+// (the static shared state, ~8.5 KB, comes on top of the dynamic part; 227 KB per CTA in all)
+static_assert(Cfg<2, true>::kSmemDyn <= 218 * 1024 && Cfg<1, true>::kSmemDyn <= 218 * 1024, "shared memory");
 
 __device__ __forceinline__ uint32_t idesc_sf(uint32_t base, uint32_t sf_id) {
     return base | (sf_id << 4) | (sf_id << 29);
@@ -169,7 +167,7 @@ struct __align__(16) SharedState {
 // column-bands in L2.  Grouped: group-major, then n-major over the group's
 // m-tiles.  Wgrad: group-major, every group the full M x N output over its
 // own K range.  `hint` carries the group found last time (tiles increase).
-template <int kTileM, bool kWgrad, typename SH>
+template <int kTileM, int kTileN, bool kWgrad, typename SH>
 __device__ __forceinline__ Tile map_tile(const GemmParams& p, const SH& sh, int64_t t, int32_t& hint) {
     Tile tl;
     tl.k0 = 0;
@@ -183,7 +181,7 @@ __device__ __forceinline__ Tile map_tile(const GemmParams& p, const SH& sh, int6
         tl.a_row = mt * kTileM;
         tl.d_row = int32_t(int64_t(g) * p.M + tl.a_row);
         tl.row_end = int32_t(int64_t(g) * p.M + imin64(p.M, int64_t(tl.a_row) + kTileM));
-        tl.n0 = nt * kBN;
+        tl.n0 = nt * kTileN;
         tl.b_row = tl.n0;
         tl.group = g;
         tl.k0 = sh.row_start[g];
@@ -200,7 +198,7 @@ __device__ __forceinline__ Tile map_tile(const GemmParams& p, const SH& sh, int6
         tl.a_row = mt * kTileM;
         tl.d_row = tl.a_row;
         tl.row_end = int32_t(imin64(p.M, int64_t(tl.a_row) + kTileM));
-        tl.n0 = nt * kBN;
+        tl.n0 = nt * kTileN;
         tl.b_row = tl.n0;
         tl.group = 0;
     } else {
@@ -214,7 +212,7 @@ __device__ __forceinline__ Tile map_tile(const GemmParams& p, const SH& sh, int6
         tl.a_row = sh.row_start[g] + mt * kTileM;
         tl.d_row = tl.a_row;
         tl.row_end = min(sh.row_start[g + 1], tl.a_row + kTileM);
-        tl.n0 = nt * kBN;
+        tl.n0 = nt * kTileN;
         tl.b_row = g * p.N + tl.n0;
         tl.group = g;
     }
@@ -545,7 +543,7 @@ __global__ void __launch_bounds__(kThreads, 1)   // 168 registers: 3 warps share
 gemm_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_constant__ CUtensorMap map_b,
             const __grid_constant__ CUtensorMap map_sfa, const __grid_constant__ CUtensorMap map_sfb,
             const GemmParams p) {
-    using C = Cfg<kPair>;
+    using C = Cfg<kPair, kF32>;
     using SH = SharedState<C::kStages>;
     extern __shared__ uint8_t smem_raw[];
     __shared__ SH sh;
@@ -576,7 +574,7 @@ gemm_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_constant__ C
         if constexpr (kF32) {
             for (int b = 0; b < 2; ++b) {
                 mbar_init(smem_u32(&sh.scr_full[b]), 1);
-                mbar_init(smem_u32(&sh.scr_empty[b]), (kEpiWarps / 2) * kPair);
+                mbar_init(smem_u32(&sh.scr_empty[b]), kEpiWarps * kPair);
             }
             for (int s = 0; s < kSfRing; ++s) mbar_init(smem_u32(&sh.sf_done[s]), kEpiWarps);
         }
@@ -615,7 +613,7 @@ gemm_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_constant__ C
             uint32_t stage = 0, phase = 0;
             bool ok = true;
             for (int64_t t = unit; t < total && ok; t += units) {
-                const Tile tl = map_tile<C::kTileM, kWgrad>(p, sh, t, hint);
+                const Tile tl = map_tile<C::kTileM, C::kBN, kWgrad>(p, sh, t, hint);
                 const int32_t a_row = tl.a_row + int32_t(rank) * kBM;
                 const int32_t b_row = tl.b_row + int32_t(rank) * C::kBRows;
                 for (int32_t k = 0; k < tl.nk; ++k) {
@@ -640,38 +638,38 @@ gemm_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_constant__ C
     } else if (warp == 1) {
         // ------------------------------------------------ MMA issuer (one lane of the MMA CTA)
         if (lane == 0 && rank == 0 && kF32) {
-            // Every K-step: for each half hb, 4 MMAs (N = 128, K = 32 each)
-            // into product buffer hb, once the epilogue warps of that half
-            // (both CTAs) read its previous product.
+            // Every K-step: 4 MMAs (N = 128, K = 32 each) into product buffer
+            // kg & 1, once the epilogue warps of both CTAs read that buffer's
+            // previous product (K-step kg - 2).
             uint32_t stage = 0, phase = 0, kg = 0;
             bool ok = true;
             for (int64_t t = unit; t < total && ok; t += units) {
-                for (int32_t k = 0; k < p.k_iters && ok; ++k, ++kg) {
+                for (int32_t k = 0; k < p.k_iters; ++k, ++kg) {
                     if (!wait_or_abort(smem_u32(&sh.full[stage]), phase, sh, p.status)) { ok = false; break; }
+                    const uint32_t b = kg & 1u;
+                    if (kg >= 2 && !wait_or_abort(smem_u32(&sh.scr_empty[b]), ((kg >> 1) - 1) & 1u, sh, p.status)) {
+                        ok = false;
+                        break;
+                    }
+                    tc_fence_after();
                     uint8_t* st = smem + stage * C::kStageBytes;
                     const uint64_t a_desc = smem_desc(smem_u32(st), 16, 1024, 2);
+                    const uint64_t b_desc = smem_desc(smem_u32(st + C::kABytes), 16, 1024, 2);
+                    const uint32_t d = tmem + uint32_t(C::kBN) * b;
 #pragma unroll
-                    for (int hb = 0; hb < 2; ++hb) {
-                        if (kg >= 1 && !wait_or_abort(smem_u32(&sh.scr_empty[hb]), (kg - 1) & 1u, sh, p.status)) {
-                            ok = false;
-                            break;
-                        }
-                        tc_fence_after();
-                        const uint64_t b_desc = smem_desc(smem_u32(st + C::kABytes + hb * C::kBHalfBytes), 16, 1024, 2);
-                        const uint32_t d = tmem + 256u + 128u * uint32_t(hb);
-#pragma unroll
-                        for (int kk = 0; kk < 4; ++kk) {
-                            if constexpr (kPair == 2)
-                                mma_f8_pair(d, a_desc + 2 * kk, b_desc + 2 * kk, C::kIdescF32, kk != 0 ? 1u : 0u);
-                            else
-                                mma_f8(d, a_desc + 2 * kk, b_desc + 2 * kk, C::kIdescF32, kk != 0 ? 1u : 0u);
-                        }
-                        if constexpr (kPair == 2) tc_commit_pair_mc(smem_u32(&sh.scr_full[hb]), 0x3);
-                        else tc_commit(smem_u32(&sh.scr_full[hb]));
+                    for (int kk = 0; kk < 4; ++kk) {
+                        if constexpr (kPair == 2)
+                            mma_f8_pair(d, a_desc + 2 * kk, b_desc + 2 * kk, C::kIdescF32, kk != 0 ? 1u : 0u);
+                        else
+                            mma_f8(d, a_desc + 2 * kk, b_desc + 2 * kk, C::kIdescF32, kk != 0 ? 1u : 0u);
                     }
-                    if (!ok) break;
-                    if constexpr (kPair == 2) tc_commit_pair_mc(smem_u32(&sh.empty[stage]), 0x3);
-                    else tc_commit(smem_u32(&sh.empty[stage]));
+                    if constexpr (kPair == 2) {
+                        tc_commit_pair_mc(smem_u32(&sh.empty[stage]), 0x3);
+                        tc_commit_pair_mc(smem_u32(&sh.scr_full[b]), 0x3);
+                    } else {
+                        tc_commit(smem_u32(&sh.empty[stage]));
+                        tc_commit(smem_u32(&sh.scr_full[b]));
+                    }
                     if (++stage == C::kStages) { stage = 0; phase ^= 1u; }
                 }
             }
@@ -682,7 +680,7 @@ gemm_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_constant__ C
             for (int64_t t = unit; t < total && ok; t += units, ++local) {
                 // K-steps of this tile (wgrad: the expert's own; 0 for an expert without tokens)
                 int32_t nk = p.k_iters;
-                if constexpr (kWgrad) nk = map_tile<C::kTileM, kWgrad>(p, sh, t, hint).nk;
+                if constexpr (kWgrad) nk = map_tile<C::kTileM, C::kBN, kWgrad>(p, sh, t, hint).nk;
                 if (local > 0) {
                     if (!wait_or_abort(smem_u32(&sh.tmem_empty), uint32_t(local - 1) & 1u, sh, p.status)) break;
                     tc_fence_after();
@@ -744,7 +742,7 @@ gemm_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_constant__ C
         Tile ltl{};
         auto seek = [&]() {               // the first tile from lt on that has scale groups
             for (; lt < total; lt += units) {
-                ltl = map_tile<C::kTileM, kWgrad>(p, sh, lt, lhint);
+                ltl = map_tile<C::kTileM, C::kBN, kWgrad>(p, sh, lt, lhint);
                 if (tile_groups(ltl) > 0) break;
             }
         };
@@ -761,7 +759,7 @@ gemm_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_constant__ C
                 return false;
             const uint32_t bar = smem_u32(&sh.sf_full[slot]);
             const uint32_t dst = smem_u32(ring + slot * kSfGroupBytes);
-            mbar_arrive_expect_tx(bar, kSfGroupBytes);
+            mbar_arrive_expect_tx(bar, kSFABytes + C::kSFBBytes);
             tma_load_2d(dst, &map_sfa, bar, ltl.sf0 + lg * 16, ltl.a_row + int32_t(rank) * kBM);
             tma_load_2d(dst + kSFABytes, &map_sfb, bar, ltl.sf0 + lg * 16, ltl.b_row);
             ++jl;
@@ -778,29 +776,26 @@ gemm_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_constant__ C
         uint32_t j = 0;
         int32_t chint = 0;
         for (int64_t t = unit; t < total && ok; t += units) {
-            const Tile ct = map_tile<C::kTileM, kWgrad>(p, sh, t, chint);
+            const Tile ct = map_tile<C::kTileM, C::kBN, kWgrad>(p, sh, t, chint);
             const int32_t ngroups = tile_groups(ct);
             for (int32_t g = 0; g < ngroups && ok; ++g, ++j) {
                 const uint32_t slot = j % kSfRing, bit = (j / kSfRing) & 1u;
                 if (!wait_or_abort(smem_u32(&sh.sf_full[slot]), bit, sh, p.status)) { ok = false; break; }
                 const uint32_t sf = smem_u32(ring + slot * kSfGroupBytes);
                 if constexpr (kF32) {
-                    // B's scales [256 columns][4 K-steps] -> [4 K-steps][256 columns] (fp32), so
+                    // B's scales [128 columns][4 K-steps] -> [4 K-steps][128 columns] (fp32), so
                     // that the epilogue reads 4 consecutive columns' scales at once; A's stay
                     // [128 rows][4 K-steps].  The whole warp reads before anyone writes.
-                    uint4 v[8];
+                    static_assert(C::kBN == 128, "one B row block of 128 columns per tile");
+                    uint4 v[4];
 #pragma unroll
-                    for (int i = 0; i < 8; ++i) v[i] = lds128(sf + kSFABytes + (8 * lane + i) * 16);
+                    for (int i = 0; i < 4; ++i) v[i] = lds128(sf + kSFABytes + (4 * lane + i) * 16);
                     __syncwarp();
-                    const uint32_t w = sf + kSFABytes + 32 * lane;
+                    const uint32_t w = sf + kSFABytes + 16 * lane;
                     sts128(w, v[0].x, v[1].x, v[2].x, v[3].x);
-                    sts128(w + 16, v[4].x, v[5].x, v[6].x, v[7].x);
-                    sts128(w + 1024, v[0].y, v[1].y, v[2].y, v[3].y);
-                    sts128(w + 1040, v[4].y, v[5].y, v[6].y, v[7].y);
-                    sts128(w + 2048, v[0].z, v[1].z, v[2].z, v[3].z);
-                    sts128(w + 2064, v[4].z, v[5].z, v[6].z, v[7].z);
-                    sts128(w + 3072, v[0].w, v[1].w, v[2].w, v[3].w);
-                    sts128(w + 3088, v[4].w, v[5].w, v[6].w, v[7].w);
+                    sts128(w + 512, v[0].y, v[1].y, v[2].y, v[3].y);
+                    sts128(w + 1024, v[0].z, v[1].z, v[2].z, v[3].z);
+                    sts128(w + 1536, v[0].w, v[1].w, v[2].w, v[3].w);
                     fence_proxy_async_smem();            // the slot is next written by TMA
                     __syncwarp();
                     if (lane == 0) {
@@ -855,11 +850,13 @@ gemm_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_constant__ C
         int32_t hint = 0, local = 0;
         uint32_t kg = 0, jg = 0;                 // FP32 scales: K-steps and scale groups consumed
         for (int64_t t = unit; t < total; t += units, ++local) {
-            const Tile tl = map_tile<C::kTileM, kWgrad>(p, sh, t, hint);
+            const Tile tl = map_tile<C::kTileM, C::kBN, kWgrad>(p, sh, t, hint);
             uint32_t acc0[64], acc1[64];
             if constexpr (kF32) {
-                // acc (TMEM columns 128 h ..) += product half h * sA[row][kb] * sB[col][kb], one
-                // K-step (128) per scale block; then the accumulator comes back as usual
+                // acc (registers: my 32 rows x 64 columns 64 h ..) += product(K-step) *
+                // sA[row][kb] * sB[col][kb], one K-step (128) per scale block
+#pragma unroll
+                for (int i = 0; i < 64; ++i) acc0[i] = 0u;
                 uint32_t slot = 0;
                 bool ok = true;
                 const uint32_t lanes = uint32_t(32 * q) << 16;
@@ -873,58 +870,49 @@ gemm_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_constant__ C
                             break;
                         }
                     }
-                    if (!__all_sync(0xFFFFFFFFu, wait_or_abort(smem_u32(&sh.scr_full[h]), kg & 1u, sh, p.status))) {
+                    const uint32_t b = kg & 1u;
+                    if (!__all_sync(0xFFFFFFFFu, wait_or_abort(smem_u32(&sh.scr_full[b]), (kg >> 1) & 1u, sh, p.status))) {
                         ok = false;
                         break;
                     }
                     tc_fence_after();
+                    uint32_t v[64];
+                    tmem_ld_32x32b_x64(tmem + lanes + uint32_t(C::kBN) * b + uint32_t(64 * h), v);
                     const uint32_t sf = smem_u32(smem + C::kStages * C::kStageBytes + slot * kSfGroupBytes);
                     const float sa = __uint_as_float(lds32(sf + (32 * q + lane) * 16 + (k & 3) * 4));
-                    const uint32_t sbt = sf + kSFABytes + (k & 3) * 1024;          // B scales [kb][256 columns]
-#pragma unroll 1
-                    for (int c = 0; c < 4; ++c) {                                   // one chunk in registers at a time
-                        const int col0 = f32_half_col<kPair>(h, 32 * c);            // 32 consecutive columns
-                        uint32_t v[32], a[32];
-                        tmem_ld_32x32b_x32(tmem + lanes + 256u + 128u * uint32_t(h) + uint32_t(32 * c), v);
-                        if (k > 0) tmem_ld_32x32b_x32(tmem + lanes + uint32_t(128 * h + 32 * c), a);
-                        tmem_ld_wait();
-                        if (p.b_2d) {
-                            const float f = sa * __uint_as_float(lds32(sbt + (col0 & ~127) * 4));
-#pragma unroll
-                            for (int j = 0; j < 32; ++j)
-                                a[j] = __float_as_uint(__fmaf_rn(__uint_as_float(v[j]), f,
-                                                                 k > 0 ? __uint_as_float(a[j]) : 0.0f));
-                        } else {
-#pragma unroll
-                            for (int j4 = 0; j4 < 8; ++j4) {
-                                const uint4 w = lds128(sbt + (col0 + 4 * j4) * 4);
-                                const float sbj[4] = {__uint_as_float(w.x), __uint_as_float(w.y), __uint_as_float(w.z),
-                                                      __uint_as_float(w.w)};
-#pragma unroll
-                                for (int i = 0; i < 4; ++i) {
-                                    const int j = 4 * j4 + i;
-                                    a[j] = __float_as_uint(__fmaf_rn(__fmul_rn(__uint_as_float(v[j]), sbj[i]), sa,
-                                                                     k > 0 ? __uint_as_float(a[j]) : 0.0f));
-                                }
-                            }
-                        }
-                        tmem_st_32x32b_x32(tmem + lanes + uint32_t(128 * h + 32 * c), a);
-                    }
-                    tmem_st_wait();
+                    const uint32_t sbt = sf + kSFABytes + (k & 3) * 512 + 256 * h;   // B scales of my 64 columns
+                    tmem_ld_wait();
                     tc_fence_before();
                     __syncwarp();
                     const bool last_of_group = (k & 3) == 3 || k == tl.nk - 1;
-                    if (lane == 0) {
-                        if constexpr (kPair == 2) mbar_arrive_cluster_relaxed(leader(sh.scr_empty[h]));
-                        else mbar_arrive(smem_u32(&sh.scr_empty[h]));
-                        if (last_of_group) mbar_arrive(smem_u32(&sh.sf_done[slot]));
+                    if (lane == 0) {                      // the product is in registers: release its buffer
+                        if constexpr (kPair == 2) mbar_arrive_cluster_relaxed(leader(sh.scr_empty[b]));
+                        else mbar_arrive(smem_u32(&sh.scr_empty[b]));
                     }
+                    if (p.b_2d) {
+                        const float f = sa * __uint_as_float(lds32(sbt - 256 * h));   // the tile is one 128-column block
+#pragma unroll
+                        for (int j = 0; j < 64; ++j)
+                            acc0[j] = __float_as_uint(__fmaf_rn(__uint_as_float(v[j]), f, __uint_as_float(acc0[j])));
+                    } else {
+#pragma unroll
+                        for (int j4 = 0; j4 < 16; ++j4) {
+                            const uint4 w = lds128(sbt + 16 * j4);
+                            const float sbj[4] = {__uint_as_float(w.x), __uint_as_float(w.y), __uint_as_float(w.z),
+                                                  __uint_as_float(w.w)};
+#pragma unroll
+                            for (int i = 0; i < 4; ++i) {
+                                const int j = 4 * j4 + i;
+                                acc0[j] = __float_as_uint(__fmaf_rn(__fmul_rn(__uint_as_float(v[j]), sbj[i]), sa,
+                                                                    __uint_as_float(acc0[j])));
+                            }
+                        }
+                    }
+                    __syncwarp();
+                    if (lane == 0 && last_of_group) mbar_arrive(smem_u32(&sh.sf_done[slot]));   // scales read
                     if (last_of_group) ++jg;
                 }
                 if (!ok) break;
-                tc_fence_after();
-                tmem_ld_32x32b_x64(tmem + lanes + uint32_t(128 * h), acc0);     // acc1: after acc0 is stored
-                tmem_ld_wait();
             } else {
             if (!__all_sync(0xFFFFFFFFu, wait_or_abort(smem_u32(&sh.tmem_full), uint32_t(local) & 1u, sh, p.status)))
                 break;                           // (all lanes together: tcgen05.ld is warp-collective)
@@ -956,23 +944,18 @@ gemm_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_constant__ C
                 const int64_t row0 = row - lane;
                 if (row0 < tl.row_end) {             // warp-uniform: some row of this warp is stored
                     const uint16_t* bias = p.has_bias ? p.bias + int64_t(tl.group) * p.N : nullptr;
-                    // output columns of acc0 / acc1 (FP32 scales: the product halves' column order)
-                    const int32_t nb0 = tl.n0 + (kF32 ? f32_half_col<kPair>(h, 0) : 128 * h);
-                    const int32_t nb1 = tl.n0 + (kF32 ? f32_half_col<kPair>(h, 64) : 128 * h + 64);
+                    // output columns of acc0 / acc1 (FP32 scales: 64 columns per warp, acc0 only)
+                    const int32_t nb0 = tl.n0 + (kF32 ? 64 * h : 128 * h);
                     const uint32_t stage = smem_u32(smem + C::kStages * C::kStageBytes + kSfRing * kSfGroupBytes) +
                                            uint32_t(e) * 4096u;
                     if (nb0 < p.N) store_64_staged<kAcc>(acc0, p, bias, row0, tl.row_end, nb0, stage, lane);
-                    if constexpr (kF32) {
-                        tmem_ld_32x32b_x64(tmem + (uint32_t(32 * q) << 16) + uint32_t(128 * h + 64), acc1);
-                        tmem_ld_wait();
-                    }
-                    if (nb1 < p.N) store_64_staged<kAcc>(acc1, p, bias, row0, tl.row_end, nb1, stage, lane);
+                    if (!kF32 && nb0 + 64 < p.N) store_64_staged<kAcc>(acc1, p, bias, row0, tl.row_end, nb0 + 64, stage, lane);
                 }
             } else {
                 // (tcgen05.ld is warp-collective: the lanes' row test guards the stores only)
                 const bool live = row < tl.row_end;
                 const uint16_t* bias = p.has_bias ? p.bias + int64_t(tl.group) * p.N : nullptr;
-                const int32_t nb = tl.n0 + 128 * h;    // single CTA: the halves' columns are in order
+                const int32_t nb = tl.n0 + (kF32 ? 64 * h : 128 * h);
                 // The next tile's operands stream in while these stores go out;
                 // a burst of D/AUX stores at the start of that tile slows its
                 // loads, so the 8 chunks are spread over about half of the
@@ -985,12 +968,7 @@ gemm_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_constant__ C
                         __nanosleep(gap_ns);
                     }
                 }
-                if constexpr (kF32) {
-                    __syncwarp();
-                    tmem_ld_32x32b_x64(tmem + (uint32_t(32 * q) << 16) + uint32_t(128 * h + 64), acc1);
-                    tmem_ld_wait();
-                }
-                if (live) {
+                if (live && !kF32) {
 #pragma unroll
                     for (int j = 0; j < 4; ++j) {
                         if (nb + 64 + 16 * j < p.N) store_chunk<kAcc>(acc1 + 16 * j, p, bias, row, nb + 64 + 16 * j);
@@ -1012,7 +990,7 @@ gemm_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_constant__ C
 
 template <int kPair, bool kAcc, bool kWgrad, bool kF32 = false>
 te_mx_status launch_gemm(const GemmArgs& a, int sms, unsigned int* status, cudaStream_t stream) {
-    using C = Cfg<kPair>;
+    using C = Cfg<kPair, kF32>;
     const bool grouped = a.groups > 0;
     const bool wg = a.wgrad;
     // Extent and pitch of the operands along the reduction axis: K for the
@@ -1034,14 +1012,14 @@ te_mx_status launch_gemm(const GemmArgs& a, int sms, unsigned int* status, cudaS
     if ((st = encode_tensor_map_2d(&msa, CU_TENSOR_MAP_DATA_TYPE_UINT8, a.sA, sfa_cols, uint64_t(a.M),
                                    sfa_pitch, 16, kBM, CU_TENSOR_MAP_SWIZZLE_NONE)) != TE_MX_OK) return st;
     if ((st = encode_tensor_map_2d(&msb, CU_TENSOR_MAP_DATA_TYPE_UINT8, a.sB, sfb_cols, b_rows,
-                                   sfb_pitch, 16, kBN, CU_TENSOR_MAP_SWIZZLE_NONE)) != TE_MX_OK) return st;
+                                   sfb_pitch, 16, C::kBN, CU_TENSOR_MAP_SWIZZLE_NONE)) != TE_MX_OK) return st;
 
     GemmParams p{};
     p.M = a.M;
     p.N = int32_t(a.N);
     p.K = int32_t(a.K);
     p.k_iters = wg ? 0 : int32_t(a.K / kBK);
-    p.n_tiles = int32_t((a.N + kBN - 1) / kBN);
+    p.n_tiles = int32_t((a.N + C::kBN - 1) / C::kBN);
     p.m_tiles = int32_t((a.M + C::kTileM - 1) / C::kTileM);
     p.total_tiles = grouped ? 0 : int64_t(p.m_tiles) * p.n_tiles;
     p.groups = a.groups;
