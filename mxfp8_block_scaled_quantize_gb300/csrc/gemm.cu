@@ -47,7 +47,8 @@ namespace {
 constexpr int kBM = 128;                 // accumulator rows per CTA (TMEM lanes)
 constexpr int kBN = 256;                 // tile columns (accumulator columns)
 constexpr int kBK = 128;                 // K per pipeline stage (bytes of E4M3)
-constexpr int kThreads = 352;
+constexpr int kThreads = 352;          // 11 warps; FP32 scales: 12 (a second MMA issuer)
+constexpr int kMma2Warp = 11;
 constexpr int kEpiWarps = 8;
 constexpr int kSfWarp = 10;
 constexpr int kGroupM = 16;              // m-tiles per raster band (L2 reuse of B)
@@ -539,7 +540,7 @@ __device__ __forceinline__ void store_64_staged(uint32_t* acc, const GemmParams&
 // operands with FP32 scales (dense only): every K-step's product lands in one
 // of two TMEM buffers and the epilogue warps accumulate it, scaled, in registers.
 template <int kPair, bool kAcc, bool kWgrad, bool kF32>
-__global__ void __launch_bounds__(kThreads, 1)   // 168 registers: 3 warps share a 16K-register sub-partition
+__global__ void __launch_bounds__(kF32 ? kThreads + 32 : kThreads, 1)   // 168 registers: 3 warps share a 16K-register sub-partition
 gemm_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_constant__ CUtensorMap map_b,
             const __grid_constant__ CUtensorMap map_sfa, const __grid_constant__ CUtensorMap map_sfb,
             const GemmParams p) {
@@ -606,6 +607,46 @@ gemm_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_constant__ C
     const uint32_t tmem = sh.tmem_base;
     const int64_t total = p.groups > 0 ? sh.grouped_tiles : p.total_tiles;
 
+    // FP32 scales: MMA issuer for the K-steps of one parity (product buffer
+    // `par`): 4 MMAs (N = 128, K = 32 each) per K-step, once the epilogue warps
+    // of both CTAs read that buffer's previous product (K-step kg - 2).  Two
+    // issuers (warps 1 and kMma2Warp) share the work: a tcgen05.mma costs its
+    // thread ~100+ cycles of issue.
+    auto mma_f32 = [&](uint32_t par) {
+        uint32_t kg = 0;
+        bool ok = true;
+        for (int64_t t = unit; t < total && ok; t += units) {
+            for (int32_t k = 0; k < p.k_iters; ++k, ++kg) {
+                if ((kg & 1u) != par) continue;
+                const uint32_t stage = kg % C::kStages, phase = (kg / C::kStages) & 1u;
+                if (!wait_or_abort(smem_u32(&sh.full[stage]), phase, sh, p.status)) { ok = false; break; }
+                if (kg >= 2 && !wait_or_abort(smem_u32(&sh.scr_empty[par]), ((kg >> 1) - 1) & 1u, sh, p.status)) {
+                    ok = false;
+                    break;
+                }
+                tc_fence_after();
+                uint8_t* st = smem + stage * C::kStageBytes;
+                const uint64_t a_desc = smem_desc(smem_u32(st), 16, 1024, 2);
+                const uint64_t b_desc = smem_desc(smem_u32(st + C::kABytes), 16, 1024, 2);
+                const uint32_t d = tmem + uint32_t(C::kBN) * par;
+#pragma unroll
+                for (int kk = 0; kk < 4; ++kk) {
+                    if constexpr (kPair == 2)
+                        mma_f8_pair(d, a_desc + 2 * kk, b_desc + 2 * kk, C::kIdescF32, kk != 0 ? 1u : 0u);
+                    else
+                        mma_f8(d, a_desc + 2 * kk, b_desc + 2 * kk, C::kIdescF32, kk != 0 ? 1u : 0u);
+                }
+                if constexpr (kPair == 2) {
+                    tc_commit_pair_mc(smem_u32(&sh.empty[stage]), 0x3);
+                    tc_commit_pair_mc(smem_u32(&sh.scr_full[par]), 0x3);
+                } else {
+                    tc_commit(smem_u32(&sh.empty[stage]));
+                    tc_commit(smem_u32(&sh.scr_full[par]));
+                }
+            }
+        }
+    };
+
     if (warp == 0) {
         // ------------------------------------------------ TMA producer (every CTA)
         if (lane == 0) {
@@ -638,41 +679,7 @@ gemm_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_constant__ C
     } else if (warp == 1) {
         // ------------------------------------------------ MMA issuer (one lane of the MMA CTA)
         if (lane == 0 && rank == 0 && kF32) {
-            // Every K-step: 4 MMAs (N = 128, K = 32 each) into product buffer
-            // kg & 1, once the epilogue warps of both CTAs read that buffer's
-            // previous product (K-step kg - 2).
-            uint32_t stage = 0, phase = 0, kg = 0;
-            bool ok = true;
-            for (int64_t t = unit; t < total && ok; t += units) {
-                for (int32_t k = 0; k < p.k_iters; ++k, ++kg) {
-                    if (!wait_or_abort(smem_u32(&sh.full[stage]), phase, sh, p.status)) { ok = false; break; }
-                    const uint32_t b = kg & 1u;
-                    if (kg >= 2 && !wait_or_abort(smem_u32(&sh.scr_empty[b]), ((kg >> 1) - 1) & 1u, sh, p.status)) {
-                        ok = false;
-                        break;
-                    }
-                    tc_fence_after();
-                    uint8_t* st = smem + stage * C::kStageBytes;
-                    const uint64_t a_desc = smem_desc(smem_u32(st), 16, 1024, 2);
-                    const uint64_t b_desc = smem_desc(smem_u32(st + C::kABytes), 16, 1024, 2);
-                    const uint32_t d = tmem + uint32_t(C::kBN) * b;
-#pragma unroll
-                    for (int kk = 0; kk < 4; ++kk) {
-                        if constexpr (kPair == 2)
-                            mma_f8_pair(d, a_desc + 2 * kk, b_desc + 2 * kk, C::kIdescF32, kk != 0 ? 1u : 0u);
-                        else
-                            mma_f8(d, a_desc + 2 * kk, b_desc + 2 * kk, C::kIdescF32, kk != 0 ? 1u : 0u);
-                    }
-                    if constexpr (kPair == 2) {
-                        tc_commit_pair_mc(smem_u32(&sh.empty[stage]), 0x3);
-                        tc_commit_pair_mc(smem_u32(&sh.scr_full[b]), 0x3);
-                    } else {
-                        tc_commit(smem_u32(&sh.empty[stage]));
-                        tc_commit(smem_u32(&sh.scr_full[b]));
-                    }
-                    if (++stage == C::kStages) { stage = 0; phase ^= 1u; }
-                }
-            }
+            mma_f32(0u);
         } else if (lane == 0 && rank == 0) {
             uint32_t stage = 0, phase = 0, grp = 0;   // grp: global index of the current scale group
             int32_t local = 0, hint = 0;
@@ -723,6 +730,8 @@ gemm_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_constant__ C
                 else tc_commit(smem_u32(&sh.tmem_full));
             }
         }
+    } else if (kF32 && warp == kMma2Warp) {
+        if (lane == 0 && rank == 0) mma_f32(1u);
     } else if (warp == kSfWarp) {
         // ------------------------------------------------ scale-factor layout (every CTA)
         // Scale groups (4 K-steps each, the last of a tile possibly shorter)
@@ -1046,7 +1055,7 @@ te_mx_status launch_gemm(const GemmArgs& a, int sms, unsigned int* status, cudaS
     if (e != cudaSuccess) return cuda_status(e, "cudaFuncSetAttribute(gemm)");
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(unsigned(units * kPair));
-    cfg.blockDim = dim3(kThreads);
+    cfg.blockDim = dim3(kF32 ? kThreads + 32 : kThreads);
     cfg.dynamicSmemBytes = C::kSmemDyn;
     cfg.stream = stream;
     cudaLaunchAttribute attr[1];
