@@ -900,9 +900,16 @@ gemm_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_constant__ C
                     }
                     if (p.b_2d) {
                         const float f = sa * __uint_as_float(lds32(sbt - 256 * h));   // the tile is one 128-column block
+                        // packed pairs: one f32x2 FMA per two columns (each half rounds as fmaf does)
 #pragma unroll
-                        for (int j = 0; j < 64; ++j)
-                            acc0[j] = __float_as_uint(__fmaf_rn(__uint_as_float(v[j]), f, __uint_as_float(acc0[j])));
+                        for (int j = 0; j < 64; j += 2) {
+                            uint64_t a2, v2, f2;
+                            asm("mov.b64 %0, {%1, %2};" : "=l"(a2) : "r"(acc0[j]), "r"(acc0[j + 1]));
+                            asm("mov.b64 %0, {%1, %2};" : "=l"(v2) : "r"(v[j]), "r"(v[j + 1]));
+                            asm("mov.b64 %0, {%1, %1};" : "=l"(f2) : "r"(__float_as_uint(f)));
+                            asm("fma.rn.f32x2 %0, %1, %2, %0;" : "+l"(a2) : "l"(v2), "l"(f2));
+                            asm("mov.b64 {%0, %1}, %2;" : "=r"(acc0[j]), "=r"(acc0[j + 1]) : "l"(a2));
+                        }
                     } else {
 #pragma unroll
                         for (int j4 = 0; j4 < 16; ++j4) {
