@@ -120,9 +120,10 @@ struct GemmParams {
     uint16_t* aux;
     bool has_bias, gelu, dgelu;          // dgelu: aux is an input (forward pre-activation)
     bool wgrad;                          // grouped wgrad: per-group K range, D = [groups x M x N]
+    bool b_2d;                           // FP32 scales: B's scales constant over 128-row blocks
+                                         // (next to the other flags: no other field moves)
     int64_t total_m;                     // wgrad: bound on the token counts' sum
     int64_t ld_code, ld_sfa, ld_sfb;     // wgrad: operand pitches (capacities)
-    bool b_2d;                           // FP32 scales: B's scales constant over 128-row blocks
     unsigned int* status;
 };
 
