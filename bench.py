@@ -47,7 +47,7 @@ def load_peaks():
         return {"hbm_gbs": 6800.0, "bf16": 1900.0, "bf16_sustained": 1700.0, "source": "fallback"}
 
 
-KERNEL_SOURCES = {"gemm": ["gemm.cu", "ptx.cuh"], "quant": ["quantize.cu", "e4m3.cuh", "ptx.cuh", "units.cuh"],
+KERNEL_SOURCES = {"gemm": ["gemm.cu", "ptx.cuh", "tcgen05.cuh"], "quant": ["quantize.cu", "e4m3.cuh", "ptx.cuh", "units.cuh"],
                   "grouped": ["grouped_quantize.cu", "e4m3.cuh", "ptx.cuh", "units.cuh"],
                   "block": ["block_quantize.cu", "e4m3.cuh", "ptx.cuh"],
                   "ln": ["layernorm_quantize.cu", "e4m3.cuh", "ptx.cuh", "units.cuh"]}

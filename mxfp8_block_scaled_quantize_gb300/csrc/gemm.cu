@@ -38,6 +38,7 @@
 #include <cuda_runtime.h>
 
 #include "ptx.cuh"
+#include "tcgen05.cuh"
 #include "temx_internal.h"
 
 namespace temx {
