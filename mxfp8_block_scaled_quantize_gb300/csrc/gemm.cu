@@ -55,10 +55,10 @@ constexpr int kSfWarp = 10;
 constexpr int kGroupM = 16;              // m-tiles per raster band (L2 reuse of B)
 constexpr int kMaxGroups = 1024;
 constexpr int kSFABytes = kBM * 16;      // 128 rows x 16 scale bytes (4 K-steps)
-constexpr int kSfGroupBytes = kSFABytes + kBN * 16;   // one scale group slot (4 K-steps; B rows of a 256 tile)
 constexpr int kSfRing = 3;               // scale-group slots in shared memory
 constexpr int kSfAhead = 2;              // scale groups loaded ahead of the one being prepared
 constexpr int kSfTmemGroups = 4;         // scale groups resident in TMEM
+constexpr int kScrBufs = 4;              // FP32 scales: K-step product buffers in TMEM (128 columns each)
 
 // kF32 (Float8BlockScaling with FP32 scales): 128-column tiles, so that an
 // epilogue thread keeps its 64 accumulator columns in registers while the
@@ -73,11 +73,12 @@ struct Cfg {
     static constexpr int kStages = kF32 ? (kPair == 2 ? 6 : 5) : (kPair == 2 ? 5 : 4);
     static constexpr int kStageBytes = kABytes + kBBytes;
     static constexpr int kSFBBytes = kBN * 16;            // every CTA holds all of the tile's B rows' scales
+    static constexpr int kSfSlotBytes = kSFABytes + kSFBBytes;   // one scale group (4 K-steps) in the ring
     // CTA pairs stage the epilogue's bf16 rows in shared memory (4 KB per
     // epilogue warp) so that global stores are written as whole lines.
     static constexpr bool kStagedStores = kPair == 2;
     static constexpr int kEpiStageBytes = kStagedStores ? kEpiWarps * 4096 : 0;
-    static constexpr int kSmemDyn = kStages * kStageBytes + kSfRing * kSfGroupBytes + kEpiStageBytes + 1024;
+    static constexpr int kSmemDyn = kStages * kStageBytes + kSfRing * kSfSlotBytes + kEpiStageBytes + 1024;
     // Instruction descriptor, kind::mxf8f6f4 with block scaling: E4M3 A and B
     // (format 0), both K-major, N >> 3 at bit 17, UE8M0 scales (bit 23),
     // M >> 4 at bit 24; scale-factor byte ids at bits 4..5 (B) and 29..30 (A).
@@ -91,7 +92,8 @@ struct Cfg {
 static_assert(Cfg<1>::kStageBytes % 1024 == 0 && Cfg<2>::kStageBytes % 1024 == 0 &&
               Cfg<1, true>::kStageBytes % 1024 == 0 && Cfg<2, true>::kStageBytes % 1024 == 0, "stage alignment");
 // (the static shared state, ~8.5 KB, comes on top of the dynamic part; 227 KB per CTA in all)
-static_assert(Cfg<2, true>::kSmemDyn <= 218 * 1024 && Cfg<1, true>::kSmemDyn <= 218 * 1024, "shared memory");
+static_assert(Cfg<2, true>::kSmemDyn <= 218 * 1024 && Cfg<1, true>::kSmemDyn <= 218 * 1024 &&
+              Cfg<2>::kSmemDyn <= 218 * 1024 && Cfg<1>::kSmemDyn <= 218 * 1024, "shared memory");
 
 __device__ __forceinline__ uint32_t idesc_sf(uint32_t base, uint32_t sf_id) {
     return base | (sf_id << 4) | (sf_id << 29);
@@ -106,6 +108,7 @@ constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kSfCol0 = 256;
 constexpr uint32_t kSfSlotCols = 12;
 constexpr uint32_t kSfSlots = 16;
+static_assert(kScrBufs * Cfg<2, true>::kBN <= int(kTmemCols), "FP32-scale product buffers fit in TMEM");
 
 struct GemmParams {
     int64_t M;               // dense: rows of A/D; grouped: total_m (rows of X/D)
@@ -153,10 +156,10 @@ struct __align__(16) SharedState {
     uint64_t tmem_full;
     uint64_t tmem_empty;                   // (MMA CTA) accumulator drained by the epilogue of every CTA
     uint64_t epi_drained;                  // this CTA's 8 epilogue warps hold their accumulator rows
-    // FP32-scale mode: the two halves of a K-step's product in TMEM (columns
-    // 256 and 384; the scaled accumulator is columns 0..255)
-    uint64_t scr_full[2];                  // a product half landed (each CTA)
-    uint64_t scr_empty[2];                 // (MMA CTA) the epilogue warps of that half (both CTAs) read it
+    // FP32-scale mode: K-step kg's product lands in TMEM buffer kg % kScrBufs
+    // (columns 128 * buffer ..; the scaled accumulator lives in registers)
+    uint64_t scr_full[kScrBufs];           // a product landed (each CTA)
+    uint64_t scr_empty[kScrBufs];          // (MMA CTA) the epilogue warps of both CTAs read that buffer
     uint64_t sf_done[kSfRing];             // this CTA's epilogue warps are done with a scale group
     uint32_t tmem_base;
     int32_t abort;
@@ -575,7 +578,7 @@ gemm_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_constant__ C
         mbar_init(smem_u32(&sh.tmem_empty), kPair);
         mbar_init(smem_u32(&sh.epi_drained), kEpiWarps);
         if constexpr (kF32) {
-            for (int b = 0; b < 2; ++b) {
+            for (int b = 0; b < kScrBufs; ++b) {
                 mbar_init(smem_u32(&sh.scr_full[b]), 1);
                 mbar_init(smem_u32(&sh.scr_empty[b]), kEpiWarps * kPair);
             }
@@ -609,11 +612,14 @@ gemm_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_constant__ C
     const uint32_t tmem = sh.tmem_base;
     const int64_t total = p.groups > 0 ? sh.grouped_tiles : p.total_tiles;
 
-    // FP32 scales: MMA issuer for the K-steps of one parity (product buffer
-    // `par`): 4 MMAs (N = 128, K = 32 each) per K-step, once the epilogue warps
-    // of both CTAs read that buffer's previous product (K-step kg - 2).  Two
-    // issuers (warps 1 and kMma2Warp) share the work: a tcgen05.mma costs its
-    // thread ~100+ cycles of issue.
+    // FP32 scales: MMA issuer for the K-steps of one parity: 4 MMAs (N = 128,
+    // K = 32 each) per K-step into product buffer kg % kScrBufs, once the
+    // epilogue warps of both CTAs read that buffer's previous product (K-step
+    // kg - kScrBufs).  Two issuers (warps 1 and kMma2Warp) alternate K-steps,
+    // so that one can wait for its operands or its buffer while the other
+    // issues (a thread's tcgen05.mma issue blocks while the tensor pipe is
+    // busy).  Four buffers let the MMAs run up to three K-steps ahead of the
+    // epilogue (and on into the next tile while the epilogue stores one).
     auto mma_f32 = [&](uint32_t par) {
         uint32_t kg = 0;
         bool ok = true;
@@ -622,7 +628,8 @@ gemm_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_constant__ C
                 if ((kg & 1u) != par) continue;
                 const uint32_t stage = kg % C::kStages, phase = (kg / C::kStages) & 1u;
                 if (!wait_or_abort(smem_u32(&sh.full[stage]), phase, sh, p.status)) { ok = false; break; }
-                if (kg >= 2 && !wait_or_abort(smem_u32(&sh.scr_empty[par]), ((kg >> 1) - 1) & 1u, sh, p.status)) {
+                const uint32_t buf = kg % kScrBufs, use = kg / kScrBufs;
+                if (use >= 1 && !wait_or_abort(smem_u32(&sh.scr_empty[buf]), (use - 1) & 1u, sh, p.status)) {
                     ok = false;
                     break;
                 }
@@ -630,7 +637,7 @@ gemm_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_constant__ C
                 uint8_t* st = smem + stage * C::kStageBytes;
                 const uint64_t a_desc = smem_desc(smem_u32(st), 16, 1024, 2);
                 const uint64_t b_desc = smem_desc(smem_u32(st + C::kABytes), 16, 1024, 2);
-                const uint32_t d = tmem + uint32_t(C::kBN) * par;
+                const uint32_t d = tmem + uint32_t(C::kBN) * buf;
 #pragma unroll
                 for (int kk = 0; kk < 4; ++kk) {
                     if constexpr (kPair == 2)
@@ -640,10 +647,10 @@ gemm_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_constant__ C
                 }
                 if constexpr (kPair == 2) {
                     tc_commit_pair_mc(smem_u32(&sh.empty[stage]), 0x3);
-                    tc_commit_pair_mc(smem_u32(&sh.scr_full[par]), 0x3);
+                    tc_commit_pair_mc(smem_u32(&sh.scr_full[buf]), 0x3);
                 } else {
                     tc_commit(smem_u32(&sh.empty[stage]));
-                    tc_commit(smem_u32(&sh.scr_full[par]));
+                    tc_commit(smem_u32(&sh.scr_full[buf]));
                 }
             }
         }
@@ -769,7 +776,7 @@ gemm_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_constant__ C
                                sh, p.status))
                 return false;
             const uint32_t bar = smem_u32(&sh.sf_full[slot]);
-            const uint32_t dst = smem_u32(ring + slot * kSfGroupBytes);
+            const uint32_t dst = smem_u32(ring + slot * C::kSfSlotBytes);
             mbar_arrive_expect_tx(bar, kSFABytes + C::kSFBBytes);
             tma_load_2d(dst, &map_sfa, bar, ltl.sf0 + lg * 16, ltl.a_row + int32_t(rank) * kBM);
             tma_load_2d(dst + kSFABytes, &map_sfb, bar, ltl.sf0 + lg * 16, ltl.b_row);
@@ -792,7 +799,7 @@ gemm_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_constant__ C
             for (int32_t g = 0; g < ngroups && ok; ++g, ++j) {
                 const uint32_t slot = j % kSfRing, bit = (j / kSfRing) & 1u;
                 if (!wait_or_abort(smem_u32(&sh.sf_full[slot]), bit, sh, p.status)) { ok = false; break; }
-                const uint32_t sf = smem_u32(ring + slot * kSfGroupBytes);
+                const uint32_t sf = smem_u32(ring + slot * C::kSfSlotBytes);
                 if constexpr (kF32) {
                     // B's scales [128 columns][4 K-steps] -> [4 K-steps][128 columns] (fp32), so
                     // that the epilogue reads 4 consecutive columns' scales at once; A's stay
@@ -881,15 +888,16 @@ gemm_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_constant__ C
                             break;
                         }
                     }
-                    const uint32_t b = kg & 1u;
-                    if (!__all_sync(0xFFFFFFFFu, wait_or_abort(smem_u32(&sh.scr_full[b]), (kg >> 1) & 1u, sh, p.status))) {
+                    const uint32_t b = kg % kScrBufs;
+                    if (!__all_sync(0xFFFFFFFFu, wait_or_abort(smem_u32(&sh.scr_full[b]), (kg / kScrBufs) & 1u, sh,
+                                                               p.status))) {
                         ok = false;
                         break;
                     }
                     tc_fence_after();
                     uint32_t v[64];
                     tmem_ld_32x32b_x64(tmem + lanes + uint32_t(C::kBN) * b + uint32_t(64 * h), v);
-                    const uint32_t sf = smem_u32(smem + C::kStages * C::kStageBytes + slot * kSfGroupBytes);
+                    const uint32_t sf = smem_u32(smem + C::kStages * C::kStageBytes + slot * C::kSfSlotBytes);
                     const float sa = __uint_as_float(lds32(sf + (32 * q + lane) * 16 + (k & 3) * 4));
                     const uint32_t sbt = sf + kSFABytes + (k & 3) * 512 + 256 * h;   // B scales of my 64 columns
                     tmem_ld_wait();
@@ -964,7 +972,7 @@ gemm_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_constant__ C
                     const uint16_t* bias = p.has_bias ? p.bias + int64_t(tl.group) * p.N : nullptr;
                     // output columns of acc0 / acc1 (FP32 scales: 64 columns per warp, acc0 only)
                     const int32_t nb0 = tl.n0 + (kF32 ? 64 * h : 128 * h);
-                    const uint32_t stage = smem_u32(smem + C::kStages * C::kStageBytes + kSfRing * kSfGroupBytes) +
+                    const uint32_t stage = smem_u32(smem + C::kStages * C::kStageBytes + kSfRing * C::kSfSlotBytes) +
                                            uint32_t(e) * 4096u;
                     if (nb0 < p.N) store_64_staged<kAcc>(acc0, p, bias, row0, tl.row_end, nb0, stage, lane);
                     if (!kF32 && nb0 + 64 < p.N) store_64_staged<kAcc>(acc1, p, bias, row0, tl.row_end, nb0 + 64, stage, lane);
