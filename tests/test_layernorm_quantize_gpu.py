@@ -6,8 +6,9 @@ rsigma (``layernorm_stat_bounds``).  Codes and scales: every one must be the
 MXFP8 quantisation of some y' within ``layernorm_error_bound`` of the exact y
 (``mx_admissible``); where only one answer is admissible (all but a small
 fraction of the elements, asserted) that is bit-exactness.  Covers chunk and
-unit edge cases (hidden not a multiple of 64, the largest hidden), several
-rows per statistics warp group, ragged rows, each orientation alone, statistics only,
+unit edge cases (hidden not a multiple of 64, long rows, the largest hidden),
+several rows per statistics warp group (with and without codes), ragged rows,
+each orientation alone, statistics only,
 constant and non-finite rows, large row means, determinism, canary-guarded
 outputs, and the full-size ffn input (sampled rows and 32-row bands).
 """
@@ -109,7 +110,8 @@ def check(x, ga, be, got, rows_idx=None, max_ambiguous=MAX_AMBIGUOUS):
 
 
 @pytest.mark.parametrize("rows,hidden", [(32, 64), (64, 96), (256, 1024), (96, 4128), (128, 7168),
-                                         (64, 2080), (32, 32768)])
+                                         (64, 2080), (32, 24576), (32, 24640),
+                                         (32, 32768)])
 def test_both_orientations(rows, hidden):
     x, ga, be = make(rows, hidden, rows * 3 + hidden)
     check(x, ga, be, run(x, ga, be))
@@ -121,13 +123,14 @@ def test_several_rows_per_statistics_warp(rows, hidden):
     # under 2048 elements, four from 2048): each group reuses its two row
     # buffers; every row's statistics and a sample of code rows are checked
     x, ga, be = make(rows, hidden, rows + 2 * hidden)
+    check(x, ga, be, run(x, ga, be, rowwise=False, colwise=False))
     got = run(x, ga, be)
     sample = np.sort(np.random.default_rng(rows).choice(rows, 48, replace=False))
     check(x, ga, be, {"mu": got["mu"], "rsigma": got["rsigma"]})
     check(x, ga, be, {k: v for k, v in got.items() if k in ("q_row", "s_row")}, sample)
 
 
-@pytest.mark.parametrize("rows,hidden", [(1, 64), (37, 512), (100, 1056)])
+@pytest.mark.parametrize("rows,hidden", [(1, 64), (37, 512), (100, 1056), (45, 24608)])
 def test_rowwise_ragged_rows(rows, hidden):
     x, ga, be = make(rows, hidden, rows + hidden)
     check(x, ga, be, run(x, ga, be, rowwise=True, colwise=False))
