@@ -53,19 +53,27 @@ KERNEL_SOURCES = {"gemm": ["gemm.cu", "ptx.cuh", "tcgen05.cuh"], "quant": ["quan
                   "ln": ["layernorm_quantize.cu", "e4m3.cuh", "ptx.cuh", "units.cuh"]}
 
 
+def code_only(text: str) -> str:
+    """A source's code lines: line comments and blank lines dropped (the
+    sources hold no block comments and no "//" inside string literals)."""
+    lines = (line.split("//", 1)[0].rstrip() for line in text.splitlines())
+    return "\n".join(line for line in lines if line)
+
+
 def source_sha256(kernel_name: str) -> str:
-    """Hash of the sources that build the kernel behind a bench kernel name."""
+    """Hash of the code (comments aside) of the sources that build the kernel
+    behind a bench kernel name."""
     h = hashlib.sha256()
     for f in KERNEL_SOURCES[kernel_name.split("_")[0]]:
-        with open(os.path.join(ROOT, "mxfp8_block_scaled_quantize_gb300", "csrc", f), "rb") as fh:
-            h.update(fh.read())
+        with open(os.path.join(ROOT, "mxfp8_block_scaled_quantize_gb300", "csrc", f)) as fh:
+            h.update(code_only(fh.read()).encode())
     return h.hexdigest()
 
 
 def measured_traffic(kernel_name: str):
     """DRAM bytes (read + write) per launch from profiles/traffic.json, recorded
-    by ncu for this workload; None unless the kernel's sources are unchanged
-    since that capture."""
+    by ncu for this workload; None unless the kernel's code (comments aside)
+    is unchanged since that capture."""
     try:
         with open(os.path.join(ROOT, "profiles", "traffic.json")) as f:
             entry = json.load(f).get(kernel_name)

@@ -62,7 +62,7 @@ constexpr int kScrBufs = 4;              // FP32 scales: K-step product buffers 
 
 // kF32 (Float8BlockScaling with FP32 scales): 128-column tiles, so that an
 // epilogue thread keeps its 64 accumulator columns in registers while the
-// K-step products are double-buffered in TMEM.
+// K-step products rotate through kScrBufs TMEM buffers.
 template <int kPair, bool kF32 = false>
 struct Cfg {
     static constexpr int kTileM = kBM * kPair;            // rows of one (pair) tile
@@ -543,7 +543,8 @@ __device__ __forceinline__ void store_64_staged(uint32_t* acc, const GemmParams&
 
 // kAcc: fp32 D accumulated into; kWgrad: grouped wgrad; kF32: Float8BlockScaling
 // operands with FP32 scales (dense only): every K-step's product lands in one
-// of two TMEM buffers and the epilogue warps accumulate it, scaled, in registers.
+// of kScrBufs TMEM buffers and the epilogue warps accumulate it, scaled, in
+// registers.
 template <int kPair, bool kAcc, bool kWgrad, bool kF32>
 __global__ void __launch_bounds__(kF32 ? kThreads + 32 : kThreads, 1)   // 168 registers: 3 warps share a 16K-register sub-partition
 gemm_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_constant__ CUtensorMap map_b,
