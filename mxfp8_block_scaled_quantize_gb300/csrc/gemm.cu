@@ -464,7 +464,8 @@ __device__ __forceinline__ void store_chunk(const uint32_t* acc, const GemmParam
 template <bool kAcc>
 __device__ __forceinline__ void store_64_staged(uint32_t* acc, const GemmParams& p, const uint16_t* bias,
                                                 int64_t row0, int64_t row_end, int32_t n, uint32_t stage,
-                                                int lane) {
+                                                int lane, const CUtensorMap* map_d, const CUtensorMap* map_aux,
+                                                bool tma) {
     float* v = reinterpret_cast<float*>(acc);
     if constexpr (kAcc) {
         // D (fp32) += acc: each lane reads, adds and writes its own row, 16
@@ -497,6 +498,9 @@ __device__ __forceinline__ void store_64_staged(uint32_t* acc, const GemmParams&
             }
         }
     }
+    // the staging tile is free once this warp's previous TMA store has read it
+    if (lane == 0) bulk_wait_read_all();
+    __syncwarp();
     if (p.dgelu) {
         // the forward pre-activation rows come in as whole lines through the
         // staging tile, then each lane takes its own row
@@ -527,6 +531,20 @@ __device__ __forceinline__ void store_64_staged(uint32_t* acc, const GemmParams&
             const uint32_t w2 = pack_bf16x2(v[8 * c + 4], v[8 * c + 5]), w3 = pack_bf16x2(v[8 * c + 6], v[8 * c + 7]);
             sts128(stage + lane * 128 + ((c ^ (lane & 7)) << 4), w0, w1, w2, w3);
         }
+        if (tma) {
+            // the staging tile is the 128-byte-swizzled 32 x 64 box of the
+            // output's tensor map: one asynchronous store; the warp goes on
+            // and waits only before it writes the tile again
+            fence_proxy_async_smem();
+            __syncwarp();
+            if (lane == 0) {
+                tma_store_2d(is_aux ? map_aux : map_d, stage, n, int32_t(row0));
+                bulk_commit();
+                if (is_aux) bulk_wait_read_all();      // D is staged next, now
+            }
+            __syncwarp();
+            continue;
+        }
         __syncwarp();
         uint16_t* out = is_aux ? p.aux : p.D;
         const int c = lane & 7;
@@ -549,6 +567,7 @@ template <int kPair, bool kAcc, bool kWgrad, bool kF32>
 __global__ void __launch_bounds__(kF32 ? kThreads + 32 : kThreads, 1)   // 168 registers: 3 warps share a 16K-register sub-partition
 gemm_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_constant__ CUtensorMap map_b,
             const __grid_constant__ CUtensorMap map_sfa, const __grid_constant__ CUtensorMap map_sfb,
+            const __grid_constant__ CUtensorMap map_d, const __grid_constant__ CUtensorMap map_aux,
             const GemmParams p) {
     using C = Cfg<kPair, kF32>;
     using SH = SharedState<C::kStages>;
@@ -975,8 +994,15 @@ gemm_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_constant__ C
                     const int32_t nb0 = tl.n0 + (kF32 ? 64 * h : 128 * h);
                     const uint32_t stage = smem_u32(smem + C::kStages * C::kStageBytes + kSfRing * C::kSfSlotBytes) +
                                            uint32_t(e) * 4096u;
-                    if (nb0 < p.N) store_64_staged<kAcc>(acc0, p, bias, row0, tl.row_end, nb0, stage, lane);
-                    if (!kF32 && nb0 + 64 < p.N) store_64_staged<kAcc>(acc1, p, bias, row0, tl.row_end, nb0 + 64, stage, lane);
+                    // TMA stores where the warp's 32 rows all belong to the tile, or run
+                    // past the end of D (clipped there); per-row stores otherwise
+                    const int64_t d_rows = kWgrad ? int64_t(p.groups) * p.M : p.M;
+                    const bool tma = !kAcc && (row0 + 32 <= tl.row_end || tl.row_end == d_rows);
+                    if (nb0 < p.N)
+                        store_64_staged<kAcc>(acc0, p, bias, row0, tl.row_end, nb0, stage, lane, &map_d, &map_aux, tma);
+                    if (!kF32 && nb0 + 64 < p.N)
+                        store_64_staged<kAcc>(acc1, p, bias, row0, tl.row_end, nb0 + 64, stage, lane, &map_d, &map_aux,
+                                              tma);
                 }
             } else {
                 // (tcgen05.ld is warp-collective: the lanes' row test guards the stores only)
@@ -1006,6 +1032,7 @@ gemm_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_constant__ C
         }
     }
 
+    if (C::kStagedStores && lane == 0) bulk_wait_all();   // this warp's TMA stores (epilogue warps)
     __syncthreads();
     if constexpr (kPair == 2) cluster_sync();      // no CTA leaves while its peer may still signal it
     if (warp == 1) {
@@ -1040,6 +1067,19 @@ te_mx_status launch_gemm(const GemmArgs& a, int sms, unsigned int* status, cudaS
                                    sfa_pitch, 16, kBM, CU_TENSOR_MAP_SWIZZLE_NONE)) != TE_MX_OK) return st;
     if ((st = encode_tensor_map_2d(&msb, CU_TENSOR_MAP_DATA_TYPE_UINT8, a.sB, sfb_cols, b_rows,
                                    sfb_pitch, 16, C::kBN, CU_TENSOR_MAP_SWIZZLE_NONE)) != TE_MX_OK) return st;
+    // bf16 D and AUX as 32 x 64 boxes in the epilogue's 128-byte-swizzled
+    // staging layout (CTA pairs store through them; unused otherwise)
+    CUtensorMap md = ma, mx = ma;
+    if (C::kStagedStores && !kAcc) {
+        const uint64_t d_rows = wg ? uint64_t(a.groups) * uint64_t(a.M) : uint64_t(a.M);
+        if ((st = encode_tensor_map_2d(&md, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, a.D, uint64_t(a.N), d_rows,
+                                       uint64_t(a.N) * 2, 64, 32, CU_TENSOR_MAP_SWIZZLE_128B)) != TE_MX_OK)
+            return st;
+        mx = md;
+        if (a.gelu && (st = encode_tensor_map_2d(&mx, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, a.aux, uint64_t(a.N), d_rows,
+                                                 uint64_t(a.N) * 2, 64, 32, CU_TENSOR_MAP_SWIZZLE_128B)) != TE_MX_OK)
+            return st;
+    }
 
     GemmParams p{};
     p.M = a.M;
@@ -1099,7 +1139,7 @@ te_mx_status launch_gemm(const GemmArgs& a, int sms, unsigned int* status, cudaS
         if (units > max_clusters) units = max_clusters;
         cfg.gridDim = dim3(unsigned(units * kPair));
     }
-    e = cudaLaunchKernelEx(&cfg, kern, ma, mb, msa, msb, p);
+    e = cudaLaunchKernelEx(&cfg, kern, ma, mb, msa, msb, md, mx, p);
     return cuda_status(e, "gemm kernel launch");
 }
 
