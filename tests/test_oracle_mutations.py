@@ -117,3 +117,37 @@ def test_fp32_scale_mutations_are_caught(monkeypatch):
     monkeypatch.setattr(O, "dequantize_fp32", lambda q, s: orig_deq(q, np.roll(np.asarray(s), 1, axis=1)))
     with pytest.raises(AssertionError):
         F.test_gemm_exact_small()
+
+
+def test_block_scale_mutations_are_caught(monkeypatch):
+    from tests import test_oracle_blockscale as B
+    # floor instead of ceil: the largest element of a block can then exceed 448 after scaling
+    orig = O.block_scale_exponent
+    monkeypatch.setattr(O, "block_scale_exponent",
+                        lambda amax: np.where(np.asarray(amax) > 0, O.floor_log2(np.asarray(amax, np.float64)) - 8,
+                                              -127).astype(np.int64))
+    with pytest.raises(AssertionError):
+        B.test_block_scale_rule_exhaustive()
+    monkeypatch.setattr(O, "block_scale_exponent", orig)
+    # 2D blocks requested, 1x128 / 128x1 blocks computed
+    orig_qb = O.quantize_block
+    monkeypatch.setattr(O, "quantize_block", lambda x, block_2d: orig_qb(x, False))
+    with pytest.raises(AssertionError):
+        B.test_2d_blocks_share_scale_across_copies()
+
+
+def test_backward_mutations_are_caught(monkeypatch):
+    from tests import test_oracle_backward as D
+    # dGELU without the term from the derivative of u (only 0.5 (1 + tanh u))
+    monkeypatch.setattr(O, "dgelu_tanh",
+                        lambda x: 0.5 * (1 + np.tanh(np.sqrt(2 / np.pi) * (np.asarray(x, np.float64)
+                                                                           + 0.044715 * np.asarray(x, np.float64) ** 3))))
+    with pytest.raises(AssertionError):
+        D.test_dgelu_matches_autograd()
+    with pytest.raises(AssertionError):
+        D.test_dgelu_matches_finite_differences()
+    # bias gradient missing the last row
+    monkeypatch.setattr(O, "column_sums",
+                        lambda xb: (O.bf16_bits_to_f64(xb)[:-1].sum(axis=0), np.abs(O.bf16_bits_to_f64(xb)).sum(axis=0)))
+    with pytest.raises(AssertionError):
+        D.test_column_sums_exact()
