@@ -151,3 +151,26 @@ def test_backward_mutations_are_caught(monkeypatch):
                         lambda xb: (O.bf16_bits_to_f64(xb)[:-1].sum(axis=0), np.abs(O.bf16_bits_to_f64(xb)).sum(axis=0)))
     with pytest.raises(AssertionError):
         D.test_column_sums_exact()
+
+
+def test_grouped_expert_index_mistake_is_caught(monkeypatch):
+    # experts numbered by non-empty groups only: every group after an empty one uses the wrong weights
+    def shifted(qx, sx, group_m, qw, sw, bias_bits=None, gelu=False):
+        nonempty = [i for i, m in enumerate(group_m) if int(m) > 0]
+        out = {"pre": None, "d": [], "aux": [] if gelu else None, "sigma": None}
+        row = 0
+        for j, g in enumerate(nonempty):
+            m = int(group_m[g])
+            r = O.mx_gemm(qx[row:row + m], sx[row:row + m], qw[j], sw[j],
+                          None if bias_bits is None else bias_bits[j], gelu)
+            out["d"].append(r["d"])
+            if gelu:
+                out["aux"].append(r["aux"])
+            row += m
+        out["d"] = np.concatenate(out["d"])
+        if gelu:
+            out["aux"] = np.concatenate(out["aux"])
+        return out
+    monkeypatch.setattr(O, "mx_grouped_gemm", shifted)
+    with pytest.raises(AssertionError):
+        G.test_grouped_equals_per_group_dense_with_empty_groups()
