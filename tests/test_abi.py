@@ -114,3 +114,46 @@ def test_host_validation_rejects_bad_arguments_before_any_launch(lib):
     binding.te_mx_block_quantize(0, 0, 128, 128, 1, 0, 0, 0, 0, 0, 0, 0)
     binding.te_mx_quantize(0, 0, 64, 64, 0, 0, 0, 0, 0, 0, 0)
     binding.te_mx_gemm(16, 16, 16, 16, 16, 16, 0, 128, 128, 0, 0, 16, 0, 0, 0, 0)
+
+
+def test_host_validation_of_the_backward_and_grouped_entry_points(lib):
+    # te_mx_quantize_dbias: checks before any launch
+    with pytest.raises(binding.TemxError, match="INVALID_ARG"):         # dbias missing
+        binding.te_mx_quantize_dbias(16, 32, 64, 64, 16, 16, 16, 0, 0, 0, 0, 16, 1 << 20, 0)
+    with pytest.raises(binding.TemxError, match="UNSUPPORTED_SHAPE"):   # cols % 32
+        binding.te_mx_quantize_dbias(16, 32, 48, 48, 16, 16, 16, 0, 0, 0, 16, 16, 1 << 20, 0)
+    # (the dbias alignment and workspace checks follow the device check, so they need a GPU)
+    assert binding.te_mx_quantize_dbias_workspace_size(32, 64) > 0
+    # te_mx_quantize_colwise_grouped
+    with pytest.raises(binding.TemxError, match="INVALID_ARG"):         # no groups
+        binding.te_mx_quantize_colwise_grouped(16, 128, 64, 64, 0, 16, 16, 256, 16, 16, 0)
+    with pytest.raises(binding.TemxError, match="INVALID_ARG"):         # more than 1024 groups
+        binding.te_mx_quantize_colwise_grouped(16, 128, 64, 64, 1025, 16, 16, 256, 16, 16, 0)
+    with pytest.raises(binding.TemxError, match="UNSUPPORTED_SHAPE"):   # cols % 32
+        binding.te_mx_quantize_colwise_grouped(16, 128, 48, 48, 2, 16, 16, 256, 16, 16, 0)
+    with pytest.raises(binding.TemxError, match="MISALIGNED"):          # ld_q % 16
+        binding.te_mx_quantize_colwise_grouped(16, 128, 64, 64, 2, 16, 16, 200, 16, 16, 0)
+    # te_mx_grouped_gemm_wgrad
+    with pytest.raises(binding.TemxError, match="UNSUPPORTED_SHAPE"):   # N % 16
+        binding.te_mx_grouped_gemm_wgrad(2, 16, 128, 16, 16, 16, 16, 128, 120, 256, 16, 0, 16, 0)
+    with pytest.raises(binding.TemxError, match="MISALIGNED"):          # ld_s < 16
+        binding.te_mx_grouped_gemm_wgrad(2, 16, 128, 16, 16, 16, 16, 128, 128, 256, 0, 0, 16, 0)
+    # the failing call left its message
+    assert binding.lib().te_mx_last_error()
+
+
+@pytest.mark.parametrize("groups", [1, 3, 128])
+def test_grouped_widths_cover_every_partition(lib, groups):
+    # the host widths suffice for any split of total_m tokens into `groups` experts
+    import numpy as np
+    rng = np.random.default_rng(groups)
+    for total in (0, 1, 127, 128, 129, 4096, 131072):
+        cw = binding.te_mx_grouped_code_width(total, groups)
+        sw = binding.te_mx_grouped_scale_width(total, groups)
+        assert cw % 16 == 0 and sw % 16 == 0 and sw >= 16
+        for _ in range(20):
+            cuts = np.sort(rng.integers(0, total + 1, groups - 1))
+            m = np.diff(np.concatenate([[0], cuts, [total]]))
+            kp = (m + 127) // 128 * 128
+            assert kp.sum() <= cw
+            assert ((kp // 32 + 15) // 16 * 16).sum() <= sw
