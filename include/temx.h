@@ -32,6 +32,15 @@
  * launching anything; te_mx_last_error() then holds a message (per thread).
  * Kernels bound every wait; a wait that runs out sets a device status word
  * that te_mx_device_status() reports (TE_MX_ERR_DEVICE_TIMEOUT).
+ *
+ * Per-device state
+ * ----------------
+ * On its first call on a device the library looks up, and then keeps for the
+ * life of the process, device addresses of its own static device memory (the
+ * status word; the scratch array of te_mx_quantize_dbias_noalloc).  They are
+ * valid for that device's primary context only: after the context is
+ * destroyed (cudaDeviceReset) no entry point may be called on that device
+ * again in the same process.
  */
 #ifndef TEMX_H
 #define TEMX_H

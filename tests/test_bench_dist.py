@@ -50,3 +50,22 @@ def test_single_process_helpers_are_identity():
     bench._dist = False
     assert bench.dist_max(3.5) == 3.5
     assert bench.whole_job_tflops(2e12, 1, 1.0) == pytest.approx(2000.0)
+
+
+def test_replica_launch_command_runs_ranks_on_cpu():
+    # the command bench.py runs for --gpus N outside torchrun, here starting two
+    # CPU replicas of a probe that uses the bench's barrier and max-over-ranks
+    import json
+    import subprocess
+    import bench
+    probe = os.path.join(os.path.dirname(os.path.abspath(__file__)), "_replica_probe.py")
+    cmd = bench.replica_command(2, probe, ["--steps", "3"], _free_port())
+    assert cmd[1:4] == ["-m", "torch.distributed.run", "--nnodes=1"] and "--nproc-per-node=2" in cmd
+    assert "--master-addr=127.0.0.1" in cmd
+    r = subprocess.run(cmd, capture_output=True, text=True, timeout=300)
+    assert r.returncode == 0, r.stderr[-2000:]
+    line = [ln for ln in r.stdout.splitlines() if ln.startswith("{")]
+    assert len(line) == 1, r.stdout
+    got = json.loads(line[0])
+    assert got["world"] == 2 and got["worst_ms"] == 2.0 and got["argv"] == ["--steps", "3"]
+    assert got["value"] == pytest.approx(2 * 1e12 / 2e-3 / 1e12)

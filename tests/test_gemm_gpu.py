@@ -4,8 +4,9 @@ Acceptance (element-wise, no exceptions): |gpu - oracle| <= 2^-7 |oracle| +
 1e-5 sum_k |a_k b_k|, oracle = the epilogue of the fp64 product of the same
 dequantised operands (rounded to bf16).  Operands for the small cases are
 quantised by the oracle and uploaded, so these tests do not depend on the GPU
-quantiser; the full-size cases run the GPU quantiser and check its sampled
-rows bit-exactly first.  Scale-pitch padding is filled with 0xFF (an E8M0
+quantiser; the full-size cases run the GPU quantiser, check every byte of
+the operand used in full and the sampled rows of the other bit-exactly, and
+check one row in every 256-row band of the output.  Scale-pitch padding is filled with 0xFF (an E8M0
 NaN) to prove it is never used, and every output has a canary tail.
 """
 import numpy as np
@@ -25,14 +26,6 @@ def rand_bits(shape, seed, std=1.0, outlier_cols=None):
     if outlier_cols is not None:
         x[..., outlier_cols] *= 64.0
     return U.bf16_bits(x.to(torch.bfloat16))
-
-
-def oracle_rowwise(bits, chunk=4096):
-    qs, ss = [], []
-    for r0 in range(0, bits.shape[0], chunk):
-        q, s = O.quantize_rowwise(bits[r0:r0 + chunk])
-        qs.append(q); ss.append(s)
-    return np.concatenate(qs), np.concatenate(ss)
 
 
 def upload(q, s):
@@ -239,21 +232,32 @@ def test_grouped_sizes_beyond_total_are_reported_and_clamped():
     binding.te_mx_device_status()          # the status word was cleared
 
 
-# ---------------------------------------------------------------- full-size workloads (sampled rows)
-
-def sample_rows(n, k, seed, tile=128):
-    rng = np.random.default_rng(seed)
-    rows = set(rng.choice(n, k, replace=False).tolist())
-    rows |= {0, n - 1, min(n - 1, tile - 1), min(n - 1, tile)}
-    return np.array(sorted(rows))
+# ---------------------------------------------------------------- full-size workloads
+#
+# The GPU quantiser's operands are checked bit-exactly first, every byte of
+# the operand that the oracle GEMM uses in full (B) and the sampled rows of A.
+# The oracle GEMM then runs on the oracle's own codes, which those checks
+# showed to be identical, so a quantiser error cannot hide inside the GEMM
+# tolerance and no oracle input comes from the GPU.  Rows: one random row in
+# every 256-row band (the row extent of a CTA-pair tile) plus the edges, so
+# every output tile row band of the persistent tile walk is checked, each
+# sampled row across all N columns (every n-tile).
 
 
 def check_sampled(d, aux, rows, qa_rows, sa_rows, qb, sb, bias_bits, gelu, what):
-    ref = O.mx_gemm(qa_rows, sa_rows, qb, sb, bias_bits, gelu)
     ri = torch.from_numpy(rows).cuda()
-    assert_within_bound(to_f64(d[ri]), ref["d"], ref["sigma"], what + " D")
-    if gelu:
-        assert_within_bound(to_f64(aux[ri]), ref["aux"], ref["sigma"], what + " AUX")
+    got_d = to_f64(d[ri])
+    got_aux = to_f64(aux[ri]) if gelu else None
+    from tests import _oracle_jobs as J
+    pool = U.oracle_pool()
+    step = 8
+    futs = [(r0, pool.submit(J.gemm_rows, qa_rows[r0:r0 + step], sa_rows[r0:r0 + step], qb, sb, bias_bits, gelu))
+            for r0 in range(0, len(rows), step)]
+    for r0, f in futs:
+        rd, raux, sigma = f.result()
+        assert_within_bound(got_d[r0:r0 + step], rd, sigma, f"{what} D (rows {rows[r0]}..)")
+        if gelu:
+            assert_within_bound(got_aux[r0:r0 + step], raux, sigma, f"{what} AUX (rows {rows[r0]}..)")
 
 
 def fprop_check(x_cpu, w_cpu, bias_cpu, gelu, seed, what):
@@ -263,10 +267,9 @@ def fprop_check(x_cpu, w_cpu, bias_cpu, gelu, seed, what):
     d, aux = binding.gemm(qx["q_row"], qx["s_row"], qw["q_row"], qw["s_row"],
                           bias=None if bias_cpu is None else bias_cpu.cuda(), gelu=gelu)
     binding.te_mx_device_status()
-    rows = sample_rows(x_cpu.shape[0], 24, seed)
-    qa, sa = O.quantize_rowwise(U.bf16_bits(x_cpu[torch.from_numpy(rows)]))
-    U.assert_bytes_equal(qx["q_row"][torch.from_numpy(rows).cuda()].cpu().numpy(), qa, what + " X codes")
-    qb, sb = oracle_rowwise(U.bf16_bits(w_cpu))
+    rows = U.band_rows(x_cpu.shape[0], 256, seed, extra=(127, 128, 255, 256))
+    qa, sa = U.check_rows_rowwise(qx["q_row"], qx["s_row"], x_cpu, rows, what + " X (sampled rows)")
+    qb, sb = U.check_every_byte(qw, w_cpu, True, False, what + " W")["row"]
     check_sampled(d, aux, rows, qa, sa, qb, sb, None if bias_cpu is None else U.bf16_bits(bias_cpu), gelu, what)
 
 
@@ -277,9 +280,9 @@ def wgrad_check(dy_cpu, x_cpu, seed, what):
     qx = binding.quantize(x, rowwise=False, colwise=True)
     dw, _ = binding.gemm(qdy["q_col"], qdy["s_col"], qx["q_col"], qx["s_col"])
     binding.te_mx_device_status()
-    rows = sample_rows(dy_cpu.shape[1], 16, seed)
-    qa, sa = O.quantize_colwise(U.bf16_bits(dy_cpu[:, torch.from_numpy(rows)]))
-    qb, sb = O.quantize_colwise(U.bf16_bits(x_cpu))
+    rows = U.band_rows(dy_cpu.shape[1], 256, seed, extra=(127, 128, 255, 256))
+    qa, sa = U.check_cols_colwise(qdy["q_col"], qdy["s_col"], dy_cpu, rows, what + " dY (sampled columns)")
+    qb, sb = U.check_every_byte(qx, x_cpu, False, True, what + " X")["col"]
     check_sampled(dw, None, rows, qa, sa, qb, sb, None, False, what)
 
 
@@ -301,27 +304,43 @@ def test_full_size_ffn_fprop_and_wgrad():
 
 
 def test_full_size_moe_grouped():
-    d = workloads.make_moe()
+    # the first and the last row of every non-empty expert (and one row in
+    # every 256-row band of the concatenated rows), each against its expert's
+    # weights; every code of X and W checked bit-exactly first
+    from tests import _oracle_jobs as J
+    d = U.moe_workload()
     counts = d["group_m"].numpy()
     G, N, K = 128, 1536, 4096
-    x, w = d["X"].cuda(), d["W"].cuda()
+    x, w = d["X"].cuda(), d["W"].view(G * N, K).cuda()
     qx = binding.quantize(x, rowwise=True)
-    qw = binding.quantize(w.view(G * N, K), rowwise=True)
+    qw = binding.quantize(w, rowwise=True)
     gm = d["group_m"].cuda()
     out, aux = binding.grouped_gemm(gm, qx["q_row"], qx["s_row"], qw["q_row"].view(G, N, K), qw["s_row"],
                                     gelu=True)
     binding.te_mx_device_status()
+    del x, w
+    qwo, swo = U.check_every_byte(qw, d["W"].view(G * N, K), True, False, "moe W")["row"]
+    del qw
     starts = np.concatenate([[0], np.cumsum(counts)])
-    nonempty = np.nonzero(counts)[0]
-    picks = {int(nonempty[np.argmax(counts[nonempty])]), int(nonempty[np.argmin(counts[nonempty])]),
-             int(nonempty[0]), int(nonempty[-1])}
-    picks |= set(np.random.default_rng(6).choice(nonempty, 3, replace=False).tolist())
-    for g in sorted(picks):
-        r0, r1 = int(starts[g]), int(starts[g + 1])
-        rows = np.unique(np.concatenate([[r0, r1 - 1], np.random.default_rng(g).integers(r0, r1, 6)]))
-        qa, sa = O.quantize_rowwise(U.bf16_bits(d["X"][torch.from_numpy(rows)]))
-        qb, sb = O.quantize_rowwise(U.bf16_bits(d["W"][g]))
-        check_sampled(out, aux, rows, qa, sa, qb, sb, None, True, f"moe group {g} (m={counts[g]})")
+    total = int(starts[-1])
+    ends = {int(starts[g + 1]) - 1 for g in range(G) if counts[g]}
+    rows = U.band_rows(total, 256, 6, extra={int(starts[g]) for g in range(G) if counts[g]} | ends)
+    qa, sa = U.check_rows_rowwise(qx["q_row"], qx["s_row"], d["X"], rows, "moe X (sampled rows)")
+    got_d = to_f64(out[torch.from_numpy(rows).cuda()])
+    got_aux = to_f64(aux[torch.from_numpy(rows).cuda()])
+    group_of = np.searchsorted(starts, rows, side="right") - 1
+    pool = U.oracle_pool()
+    futs = []
+    for g in np.unique(group_of):
+        sel = np.nonzero(group_of == g)[0]
+        wq, ws = qwo[g * N:(g + 1) * N], swo[g * N:(g + 1) * N]
+        futs.append((g, sel, pool.submit(J.gemm_rows, qa[sel], sa[sel], wq, ws, None, True)))
+    assert len(futs) == int((counts > 0).sum())
+    for g, sel, f in futs:
+        rd, raux, sigma = f.result()
+        what = f"moe expert {g} (m={counts[g]}, rows {rows[sel][0]}..{rows[sel][-1]})"
+        assert_within_bound(got_d[sel], rd, sigma, what + " D")
+        assert_within_bound(got_aux[sel], raux, sigma, what + " AUX")
 
 
 # ---------------------------------------------------------------- backward: dGELU epilogue, dgrad
@@ -372,7 +391,7 @@ def test_full_size_fc1_dgrad_on_colwise_weight():
     qw = binding.quantize(w, rowwise=False, colwise=True)
     dx, _ = binding.gemm(qdy["q_row"], qdy["s_row"], qw["q_col"], qw["s_col"])
     binding.te_mx_device_status()
-    rows = sample_rows(d["dY"].shape[0], 16, 8)
-    qa, sa = O.quantize_rowwise(U.bf16_bits(d["dY"][torch.from_numpy(rows)]))
-    qb, sb = O.quantize_colwise(U.bf16_bits(d["W"]))
+    rows = U.band_rows(d["dY"].shape[0], 256, 8)
+    qa, sa = U.check_rows_rowwise(qdy["q_row"], qdy["s_row"], d["dY"], rows, "fc1 dY (sampled rows)")
+    qb, sb = U.check_every_byte(qw, d["W"], False, True, "fc1 W1")["col"]
     check_sampled(dx, None, rows, qa, sa, qb, sb, None, False, "fc1 dgrad")

@@ -2,8 +2,9 @@
 
 Covers small and ragged shapes spanning several units and a ragged tail,
 every bf16 bit pattern, the hand-worked golden blocks, wide exponent ranges,
-and the full-size workload tensors (sampled rows and columns), with canary
-guards around every output.
+with canary guards around every output; every code and scale byte of every
+tensor the five workloads quantise (the oracle runs slab by slab in a spawn
+process pool); and an input larger than 2^31 bytes.
 """
 import numpy as np
 import pytest
@@ -106,34 +107,71 @@ def test_empty_is_noop():
     binding.te_mx_device_status()
 
 
-def _sampled_full_size(x_cpu: torch.Tensor, seed: int, n_rows=48, n_cols=64):
+def _every_byte(x_cpu, rowwise, colwise, what):
     x = x_cpu.cuda()
+    out = binding.quantize(x, rowwise=rowwise, colwise=colwise)
+    binding.te_mx_device_status()
+    U.check_every_byte(out, x_cpu, rowwise, colwise, what)
+
+
+def test_full_size_tiny_every_byte():
+    d = workloads.make_tiny()
+    _every_byte(d["A"], True, True, "tiny A")
+    _every_byte(d["B"], True, True, "tiny B")
+
+
+def test_full_size_qkv_every_byte():
+    d = workloads.make_qkv()
+    _every_byte(d["X"], True, True, "qkv X")
+    _every_byte(d["W"], True, True, "qkv W")
+
+
+def test_full_size_fc1_every_byte():
+    d = workloads.make_fc1()
+    for key in ("X", "W", "dY"):
+        _every_byte(d[key], True, True, "fc1 " + key)
+
+
+def test_full_size_ffn_every_byte():
+    d = workloads.make_ffn()
+    _every_byte(d["X"], True, True, "ffn X")
+    _every_byte(d["W"], True, True, "ffn W")         # row-wise: fprop; column-wise: dgrad
+    _every_byte(d["dY"], True, True, "ffn dY")
+
+
+def test_full_size_moe_every_byte():
+    # the grouped GEMM's operands: X [131072 x 4096] and the stacked expert
+    # weights [128*1536 x 4096] (1.6 GB of bf16), row-wise
+    d = U.moe_workload()
+    _every_byte(d["X"], True, False, "moe X")
+    _every_byte(d["W"].view(128 * 1536, 4096), True, False, "moe W")
+
+
+def _big_rows(base, rows):
+    """Rows of the 2 GiB test matrix: row r = base[r % 4096] * 2^((r // 4096) % 16 - 8)
+    (a power-of-two scaling, exact in bf16)."""
+    rows = torch.as_tensor(rows)
+    k = ((rows // 4096) % 16 - 8).to(torch.float32)
+    return (base[rows % 4096].float() * torch.pow(2.0, k)[:, None]).to(torch.bfloat16)
+
+
+def test_input_and_outputs_past_2_31_bytes():
+    # [262208 x 4096] bf16 = 2^31 + 512 KiB of input: the last 64 rows (and
+    # their column blocks) are read past byte 2^31; 64-bit offsets everywhere
+    C = 4096
+    R = (1 << 31) // (2 * C) + 64
+    base = workloads.normal_bf16((4096, C), 1.0, 90)
+    bd = base.cuda()
+    x = torch.empty(R, C, dtype=torch.bfloat16, device="cuda")
+    for b0 in range(0, R, 4096):
+        n = min(4096, R - b0)
+        x[b0:b0 + n] = _big_rows(bd, torch.arange(b0, b0 + n, device="cuda"))
     out = binding.quantize(x, rowwise=True, colwise=True)
     binding.te_mx_device_status()
-    rows, cols = x_cpu.shape
-    rng = np.random.default_rng(seed)
-    r_idx = np.sort(rng.choice(rows, n_rows, replace=False))
-    c_idx = np.sort(rng.choice(cols, n_cols, replace=False))
-    r_idx[-1], c_idx[-1] = rows - 1, cols - 1          # include the last row / column
-    bits_r = U.bf16_bits(x_cpu[torch.from_numpy(r_idx)])
-    q, s = O.quantize_rowwise(bits_r)
-    ri = torch.from_numpy(r_idx).cuda()
-    U.assert_bytes_equal(out["q_row"][ri].cpu().numpy(), q, "row-wise codes (sampled rows)")
-    U.assert_bytes_equal(out["s_row"][ri][:, : cols // 32].cpu().numpy(), s, "row-wise scales (sampled rows)")
-    bits_c = U.bf16_bits(x_cpu[:, torch.from_numpy(c_idx)])
-    q, s = O.quantize_colwise(bits_c)
-    ci = torch.from_numpy(c_idx).cuda()
-    U.assert_bytes_equal(out["q_col"][ci].cpu().numpy(), q, "column-wise codes (sampled columns)")
-    U.assert_bytes_equal(out["s_col"][ci][:, : rows // 32].cpu().numpy(), s, "column-wise scales (sampled columns)")
-
-
-def test_full_size_fc1_tensors():
-    d = workloads.make_fc1()
-    _sampled_full_size(d["X"], 1)
-    _sampled_full_size(d["dY"], 2)
-
-
-def test_full_size_ffn_tensors():
-    d = workloads.make_ffn()
-    for i, key in enumerate(("X", "W", "dY")):
-        _sampled_full_size(d[key], 10 + i)
+    rows = U.band_rows(R, 4096, 3, extra=list(range(R - 64, R)) + [R - 65, (1 << 31) // (2 * C) - 1])
+    U.check_rows_rowwise(out["q_row"], out["s_row"], _big_rows(base, rows), rows, "row-wise, rows", only_rows=True)
+    # whole columns (each spans every row, so their last blocks are read past 2^31)
+    cols = np.array([0, 1, 777, 2048, C - 1])
+    xc = _big_rows(base[:, torch.from_numpy(cols)], torch.arange(R))
+    U.check_cols_colwise(out["q_col"], out["s_col"], xc, np.arange(len(cols)), "column-wise, columns",
+                         dev_index=cols)
