@@ -368,17 +368,59 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
     return r;
 }
 
-// GELU, tanh form: 0.5 x (1 + tanh u) with u = sqrt(2/pi) (x + 0.044715 x^3),
-// evaluated as the algebraically equal x / (1 + exp(-2u)), which keeps its
-// relative accuracy for large negative x (no 1 + tanh cancellation).
-__device__ __forceinline__ float gelu_tanh_f(float x) {
-    constexpr float kTwoC0 = 2.0f * 0.7978845608028654f;          // 2 sqrt(2/pi)
-    constexpr float kTwoC1 = 2.0f * 0.7978845608028654f * 0.044715f;
-    constexpr float kLog2e = 1.4426950408889634f;
-    const float two_u = x * fmaf(x * x, kTwoC1, kTwoC0);
-    float e;
-    asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(e) : "f"(-two_u * kLog2e));
-    return __fdividef(x, 1.0f + e);
+// Packed fp32 pairs (two lanes of one 64-bit register) for the f32x2 forms of
+// add, sub, mul and fma, which issue two operations per instruction.
+__device__ __forceinline__ uint64_t f2_pack(float lo, float hi) {
+    uint64_t r;
+    asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(lo), "f"(hi));
+    return r;
+}
+__device__ __forceinline__ void f2_unpack(uint64_t v, float& lo, float& hi) {
+    asm("mov.b64 {%0, %1}, %2;" : "=f"(lo), "=f"(hi) : "l"(v));
+}
+__device__ __forceinline__ uint64_t f2_add(uint64_t a, uint64_t b) {
+    uint64_t r;
+    asm("add.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(a), "l"(b));
+    return r;
+}
+__device__ __forceinline__ uint64_t f2_sub(uint64_t a, uint64_t b) {
+    uint64_t r;
+    asm("sub.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(a), "l"(b));
+    return r;
+}
+__device__ __forceinline__ uint64_t f2_mul(uint64_t a, uint64_t b) {
+    uint64_t r;
+    asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(a), "l"(b));
+    return r;
+}
+__device__ __forceinline__ uint64_t f2_fma(uint64_t a, uint64_t b, uint64_t c) {
+    uint64_t r;
+    asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(r) : "l"(a), "l"(b), "l"(c));
+    return r;
+}
+
+// GELU (tanh form) of two values: 0.5 x (1 + tanh u) with
+// u = sqrt(2/pi) (x + 0.044715 x^3), evaluated as the algebraically equal
+// x / (1 + 2^t), t = -2 log2(e) u, which keeps its relative accuracy for large
+// negative x (no 1 + tanh cancellation).  The epilogue is bound by instruction
+// issue, so the arithmetic runs as packed f32x2 operations (t = x (A x^2 + B)
+// with the constants folded in, 1 + 2^t, the final product) around the two
+// MUFU operations per value (ex2, reciprocal): 4.5 instructions per value.
+__device__ __forceinline__ void gelu_tanh_f2(float& x0, float& x1) {
+    constexpr float kA = -2.0f * 1.4426950408889634f * 0.7978845608028654f * 0.044715f;
+    constexpr float kB = -2.0f * 1.4426950408889634f * 0.7978845608028654f;
+    const uint64_t x = f2_pack(x0, x1);
+    float t0, t1;
+    f2_unpack(f2_mul(x, f2_fma(f2_mul(x, x), f2_pack(kA, kA), f2_pack(kB, kB))), t0, t1);
+    float e0, e1;
+    asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(e0) : "f"(t0));
+    asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(e1) : "f"(t1));
+    float d0, d1;
+    f2_unpack(f2_add(f2_pack(e0, e1), f2_pack(1.0f, 1.0f)), d0, d1);
+    float r0, r1;
+    asm("rcp.approx.ftz.f32 %0, %1;" : "=f"(r0) : "f"(d0));
+    asm("rcp.approx.ftz.f32 %0, %1;" : "=f"(r1) : "f"(d1));
+    f2_unpack(f2_mul(x, f2_pack(r0, r1)), x0, x1);
 }
 
 // Derivative of the tanh-form GELU: with s = sigmoid(2u) = 0.5 (1 + tanh u)
@@ -448,7 +490,7 @@ __device__ __forceinline__ void store_chunk(const uint32_t* acc, const GemmParam
         st_global_v4(p.aux + off, o[0], o[1], o[2], o[3]);
         st_global_v4(p.aux + off + 8, o[4], o[5], o[6], o[7]);
 #pragma unroll
-        for (int i = 0; i < 16; ++i) v[i] = gelu_tanh_f(v[i]);
+        for (int i = 0; i < 16; i += 2) gelu_tanh_f2(v[i], v[i + 1]);
     }
 #pragma unroll
     for (int i = 0; i < 8; ++i) o[i] = pack_bf16x2(v[2 * i], v[2 * i + 1]);
@@ -491,9 +533,10 @@ __device__ __forceinline__ void store_64_staged(uint32_t* acc, const GemmParams&
                 const uint4 b = __ldg(reinterpret_cast<const uint4*>(bias + n + 8 * c));
                 const uint32_t bw[4] = {b.x, b.y, b.z, b.w};
 #pragma unroll
-                for (int i = 0; i < 4; ++i) {
-                    v[8 * c + 2 * i] += __uint_as_float(bw[i] << 16);
-                    v[8 * c + 2 * i + 1] += __uint_as_float(bw[i] & 0xFFFF0000u);
+                for (int i = 0; i < 4; ++i) {          // bf16 -> fp32 is a 16-bit shift; one packed add per pair
+                    const uint64_t sum = f2_add(f2_pack(v[8 * c + 2 * i], v[8 * c + 2 * i + 1]),
+                                                f2_pack(__uint_as_float(bw[i] << 16), __uint_as_float(bw[i] & 0xFFFF0000u)));
+                    f2_unpack(sum, v[8 * c + 2 * i], v[8 * c + 2 * i + 1]);
                 }
             }
         }
@@ -523,7 +566,7 @@ __device__ __forceinline__ void store_64_staged(uint32_t* acc, const GemmParams&
         const bool is_aux = p.gelu && pass == 0;
         if (p.gelu && pass == 1) {
 #pragma unroll
-            for (int i = 0; i < 64; ++i) v[i] = gelu_tanh_f(v[i]);
+            for (int i = 0; i < 64; i += 2) gelu_tanh_f2(v[i], v[i + 1]);
         }
 #pragma unroll
         for (int c = 0; c < 8; ++c) {
@@ -622,6 +665,11 @@ gemm_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_constant__ C
         }
         tc_fence_before();
     }
+    // Everything above touches only shared memory, TMEM and the kernel
+    // parameters, so it overlaps the previous kernel in the stream; every
+    // global-memory access comes after this wait.
+    grid_dependency_wait();
+    grid_launch_dependents();
     if (p.groups > 0 && warp == 2) {
         if constexpr (kWgrad) wgrad_prefix(p, sh, lane);
         else group_prefix<C::kTileM>(p, sh, lane);
@@ -1116,13 +1164,17 @@ te_mx_status launch_gemm(const GemmArgs& a, int sms, unsigned int* status, cudaS
     cfg.blockDim = dim3(kF32 ? kThreads + 32 : kThreads);
     cfg.dynamicSmemBytes = C::kSmemDyn;
     cfg.stream = stream;
-    cudaLaunchAttribute attr[1];
+    cudaLaunchAttribute attr[2];
     attr[0].id = cudaLaunchAttributeClusterDimension;
     attr[0].val.clusterDim.x = kPair;
     attr[0].val.clusterDim.y = 1;
     attr[0].val.clusterDim.z = 1;
+    // programmatic dependent launch: the CTAs may start, and set up their
+    // barriers and TMEM, while the previous kernel in the stream finishes
+    attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[1].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
-    cfg.numAttrs = 1;
+    cfg.numAttrs = 2;
     if constexpr (kPair == 2) {
         // persistent grid: never more pairs than can be resident together (the
         // occupancy query is slow, so its answer is kept per device)
@@ -1151,12 +1203,16 @@ te_mx_status gemm_launch(const GemmArgs& a, cudaStream_t stream) {
     if (st != TE_MX_OK) return st;
     int sms = 0;
     if ((st = device_sm_count(&sms)) != TE_MX_OK) return st;
-    // CTA pairs once there are enough 256-row tiles to fill the GPU; single
-    // CTAs for small problems (finer tiles, more of them).
+    // CTA pairs whenever the rows fill a 256-row pair tile: an SM of a pair
+    // loads 32 KB per K-step for the same MMA work for which a single CTA
+    // loads 48 KB, and operand ingress is what bounds the mainloop, so pairs
+    // are faster even when fewer tiles than pairs exist (a single-CTA split
+    // would keep the same number of SMs busy).  FP32 scales: CTA pairs once
+    // there are enough 256-row tiles to fill the GPU.
     const int64_t pair_tiles = ((a.M + 255) / 256) * ((a.N + kBN - 1) / kBN);
-    const bool pair = a.wgrad ? a.M >= 256 : (a.groups > 0 ? a.M >= 256 * 8 : pair_tiles >= sms / 2);
-    if (a.f32_scales) return pair ? launch_gemm<2, false, false, true>(a, sms, status, stream)
-                                  : launch_gemm<1, false, false, true>(a, sms, status, stream);
+    const bool pair = a.wgrad ? a.M >= 256 : (a.groups > 0 ? a.M >= 256 * 8 : a.M >= 256);
+    if (a.f32_scales) return pair_tiles >= sms / 2 ? launch_gemm<2, false, false, true>(a, sms, status, stream)
+                                                   : launch_gemm<1, false, false, true>(a, sms, status, stream);
     if (a.wgrad) {
         if (a.acc_f32) return pair ? launch_gemm<2, true, true>(a, sms, status, stream)
                                    : launch_gemm<1, true, true>(a, sms, status, stream);

@@ -71,6 +71,24 @@ __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, unsigne
     }
 }
 
+// ---------------------------------------------------------------- programmatic dependent launch
+
+// A kernel launched with programmatic stream serialisation may start while the
+// kernel before it in the stream is still running.  grid_dependency_wait()
+// returns once that kernel has completed and its memory operations are
+// visible, so it must come before this kernel's first global-memory access
+// (it returns at once when the launch carried no such dependency).
+// grid_launch_dependents() lets the next such kernel in the stream be
+// scheduled before this one completes; it changes scheduling only, never what
+// the next kernel's grid_dependency_wait() waits for.
+__device__ __forceinline__ void grid_dependency_wait() {
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+}
+
+__device__ __forceinline__ void grid_launch_dependents() {
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
 // ---------------------------------------------------------------- fences
 
 // Order this thread's generic-proxy shared-memory accesses before later

@@ -146,6 +146,8 @@ quantize_kernel(const __grid_constant__ CUtensorMap x_map, const __grid_constant
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int64_t gwarp = int64_t(blockIdx.x) * kWarps + warp;
     const int64_t nwarps = int64_t(gridDim.x) * kWarps;
+    grid_dependency_wait();              // launched as a programmatic dependent: no global access before this
+    grid_launch_dependents();
     if (gwarp >= p.units) return;
     const int64_t n_mine = (p.units - gwarp + nwarps - 1) / nwarps;
     const uint32_t ring = smem_u32(smem + warp * (kStages * kUnitBytes));
@@ -303,8 +305,19 @@ cudaError_t launch(const CUtensorMap& xm, const CUtensorMap& qr, const CUtensorM
     if (e != cudaSuccess) return e;
     const int64_t want = (p.units + kWarps - 1) / kWarps;
     const int grid = int(want < sms ? want : sms);
-    k<<<grid, kWarps * 32, kSmemBytes, stream>>>(xm, qr, qc, p);
-    return cudaGetLastError();
+    // programmatic dependent launch: the CTAs may start while the previous
+    // kernel in the stream finishes (the kernel waits before touching memory)
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(unsigned(grid));
+    cfg.blockDim = dim3(kWarps * 32);
+    cfg.dynamicSmemBytes = kSmemBytes;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, k, xm, qr, qc, p);
 }
 
 }  // namespace
