@@ -78,7 +78,10 @@ struct Cfg {
     // epilogue warp) so that global stores are written as whole lines.
     static constexpr bool kStagedStores = kPair == 2;
     static constexpr int kEpiStageBytes = kStagedStores ? kEpiWarps * 4096 : 0;
-    static constexpr int kSmemDyn = kStages * kStageBytes + kSfRing * kSfSlotBytes + kEpiStageBytes + 1024;
+    // ... and each epilogue warp's 128 bias values, fetched while the tile's
+    // MMAs run (a global load at store time costs an L2 round trip under load)
+    static constexpr int kBiasBytes = kStagedStores ? kEpiWarps * 256 : 0;
+    static constexpr int kSmemDyn = kStages * kStageBytes + kSfRing * kSfSlotBytes + kEpiStageBytes + kBiasBytes + 1024;
     // Instruction descriptor, kind::mxf8f6f4 with block scaling: E4M3 A and B
     // (format 0), both K-major, N >> 3 at bit 17, UE8M0 scales (bit 23),
     // M >> 4 at bit 24; scale-factor byte ids at bits 4..5 (B) and 29..30 (A).
@@ -503,8 +506,10 @@ __device__ __forceinline__ void store_chunk(const uint32_t* acc, const GemmParam
 // bytes into the warp's staging tile (16-byte chunks XOR-swizzled by row, so
 // neither the writes nor the reads conflict), then every store instruction
 // writes 4 complete rows.
+// `bias_sm` is the shared-memory address of column n's bf16 bias (the warp's
+// slice, copied there beforehand).
 template <bool kAcc>
-__device__ __forceinline__ void store_64_staged(uint32_t* acc, const GemmParams& p, const uint16_t* bias,
+__device__ __forceinline__ void store_64_staged(uint32_t* acc, const GemmParams& p, uint32_t bias_sm,
                                                 int64_t row0, int64_t row_end, int32_t n, uint32_t stage,
                                                 int lane, const CUtensorMap* map_d, const CUtensorMap* map_aux,
                                                 bool tma) {
@@ -530,7 +535,7 @@ __device__ __forceinline__ void store_64_staged(uint32_t* acc, const GemmParams&
 #pragma unroll
         for (int c = 0; c < 8; ++c) {
             if (n + 8 * c < p.N) {
-                const uint4 b = __ldg(reinterpret_cast<const uint4*>(bias + n + 8 * c));
+                const uint4 b = lds128(bias_sm + 16 * c);
                 const uint32_t bw[4] = {b.x, b.y, b.z, b.w};
 #pragma unroll
                 for (int i = 0; i < 4; ++i) {          // bf16 -> fp32 is a 16-bit shift; one packed add per pair
@@ -567,6 +572,9 @@ __device__ __forceinline__ void store_64_staged(uint32_t* acc, const GemmParams&
         if (p.gelu && pass == 1) {
 #pragma unroll
             for (int i = 0; i < 64; i += 2) gelu_tanh_f2(v[i], v[i + 1]);
+            // the AUX store issued before the GELU has read the staging tile by now
+            if (tma && lane == 0) bulk_wait_read_all();
+            __syncwarp();
         }
 #pragma unroll
         for (int c = 0; c < 8; ++c) {
@@ -583,7 +591,6 @@ __device__ __forceinline__ void store_64_staged(uint32_t* acc, const GemmParams&
             if (lane == 0) {
                 tma_store_2d(is_aux ? map_aux : map_d, stage, n, int32_t(row0));
                 bulk_commit();
-                if (is_aux) bulk_wait_read_all();      // D is staged next, now
             }
             __syncwarp();
             continue;
@@ -937,6 +944,12 @@ gemm_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_constant__ C
         uint32_t kg = 0, jg = 0;                 // FP32 scales: K-steps and scale groups consumed
         for (int64_t t = unit; t < total; t += units, ++local) {
             const Tile tl = map_tile<C::kTileM, C::kBN, kWgrad>(p, sh, t, hint);
+            // this warp's output columns (FP32 scales: 64, otherwise 128); their
+            // bias is loaded now, while the tile's MMAs run
+            const int32_t nbw = tl.n0 + (kF32 ? 64 * h : 128 * h);
+            uint4 bias_pre = make_uint4(0u, 0u, 0u, 0u);
+            if (C::kStagedStores && p.has_bias && lane < 16 && nbw + 8 * lane < p.N)
+                bias_pre = __ldg(reinterpret_cast<const uint4*>(p.bias + int64_t(tl.group) * p.N + nbw + 8 * lane));
             uint32_t acc0[64], acc1[64];
             if constexpr (kF32) {
                 // acc (registers: my 32 rows x 64 columns 64 h ..) += product(K-step) *
@@ -1037,11 +1050,15 @@ gemm_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_constant__ C
             if constexpr (C::kStagedStores) {
                 const int64_t row0 = row - lane;
                 if (row0 < tl.row_end) {             // warp-uniform: some row of this warp is stored
-                    const uint16_t* bias = p.has_bias ? p.bias + int64_t(tl.group) * p.N : nullptr;
                     // output columns of acc0 / acc1 (FP32 scales: 64 columns per warp, acc0 only)
-                    const int32_t nb0 = tl.n0 + (kF32 ? 64 * h : 128 * h);
-                    const uint32_t stage = smem_u32(smem + C::kStages * C::kStageBytes + kSfRing * C::kSfSlotBytes) +
-                                           uint32_t(e) * 4096u;
+                    const int32_t nb0 = nbw;
+                    const uint32_t epi = smem_u32(smem + C::kStages * C::kStageBytes + kSfRing * C::kSfSlotBytes);
+                    const uint32_t stage = epi + uint32_t(e) * 4096u;
+                    const uint32_t bias = epi + uint32_t(C::kEpiStageBytes) + uint32_t(e) * 256u;
+                    if (p.has_bias) {                // (the warp read its previous tile's slice in program order)
+                        if (lane < 16) sts128(bias + 16 * lane, bias_pre.x, bias_pre.y, bias_pre.z, bias_pre.w);
+                        __syncwarp();
+                    }
                     // TMA stores where the warp's 32 rows all belong to the tile, or run
                     // past the end of D (clipped there); per-row stores otherwise
                     const int64_t d_rows = kWgrad ? int64_t(p.groups) * p.M : p.M;
@@ -1049,8 +1066,8 @@ gemm_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_constant__ C
                     if (nb0 < p.N)
                         store_64_staged<kAcc>(acc0, p, bias, row0, tl.row_end, nb0, stage, lane, &map_d, &map_aux, tma);
                     if (!kF32 && nb0 + 64 < p.N)
-                        store_64_staged<kAcc>(acc1, p, bias, row0, tl.row_end, nb0 + 64, stage, lane, &map_d, &map_aux,
-                                              tma);
+                        store_64_staged<kAcc>(acc1, p, bias + 128u, row0, tl.row_end, nb0 + 64, stage, lane, &map_d,
+                                              &map_aux, tma);
                 }
             } else {
                 // (tcgen05.ld is warp-collective: the lanes' row test guards the stores only)
