@@ -121,11 +121,14 @@ def test_dense_vs_oracle(M, N, K, bias, gelu):
     check_dense(M, N, K, bias, gelu, seed=M + N + K)
 
 
-# Shapes with at least 76 tiles of 256 x 256 run on CTA pairs (cta_group::2).
+# Shapes with M >= 256 run on CTA pairs (cta_group::2); the last two give
+# every CTA pair several tiles.
 @pytest.mark.parametrize("M,N,K,bias,gelu", [
     (2048, 2560, 256, True, True),
     (2000, 2624, 640, False, False),
     (2304, 2304, 384, True, False),
+    (10240, 512, 256, True, True),
+    (20480, 256, 128, True, False),
 ])
 def test_dense_pair_tiles_vs_oracle(M, N, K, bias, gelu):
     check_dense(M, N, K, bias, gelu, seed=M + N + K + 1)
