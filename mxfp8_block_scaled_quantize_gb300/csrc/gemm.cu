@@ -695,16 +695,23 @@ gemm_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_constant__ C
     // issues (a thread's tcgen05.mma issue blocks while the tensor pipe is
     // busy).  Four buffers let the MMAs run up to three K-steps ahead of the
     // epilogue (and on into the next tile while the epilogue stores one).
+    // (run by a whole warp, values warp-uniform; lane 0's tcgen05 operations
+    // are predicated on)
     auto mma_f32 = [&](uint32_t par) {
+        const uint32_t issue = lane == 0 ? 1u : 0u;
         uint32_t kg = 0;
         bool ok = true;
         for (int64_t t = unit; t < total && ok; t += units) {
             for (int32_t k = 0; k < p.k_iters; ++k, ++kg) {
                 if ((kg & 1u) != par) continue;
                 const uint32_t stage = kg % C::kStages, phase = (kg / C::kStages) & 1u;
-                if (!wait_or_abort(smem_u32(&sh.full[stage]), phase, sh, p.status)) { ok = false; break; }
+                if (!__all_sync(0xFFFFFFFFu, wait_or_abort(smem_u32(&sh.full[stage]), phase, sh, p.status))) {
+                    ok = false;
+                    break;
+                }
                 const uint32_t buf = kg % kScrBufs, use = kg / kScrBufs;
-                if (use >= 1 && !wait_or_abort(smem_u32(&sh.scr_empty[buf]), (use - 1) & 1u, sh, p.status)) {
+                if (use >= 1 && !__all_sync(0xFFFFFFFFu, wait_or_abort(smem_u32(&sh.scr_empty[buf]), (use - 1) & 1u,
+                                                                       sh, p.status))) {
                     ok = false;
                     break;
                 }
@@ -716,16 +723,16 @@ gemm_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_constant__ C
 #pragma unroll
                 for (int kk = 0; kk < 4; ++kk) {
                     if constexpr (kPair == 2)
-                        mma_f8_pair(d, a_desc + 2 * kk, b_desc + 2 * kk, C::kIdescF32, kk != 0 ? 1u : 0u);
+                        mma_f8_pair_if(d, a_desc + 2 * kk, b_desc + 2 * kk, C::kIdescF32, kk != 0 ? 1u : 0u, issue);
                     else
-                        mma_f8(d, a_desc + 2 * kk, b_desc + 2 * kk, C::kIdescF32, kk != 0 ? 1u : 0u);
+                        mma_f8_if(d, a_desc + 2 * kk, b_desc + 2 * kk, C::kIdescF32, kk != 0 ? 1u : 0u, issue);
                 }
                 if constexpr (kPair == 2) {
-                    tc_commit_pair_mc(smem_u32(&sh.empty[stage]), 0x3);
-                    tc_commit_pair_mc(smem_u32(&sh.scr_full[buf]), 0x3);
+                    tc_commit_pair_mc_if(smem_u32(&sh.empty[stage]), 0x3, issue);
+                    tc_commit_pair_mc_if(smem_u32(&sh.scr_full[buf]), 0x3, issue);
                 } else {
-                    tc_commit(smem_u32(&sh.empty[stage]));
-                    tc_commit(smem_u32(&sh.scr_full[buf]));
+                    tc_commit_if(smem_u32(&sh.empty[stage]), issue);
+                    tc_commit_if(smem_u32(&sh.scr_full[buf]), issue);
                 }
             }
         }
@@ -762,7 +769,7 @@ gemm_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_constant__ C
         }
     } else if (warp == 1) {
         // ------------------------------------------------ MMA issuer (the MMA CTA)
-        if (lane == 0 && rank == 0 && kF32) {
+        if (rank == 0 && kF32) {
             mma_f32(0u);
         } else if (rank == 0 && !kF32) {
             // The whole warp runs the loop (its values stay warp-uniform) and
@@ -827,7 +834,7 @@ gemm_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_constant__ C
             }
         }
     } else if (kF32 && warp == kMma2Warp) {
-        if (lane == 0 && rank == 0) mma_f32(1u);
+        if (rank == 0) mma_f32(1u);
     } else if (warp == kSfWarp) {
         // ------------------------------------------------ scale-factor layout (every CTA)
         // Scale groups (4 K-steps each, the last of a tile possibly shorter)
