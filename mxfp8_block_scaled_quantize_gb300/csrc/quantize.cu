@@ -9,16 +9,22 @@
 // and a block holding NaN/inf gets s = 0xFF, q = 0x7F.
 //
 // Work decomposition.  The input is cut into units of 64 rows x 64 columns
-// (8 KB of bf16).  Every warp runs its own pipeline over a kStages-deep ring:
-// lane 0 loads units with TMA (128-byte swizzle, so both the row reads and the
-// column reads below are bank-conflict free) and the whole warp consumes them:
+// (8 KB of bf16), and units into strips of 8 along a band (64 x 512).  The
+// CTAs walk the strips with stride gridDim.x, so the strips in flight are
+// contiguous in memory; warp w of a CTA takes unit w of each strip.  Every
+// warp runs its own pipeline over a kStages-deep ring: lane 0 loads units
+// with TMA (128-byte swizzle, so both the row reads and the column reads below
+// are bank-conflict free) and the whole warp consumes them:
 //   column-wise: lane l owns columns 2l and 2l+1 (two 32-row blocks each);
 //   row-wise:    lane l owns rows l and l+32 (two 32-column blocks each).
 // Once every lane has read the unit, the codes (64 x 64 bytes per orientation)
 // are written into the same 8 KB of shared memory with a 64-byte swizzle and
 // leave with two TMA tensor stores, so global writes are whole lines instead
-// of 32 scattered sectors per instruction.  Scale bytes (2 per row or column
-// per unit) are stored directly.  Warps never wait on each other.
+// of 32 scattered sectors per instruction.  The row-wise scale bytes of a
+// strip (8 units x 2 per row) meet in shared memory and leave as one 16-byte
+// store per row after a barrier of the CTA's warps (per-unit stores of 2
+// bytes into each of 64 rows cost ~10 % of the kernel's time); column-wise
+// scale bytes (2 per column per unit) are stored directly.
 #include <cuda_bf16.h>
 #include <mutex>
 #include <cuda_runtime.h>
@@ -35,8 +41,8 @@ namespace {
 constexpr int kRows = 64;                    // unit height (two column-wise blocks)
 constexpr int kCols = 64;                    // unit width in bf16 (= 128-byte swizzle row)
 constexpr int kUnitBytes = kRows * kCols * 2;
-constexpr int kWarps = 12;
-constexpr int kStages = 2;
+constexpr int kWarps = 8;                    // = units per strip: 8 x 2 scale bytes = 16 per row
+constexpr int kStages = 3;
 constexpr int kSmemBytes = kWarps * kStages * kUnitBytes + 1024;
 static_assert(kRows == kDbiasBandRows, "bias-gradient bands are the unit rows");
 
@@ -132,6 +138,15 @@ __device__ __forceinline__ void col_sums(uint32_t tile, int lane, float& sum_lo,
     }
 }
 
+__device__ __forceinline__ void sts16(uint32_t addr, uint32_t v) {
+    asm volatile("st.shared.b16 [%0], %1;" :: "r"(addr), "h"(static_cast<uint16_t>(v)) : "memory");
+}
+
+// Barrier `id` over `n` threads (whole warps) of the CTA.
+__device__ __forceinline__ void named_barrier_sync(uint32_t id, uint32_t n) {
+    asm volatile("bar.sync %0, %1;" :: "r"(id), "r"(n) : "memory");
+}
+
 // Byte offset of 16-byte chunk c of 64-byte row r in a 64-byte-swizzled tile.
 __device__ __forceinline__ uint32_t sw64(int r, int c) { return uint32_t(r * 64 + ((c ^ ((r >> 1) & 3)) << 4)); }
 
@@ -141,21 +156,37 @@ quantize_kernel(const __grid_constant__ CUtensorMap x_map, const __grid_constant
                 const __grid_constant__ CUtensorMap qcol_map, const QuantizeParams p) {
     extern __shared__ uint8_t smem_raw[];
     __shared__ __align__(8) uint64_t bars[kWarps][kStages];
+    // row-wise scale bytes of a strip (64 rows x 16 bytes), double-buffered by round
+    __shared__ __align__(16) uint8_t row_scales[2][kRows][16];
 
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int64_t gwarp = int64_t(blockIdx.x) * kWarps + warp;
-    const int64_t nwarps = int64_t(gridDim.x) * kWarps;
     grid_dependency_wait();              // launched as a programmatic dependent: no global access before this
     grid_launch_dependents();
-    if (gwarp >= p.units) return;
-    const int64_t n_mine = (p.units - gwarp + nwarps - 1) / nwarps;
+    // The CTAs walk strips of kWarps units along a band (64 rows x 512 columns)
+    // with stride gridDim.x, so that the strips in flight are contiguous in
+    // memory; warp w takes unit w of each strip (or none past the band's end).
+    const int64_t strips_per_band = (p.col_units + kWarps - 1) / kWarps;
+    const int64_t n_strips = ((p.rows + kRows - 1) / kRows) * strips_per_band;
+    if (int64_t(blockIdx.x) >= n_strips) return;                         // (uniform over the CTA)
+    const int64_t n_mine = (n_strips - blockIdx.x + gridDim.x - 1) / gridDim.x;
     const uint32_t ring = smem_u32(smem + warp * (kStages * kUnitBytes));
-    // (band, column unit) of this unit and of the next load (lane 0)
-    const UnitWalk walk(nwarps, p.col_units);
-    int32_t band, col;
-    walk.start(gwarp, band, col);
-    int32_t lband = band, lcol = col;
+    // (band, strip) of this round and of the next load (lane 0)
+    const UnitWalk walk(gridDim.x, strips_per_band);
+    int32_t band, strip;
+    walk.start(blockIdx.x, band, strip);
+    int32_t lband = band, lstrip = strip;
+    auto unit_col = [&](int32_t st) { return st * kWarps + warp; };       // this warp's column unit
+    // lane 0: load this warp's unit of the round (or, past the band's end,
+    // complete the stage's barrier without data)
+    auto load = [&](uint32_t bar, uint32_t dst, int32_t b, int32_t st) {
+        if (unit_col(st) < p.col_units) {
+            mbar_arrive_expect_tx(bar, kUnitBytes);
+            tma_load_2d(dst, &x_map, bar, unit_col(st) * kCols, b * kRows);
+        } else {
+            mbar_arrive(bar);
+        }
+    };
 
     if (lane == 0) {
         tma_prefetch_desc(&x_map);
@@ -164,107 +195,127 @@ quantize_kernel(const __grid_constant__ CUtensorMap x_map, const __grid_constant
         for (int s = 0; s < kStages; ++s) mbar_init(smem_u32(&bars[warp][s]), 1);
         fence_mbarrier_init();
         for (int s = 0; s < kStages && s < n_mine; ++s) {
-            const uint32_t bar = smem_u32(&bars[warp][s]);
-            mbar_arrive_expect_tx(bar, kUnitBytes);
-            tma_load_2d(ring + s * kUnitBytes, &x_map, bar, lcol * kCols, lband * kRows);
-            walk.step(lband, lcol);
+            load(smem_u32(&bars[warp][s]), ring + s * kUnitBytes, lband, lstrip);
+            walk.step(lband, lstrip);
         }
     }
     __syncwarp();
 
     int s = 0;
     uint32_t parity = 0;
+    bool ok = true;                      // false once a wait gave up: the warp then only keeps the barriers
     for (int64_t i = 0; i < n_mine; ++i) {
         const uint32_t bar = smem_u32(&bars[warp][s]);
-        if (!__all_sync(0xFFFFFFFFu, mbar_wait(bar, parity, p.status))) {
+        const int32_t col = unit_col(strip);
+        const bool mine = col < p.col_units;
+        if (ok && !__all_sync(0xFFFFFFFFu, mbar_wait(bar, parity, p.status))) {
+            ok = false;
             if (lane == 0)                       // gave up: let this warp's loads still in flight land
                 for (int64_t j = i; j < i + kStages && j < n_mine; ++j)
                     mbar_wait(smem_u32(&bars[warp][j % kStages]), uint32_t((j / kStages) & 1), p.status);
-            break;
         }
         const uint32_t tile = ring + s * kUnitBytes;
         const int64_t r0 = int64_t(band) * kRows, c0 = int64_t(col) * kCols;
-
-        uint32_t cc[2][2][8];             // column codes [half][column 2l / 2l+1][words]
-        uint32_t rc[2][2][8];             // row codes [row l / l+32][block][words]
-        float sum_lo = 0.0f, sum_hi = 0.0f;               // bias-gradient band sums
-        if (kColwise) {
-            const bool second = r0 + 32 < p.rows;          // rows % 32 == 0 here
-            uint32_t s_lo[2] = {0, 0}, s_hi[2] = {0, 0};
-            col_blocks(tile, 0, lane, cc[0][0], cc[0][1], s_lo[0], s_hi[0], sum_lo, sum_hi);
-            col_blocks(tile, 32, lane, cc[1][0], cc[1][1], s_lo[1], s_hi[1], sum_lo, sum_hi);
-            const int64_t c = c0 + 2 * lane;
-            if (c < p.cols) {                              // cols % 32 == 0: c + 1 valid too
-                uint8_t* sp = p.s_col + c * p.ld_s_col + (r0 >> 5);
-                if (second) {
-                    st_global_u16(sp, s_lo[0] | (s_lo[1] << 8));
-                    st_global_u16(sp + p.ld_s_col, s_hi[0] | (s_hi[1] << 8));
-                } else {
-                    st_global_u8(sp, s_lo[0]);
-                    st_global_u8(sp + p.ld_s_col, s_hi[0]);
-                }
-            }
-        }
-        if (kDbias) {
-            if (!kColwise) col_sums(tile, lane, sum_lo, sum_hi);
-            const int64_t c = c0 + 2 * lane;
-            if (c < p.cols)                                // rows past the end were loaded as 0
-                *reinterpret_cast<float2*>(p.partial + (r0 / kDbiasBandRows) * p.cols + c) =
-                    make_float2(sum_lo, sum_hi);
-        }
-        if (kRowwise) {
-#pragma unroll
-            for (int rr = 0; rr < 2; ++rr) {
-                uint32_t sb[2];
-                row_blocks(tile + (lane + 32 * rr) * 128, lane & 7, rc[rr], sb);
-                const int64_t r = r0 + lane + 32 * rr;
-                if (r < p.rows) {
-                    uint8_t* sp = p.s_row + r * p.ld_s_row + (c0 >> 5);
-                    if (c0 + 32 < p.cols) st_global_u16(sp, sb[0] | (sb[1] << 8));
-                    else st_global_u8(sp, sb[0]);
-                }
-            }
-        }
-        __syncwarp();                     // every lane has read the unit: reuse it for the codes
-        if (kRowwise) {
-#pragma unroll
-            for (int rr = 0; rr < 2; ++rr) {
-                const int r = lane + 32 * rr;
-#pragma unroll
-                for (int c = 0; c < 4; ++c) {
-                    const uint32_t* w = rc[rr][c >> 1] + 4 * (c & 1);
-                    sts128(tile + sw64(r, c), w[0], w[1], w[2], w[3]);
-                }
-            }
-        }
-        if (kColwise) {
-#pragma unroll
-            for (int j = 0; j < 2; ++j) {
-                const int cl = 2 * lane + j;
-#pragma unroll
-                for (int h = 0; h < 2; ++h)
-#pragma unroll
-                    for (int t = 0; t < 2; ++t) {
-                        const uint32_t* w = cc[h][j] + 4 * t;
-                        sts128(tile + 4096 + sw64(cl, 2 * h + t), w[0], w[1], w[2], w[3]);
+        if (ok && mine) {
+            uint32_t cc[2][2][8];             // column codes [half][column 2l / 2l+1][words]
+            uint32_t rc[2][2][8];             // row codes [row l / l+32][block][words]
+            float sum_lo = 0.0f, sum_hi = 0.0f;               // bias-gradient band sums
+            if (kColwise) {
+                const bool second = r0 + 32 < p.rows;          // rows % 32 == 0 here
+                uint32_t s_lo[2] = {0, 0}, s_hi[2] = {0, 0};
+                col_blocks(tile, 0, lane, cc[0][0], cc[0][1], s_lo[0], s_hi[0], sum_lo, sum_hi);
+                col_blocks(tile, 32, lane, cc[1][0], cc[1][1], s_lo[1], s_hi[1], sum_lo, sum_hi);
+                const int64_t c = c0 + 2 * lane;
+                if (c < p.cols) {                              // cols % 32 == 0: c + 1 valid too
+                    uint8_t* sp = p.s_col + c * p.ld_s_col + (r0 >> 5);
+                    if (second) {
+                        st_global_u16(sp, s_lo[0] | (s_lo[1] << 8));
+                        st_global_u16(sp + p.ld_s_col, s_hi[0] | (s_hi[1] << 8));
+                    } else {
+                        st_global_u8(sp, s_lo[0]);
+                        st_global_u8(sp + p.ld_s_col, s_hi[0]);
                     }
+                }
+            }
+            if (kDbias) {
+                if (!kColwise) col_sums(tile, lane, sum_lo, sum_hi);
+                const int64_t c = c0 + 2 * lane;
+                if (c < p.cols)                                // rows past the end were loaded as 0
+                    *reinterpret_cast<float2*>(p.partial + (r0 / kDbiasBandRows) * p.cols + c) =
+                        make_float2(sum_lo, sum_hi);
+            }
+            if (kRowwise) {
+#pragma unroll
+                for (int rr = 0; rr < 2; ++rr) {
+                    uint32_t sb[2];
+                    row_blocks(tile + (lane + 32 * rr) * 128, lane & 7, rc[rr], sb);
+                    // this unit's two scale bytes at byte 2 warp of the strip's rows
+                    sts16(smem_u32(&row_scales[i & 1][lane + 32 * rr][2 * warp]), sb[0] | (sb[1] << 8));
+                }
+            }
+            __syncwarp();                     // every lane has read the unit: reuse it for the codes
+            if (kRowwise) {
+#pragma unroll
+                for (int rr = 0; rr < 2; ++rr) {
+                    const int r = lane + 32 * rr;
+#pragma unroll
+                    for (int c = 0; c < 4; ++c) {
+                        const uint32_t* w = rc[rr][c >> 1] + 4 * (c & 1);
+                        sts128(tile + sw64(r, c), w[0], w[1], w[2], w[3]);
+                    }
+                }
+            }
+            if (kColwise) {
+#pragma unroll
+                for (int j = 0; j < 2; ++j) {
+                    const int cl = 2 * lane + j;
+#pragma unroll
+                    for (int h = 0; h < 2; ++h)
+#pragma unroll
+                        for (int t = 0; t < 2; ++t) {
+                            const uint32_t* w = cc[h][j] + 4 * t;
+                            sts128(tile + 4096 + sw64(cl, 2 * h + t), w[0], w[1], w[2], w[3]);
+                        }
+                }
+            }
+            fence_proxy_async_smem();         // make the staged codes visible to the TMA engine
+            __syncwarp();
+            if (lane == 0) {
+                if (kRowwise) tma_store_2d(&qrow_map, tile, int32_t(c0), int32_t(r0));
+                if (kColwise) tma_store_2d(&qcol_map, tile + 4096, int32_t(r0), int32_t(c0));
+                bulk_commit();             // (an empty group when only the bias gradient is produced)
             }
         }
-        fence_proxy_async_smem();         // make the staged codes visible to the TMA engine
-        __syncwarp();
-        if (lane == 0) {
-            if (kRowwise) tma_store_2d(&qrow_map, tile, int32_t(c0), int32_t(r0));
-            if (kColwise) tma_store_2d(&qcol_map, tile + 4096, int32_t(r0), int32_t(c0));
-            bulk_commit();             // (an empty group when only the bias gradient is produced)
-            if (i + kStages < n_mine) {
-                bulk_wait_read_all();     // the stores have read the tile: refill it
-                mbar_arrive_expect_tx(bar, kUnitBytes);
-                tma_load_2d(tile, &x_map, bar, lcol * kCols, lband * kRows);
-                walk.step(lband, lcol);
-            }
+        if (ok && lane == 0 && i + kStages < n_mine) {
+            bulk_wait_read_all();         // the stores have read the tile: refill it
+            load(bar, tile, lband, lstrip);
+            walk.step(lband, lstrip);
         }
         __syncwarp();
-        walk.step(band, col);
+        if (kRowwise) {
+            // the strip's row scales: 16 bytes per row, one store per row (warps 0-1,
+            // lane = row); a strip cut by the band's end writes its bytes one by one
+            named_barrier_sync(1, kWarps * 32);
+            if (warp < 2) {
+                const int rl = warp * 32 + lane;
+                const int64_t r = r0 + rl;
+                const int64_t first = int64_t(strip) * kWarps * 2;             // the strip's first scale byte
+                const int64_t valid = (p.cols + 31) / 32 - first;               // scale bytes of the row left
+                if (r < p.rows) {
+                    uint8_t* sp = p.s_row + r * p.ld_s_row + first;
+                    const uint4 v = lds128(smem_u32(&row_scales[i & 1][rl][0]));
+                    if (valid >= 16) {
+                        st_global_v4(sp, v.x, v.y, v.z, v.w);
+                    } else {
+                        const uint32_t w4[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+                        for (int k = 0; k < 16; ++k)
+                            if (k < valid) st_global_u8(sp + k, (w4[k >> 2] >> (8 * (k & 3))) & 0xFFu);
+                    }
+                }
+            }
+        }
+        walk.step(band, strip);
         if (++s == kStages) {
             s = 0;
             parity ^= 1u;
@@ -303,7 +354,7 @@ cudaError_t launch(const CUtensorMap& xm, const CUtensorMap& qr, const CUtensorM
     auto k = quantize_kernel<R, C, D>;
     cudaError_t e = set_smem_attribute_once(reinterpret_cast<const void*>(k), kSmemBytes);
     if (e != cudaSuccess) return e;
-    const int64_t want = (p.units + kWarps - 1) / kWarps;
+    const int64_t want = ((p.rows + kRows - 1) / kRows) * ((p.col_units + kWarps - 1) / kWarps);   // strips
     const int grid = int(want < sms ? want : sms);
     // programmatic dependent launch: the CTAs may start while the previous
     // kernel in the stream finishes (the kernel waits before touching memory)
