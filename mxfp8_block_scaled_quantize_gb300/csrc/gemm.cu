@@ -33,6 +33,12 @@
 //               CTA's 128 x 256 accumulator into registers, releases TMEM at
 //               once (so the next tile's MMAs overlap this tile's epilogue),
 //               then applies bias / GELU and stores bf16 D (and AUX).
+// FP32 block scales (Float8BlockScaling) use the same tiles with 12 warps in
+// three warp groups: warps 0-3 producer, MMA issuer, scale warp and a second
+// MMA issuer (registers lowered to 64 per thread), warps 4-11 epilogue
+// (raised to 216): every K-step's product lands in one of two 256-column TMEM
+// buffers and each epilogue thread adds it, scaled, to the 128 accumulator
+// columns of its row that it keeps in registers.
 // Every mbarrier wait is bounded; a wait that gives up aborts the CTA cleanly
 // and sets the device status word.
 #include <cuda_runtime.h>
@@ -49,28 +55,32 @@ constexpr int kBM = 128;                 // accumulator rows per CTA (TMEM lanes
 constexpr int kBN = 256;                 // tile columns (accumulator columns)
 constexpr int kBK = 128;                 // K per pipeline stage (bytes of E4M3)
 constexpr int kThreads = 352;          // 11 warps; FP32 scales: 12 (a second MMA issuer)
-constexpr int kMma2Warp = 11;
+constexpr int kMma2Warp = 3;             // FP32 scales only
 constexpr int kEpiWarps = 8;
-constexpr int kSfWarp = 10;
 constexpr int kGroupM = 16;              // m-tiles per raster band (L2 reuse of B)
 constexpr int kMaxGroups = 1024;
 constexpr int kSFABytes = kBM * 16;      // 128 rows x 16 scale bytes (4 K-steps)
 constexpr int kSfRing = 3;               // scale-group slots in shared memory
 constexpr int kSfAhead = 2;              // scale groups loaded ahead of the one being prepared
 constexpr int kSfTmemGroups = 4;         // scale groups resident in TMEM
-constexpr int kScrBufs = 4;              // FP32 scales: K-step product buffers in TMEM (128 columns each)
+constexpr int kScrBufs = 2;              // FP32 scales: K-step product buffers in TMEM (256 columns each)
+// FP32 scales: registers per thread after the split (warp group 0 / 1 and 2);
+// 4 x 64 + 8 x 216 = 1984 <= 12 x 168, the launch's 168 per thread
+constexpr int kRegsRoles = 64;
+constexpr int kRegsEpi = 216;
 
-// kF32 (Float8BlockScaling with FP32 scales): 128-column tiles, so that an
-// epilogue thread keeps its 64 accumulator columns in registers while the
-// K-step products rotate through kScrBufs TMEM buffers.
+// kF32 (Float8BlockScaling with FP32 scales): the same 256-column tiles; the
+// warp roles move so that the 8 epilogue warps form warp groups 1 and 2.
 template <int kPair, bool kF32 = false>
 struct Cfg {
     static constexpr int kTileM = kBM * kPair;            // rows of one (pair) tile
-    static constexpr int kBN = kF32 ? 128 : ::temx::kBN;  // tile columns
+    static constexpr int kBN = ::temx::kBN;               // tile columns
     static constexpr int kBRows = kBN / kPair;            // B rows loaded per CTA
     static constexpr int kABytes = kBM * kBK;             // 16 KB
-    static constexpr int kBBytes = kBRows * kBK;          // 32, 16 or 8 KB
-    static constexpr int kStages = kF32 ? (kPair == 2 ? 6 : 5) : (kPair == 2 ? 5 : 4);
+    static constexpr int kBBytes = kBRows * kBK;          // 32 or 16 KB
+    static constexpr int kStages = kPair == 2 ? 5 : 4;
+    static constexpr int kSfWarp = kF32 ? 2 : 10;         // scale-factor warp
+    static constexpr int kEpiWarp0 = kF32 ? 4 : 2;        // first epilogue warp
     static constexpr int kStageBytes = kABytes + kBBytes;
     static constexpr int kSFBBytes = kBN * 16;            // every CTA holds all of the tile's B rows' scales
     static constexpr int kSfSlotBytes = kSFABytes + kSFBBytes;   // one scale group (4 K-steps) in the ring
@@ -112,6 +122,7 @@ constexpr uint32_t kSfCol0 = 256;
 constexpr uint32_t kSfSlotCols = 12;
 constexpr uint32_t kSfSlots = 16;
 static_assert(kScrBufs * Cfg<2, true>::kBN <= int(kTmemCols), "FP32-scale product buffers fit in TMEM");
+static_assert(4 * kRegsRoles + 8 * kRegsEpi <= 12 * 168, "FP32-scale register split");
 
 struct GemmParams {
     int64_t M;               // dense: rows of A/D; grouped: total_m (rows of X/D)
@@ -160,7 +171,7 @@ struct __align__(16) SharedState {
     uint64_t tmem_empty;                   // (MMA CTA) accumulator drained by the epilogue of every CTA
     uint64_t epi_drained;                  // this CTA's 8 epilogue warps hold their accumulator rows
     // FP32-scale mode: K-step kg's product lands in TMEM buffer kg % kScrBufs
-    // (columns 128 * buffer ..; the scaled accumulator lives in registers)
+    // (columns 256 * buffer ..; the scaled accumulator lives in registers)
     uint64_t scr_full[kScrBufs];           // a product landed (each CTA)
     uint64_t scr_empty[kScrBufs];          // (MMA CTA) the epilogue warps of both CTAs read that buffer
     uint64_t sf_done[kSfRing];             // this CTA's epilogue warps are done with a scale group
@@ -609,6 +620,44 @@ __device__ __forceinline__ void store_64_staged(uint32_t* acc, const GemmParams&
     }
 }
 
+// FP32 scales: acc[j] += v[j] * (sA sB) for 64 columns of one row.  2D weight
+// blocks: one factor f = sA sB for all of them, acc = fma(v, f, acc);
+// otherwise sB per column from the [4 K-steps][256 columns] shared table at
+// sbt: acc = fma(v sB, sA, acc).  Packed pairs (f32x2: each half rounds as the
+// scalar mul / fma does).
+__device__ __forceinline__ void scale_accumulate_64(uint32_t (&acc)[64], const uint32_t (&v)[64], bool b_2d, float f,
+                                                    float sa, uint32_t sbt) {
+    if (b_2d) {
+#pragma unroll
+        for (int j = 0; j < 64; j += 2) {
+            uint64_t a2, v2, f2;
+            asm("mov.b64 %0, {%1, %2};" : "=l"(a2) : "r"(acc[j]), "r"(acc[j + 1]));
+            asm("mov.b64 %0, {%1, %2};" : "=l"(v2) : "r"(v[j]), "r"(v[j + 1]));
+            asm("mov.b64 %0, {%1, %1};" : "=l"(f2) : "r"(__float_as_uint(f)));
+            asm("fma.rn.f32x2 %0, %1, %2, %0;" : "+l"(a2) : "l"(v2), "l"(f2));
+            asm("mov.b64 {%0, %1}, %2;" : "=r"(acc[j]), "=r"(acc[j + 1]) : "l"(a2));
+        }
+    } else {
+        uint64_t sa2;
+        asm("mov.b64 %0, {%1, %1};" : "=l"(sa2) : "r"(__float_as_uint(sa)));
+#pragma unroll
+        for (int j4 = 0; j4 < 16; ++j4) {
+            const uint4 w = lds128(sbt + 16 * j4);
+#pragma unroll
+            for (int i = 0; i < 4; i += 2) {
+                const int j = 4 * j4 + i;
+                uint64_t a2, v2, s2;
+                asm("mov.b64 %0, {%1, %2};" : "=l"(a2) : "r"(acc[j]), "r"(acc[j + 1]));
+                asm("mov.b64 %0, {%1, %2};" : "=l"(v2) : "r"(v[j]), "r"(v[j + 1]));
+                asm("mov.b64 %0, {%1, %2};" : "=l"(s2) : "r"(i == 0 ? w.x : w.z), "r"(i == 0 ? w.y : w.w));
+                asm("mul.rn.f32x2 %0, %0, %1;" : "+l"(v2) : "l"(s2));
+                asm("fma.rn.f32x2 %0, %1, %2, %0;" : "+l"(a2) : "l"(v2), "l"(sa2));
+                asm("mov.b64 {%0, %1}, %2;" : "=r"(acc[j]), "=r"(acc[j + 1]) : "l"(a2));
+            }
+        }
+    }
+}
+
 // kAcc: fp32 D accumulated into; kWgrad: grouped wgrad; kF32: Float8BlockScaling
 // operands with FP32 scales (dense only): every K-step's product lands in one
 // of kScrBufs TMEM buffers and the epilogue warps accumulate it, scaled, in
@@ -687,14 +736,14 @@ gemm_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_constant__ C
     const uint32_t tmem = sh.tmem_base;
     const int64_t total = p.groups > 0 ? sh.grouped_tiles : p.total_tiles;
 
-    // FP32 scales: MMA issuer for the K-steps of one parity: 4 MMAs (N = 128,
-    // K = 32 each) per K-step into product buffer kg % kScrBufs, once the
-    // epilogue warps of both CTAs read that buffer's previous product (K-step
-    // kg - kScrBufs).  Two issuers (warps 1 and kMma2Warp) alternate K-steps,
-    // so that one can wait for its operands or its buffer while the other
-    // issues (a thread's tcgen05.mma issue blocks while the tensor pipe is
-    // busy).  Four buffers let the MMAs run up to three K-steps ahead of the
-    // epilogue (and on into the next tile while the epilogue stores one).
+    // FP32 scales: MMA issuer for the K-steps of one parity: 4 MMAs (N = 256,
+    // K = 32 each) per K-step into product buffer kg % kScrBufs (= the parity),
+    // once the epilogue warps of both CTAs read that buffer's previous product
+    // (K-step kg - kScrBufs).  Two issuers (warps 1 and kMma2Warp) alternate
+    // K-steps, so that one can wait for its operands or its buffer while the
+    // other issues (a thread's tcgen05.mma issue blocks while the tensor pipe
+    // is busy).  The MMAs run up to one K-step ahead of the epilogue, and on
+    // into the next tile while the epilogue stores one.
     // (run by a whole warp, values warp-uniform; lane 0's tcgen05 operations
     // are predicated on)
     auto mma_f32 = [&](uint32_t par) {
@@ -738,243 +787,258 @@ gemm_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_constant__ C
         }
     };
 
-    if (warp == 0) {
-        // ------------------------------------------------ TMA producer (every CTA)
-        if (lane == 0) {
-            int32_t hint = 0;
-            uint32_t stage = 0, phase = 0;
-            bool ok = true;
-            for (int64_t t = unit; t < total && ok; t += units) {
-                const Tile tl = map_tile<C::kTileM, C::kBN, kWgrad>(p, sh, t, hint);
-                const int32_t a_row = tl.a_row + int32_t(rank) * kBM;
-                const int32_t b_row = tl.b_row + int32_t(rank) * C::kBRows;
-                for (int32_t k = 0; k < tl.nk; ++k) {
-                    const int32_t kx = (tl.k0 + k) * kBK;
-                    if (!wait_or_abort(smem_u32(&sh.empty[stage]), phase ^ 1u, sh, p.status)) { ok = false; break; }
-                    uint8_t* st = smem + stage * C::kStageBytes;
-                    const uint32_t full = leader(sh.full[stage]);
-                    if constexpr (kPair == 2) {
-                        if (rank == 0) mbar_arrive_expect_tx(smem_u32(&sh.full[stage]), C::kABytes + C::kBBytes);
-                        else mbar_arrive_expect_tx_cluster_relaxed(full, C::kABytes + C::kBBytes);
-                        tma_load_2d_pair(smem_u32(st), &map_a, full, kx, a_row);
-                        tma_load_2d_pair(smem_u32(st + C::kABytes), &map_b, full, kx, b_row);
-                    } else {
-                        mbar_arrive_expect_tx(full, C::kABytes + C::kBBytes);
-                        tma_load_2d(smem_u32(st), &map_a, full, kx, a_row);
-                        tma_load_2d(smem_u32(st + C::kABytes), &map_b, full, kx, b_row);
+    // Role warps (for FP32 scales warp group 0) and epilogue warps.  With FP32
+    // scales the role warp group gives registers to the epilogue warp groups,
+    // whose threads hold 128 accumulator columns and a product slice each
+    // (the host checked that the split fits); each side changes its count
+    // first, before the warps of a group part ways.
+    const bool role_warp = kF32 ? warp < 4 : (warp < 2 || warp == C::kSfWarp);
+    if (role_warp) {
+        if constexpr (kF32) regs_lower<kRegsRoles>();
+        if (warp == 0) {
+            // ------------------------------------------------ TMA producer (every CTA)
+            if (lane == 0) {
+                int32_t hint = 0;
+                uint32_t stage = 0, phase = 0;
+                bool ok = true;
+                for (int64_t t = unit; t < total && ok; t += units) {
+                    const Tile tl = map_tile<C::kTileM, C::kBN, kWgrad>(p, sh, t, hint);
+                    const int32_t a_row = tl.a_row + int32_t(rank) * kBM;
+                    const int32_t b_row = tl.b_row + int32_t(rank) * C::kBRows;
+                    for (int32_t k = 0; k < tl.nk; ++k) {
+                        const int32_t kx = (tl.k0 + k) * kBK;
+                        if (!wait_or_abort(smem_u32(&sh.empty[stage]), phase ^ 1u, sh, p.status)) { ok = false; break; }
+                        uint8_t* st = smem + stage * C::kStageBytes;
+                        const uint32_t full = leader(sh.full[stage]);
+                        if constexpr (kPair == 2) {
+                            if (rank == 0) mbar_arrive_expect_tx(smem_u32(&sh.full[stage]), C::kABytes + C::kBBytes);
+                            else mbar_arrive_expect_tx_cluster_relaxed(full, C::kABytes + C::kBBytes);
+                            tma_load_2d_pair(smem_u32(st), &map_a, full, kx, a_row);
+                            tma_load_2d_pair(smem_u32(st + C::kABytes), &map_b, full, kx, b_row);
+                        } else {
+                            mbar_arrive_expect_tx(full, C::kABytes + C::kBBytes);
+                            tma_load_2d(smem_u32(st), &map_a, full, kx, a_row);
+                            tma_load_2d(smem_u32(st + C::kABytes), &map_b, full, kx, b_row);
+                        }
+                        if (++stage == C::kStages) { stage = 0; phase ^= 1u; }
                     }
-                    if (++stage == C::kStages) { stage = 0; phase ^= 1u; }
                 }
             }
-        }
-    } else if (warp == 1) {
-        // ------------------------------------------------ MMA issuer (the MMA CTA)
-        if (rank == 0 && kF32) {
-            mma_f32(0u);
-        } else if (rank == 0 && !kF32) {
-            // The whole warp runs the loop (its values stay warp-uniform) and
-            // lane 0's tcgen05.mma / tcgen05.commit are predicated on: about 4 %
-            // fewer cycles per K-step than a loop that lane 0 runs alone.
-            const uint32_t issue = lane == 0 ? 1u : 0u;
-            uint32_t stage = 0, phase = 0, grp = 0;   // grp: global index of the current scale group
-            int32_t local = 0, hint = 0;
-            bool ok = true;
-            for (int64_t t = unit; t < total && ok; t += units, ++local) {
-                // K-steps of this tile (wgrad: the expert's own; 0 for an expert without tokens)
-                int32_t nk = p.k_iters;
-                if constexpr (kWgrad) nk = map_tile<C::kTileM, C::kBN, kWgrad>(p, sh, t, hint).nk;
-                if (local > 0) {
-                    if (!__all_sync(0xFFFFFFFFu, wait_or_abort(smem_u32(&sh.tmem_empty), uint32_t(local - 1) & 1u, sh,
-                                                               p.status)))
-                        break;
-                    tc_fence_after();
-                }
-                for (int32_t k = 0; k < nk; ++k) {
-                    if (!__all_sync(0xFFFFFFFFu, wait_or_abort(smem_u32(&sh.full[stage]), phase, sh, p.status))) {
-                        ok = false;
-                        break;
+        } else if (warp == 1) {
+            // ------------------------------------------------ MMA issuer (the MMA CTA)
+            if (rank == 0 && kF32) {
+                mma_f32(0u);
+            } else if (rank == 0 && !kF32) {
+                // The whole warp runs the loop (its values stay warp-uniform) and
+                // lane 0's tcgen05.mma / tcgen05.commit are predicated on: about 4 %
+                // fewer cycles per K-step than a loop that lane 0 runs alone.
+                const uint32_t issue = lane == 0 ? 1u : 0u;
+                uint32_t stage = 0, phase = 0, grp = 0;   // grp: global index of the current scale group
+                int32_t local = 0, hint = 0;
+                bool ok = true;
+                for (int64_t t = unit; t < total && ok; t += units, ++local) {
+                    // K-steps of this tile (wgrad: the expert's own; 0 for an expert without tokens)
+                    int32_t nk = p.k_iters;
+                    if constexpr (kWgrad) nk = map_tile<C::kTileM, C::kBN, kWgrad>(p, sh, t, hint).nk;
+                    if (local > 0) {
+                        if (!__all_sync(0xFFFFFFFFu, wait_or_abort(smem_u32(&sh.tmem_empty), uint32_t(local - 1) & 1u, sh,
+                                                                   p.status)))
+                            break;
+                        tc_fence_after();
                     }
-                    uint8_t* st = smem + stage * C::kStageBytes;
-                    if ((k & 3) == 0) {
-                        if (!__all_sync(0xFFFFFFFFu, wait_or_abort(smem_u32(&sh.sf_ready[grp % kSfRing]),
-                                                                   (grp / kSfRing) & 1u, sh, p.status))) {
+                    for (int32_t k = 0; k < nk; ++k) {
+                        if (!__all_sync(0xFFFFFFFFu, wait_or_abort(smem_u32(&sh.full[stage]), phase, sh, p.status))) {
                             ok = false;
                             break;
                         }
-                        tc_fence_after();
+                        uint8_t* st = smem + stage * C::kStageBytes;
+                        if ((k & 3) == 0) {
+                            if (!__all_sync(0xFFFFFFFFu, wait_or_abort(smem_u32(&sh.sf_ready[grp % kSfRing]),
+                                                                       (grp / kSfRing) & 1u, sh, p.status))) {
+                                ok = false;
+                                break;
+                            }
+                            tc_fence_after();
+                        }
+                        const uint32_t sf_col =
+                            tmem + kSfCol0 + ((grp % kSfTmemGroups) * 4 + uint32_t(k & 3)) * kSfSlotCols;
+                        const uint64_t a_desc = smem_desc(smem_u32(st), 16, 1024, 2);
+                        const uint64_t b_desc = smem_desc(smem_u32(st + C::kABytes), 16, 1024, 2);
+    #pragma unroll
+                        for (int kk = 0; kk < 4; ++kk) {
+                            // +32 bytes along K inside the 128-byte swizzled row = +2 in the address field
+                            const uint32_t idesc = idesc_sf(C::kIdescBase, uint32_t(kk));
+                            const uint32_t acc = (k | kk) != 0 ? 1u : 0u;
+                            if constexpr (kPair == 2)
+                                mma_mxf8_pair_if(tmem, a_desc + 2 * kk, b_desc + 2 * kk, idesc, sf_col, sf_col + 4, acc,
+                                                 issue);
+                            else
+                                mma_mxf8_if(tmem, a_desc + 2 * kk, b_desc + 2 * kk, idesc, sf_col, sf_col + 4, acc, issue);
+                        }
+                        if constexpr (kPair == 2) tc_commit_pair_mc_if(smem_u32(&sh.empty[stage]), 0x3, issue);
+                        else tc_commit_if(smem_u32(&sh.empty[stage]), issue);
+                        if ((k & 3) == 3 || k == nk - 1) {             // last K-step of the scale group
+                            if constexpr (kPair == 2)
+                                tc_commit_pair_mc_if(smem_u32(&sh.grp_done[grp % kSfTmemGroups]), 0x1, issue);
+                            else tc_commit_if(smem_u32(&sh.grp_done[grp % kSfTmemGroups]), issue);
+                            ++grp;
+                        }
+                        if (++stage == C::kStages) { stage = 0; phase ^= 1u; }
                     }
-                    const uint32_t sf_col =
-                        tmem + kSfCol0 + ((grp % kSfTmemGroups) * 4 + uint32_t(k & 3)) * kSfSlotCols;
-                    const uint64_t a_desc = smem_desc(smem_u32(st), 16, 1024, 2);
-                    const uint64_t b_desc = smem_desc(smem_u32(st + C::kABytes), 16, 1024, 2);
-#pragma unroll
-                    for (int kk = 0; kk < 4; ++kk) {
-                        // +32 bytes along K inside the 128-byte swizzled row = +2 in the address field
-                        const uint32_t idesc = idesc_sf(C::kIdescBase, uint32_t(kk));
-                        const uint32_t acc = (k | kk) != 0 ? 1u : 0u;
-                        if constexpr (kPair == 2)
-                            mma_mxf8_pair_if(tmem, a_desc + 2 * kk, b_desc + 2 * kk, idesc, sf_col, sf_col + 4, acc,
-                                             issue);
-                        else
-                            mma_mxf8_if(tmem, a_desc + 2 * kk, b_desc + 2 * kk, idesc, sf_col, sf_col + 4, acc, issue);
-                    }
-                    if constexpr (kPair == 2) tc_commit_pair_mc_if(smem_u32(&sh.empty[stage]), 0x3, issue);
-                    else tc_commit_if(smem_u32(&sh.empty[stage]), issue);
-                    if ((k & 3) == 3 || k == nk - 1) {             // last K-step of the scale group
-                        if constexpr (kPair == 2)
-                            tc_commit_pair_mc_if(smem_u32(&sh.grp_done[grp % kSfTmemGroups]), 0x1, issue);
-                        else tc_commit_if(smem_u32(&sh.grp_done[grp % kSfTmemGroups]), issue);
-                        ++grp;
-                    }
-                    if (++stage == C::kStages) { stage = 0; phase ^= 1u; }
+                    if (!ok) break;
+                    if constexpr (kPair == 2) tc_commit_pair_mc_if(smem_u32(&sh.tmem_full), 0x3, issue);
+                    else tc_commit_if(smem_u32(&sh.tmem_full), issue);
                 }
-                if (!ok) break;
-                if constexpr (kPair == 2) tc_commit_pair_mc_if(smem_u32(&sh.tmem_full), 0x3, issue);
-                else tc_commit_if(smem_u32(&sh.tmem_full), issue);
             }
-        }
-    } else if (kF32 && warp == kMma2Warp) {
-        if (rank == 0) mma_f32(1u);
-    } else if (warp == kSfWarp) {
-        // ------------------------------------------------ scale-factor layout (every CTA)
-        // Scale groups (4 K-steps each, the last of a tile possibly shorter)
-        // go through a kSfRing-slot ring: lane 0 loads group j + kSfAhead
-        // while group j is prepared.  Group j is copied into TMEM only after
-        // the MMAs of group j - 3 completed (grp_done); that keeps its TMEM
-        // slots free and also means the MMA warp has passed its wait on
-        // sf_ready of group j - 3, the previous user of this ring slot.  A ring
-        // slot is reloaded only after the copies of its previous group landed
-        // (sf_ready).  So every barrier phase here is observed by its waiter
-        // before the barrier can complete again.
-        uint8_t* ring = smem + C::kStages * C::kStageBytes;
-        auto tile_groups = [](const Tile& t) { return (t.nk + 3) / 4; };
-        int64_t lt = unit;                // next group to load: tile lt, group lg
-        int32_t lg = 0, lhint = 0;
-        uint32_t jl = 0;                  // its global index
-        Tile ltl{};
-        auto seek = [&]() {               // the first tile from lt on that has scale groups
-            for (; lt < total; lt += units) {
-                ltl = map_tile<C::kTileM, C::kBN, kWgrad>(p, sh, lt, lhint);
-                if (tile_groups(ltl) > 0) break;
-            }
-        };
-        seek();
-        bool ok = true;
-        auto load_next = [&]() -> bool {  // lane 0
-            if (lt >= total) return true;
-            const uint32_t slot = jl % kSfRing;
-            // reuse a slot once its previous group is consumed: copied into
-            // TMEM (MX), or read by this CTA's epilogue warps (FP32 scales)
-            if (jl >= kSfRing &&
-                !wait_or_abort(smem_u32(kF32 ? &sh.sf_done[slot] : &sh.sf_ready[slot]), ((jl / kSfRing) - 1) & 1u,
-                               sh, p.status))
-                return false;
-            const uint32_t bar = smem_u32(&sh.sf_full[slot]);
-            const uint32_t dst = smem_u32(ring + slot * C::kSfSlotBytes);
-            mbar_arrive_expect_tx(bar, kSFABytes + C::kSFBBytes);
-            tma_load_2d(dst, &map_sfa, bar, ltl.sf0 + lg * 16, ltl.a_row + int32_t(rank) * kBM);
-            tma_load_2d(dst + kSFABytes, &map_sfb, bar, ltl.sf0 + lg * 16, ltl.b_row);
-            ++jl;
-            if (++lg == tile_groups(ltl)) {
-                lg = 0;
-                lt += units;
-                seek();
-            }
-            return true;
-        };
-        if (lane == 0)
-            for (int i = 0; i < kSfAhead && ok; ++i) ok = load_next();
-        ok = __shfl_sync(0xFFFFFFFFu, ok, 0);
-        uint32_t j = 0;
-        int32_t chint = 0;
-        for (int64_t t = unit; t < total && ok; t += units) {
-            const Tile ct = map_tile<C::kTileM, C::kBN, kWgrad>(p, sh, t, chint);
-            const int32_t ngroups = tile_groups(ct);
-            for (int32_t g = 0; g < ngroups && ok; ++g, ++j) {
-                const uint32_t slot = j % kSfRing, bit = (j / kSfRing) & 1u;
-                if (!wait_or_abort(smem_u32(&sh.sf_full[slot]), bit, sh, p.status)) { ok = false; break; }
-                const uint32_t sf = smem_u32(ring + slot * C::kSfSlotBytes);
-                if constexpr (kF32) {
-                    // B's scales [128 columns][4 K-steps] -> [4 K-steps][128 columns] (fp32), so
-                    // that the epilogue reads 4 consecutive columns' scales at once; A's stay
-                    // [128 rows][4 K-steps].  The whole warp reads before anyone writes.
-                    static_assert(C::kBN == 128, "one B row block of 128 columns per tile");
-                    uint4 v[4];
-#pragma unroll
-                    for (int i = 0; i < 4; ++i) v[i] = lds128(sf + kSFABytes + (4 * lane + i) * 16);
-                    __syncwarp();
-                    const uint32_t w = sf + kSFABytes + 16 * lane;
-                    sts128(w, v[0].x, v[1].x, v[2].x, v[3].x);
-                    sts128(w + 512, v[0].y, v[1].y, v[2].y, v[3].y);
-                    sts128(w + 1024, v[0].z, v[1].z, v[2].z, v[3].z);
-                    sts128(w + 1536, v[0].w, v[1].w, v[2].w, v[3].w);
-                    fence_proxy_async_smem();            // the slot is next written by TMA
+        } else if (kF32 && warp == kMma2Warp) {
+            if (rank == 0) mma_f32(1u);
+        } else {                                   // the scale-factor warp
+            // ------------------------------------------------ scale-factor layout (every CTA)
+            // Scale groups (4 K-steps each, the last of a tile possibly shorter)
+            // go through a kSfRing-slot ring: lane 0 loads group j + kSfAhead
+            // while group j is prepared.  Group j is copied into TMEM only after
+            // the MMAs of group j - 3 completed (grp_done); that keeps its TMEM
+            // slots free and also means the MMA warp has passed its wait on
+            // sf_ready of group j - 3, the previous user of this ring slot.  A ring
+            // slot is reloaded only after the copies of its previous group landed
+            // (sf_ready).  So every barrier phase here is observed by its waiter
+            // before the barrier can complete again.
+            uint8_t* ring = smem + C::kStages * C::kStageBytes;
+            auto tile_groups = [](const Tile& t) { return (t.nk + 3) / 4; };
+            int64_t lt = unit;                // next group to load: tile lt, group lg
+            int32_t lg = 0, lhint = 0;
+            uint32_t jl = 0;                  // its global index
+            Tile ltl{};
+            auto seek = [&]() {               // the first tile from lt on that has scale groups
+                for (; lt < total; lt += units) {
+                    ltl = map_tile<C::kTileM, C::kBN, kWgrad>(p, sh, lt, lhint);
+                    if (tile_groups(ltl) > 0) break;
+                }
+            };
+            seek();
+            bool ok = true;
+            auto load_next = [&]() -> bool {  // lane 0
+                if (lt >= total) return true;
+                const uint32_t slot = jl % kSfRing;
+                // reuse a slot once its previous group is consumed: copied into
+                // TMEM (MX), or read by this CTA's epilogue warps (FP32 scales)
+                if (jl >= kSfRing &&
+                    !wait_or_abort(smem_u32(kF32 ? &sh.sf_done[slot] : &sh.sf_ready[slot]), ((jl / kSfRing) - 1) & 1u,
+                                   sh, p.status))
+                    return false;
+                const uint32_t bar = smem_u32(&sh.sf_full[slot]);
+                const uint32_t dst = smem_u32(ring + slot * C::kSfSlotBytes);
+                mbar_arrive_expect_tx(bar, kSFABytes + C::kSFBBytes);
+                tma_load_2d(dst, &map_sfa, bar, ltl.sf0 + lg * 16, ltl.a_row + int32_t(rank) * kBM);
+                tma_load_2d(dst + kSFABytes, &map_sfb, bar, ltl.sf0 + lg * 16, ltl.b_row);
+                ++jl;
+                if (++lg == tile_groups(ltl)) {
+                    lg = 0;
+                    lt += units;
+                    seek();
+                }
+                return true;
+            };
+            if (lane == 0)
+                for (int i = 0; i < kSfAhead && ok; ++i) ok = load_next();
+            ok = __shfl_sync(0xFFFFFFFFu, ok, 0);
+            uint32_t j = 0;
+            int32_t chint = 0;
+            for (int64_t t = unit; t < total && ok; t += units) {
+                const Tile ct = map_tile<C::kTileM, C::kBN, kWgrad>(p, sh, t, chint);
+                const int32_t ngroups = tile_groups(ct);
+                for (int32_t g = 0; g < ngroups && ok; ++g, ++j) {
+                    const uint32_t slot = j % kSfRing, bit = (j / kSfRing) & 1u;
+                    if (!wait_or_abort(smem_u32(&sh.sf_full[slot]), bit, sh, p.status)) { ok = false; break; }
+                    const uint32_t sf = smem_u32(ring + slot * C::kSfSlotBytes);
+                    if constexpr (kF32) {
+                        // B's scales [256 columns][4 K-steps] -> [4 K-steps][256 columns] (fp32), so
+                        // that the epilogue reads 4 consecutive columns' scales at once; A's stay
+                        // [128 rows][4 K-steps].  The whole warp reads before anyone writes.
+                        static_assert(C::kBN == 256, "the transpose covers 256 B rows");
+                        uint4 v[8];
+    #pragma unroll
+                        for (int i = 0; i < 8; ++i) v[i] = lds128(sf + kSFABytes + (128 * (i >> 2) + 4 * lane + (i & 3)) * 16);
+                        __syncwarp();
+    #pragma unroll
+                        for (int hb = 0; hb < 2; ++hb) {       // columns 128 hb + 4 lane .. + 3
+                            const uint32_t w = sf + kSFABytes + 512 * hb + 16 * lane;
+                            const uint4* u = v + 4 * hb;
+                            sts128(w, u[0].x, u[1].x, u[2].x, u[3].x);
+                            sts128(w + 1024, u[0].y, u[1].y, u[2].y, u[3].y);
+                            sts128(w + 2048, u[0].z, u[1].z, u[2].z, u[3].z);
+                            sts128(w + 3072, u[0].w, u[1].w, u[2].w, u[3].w);
+                        }
+                        fence_proxy_async_smem();            // the slot is next written by TMA
+                        __syncwarp();
+                        if (lane == 0) {
+                            mbar_arrive(smem_u32(&sh.sf_ready[slot]));
+                            ok = load_next();
+                        }
+                        ok = __shfl_sync(0xFFFFFFFFu, ok, 0);
+                        continue;
+                    }
+                    sf_to_tmem_layout(sf, lane);
+                    fence_proxy_async_smem();
                     __syncwarp();
                     if (lane == 0) {
-                        mbar_arrive(smem_u32(&sh.sf_ready[slot]));
-                        ok = load_next();
+                        if (kPair == 2 && rank != 0) {
+                            mbar_arrive_cluster(leader(sh.sf_peer[slot]));
+                        } else {
+                            if (kPair == 2) ok = wait_or_abort(smem_u32(&sh.sf_peer[slot]), bit, sh, p.status);
+                            if (ok && j >= 3)
+                                ok = wait_or_abort(smem_u32(&sh.grp_done[(j - 3) % kSfTmemGroups]),
+                                                   ((j - 3) / kSfTmemGroups) & 1u, sh, p.status);
+                            if (ok) {
+                                tc_fence_after();
+                                const int nchunks = min(4, ct.nk - 4 * g);
+                                for (int c = 0; c < nchunks; ++c) {
+                                    const uint32_t col = tmem + kSfCol0 + ((j % kSfTmemGroups) * 4 + c) * kSfSlotCols;
+                                    const uint64_t d0 = smem_desc(sf + c * 512, 0, 128, 0);
+                                    const uint64_t d1 = smem_desc(sf + 2048 + c * 512, 0, 128, 0);
+                                    const uint64_t d2 = smem_desc(sf + 4096 + c * 512, 0, 128, 0);
+                                    if constexpr (kPair == 2) {
+                                        tc_cp_32x128b_warpx4_pair(col + 0, d0);
+                                        tc_cp_32x128b_warpx4_pair(col + 4, d1);
+                                        tc_cp_32x128b_warpx4_pair(col + 8, d2);
+                                    } else {
+                                        tc_cp_32x128b_warpx4(col + 0, d0);
+                                        tc_cp_32x128b_warpx4(col + 4, d1);
+                                        tc_cp_32x128b_warpx4(col + 8, d2);
+                                    }
+                                }
+                                // sf_ready completes once these copies landed (in both CTAs of a pair)
+                                if constexpr (kPair == 2) tc_commit_pair_mc(smem_u32(&sh.sf_ready[slot]), 0x3);
+                                else tc_commit(smem_u32(&sh.sf_ready[slot]));
+                            }
+                        }
+                        if (ok) ok = load_next();
                     }
                     ok = __shfl_sync(0xFFFFFFFFu, ok, 0);
-                    continue;
                 }
-                sf_to_tmem_layout(sf, lane);
-                fence_proxy_async_smem();
-                __syncwarp();
-                if (lane == 0) {
-                    if (kPair == 2 && rank != 0) {
-                        mbar_arrive_cluster(leader(sh.sf_peer[slot]));
-                    } else {
-                        if (kPair == 2) ok = wait_or_abort(smem_u32(&sh.sf_peer[slot]), bit, sh, p.status);
-                        if (ok && j >= 3)
-                            ok = wait_or_abort(smem_u32(&sh.grp_done[(j - 3) % kSfTmemGroups]),
-                                               ((j - 3) / kSfTmemGroups) & 1u, sh, p.status);
-                        if (ok) {
-                            tc_fence_after();
-                            const int nchunks = min(4, ct.nk - 4 * g);
-                            for (int c = 0; c < nchunks; ++c) {
-                                const uint32_t col = tmem + kSfCol0 + ((j % kSfTmemGroups) * 4 + c) * kSfSlotCols;
-                                const uint64_t d0 = smem_desc(sf + c * 512, 0, 128, 0);
-                                const uint64_t d1 = smem_desc(sf + 2048 + c * 512, 0, 128, 0);
-                                const uint64_t d2 = smem_desc(sf + 4096 + c * 512, 0, 128, 0);
-                                if constexpr (kPair == 2) {
-                                    tc_cp_32x128b_warpx4_pair(col + 0, d0);
-                                    tc_cp_32x128b_warpx4_pair(col + 4, d1);
-                                    tc_cp_32x128b_warpx4_pair(col + 8, d2);
-                                } else {
-                                    tc_cp_32x128b_warpx4(col + 0, d0);
-                                    tc_cp_32x128b_warpx4(col + 4, d1);
-                                    tc_cp_32x128b_warpx4(col + 8, d2);
-                                }
-                            }
-                            // sf_ready completes once these copies landed (in both CTAs of a pair)
-                            if constexpr (kPair == 2) tc_commit_pair_mc(smem_u32(&sh.sf_ready[slot]), 0x3);
-                            else tc_commit(smem_u32(&sh.sf_ready[slot]));
-                        }
-                    }
-                    if (ok) ok = load_next();
-                }
-                ok = __shfl_sync(0xFFFFFFFFu, ok, 0);
             }
         }
     } else {
+        if constexpr (kF32) regs_raise<kRegsEpi>();
         // ------------------------------------------------ epilogue (every CTA)
-        const int e = warp - 2, q = warp & 3, h = e >> 2;
+        const int e = warp - C::kEpiWarp0, q = warp & 3, h = e >> 2;
         int32_t hint = 0, local = 0;
         uint32_t kg = 0, jg = 0;                 // FP32 scales: K-steps and scale groups consumed
         for (int64_t t = unit; t < total; t += units, ++local) {
             const Tile tl = map_tile<C::kTileM, C::kBN, kWgrad>(p, sh, t, hint);
-            // this warp's output columns (FP32 scales: 64, otherwise 128); their
-            // bias is loaded now, while the tile's MMAs run
-            const int32_t nbw = tl.n0 + (kF32 ? 64 * h : 128 * h);
+            // this warp's 128 output columns; their bias is loaded now, while
+            // the tile's MMAs run
+            const int32_t nbw = tl.n0 + 128 * h;
             uint4 bias_pre = make_uint4(0u, 0u, 0u, 0u);
             if (C::kStagedStores && p.has_bias && lane < 16 && nbw + 8 * lane < p.N)
                 bias_pre = __ldg(reinterpret_cast<const uint4*>(p.bias + int64_t(tl.group) * p.N + nbw + 8 * lane));
             uint32_t acc0[64], acc1[64];
             if constexpr (kF32) {
-                // acc (registers: my 32 rows x 64 columns 64 h ..) += product(K-step) *
-                // sA[row][kb] * sB[col][kb], one K-step (128) per scale block
+                // acc (registers: my row x the warp's 128 columns 128 h ..) +=
+                // product(K-step) * sA[row][kb] * sB[col][kb], one K-step (128)
+                // per scale block
 #pragma unroll
-                for (int i = 0; i < 64; ++i) acc0[i] = 0u;
+                for (int i = 0; i < 64; ++i) acc0[i] = acc1[i] = 0u;
                 uint32_t slot = 0;
                 bool ok = true;
                 const uint32_t lanes = uint32_t(32 * q) << 16;
@@ -995,11 +1059,18 @@ gemm_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_constant__ C
                         break;
                     }
                     tc_fence_after();
+                    const uint32_t src = tmem + lanes + uint32_t(C::kBN) * b + uint32_t(128 * h);
                     uint32_t v[64];
-                    tmem_ld_32x32b_x64(tmem + lanes + uint32_t(C::kBN) * b + uint32_t(64 * h), v);
+                    tmem_ld_32x32b_x64(src, v);
                     const uint32_t sf = smem_u32(smem + C::kStages * C::kStageBytes + slot * C::kSfSlotBytes);
                     const float sa = __uint_as_float(lds32(sf + (32 * q + lane) * 16 + (k & 3) * 4));
-                    const uint32_t sbt = sf + kSFABytes + (k & 3) * 512 + 256 * h;   // B scales of my 64 columns
+                    // B scales of my 128 columns: [4 K-steps][256 columns] fp32
+                    const uint32_t sbt = sf + kSFABytes + (k & 3) * 1024 + 512 * h;
+                    // 2D weight blocks: the warp's 128 columns are one 128 x 128 block
+                    const float f = p.b_2d ? sa * __uint_as_float(lds32(sbt)) : 0.0f;
+                    tmem_ld_wait();
+                    scale_accumulate_64(acc0, v, p.b_2d, f, sa, sbt);
+                    tmem_ld_32x32b_x64(src + 64, v);
                     tmem_ld_wait();
                     tc_fence_before();
                     __syncwarp();
@@ -1008,32 +1079,7 @@ gemm_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_constant__ C
                         if constexpr (kPair == 2) mbar_arrive_cluster_relaxed(leader(sh.scr_empty[b]));
                         else mbar_arrive(smem_u32(&sh.scr_empty[b]));
                     }
-                    if (p.b_2d) {
-                        const float f = sa * __uint_as_float(lds32(sbt - 256 * h));   // the tile is one 128-column block
-                        // packed pairs: one f32x2 FMA per two columns (each half rounds as fmaf does)
-#pragma unroll
-                        for (int j = 0; j < 64; j += 2) {
-                            uint64_t a2, v2, f2;
-                            asm("mov.b64 %0, {%1, %2};" : "=l"(a2) : "r"(acc0[j]), "r"(acc0[j + 1]));
-                            asm("mov.b64 %0, {%1, %2};" : "=l"(v2) : "r"(v[j]), "r"(v[j + 1]));
-                            asm("mov.b64 %0, {%1, %1};" : "=l"(f2) : "r"(__float_as_uint(f)));
-                            asm("fma.rn.f32x2 %0, %1, %2, %0;" : "+l"(a2) : "l"(v2), "l"(f2));
-                            asm("mov.b64 {%0, %1}, %2;" : "=r"(acc0[j]), "=r"(acc0[j + 1]) : "l"(a2));
-                        }
-                    } else {
-#pragma unroll
-                        for (int j4 = 0; j4 < 16; ++j4) {
-                            const uint4 w = lds128(sbt + 16 * j4);
-                            const float sbj[4] = {__uint_as_float(w.x), __uint_as_float(w.y), __uint_as_float(w.z),
-                                                  __uint_as_float(w.w)};
-#pragma unroll
-                            for (int i = 0; i < 4; ++i) {
-                                const int j = 4 * j4 + i;
-                                acc0[j] = __float_as_uint(__fmaf_rn(__fmul_rn(__uint_as_float(v[j]), sbj[i]), sa,
-                                                                    __uint_as_float(acc0[j])));
-                            }
-                        }
-                    }
+                    scale_accumulate_64(acc1, v, p.b_2d, f, sa, sbt + 256);
                     __syncwarp();
                     if (lane == 0 && last_of_group) mbar_arrive(smem_u32(&sh.sf_done[slot]));   // scales read
                     if (last_of_group) ++jg;
@@ -1069,7 +1115,7 @@ gemm_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_constant__ C
             if constexpr (C::kStagedStores) {
                 const int64_t row0 = row - lane;
                 if (row0 < tl.row_end) {             // warp-uniform: some row of this warp is stored
-                    // output columns of acc0 / acc1 (FP32 scales: 64 columns per warp, acc0 only)
+                    // output columns of acc0 / acc1
                     const int32_t nb0 = nbw;
                     const uint32_t epi = smem_u32(smem + C::kStages * C::kStageBytes + kSfRing * C::kSfSlotBytes);
                     const uint32_t stage = epi + uint32_t(e) * 4096u;
@@ -1084,7 +1130,7 @@ gemm_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_constant__ C
                     const bool tma = !kAcc && (row0 + 32 <= tl.row_end || tl.row_end == d_rows);
                     if (nb0 < p.N)
                         store_64_staged<kAcc>(acc0, p, bias, row0, tl.row_end, nb0, stage, lane, &map_d, &map_aux, tma);
-                    if (!kF32 && nb0 + 64 < p.N)
+                    if (nb0 + 64 < p.N)
                         store_64_staged<kAcc>(acc1, p, bias + 128u, row0, tl.row_end, nb0 + 64, stage, lane, &map_d,
                                               &map_aux, tma);
                 }
@@ -1092,7 +1138,7 @@ gemm_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_constant__ C
                 // (tcgen05.ld is warp-collective: the lanes' row test guards the stores only)
                 const bool live = row < tl.row_end;
                 const uint16_t* bias = p.has_bias ? p.bias + int64_t(tl.group) * p.N : nullptr;
-                const int32_t nb = tl.n0 + (kF32 ? 64 * h : 128 * h);
+                const int32_t nb = tl.n0 + 128 * h;
                 // The next tile's operands stream in while these stores go out;
                 // a burst of D/AUX stores at the start of that tile slows its
                 // loads, so the 8 chunks are spread over about half of the
@@ -1105,7 +1151,7 @@ gemm_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_constant__ C
                         __nanosleep(gap_ns);
                     }
                 }
-                if (live && !kF32) {
+                if (live) {
 #pragma unroll
                     for (int j = 0; j < 4; ++j) {
                         if (nb + 64 + 16 * j < p.N) store_chunk<kAcc>(acc1 + 16 * j, p, bias, row, nb + 64 + 16 * j);
@@ -1195,6 +1241,16 @@ te_mx_status launch_gemm(const GemmArgs& a, int sms, unsigned int* status, cudaS
     auto kern = gemm_kernel<kPair, kAcc, kWgrad, kF32>;
     cudaError_t e = set_smem_attribute_once(reinterpret_cast<const void*>(kern), C::kSmemDyn);
     if (e != cudaSuccess) return cuda_status(e, "cudaFuncSetAttribute(gemm)");
+    if constexpr (kF32) {
+        // the kernel moves registers between warp groups (setmaxnreg): the
+        // block must be launched with at least the registers the split hands
+        // out, or a raise would wait for ever
+        cudaFuncAttributes fa{};
+        if ((e = cudaFuncGetAttributes(&fa, kern)) != cudaSuccess) return cuda_status(e, "cudaFuncGetAttributes(gemm)");
+        if (fa.numRegs * 12 < 4 * kRegsRoles + 8 * kRegsEpi)
+            return set_error(TE_MX_ERR_CUDA, "GEMM with FP32 scales built with %d registers per thread; its register "
+                             "split needs %d", fa.numRegs, (4 * kRegsRoles + 8 * kRegsEpi) / 12);
+    }
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(unsigned(units * kPair));
     cfg.blockDim = dim3(kF32 ? kThreads + 32 : kThreads);
@@ -1243,12 +1299,10 @@ te_mx_status gemm_launch(const GemmArgs& a, cudaStream_t stream) {
     // loads 32 KB per K-step for the same MMA work for which a single CTA
     // loads 48 KB, and operand ingress is what bounds the mainloop, so pairs
     // are faster even when fewer tiles than pairs exist (a single-CTA split
-    // would keep the same number of SMs busy).  FP32 scales: CTA pairs once
-    // there are enough 256-row tiles to fill the GPU.
-    const int64_t pair_tiles = ((a.M + 255) / 256) * ((a.N + kBN - 1) / kBN);
+    // would keep the same number of SMs busy).  FP32 scales: the same rule.
     const bool pair = a.wgrad ? a.M >= 256 : (a.groups > 0 ? a.M >= 256 * 8 : a.M >= 256);
-    if (a.f32_scales) return pair_tiles >= sms / 2 ? launch_gemm<2, false, false, true>(a, sms, status, stream)
-                                                   : launch_gemm<1, false, false, true>(a, sms, status, stream);
+    if (a.f32_scales) return pair ? launch_gemm<2, false, false, true>(a, sms, status, stream)
+                                  : launch_gemm<1, false, false, true>(a, sms, status, stream);
     if (a.wgrad) {
         if (a.acc_f32) return pair ? launch_gemm<2, true, true>(a, sms, status, stream)
                                    : launch_gemm<1, true, true>(a, sms, status, stream);

@@ -267,4 +267,17 @@ __device__ __forceinline__ void tc_commit_if(uint32_t bar, uint32_t issue) {
                  :: "r"(bar), "r"(issue) : "memory");
 }
 
+// Register reallocation between warp groups (setmaxnreg; every thread of the
+// warp group executes the same one).  An increase waits until enough registers
+// are free in the block's pool, so the sum over the block's warps must not
+// exceed what the block was launched with.
+template <int kRegs>
+__device__ __forceinline__ void regs_raise() {
+    asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" :: "n"(kRegs));
+}
+template <int kRegs>
+__device__ __forceinline__ void regs_lower() {
+    asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" :: "n"(kRegs));
+}
+
 }  // namespace temx
