@@ -121,6 +121,7 @@ constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kSfCol0 = 256;
 constexpr uint32_t kSfSlotCols = 12;
 constexpr uint32_t kSfSlots = 16;
+static_assert(kSfCol0 + kSfSlots * kSfSlotCols <= kTmemCols, "scale-factor slots fit in TMEM");
 static_assert(kScrBufs * Cfg<2, true>::kBN <= int(kTmemCols), "FP32-scale product buffers fit in TMEM");
 static_assert(4 * kRegsRoles + 8 * kRegsEpi <= 12 * 168, "FP32-scale register split");
 
@@ -395,11 +396,6 @@ __device__ __forceinline__ void f2_unpack(uint64_t v, float& lo, float& hi) {
 __device__ __forceinline__ uint64_t f2_add(uint64_t a, uint64_t b) {
     uint64_t r;
     asm("add.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(a), "l"(b));
-    return r;
-}
-__device__ __forceinline__ uint64_t f2_sub(uint64_t a, uint64_t b) {
-    uint64_t r;
-    asm("sub.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(a), "l"(b));
     return r;
 }
 __device__ __forceinline__ uint64_t f2_mul(uint64_t a, uint64_t b) {
