@@ -9,7 +9,7 @@
 // for MoE experts (ROCm/TransformerEngine README, "Single-Launch Grouped GEMM
 // Backends on ROCm").
 //
-// Kernel structure (persistent, one CTA per SM, 11 warps), in two shapes:
+// Kernel structure (persistent, one CTA per SM, 12 warps), in two shapes:
 //   kPair = 1: one CTA computes a 128 x 256 tile (cta_group::1);
 //   kPair = 2: a cluster of two CTAs computes a 256 x 256 tile with
 //              cta_group::2 MMAs: each CTA holds 128 rows of A and 128 rows of
@@ -21,10 +21,14 @@
 //   warp 0      TMA producer: A/B tiles (128-byte swizzle) into a kStages ring
 //               (completion on the MMA CTA's barrier) and, every 4th K-step,
 //               the row-major scale tiles (completion on the CTA's own barrier);
-//   warp 1      TMEM owner; in the MMA CTA one lane issues 4 block-scaled MMAs
+//   warps 1, 11 MMA issuers (warp 1 also owns TMEM): in the MMA CTA they take
+//               alternate K-steps, one lane issuing 4 block-scaled MMAs
 //               (K = 32 each) per 128-wide K-step and nothing else (a tcgen05
-//               instruction costs ~80-90 issue cycles, so the MMA thread has
-//               no slack for the scale copies);
+//               instruction costs ~80-90 issue cycles and blocks while the
+//               tensor pipe is busy, so one issuer waits while the other
+//               issues, and neither has slack for the scale copies); dense
+//               GEMMs of fewer than 16 K-steps and the grouped wgrad use warp
+//               1 alone;
 //   warp 10     scale-factor warp: turns each landed scale tile into the
 //               tcgen05 scale-factor layout in place (a 4x4 word transpose),
 //               copies the group's scale factors into TMEM (tcgen05.cp, from the
@@ -54,8 +58,7 @@ namespace {
 constexpr int kBM = 128;                 // accumulator rows per CTA (TMEM lanes)
 constexpr int kBN = 256;                 // tile columns (accumulator columns)
 constexpr int kBK = 128;                 // K per pipeline stage (bytes of E4M3)
-constexpr int kThreads = 352;          // 11 warps; FP32 scales: 12 (a second MMA issuer)
-constexpr int kMma2Warp = 3;             // FP32 scales only
+constexpr int kThreads = 384;            // 12 warps
 constexpr int kEpiWarps = 8;
 constexpr int kGroupM = 16;              // m-tiles per raster band (L2 reuse of B)
 constexpr int kMaxGroups = 1024;
@@ -63,6 +66,7 @@ constexpr int kSFABytes = kBM * 16;      // 128 rows x 16 scale bytes (4 K-steps
 constexpr int kSfRing = 3;               // scale-group slots in shared memory
 constexpr int kSfAhead = 2;              // scale groups loaded ahead of the one being prepared
 constexpr int kSfTmemGroups = 4;         // scale groups resident in TMEM
+constexpr int kSplitMinK = 16;           // MXFP8: dense GEMMs of at least this many K-steps use both MMA issuers
 constexpr int kScrBufs = 2;              // FP32 scales: K-step product buffers in TMEM (256 columns each)
 // FP32 scales: registers per thread after the split (warp group 0 / 1 and 2);
 // 4 x 64 + 8 x 216 = 1984 <= 12 x 168, the launch's 168 per thread
@@ -80,6 +84,7 @@ struct Cfg {
     static constexpr int kBBytes = kBRows * kBK;          // 32 or 16 KB
     static constexpr int kStages = kPair == 2 ? 5 : 4;
     static constexpr int kSfWarp = kF32 ? 2 : 10;         // scale-factor warp
+    static constexpr int kMma2Warp = kF32 ? 3 : 11;       // second MMA issuer
     static constexpr int kEpiWarp0 = kF32 ? 4 : 2;        // first epilogue warp
     static constexpr int kStageBytes = kABytes + kBBytes;
     static constexpr int kSFBBytes = kBN * 16;            // every CTA holds all of the tile's B rows' scales
@@ -171,6 +176,7 @@ struct __align__(16) SharedState {
     uint64_t tmem_full;
     uint64_t tmem_empty;                   // (MMA CTA) accumulator drained by the epilogue of every CTA
     uint64_t epi_drained;                  // this CTA's 8 epilogue warps hold their accumulator rows
+    uint64_t first_done;                   // (MMA CTA) the MMAs of a tile's first K-step completed
     // FP32-scale mode: K-step kg's product lands in TMEM buffer kg % kScrBufs
     // (columns 256 * buffer ..; the scaled accumulator lives in registers)
     uint64_t scr_full[kScrBufs];           // a product landed (each CTA)
@@ -659,7 +665,7 @@ __device__ __forceinline__ void scale_accumulate_64(uint32_t (&acc)[64], const u
 // of kScrBufs TMEM buffers and the epilogue warps accumulate it, scaled, in
 // registers.
 template <int kPair, bool kAcc, bool kWgrad, bool kF32>
-__global__ void __launch_bounds__(kF32 ? kThreads + 32 : kThreads, 1)   // 168 registers: 3 warps share a 16K-register sub-partition
+__global__ void __launch_bounds__(kThreads, 1)   // 168 registers: 3 warps share a 16K-register sub-partition
 gemm_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_constant__ CUtensorMap map_b,
             const __grid_constant__ CUtensorMap map_sfa, const __grid_constant__ CUtensorMap map_sfb,
             const __grid_constant__ CUtensorMap map_d, const __grid_constant__ CUtensorMap map_aux,
@@ -677,6 +683,10 @@ gemm_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_constant__ C
     auto leader = [&](const uint64_t& bar) -> uint32_t {
         return kPair == 2 ? mapa_shared(smem_u32(&bar), 0) : smem_u32(&bar);
     };
+    // MXFP8: two MMA issuers for dense GEMMs of at least kSplitMinK K-steps;
+    // otherwise (short K, or the grouped wgrad's per-expert K ranges) warp 1
+    // alone issues and commits, and the barriers count its arrivals only
+    const bool two_issuers = !kWgrad && p.k_iters >= kSplitMinK;
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < C::kStages; ++s) {
@@ -688,8 +698,9 @@ gemm_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_constant__ C
             mbar_init(smem_u32(&sh.sf_ready[s]), 1);
             mbar_init(smem_u32(&sh.sf_peer[s]), 1);
         }
-        for (int s = 0; s < kSfTmemGroups; ++s) mbar_init(smem_u32(&sh.grp_done[s]), 1);
-        mbar_init(smem_u32(&sh.tmem_full), 1);
+        for (int s = 0; s < kSfTmemGroups; ++s) mbar_init(smem_u32(&sh.grp_done[s]), two_issuers ? 2 : 1);
+        mbar_init(smem_u32(&sh.tmem_full), two_issuers ? 2 : 1);
+        mbar_init(smem_u32(&sh.first_done), 1);
         mbar_init(smem_u32(&sh.tmem_empty), kPair);
         mbar_init(smem_u32(&sh.epi_drained), kEpiWarps);
         if constexpr (kF32) {
@@ -783,12 +794,93 @@ gemm_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_constant__ C
         }
     };
 
+    // MXFP8: MMA issuer for the K-steps of one parity of the global K-step
+    // count: 4 block-scaled MMAs (K = 32 each) per 128-wide K-step.  Two
+    // issuers (warps 1 and kMma2Warp) alternate K-steps, so that one waits for
+    // its operands or blocks in a tcgen05.mma issue while the other issues.
+    // MMAs of different threads may run in either order, which only reorders
+    // the fp32 additions, except for a tile's first K-step, which overwrites
+    // the accumulator: the issuer that does not own it waits until its MMAs
+    // completed (first_done) before issuing any of the tile's MMAs.  That
+    // wait costs about one K-step's latency per tile, so only dense GEMMs of
+    // at least kSplitMinK K-steps use two issuers (two_issuers).  Both
+    // issuers wait for the accumulator, each scale group and the operands of
+    // their own K-steps, and both commit every scale group (grp_done) and
+    // every tile (tmem_full), whose barriers count two arrivals.
+    // (run by a whole warp, values warp-uniform; lane 0's tcgen05 operations
+    // are predicated on: about 4 % fewer cycles per K-step than a loop that
+    // lane 0 runs alone)
+    auto mma_mx = [&](uint32_t par) {
+        const uint32_t issue = lane == 0 ? 1u : 0u;
+        uint32_t g = 0, grp = 0;   // global K-step and scale-group counts (both issuers' K-steps)
+        int32_t local = 0;
+        bool ok = true;
+        auto wait = [&](const uint64_t& bar, uint32_t parity) -> bool {
+            // (the lanes decide together: warp-collective tcgen05 operations follow)
+            return __all_sync(0xFFFFFFFFu, wait_or_abort(smem_u32(&bar), parity, sh, p.status));
+        };
+        for (int64_t t = unit; t < total && ok; t += units, ++local) {
+            const int32_t nk = p.k_iters;
+            if (local > 0) {
+                if (!wait(sh.tmem_empty, uint32_t(local - 1) & 1u)) break;
+                tc_fence_after();
+            }
+            if ((g & 1u) != par) {               // the other issuer owns the tile's first K-step
+                if (!wait(sh.first_done, uint32_t(local) & 1u)) break;
+                tc_fence_after();
+            }
+            for (int32_t k = 0; k < nk; ++k, ++g) {
+                const bool mine = (g & 1u) == par;
+                const uint32_t stage = g % C::kStages, phase = (g / C::kStages) & 1u;
+                // (the operands first, then a new scale group's factors, as in
+                // the single-issuer loop)
+                if (mine && !wait(sh.full[stage], phase)) { ok = false; break; }
+                if ((k & 3) == 0) {
+                    if (!wait(sh.sf_ready[grp % kSfRing], (grp / kSfRing) & 1u)) { ok = false; break; }
+                    tc_fence_after();
+                }
+                if (mine) {
+                    uint8_t* st = smem + stage * C::kStageBytes;
+                    const uint32_t sf_col = tmem + kSfCol0 + ((grp % kSfTmemGroups) * 4 + uint32_t(k & 3)) * kSfSlotCols;
+                    const uint64_t a_desc = smem_desc(smem_u32(st), 16, 1024, 2);
+                    const uint64_t b_desc = smem_desc(smem_u32(st + C::kABytes), 16, 1024, 2);
+#pragma unroll
+                    for (int kk = 0; kk < 4; ++kk) {
+                        // +32 bytes along K inside the 128-byte swizzled row = +2 in the address field
+                        const uint32_t idesc = idesc_sf(C::kIdescBase, uint32_t(kk));
+                        const uint32_t acc = (k | kk) != 0 ? 1u : 0u;
+                        if constexpr (kPair == 2)
+                            mma_mxf8_pair_if(tmem, a_desc + 2 * kk, b_desc + 2 * kk, idesc, sf_col, sf_col + 4, acc,
+                                             issue);
+                        else
+                            mma_mxf8_if(tmem, a_desc + 2 * kk, b_desc + 2 * kk, idesc, sf_col, sf_col + 4, acc, issue);
+                    }
+                    if constexpr (kPair == 2) tc_commit_pair_mc_if(smem_u32(&sh.empty[stage]), 0x3, issue);
+                    else tc_commit_if(smem_u32(&sh.empty[stage]), issue);
+                    if (k == 0) {
+                        if constexpr (kPair == 2) tc_commit_pair_mc_if(smem_u32(&sh.first_done), 0x1, issue);
+                        else tc_commit_if(smem_u32(&sh.first_done), issue);
+                    }
+                }
+                if ((k & 3) == 3 || k == nk - 1) {             // last K-step of the scale group
+                    if constexpr (kPair == 2)
+                        tc_commit_pair_mc_if(smem_u32(&sh.grp_done[grp % kSfTmemGroups]), 0x1, issue);
+                    else tc_commit_if(smem_u32(&sh.grp_done[grp % kSfTmemGroups]), issue);
+                    ++grp;
+                }
+            }
+            if (!ok) break;
+            if constexpr (kPair == 2) tc_commit_pair_mc_if(smem_u32(&sh.tmem_full), 0x3, issue);
+            else tc_commit_if(smem_u32(&sh.tmem_full), issue);
+        }
+    };
+
     // Role warps (for FP32 scales warp group 0) and epilogue warps.  With FP32
     // scales the role warp group gives registers to the epilogue warp groups,
     // whose threads hold 128 accumulator columns and a product slice each
     // (the host checked that the split fits); each side changes its count
     // first, before the warps of a group part ways.
-    const bool role_warp = kF32 ? warp < 4 : (warp < 2 || warp == C::kSfWarp);
+    const bool role_warp = kF32 ? warp < 4 : (warp < 2 || warp == C::kSfWarp || warp == C::kMma2Warp);
     if (role_warp) {
         if constexpr (kF32) regs_lower<kRegsRoles>();
         if (warp == 0) {
@@ -824,7 +916,9 @@ gemm_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_constant__ C
             // ------------------------------------------------ MMA issuer (the MMA CTA)
             if (rank == 0 && kF32) {
                 mma_f32(0u);
-            } else if (rank == 0 && !kF32) {
+            } else if (rank == 0 && two_issuers) {
+                mma_mx(0u);
+            } else if (rank == 0) {
                 // The whole warp runs the loop (its values stay warp-uniform) and
                 // lane 0's tcgen05.mma / tcgen05.commit are predicated on: about 4 %
                 // fewer cycles per K-step than a loop that lane 0 runs alone.
@@ -860,7 +954,7 @@ gemm_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_constant__ C
                             tmem + kSfCol0 + ((grp % kSfTmemGroups) * 4 + uint32_t(k & 3)) * kSfSlotCols;
                         const uint64_t a_desc = smem_desc(smem_u32(st), 16, 1024, 2);
                         const uint64_t b_desc = smem_desc(smem_u32(st + C::kABytes), 16, 1024, 2);
-    #pragma unroll
+#pragma unroll
                         for (int kk = 0; kk < 4; ++kk) {
                             // +32 bytes along K inside the 128-byte swizzled row = +2 in the address field
                             const uint32_t idesc = idesc_sf(C::kIdescBase, uint32_t(kk));
@@ -886,8 +980,11 @@ gemm_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_constant__ C
                     else tc_commit_if(smem_u32(&sh.tmem_full), issue);
                 }
             }
-        } else if (kF32 && warp == kMma2Warp) {
-            if (rank == 0) mma_f32(1u);
+        } else if (warp == C::kMma2Warp) {
+            if (rank == 0) {
+                if constexpr (kF32) mma_f32(1u);
+                else if (two_issuers) mma_mx(1u);
+            }
         } else {                                   // the scale-factor warp
             // ------------------------------------------------ scale-factor layout (every CTA)
             // Scale groups (4 K-steps each, the last of a tile possibly shorter)
@@ -1249,7 +1346,7 @@ te_mx_status launch_gemm(const GemmArgs& a, int sms, unsigned int* status, cudaS
     }
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(unsigned(units * kPair));
-    cfg.blockDim = dim3(kF32 ? kThreads + 32 : kThreads);
+    cfg.blockDim = dim3(kThreads);
     cfg.dynamicSmemBytes = C::kSmemDyn;
     cfg.stream = stream;
     cudaLaunchAttribute attr[2];
