@@ -602,7 +602,7 @@ __device__ __forceinline__ void store_64_staged(uint32_t* acc, const GemmParams&
             fence_proxy_async_smem();
             __syncwarp();
             if (lane == 0) {
-                tma_store_2d(is_aux ? map_aux : map_d, stage, n, int32_t(row0));
+                tma_store_2d_evict_first(is_aux ? map_aux : map_d, stage, n, int32_t(row0));
                 bulk_commit();
             }
             __syncwarp();

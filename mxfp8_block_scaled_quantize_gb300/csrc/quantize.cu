@@ -158,6 +158,8 @@ quantize_kernel(const __grid_constant__ CUtensorMap x_map, const __grid_constant
     __shared__ __align__(8) uint64_t bars[kWarps][kStages];
     // row-wise scale bytes of a strip (64 rows x 16 bytes), double-buffered by round
     __shared__ __align__(16) uint8_t row_scales[2][kRows][16];
+    // bias-gradient band sums of a strip (8 units x 64 columns), double-buffered by round
+    __shared__ __align__(16) float part_stage[2][kWarps * kCols];
 
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -239,10 +241,8 @@ quantize_kernel(const __grid_constant__ CUtensorMap x_map, const __grid_constant
             }
             if (kDbias) {
                 if (!kColwise) col_sums(tile, lane, sum_lo, sum_hi);
-                const int64_t c = c0 + 2 * lane;
-                if (c < p.cols)                                // rows past the end were loaded as 0
-                    *reinterpret_cast<float2*>(p.partial + (r0 / kDbiasBandRows) * p.cols + c) =
-                        make_float2(sum_lo, sum_hi);
+                // (rows past the end were loaded as 0; columns past the end are not copied out)
+                *reinterpret_cast<float2*>(&part_stage[i & 1][warp * kCols + 2 * lane]) = make_float2(sum_lo, sum_hi);
             }
             if (kRowwise) {
 #pragma unroll
@@ -286,17 +286,22 @@ quantize_kernel(const __grid_constant__ CUtensorMap x_map, const __grid_constant
                 bulk_commit();             // (an empty group when only the bias gradient is produced)
             }
         }
-        if (ok && lane == 0 && i + kStages < n_mine) {
+        const bool refill = ok && i + kStages < n_mine;
+        if (refill && lane == 0) {
             bulk_wait_read_all();         // the stores have read the tile: refill it
             load(bar, tile, lband, lstrip);
             walk.step(lband, lstrip);
         }
+        // warp 2 copies a strip's band sums out after the barrier below; the copy
+        // of round i - 1 must have read its staging area before the barrier of
+        // round i, after which the warps write it again (a refill waited for it)
+        if (kDbias && warp == 2 && lane == 0 && !refill) bulk_wait_read_all();
         __syncwarp();
-        if (kRowwise) {
-            // the strip's row scales: 16 bytes per row, one store per row (warps 0-1,
-            // lane = row); a strip cut by the band's end writes its bytes one by one
+        if (kRowwise || kDbias) {
             named_barrier_sync(1, kWarps * 32);
-            if (warp < 2) {
+            if (kRowwise && warp < 2) {
+                // the strip's row scales: 16 bytes per row, one store per row (warps 0-1,
+                // lane = row); a strip cut by the band's end writes its bytes one by one
                 const int rl = warp * 32 + lane;
                 const int64_t r = r0 + rl;
                 const int64_t first = int64_t(strip) * kWarps * 2;             // the strip's first scale byte
@@ -313,6 +318,15 @@ quantize_kernel(const __grid_constant__ CUtensorMap x_map, const __grid_constant
                             if (k < valid) st_global_u8(sp + k, (w4[k >> 2] >> (8 * (k & 3))) & 0xFFu);
                     }
                 }
+            }
+            if (kDbias && warp == 2 && lane == 0) {
+                // the strip's band sums: one bulk copy of its (at most 512) columns
+                const int64_t cs = int64_t(strip) * kWarps * kCols;
+                const int64_t n = p.cols - cs < kWarps * kCols ? p.cols - cs : kWarps * kCols;   // a multiple of 32
+                float* dst = p.partial + int64_t(band) * p.cols + cs;
+                asm volatile("cp.async.bulk.global.shared::cta.bulk_group [%0], [%1], %2;"
+                             :: "l"(dst), "r"(smem_u32(&part_stage[i & 1][0])), "r"(uint32_t(n) * 4u) : "memory");
+                bulk_commit();
             }
         }
         walk.step(band, strip);

@@ -267,6 +267,16 @@ __device__ __forceinline__ void tc_commit_if(uint32_t bar, uint32_t issue) {
                  :: "r"(bar), "r"(issue) : "memory");
 }
 
+// TMA store of a shared-memory tile with an L2 evict-first policy: the GEMM's
+// outputs are not read again by it, and without the hint they displace the
+// operand rows that later tiles reuse from L2.
+__device__ __forceinline__ void tma_store_2d_evict_first(const CUtensorMap* desc, uint32_t src, int32_t x, int32_t y) {
+    uint64_t policy;
+    asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(policy));
+    asm volatile("cp.async.bulk.tensor.2d.global.shared::cta.bulk_group.L2::cache_hint [%0, {%2, %3}], [%1], %4;"
+                 :: "l"(reinterpret_cast<uint64_t>(desc)), "r"(src), "r"(x), "r"(y), "l"(policy) : "memory");
+}
+
 // Register reallocation between warp groups (setmaxnreg; every thread of the
 // warp group executes the same one).  An increase waits until enough registers
 // are free in the block's pool, so the sum over the block's warps must not
