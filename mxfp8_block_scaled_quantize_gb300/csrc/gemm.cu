@@ -602,7 +602,11 @@ __device__ __forceinline__ void store_64_staged(uint32_t* acc, const GemmParams&
             fence_proxy_async_smem();
             __syncwarp();
             if (lane == 0) {
-                tma_store_2d_evict_first(is_aux ? map_aux : map_d, stage, n, int32_t(row0));
+                // (evict-first for the dense GEMMs; the grouped forward GEMM's
+                // outputs keep the default policy: with the hint, the MXFP8
+                // quantisation launched after it measured slower)
+                if (p.groups > 0 && !p.wgrad) tma_store_2d(is_aux ? map_aux : map_d, stage, n, int32_t(row0));
+                else tma_store_2d_evict_first(is_aux ? map_aux : map_d, stage, n, int32_t(row0));
                 bulk_commit();
             }
             __syncwarp();
