@@ -174,8 +174,7 @@ struct __align__(16) SharedState {
     uint64_t sf_peer[kSfRing];             // (MMA CTA of a pair) the peer's scale group is in copy layout
     uint64_t grp_done[kSfTmemGroups];      // (MMA CTA) the MMAs of a scale group completed
     uint64_t tmem_full;
-    uint64_t tmem_empty;                   // (MMA CTA) accumulator drained by the epilogue of every CTA
-    uint64_t epi_drained;                  // this CTA's 8 epilogue warps hold their accumulator rows
+    uint64_t tmem_empty;                   // (MMA CTA) accumulator drained by every epilogue warp of the pair
     uint64_t first_done;                   // (MMA CTA) the MMAs of a tile's first K-step completed
     // FP32-scale mode: K-step kg's product lands in TMEM buffer kg % kScrBufs
     // (columns 256 * buffer ..; the scaled accumulator lives in registers)
@@ -705,8 +704,7 @@ gemm_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_constant__ C
         for (int s = 0; s < kSfTmemGroups; ++s) mbar_init(smem_u32(&sh.grp_done[s]), two_issuers ? 2 : 1);
         mbar_init(smem_u32(&sh.tmem_full), two_issuers ? 2 : 1);
         mbar_init(smem_u32(&sh.first_done), 1);
-        mbar_init(smem_u32(&sh.tmem_empty), kPair);
-        mbar_init(smem_u32(&sh.epi_drained), kEpiWarps);
+        mbar_init(smem_u32(&sh.tmem_empty), kPair * kEpiWarps);
         if constexpr (kF32) {
             for (int b = 0; b < kScrBufs; ++b) {
                 mbar_init(smem_u32(&sh.scr_full[b]), 1);
@@ -1196,17 +1194,13 @@ gemm_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_constant__ C
                 for (int i = 0; i < 64; ++i) acc0[i] = acc1[i] = 0u;
             }
             tc_fence_before();
-            // Once all 8 epilogue warps hold their registers, one relaxed arrive
-            // per CTA releases the accumulator (the reads retired at wait::ld;
-            // a release here would wait for this warp's earlier global stores).
+            // Each epilogue warp releases its part of the accumulator with one
+            // relaxed arrive on the MMA CTA's barrier, which completes once all
+            // the warps of the CTA (of both CTAs of a pair) hold their registers
+            // (the reads retired at wait::ld; a release arrive would also wait
+            // for this warp's earlier global stores).
             __syncwarp();
-            if (lane == 0) mbar_arrive(smem_u32(&sh.epi_drained));
-            if (warp == 2 && lane == 0) {
-                if (wait_or_abort(smem_u32(&sh.epi_drained), uint32_t(local) & 1u, sh, p.status)) {
-                    if constexpr (kPair == 2) mbar_arrive_cluster_relaxed(leader(sh.tmem_empty));
-                    else mbar_arrive(smem_u32(&sh.tmem_empty));
-                }
-            }
+            if (lane == 0) mbar_arrive_cluster_relaxed(leader(sh.tmem_empty));
             }
             const int64_t row = int64_t(tl.d_row) + int64_t(rank) * kBM + 32 * q + lane;
             if constexpr (C::kStagedStores) {
