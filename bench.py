@@ -299,21 +299,26 @@ def time_device(step, steps, warmup, sampler):
     return total_ms, per_kernel, clocks
 
 
-def time_next(step, reps, fp8_peak, hbm_gbs):
-    """CUDA-event time of each backward kernel (after the step ran once)."""
+def time_next(step, reps, fp8_peak, hbm_gbs, batches=5):
+    """CUDA-event time of each backward kernel (after the step ran once): the
+    median over `batches` batches of `reps` back-to-back launches (a single
+    batch swung by up to 8 % between runs on the longer kernels)."""
     step.run()
     torch.cuda.synchronize()
     res = {}
     for name, fn in step.next_kernels:
         fn()
         torch.cuda.synchronize()
-        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        a.record()
-        for _ in range(reps):
-            fn()
-        b.record()
-        torch.cuda.synchronize()
-        ms = a.elapsed_time(b) / reps
+        per = []
+        for _ in range(batches):
+            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            a.record()
+            for _ in range(reps):
+                fn()
+            b.record()
+            torch.cuda.synchronize()
+            per.append(a.elapsed_time(b) / reps)
+        ms = sorted(per)[len(per) // 2]
         if name in step.next_flops:
             ach = step.next_flops[name] / (ms * 1e-3) / 1e12
             res[name] = {"us": ms * 1e3, "achieved": ach, "unit": "TFLOP/s", "frac": ach / fp8_peak}
@@ -910,7 +915,7 @@ def main():
     qms = sum(per_kernel[n] for n in step.bytes)
     gms = sum(per_kernel[n] for n in step.flops)
 
-    next_rows = time_next(step, 20, fp8_peak, peaks["hbm_gbs"])
+    next_rows = time_next(step, 6, fp8_peak, peaks["hbm_gbs"])
     configs = time_configs(dev, fp8_peak, peaks["hbm_gbs"])
     e2e_ms, h2d, d2h = time_e2e((step, Step(host, dev)), host, max(4, args.steps // 4), args.warmup)
     e2e_ms = dist_max(e2e_ms)
