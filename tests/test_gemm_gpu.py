@@ -134,6 +134,19 @@ def test_dense_pair_tiles_vs_oracle(M, N, K, bias, gelu):
     check_dense(M, N, K, bias, gelu, seed=M + N + K + 1)
 
 
+# K of 16 or more K-steps: two MMA issuers take alternate K-steps.  An odd
+# number of K-steps (K = 17 x 128) makes the owner of a tile's first K-step
+# alternate from tile to tile, so each issuer both waits for the other's first
+# K-step and is waited for; the CTA pairs take several tiles each.
+@pytest.mark.parametrize("M,N,K,bias,gelu", [
+    (4096, 2048, 2176, True, True),
+    (2304, 1280, 2048, False, False),
+    (200, 528, 2176, True, False),
+])
+def test_dense_two_issuers_vs_oracle(M, N, K, bias, gelu):
+    check_dense(M, N, K, bias, gelu, seed=M + N + K + 2)
+
+
 def test_identity_b_pair_tiles_is_bit_exact():
     m, k = 2048, 2560
     qa, sa = O.quantize_rowwise(rand_bits((m, k), 41, std=3.0))
@@ -203,6 +216,7 @@ def run_grouped(group_m, total_m, N, K, bias, gelu, seed):
     ([0, 5, 130, 0, 256, 77], 160, 256, True, True),
     ([700, 0, 1, 513, 900, 0, 300], 256, 256, True, True),        # >= 2048 rows: CTA pairs
     ([300], 256, 512, False, False),
+    ([700, 0, 513, 900, 300], 256, 2176, True, True),               # two MMA issuers, odd K-steps
     ([1, 0, 0, 129, 127, 128, 0, 2], 272, 384, True, False),
 ])
 def test_grouped_vs_oracle(group_m, N, K, bias, gelu):
